@@ -1,0 +1,255 @@
+/*
+ * tf.h -- C ABI of the exact speculative-decoding verify pass for GB300 (sm_103a).
+ *
+ * The method (TensorFold README, section on its two guarantees):
+ *   1. every token is the model's own sample: the token at position p is the
+ *      argmax over the top-k / top-p candidates of  logit / T + g(seed, p, token),
+ *      g being Gumbel noise from a hash of the seed, the position and the token id;
+ *   2. a row of a multi-row verify pass gets the same bits as a one-row step;
+ * so a draft is accepted exactly when it equals the token serial decoding
+ * would sample there, and drafted decoding writes the same bytes as serial
+ * decoding.  Weights are 4-bit codes with one fp16 scale per group of 64
+ * (dense model) or 32 (MoE model) input features (README, "What each
+ * checkpoint needs").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All pointers marked "dev" are CUDA device pointers owned by the caller.
+ *   The library never allocates, frees or retains device memory; it keeps no
+ *   global state besides a thread-local error message.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Every compute call only enqueues work on that stream and returns;
+ *   outputs are valid once the stream has reached that point.
+ * - `ws` is caller-provided device scratch ("workspace") of at least the size
+ *   the matching *_workspace_bytes() query returns, 256-byte aligned, and
+ *   zero-filled before its first use (the kernels leave the parts they
+ *   need zeroed when they finish, so a workspace can be reused by later calls
+ *   on the same stream without clearing it again).  Calls that overlap in time
+ *   must not share a workspace.
+ * - Host-side argument errors return TF_ERR_INVALID_ARG / TF_ERR_UNSUPPORTED
+ *   before anything is enqueued; tf_last_error() then describes the problem.
+ *   Errors that only the device can see (a non-finite logit, an out-of-range
+ *   token id, a bounded wait that ran out) are recorded in the first word of
+ *   the workspace; read them with tf_workspace_status().  Nothing traps,
+ *   aborts or throws across this boundary.
+ * - Row counts R are 1..TF_MAX_ROWS.  R = 1 is the serial reference
+ *   (README: "draft": false decodes one token a round).
+ * - bf16 / fp16 values are passed as their 16-bit IEEE bit patterns (uint16_t).
+ */
+#ifndef TF_H
+#define TF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TF_API __attribute__((visibility("default")))
+#else
+#define TF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TF_MAX_ROWS 16
+#define TF_MAX_TOP_K 64
+
+typedef enum tf_status {
+    TF_OK = 0,
+    TF_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or value */
+    TF_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels implement */
+    TF_ERR_CUDA = 3,          /* a CUDA runtime call failed (message in tf_last_error) */
+    TF_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out (device status) */
+    TF_ERR_WORKSPACE = 5      /* workspace missing, misaligned or too small */
+} tf_status;
+
+/* Device-status codes stored in the first 32-bit word of a workspace. */
+#define TF_DEV_OK 0
+#define TF_DEV_TIMEOUT 1          /* an mbarrier wait exceeded its iteration limit */
+#define TF_DEV_NONFINITE_LOGIT 2  /* a logit was NaN or +-inf (its row's token is -1) */
+#define TF_DEV_BAD_TOKEN 3        /* a token id outside [0, vocab) reached the embedding */
+
+/* Thread-local description of the last host-side error ("" when none). */
+TF_API const char *tf_last_error(void);
+TF_API const char *tf_status_string(tf_status s);
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+TF_API int tf_version(void);
+
+/*
+ * Read and clear the device-status word of a workspace.  Synchronises `stream`
+ * first.  *code receives one of the TF_DEV_* values.  Returns TF_OK, or
+ * TF_ERR_CUDA if the copy failed.
+ */
+TF_API tf_status tf_workspace_status(void *ws, void *stream, int32_t *code);
+
+/* ------------------------------------------------------------------------
+ * W4 weights
+ * ------------------------------------------------------------------------
+ * Canonical layout (the input of tf_pack_w4), for a linear layer with K
+ * input and N output features and group size G (32 or 64):
+ *   codes  uint8  [N][K/2]  element (n, k) is the low nibble of byte k/2 when k
+ *                           is even and the high nibble when k is odd; each
+ *                           nibble is a two's-complement integer in [-8, 7];
+ *   scales uint16 [N][K/G]  fp16 scale of group g = k / G of row n;
+ *   w[n][k] = code(n, k) * scale(n, k / G)   (symmetric, no zero point).
+ * The kernels read a private "packed" layout produced on the device by
+ * tf_pack_w4 (a load-time step).  Its size is tf_w4_packed_bytes(); N is padded
+ * up to a multiple of 256 with zero weights inside it.
+ */
+typedef struct tf_w4_matrix {
+    const void *packed;   /* dev, tf_w4_packed_bytes(K, N, group) bytes, 256-B aligned */
+    int32_t K;            /* input features, a positive multiple of 64 */
+    int32_t N;            /* output features, >= 1 */
+    int32_t group;        /* 32 or 64 */
+} tf_w4_matrix;
+
+/* Bytes of the packed layout, or 0 if (K, N, group) is unsupported. */
+TF_API size_t tf_w4_packed_bytes(int32_t K, int32_t N, int32_t group);
+
+/*
+ * Repack canonical codes + scales (dev) into the kernel layout `packed` (dev,
+ * packed_bytes >= tf_w4_packed_bytes).  Not on the hot path.  Pure
+ * permutation: the codes and the scale bits are preserved exactly.
+ */
+TF_API tf_status tf_pack_w4(const uint8_t *codes, const uint16_t *scales, int32_t K, int32_t N,
+                     int32_t group, void *packed, size_t packed_bytes, void *stream);
+
+/*
+ * Pack the fused gate/up projection of a SwiGLU layer: canonical rows
+ * 0..ffn-1 are the gate rows, ffn..2*ffn-1 the up rows (N = 2*ffn).  The packed
+ * layout interleaves each 16 gate rows with the matching 16 up rows so the
+ * kernel can apply silu(gate) * up in its epilogue.  Matrices packed this way
+ * are consumed by tf_moe_w4 and tf_verify_step (not by tf_lane_gemm_w4).
+ * Size: tf_w4_packed_bytes(K, 2 * ffn, group).
+ */
+TF_API tf_status tf_pack_w4_gate_up(const uint8_t *codes, const uint16_t *scales, int32_t K, int32_t ffn,
+                             int32_t group, void *packed, size_t packed_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * tf_lane_gemm_w4 -- the verify pass's linear layer
+ * ------------------------------------------------------------------------
+ * README, "Every token ..." / "A row of a multi-row verify pass gets the same
+ * bits as a one-row step": all R drafted rows go through one launch that reads
+ * each weight once, and row r's result is bit-identical whatever R is.
+ *
+ *   y[r][n] = sum_g scale(n, g) * ( sum_{k in g} code(n, k) * x[r][k] )
+ *
+ * x   dev bf16 [R][ldx]   (ldx >= K, ldx % 8 == 0, 16-B aligned)
+ * y   dev fp32 [R][ldy]   (ldy >= N)
+ * Each group's partial sum is formed exactly (integer codes times bf16
+ * activations, fp32 accumulation) and then scaled in fp32; groups, and the
+ * fixed split-K partials, are added in an order that depends only on
+ * (K, N, group) and the GPU's SM count -- never on R.
+ */
+TF_API size_t tf_lane_gemm_workspace_bytes(int32_t K, int32_t N, int32_t group);
+TF_API tf_status tf_lane_gemm_w4(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R,
+                          float *y, int32_t ldy, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * tf_keyed_sample -- keyed Gumbel-max sampling over top-k / top-p
+ * ------------------------------------------------------------------------
+ * README, "Every token is the model's own sample", and the CLI table
+ * ("--temperature 0 is greedy").  Per row r, at position pos[r]:
+ *   T == 0: token = argmax_i logit_i (ties: lower id);
+ *   T  > 0: order the V tokens by (logit desc, id asc); keep the first
+ *           k' = (top_k <= 0 || top_k >= V) ? V : top_k; if top_p < 1 keep the
+ *           shortest prefix whose renormalised mass q_i = exp((l_i-l_0)/T)/Z
+ *           (fp64, summed left to right in rank order) reaches top_p;
+ *           token = argmax over the kept ids of (double)l/(double)T + g,
+ *           g = -ln(-ln u), u = ((h >> 11) + 0.5) / 2^53 (fp64),
+ *           h = sm(sm(sm(seed) ^ pos) ^ (uint32)token), sm = SplitMix64
+ *           finaliser; ties: lower id.
+ * logits dev fp32 [R][ldl] (ldl >= V); pos dev int64 [R]; tokens dev int32 [R].
+ * Supported: 1 <= V <= 2^31-1, k' <= TF_MAX_TOP_K when T > 0 (else
+ * TF_ERR_UNSUPPORTED), T >= 0 finite.  A non-finite logit sets
+ * TF_DEV_NONFINITE_LOGIT and that row's token to -1.
+ */
+typedef struct tf_sampling {
+    float temperature;  /* 0 = greedy */
+    int32_t top_k;      /* <= 0: no top-k limit */
+    float top_p;        /* >= 1: no top-p limit */
+} tf_sampling;
+
+TF_API size_t tf_keyed_sample_workspace_bytes(int32_t R, int32_t V);
+TF_API tf_status tf_keyed_sample(const float *logits, int32_t ldl, int32_t R, int32_t V, const tf_sampling *p,
+                          uint64_t seed, const int64_t *pos, int32_t *tokens, void *ws,
+                          size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * tf_accept -- longest-prefix acceptance
+ * ------------------------------------------------------------------------
+ * README: "a draft is accepted exactly when it equals the token one-token-
+ * at-a-time decoding would sample there".  Row i samples position pos0 + i;
+ * draft d[i] (i < R-1) proposes position pos0 + i.
+ *   a = first i with d[i] != t[i], else R-1;  commit t[0..a];  bonus = t[a].
+ * drafts dev int32 [R-1] (may be NULL when R == 1); sampled dev int32 [R];
+ * accepted, bonus dev int32 [1].
+ */
+TF_API tf_status tf_accept(const int32_t *drafts, const int32_t *sampled, int32_t R, int32_t *accepted,
+                    int32_t *bonus, void *stream);
+
+/* ------------------------------------------------------------------------
+ * tf_moe_w4 -- top-k routed W4 SwiGLU experts (30B-A3B-class MoE layer)
+ * ------------------------------------------------------------------------
+ * README, "What each checkpoint needs" (MoE kernels read 4-bit weights in
+ * groups of 32) and source layout (fused MoE kernels).  Per row r:
+ *   experts ranked by (router logit desc, id asc), the first top_k kept,
+ *   weights w_j = exp(z_j - z_0) / sum_{i<top_k} exp(z_i - z_0) (fp64, then fp32);
+ *   for each kept expert e: h = bf16(silu(x Wg_e) * (x Wu_e)), y_e = h Wd_e;
+ *   out[r] = sum_j w_j * y_{e_j} in rank order (fp32).
+ * Every touched expert's weights are read once for all R rows, and each row's
+ * y_e is bit-identical to the one its 1-row launch produces.
+ * gate_up: n_experts matrices of K = hidden, N = 2*ffn, each packed with
+ *          tf_pack_w4_gate_up, back to back: expert e at byte
+ *          e * tf_w4_packed_bytes(hidden, 2*ffn, group);
+ * down:    n_experts matrices of K = ffn, N = hidden, packed likewise.
+ * x dev bf16 [R][hidden]; router dev fp32 [R][n_experts]; out dev fp32 [R][hidden].
+ */
+typedef struct tf_moe_layer {
+    const void *gate_up;   /* dev */
+    const void *down;      /* dev */
+    int32_t hidden;        /* multiple of 64 */
+    int32_t ffn;           /* multiple of 64 */
+    int32_t n_experts;     /* 1..256 */
+    int32_t top_k;         /* 1..8, <= n_experts */
+    int32_t group;         /* 32 or 64 */
+} tf_moe_layer;
+
+TF_API size_t tf_moe_workspace_bytes(const tf_moe_layer *L, int32_t R);
+TF_API tf_status tf_moe_w4(const tf_moe_layer *L, const uint16_t *x, const float *router_logits, int32_t R,
+                    float *out, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * tf_verify_step -- one verify pass of the attention-free synthetic decoder
+ * ------------------------------------------------------------------------
+ * Stand-in for the pages' 27B-class dense model (weights not available):
+ *   x = emb[token];  n_blocks x { n = bf16(rms(x)); h = bf16(silu(n Wg) * (n Wu));
+ *   x += h Wd };  logits = bf16(rms(x)) Wlm;  then keyed sampling and acceptance.
+ * rms(x) = x / sqrt(mean(x^2) + eps); residual kept in fp32.
+ * Inputs of row 0: *last_token at position *pos; row i > 0: drafts[i-1] at
+ * position *pos + i.  On completion tokens[0..R-1] hold the samples,
+ * *accepted = a, *last_token = bonus t[a] and *pos += a + 1, so consecutive
+ * steps chain on the device.  logits (dev fp32 [R][vocab]) may be NULL.
+ */
+typedef struct tf_model {
+    int32_t vocab, hidden, ffn, n_blocks, group;
+    float rms_eps;
+    const uint16_t *embedding;     /* dev bf16 [vocab][hidden] */
+    const tf_w4_matrix *gate_up;   /* host array [n_blocks]: K = hidden, N = 2*ffn (tf_pack_w4_gate_up) */
+    const tf_w4_matrix *down;      /* host array [n_blocks]: K = ffn, N = hidden */
+    tf_w4_matrix lm_head;          /* K = hidden, N = vocab */
+} tf_model;
+
+TF_API size_t tf_verify_step_workspace_bytes(const tf_model *m, int32_t R);
+TF_API tf_status tf_verify_step(const tf_model *m, int32_t R, int32_t *last_token, int64_t *pos,
+                         const int32_t *drafts, const tf_sampling *p, uint64_t seed, int32_t *tokens,
+                         int32_t *accepted, float *logits, void *ws, size_t ws_bytes, void *stream);
+
+/* Number of SMs the split-K decomposition is sized for on the current device. */
+TF_API int32_t tf_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TF_H */

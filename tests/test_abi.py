@@ -1,0 +1,118 @@
+"""The C-ABI library builds, loads and exports every symbol include/tf.h declares;
+host-side argument validation answers before any device work is enqueued.
+
+These run without a GPU: no call here launches a kernel.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tf.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^TF_API\s+[\w\s\*]+?\b(tf_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from w4_gemm_keyed_gb300 import build, tf
+    build.build()
+    return tf.load()
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("tf_lane_gemm_w4", "tf_keyed_sample", "tf_accept", "tf_verify_step", "tf_pack_w4",
+                 "tf_moe_w4", "tf_last_error", "tf_workspace_status"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from w4_gemm_keyed_gb300 import tf
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    bound = {n for n, _, _ in tf.SIGNATURES}
+    assert bound == set(declared_symbols())
+
+
+def test_only_declared_symbols_are_exported(lib):
+    import subprocess
+    from w4_gemm_keyed_gb300 import tf
+    out = subprocess.run(["nm", "-D", "--defined-only", tf.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l and l.split()[-1].startswith("tf_")}
+    assert exported == set(declared_symbols())
+
+
+def test_packed_size_and_status_strings(lib):
+    from w4_gemm_keyed_gb300 import tf
+    # 256-feature tiles x 64-wide k slices; G=64 -> 4*(2048+128) bytes per stage
+    assert tf.packed_bytes(5120, 17408, 64) == 68 * 80 * 4 * 2176
+    assert tf.packed_bytes(256, 1000, 64) == 4 * 4 * 4 * 2176         # N padded to 1024
+    assert tf.packed_bytes(2048, 1536, 32) == 6 * 32 * 4 * 2304
+    assert tf.packed_bytes(100, 64, 64) == 0                           # K not a multiple of 64
+    assert tf.packed_bytes(256, 64, 16) == 0                           # unsupported group
+    assert lib.tf_status_string(0) == b"ok"
+    assert lib.tf_version() >= 100
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    from w4_gemm_keyed_gb300 import tf
+    W = tf.W4MatrixC(None, 256, 64, 64)
+    st = lib.tf_lane_gemm_w4(ctypes.byref(W), None, 256, 1, None, 64, None, 0, None)
+    assert st == tf.TF_ERR_INVALID_ARG and b"packed" in lib.tf_last_error()
+    W = tf.W4MatrixC(256, 100, 64, 64)   # K not a multiple of 64
+    assert lib.tf_lane_gemm_w4(ctypes.byref(W), 256, 128, 1, 256, 64, 256, 1 << 30, None) == tf.TF_ERR_UNSUPPORTED
+    W = tf.W4MatrixC(256, 256, 64, 64)
+    assert lib.tf_lane_gemm_w4(ctypes.byref(W), 256, 256, 0, 256, 64, 256, 1 << 30, None) == tf.TF_ERR_INVALID_ARG
+    assert lib.tf_lane_gemm_w4(ctypes.byref(W), 256, 256, 17, 256, 64, 256, 1 << 30, None) == tf.TF_ERR_INVALID_ARG
+    assert lib.tf_lane_gemm_w4(ctypes.byref(W), 258, 256, 1, 256, 64, 256, 1 << 30, None) == tf.TF_ERR_INVALID_ARG
+    assert lib.tf_lane_gemm_w4(ctypes.byref(W), 256, 256, 1, 256, 64, None, 0, None) == tf.TF_ERR_WORKSPACE
+    sp = tf.SamplingC(0.7, 100, 0.9)  # k' = 100 > 64
+    st = lib.tf_keyed_sample(256, 1000, 1, 1000, ctypes.byref(sp), 1, 256, 256, 256, 1 << 30, None)
+    assert st == tf.TF_ERR_UNSUPPORTED
+    sp = tf.SamplingC(-1.0, 20, 0.9)
+    assert lib.tf_keyed_sample(256, 1000, 1, 1000, ctypes.byref(sp), 1, 256, 256, 256, 1 << 30, None) == \
+        tf.TF_ERR_INVALID_ARG
+    sp = tf.SamplingC(0.7, 20, 0.9)      # T > 0 needs positions
+    assert lib.tf_keyed_sample(256, 1000, 1, 1000, ctypes.byref(sp), 1, None, 256, 256, 1 << 30, None) == \
+        tf.TF_ERR_INVALID_ARG
+    assert lib.tf_accept(None, 256, 2, 256, 256, None) == tf.TF_ERR_INVALID_ARG
+    assert lib.tf_accept(None, 256, 0, 256, 256, None) == tf.TF_ERR_INVALID_ARG
+    L = tf.MoeLayerC(256, 256, 2048, 768, 128, 9, 32)   # top_k > 8
+    assert lib.tf_moe_w4(ctypes.byref(L), 256, 256, 1, 256, 256, 1 << 30, None) == tf.TF_ERR_UNSUPPORTED
+    assert lib.tf_last_error() != b""
+
+
+def _cta_of(i, Pv, tot):
+    return ((i + 1) * Pv - 1) // tot
+
+
+@pytest.mark.parametrize("T,Kc,Pv", [(4, 4, 16), (68, 80, 152), (20, 272, 152), (594, 80, 152), (6, 32, 16),
+                                     (8, 12, 16), (1, 1, 1), (3, 5, 11)])
+def test_stream_k_cut_formulas(T, Kc, Pv):
+    """The split-K cut used by the GEMM kernel: ranges tile the iteration space,
+    cta_of() inverts them, and every tile's segment slots are distinct."""
+    tot = T * Kc
+    Pv = min(Pv, tot)
+    b = [p * tot // Pv for p in range(Pv + 1)]
+    assert b[0] == 0 and b[-1] == tot and all(b[p] < b[p + 1] for p in range(Pv))
+    for i in range(tot):
+        p = _cta_of(i, Pv, tot)
+        assert b[p] <= i < b[p + 1]
+    slots = set()
+    for t in range(T):
+        lo, hi = _cta_of(t * Kc, Pv, tot), _cta_of((t + 1) * Kc - 1, Pv, tot)
+        segs = [p for p in range(lo, hi + 1) if b[p] < b[p + 1]]
+        covered = sum(min(b[p + 1], (t + 1) * Kc) - max(b[p], t * Kc) for p in segs)
+        assert covered == Kc
+        if len(segs) > 1:
+            for p in segs:
+                which = 0 if t == b[p] // Kc else 1
+                assert (p, which) not in slots
+                slots.add((p, which))

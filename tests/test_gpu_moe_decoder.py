@@ -1,0 +1,155 @@
+"""MoE verify and the synthetic decoder on the GPU against the oracle.
+
+MoE: output within 1e-3 * rms(row) of the fp64 oracle (after the bf16
+rounding of h, which both sides apply), and every row byte-equal to its own
+1-row launch (the 30B-A3B-class shape: 128 experts, top-8, hidden 2048,
+expert FFN 768, group 32, R in {1, 4, 8, 16}).
+
+Decoder: drafted decoding on the GPU writes the same tokens (token_sha) as
+serial decoding on the GPU; teacher-forced logits match the oracle within
+tolerance; the GPU's tokens equal the oracle sampler's on the GPU's logits.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import decoder as odec
+from oracle import moe as omoe
+from oracle import sampling as osamp
+from w4_gemm_keyed_gb300 import inputs
+from gpu_util import assert_close_rows, dev_bits16, dev_u8
+
+pytestmark = pytest.mark.gpu
+
+
+def make_moe(tf, rng, E, H, F, G, top_k):
+    W = {k: [] for k in ("gate_codes", "gate_scales", "up_codes", "up_scales", "down_codes", "down_scales")}
+    for _ in range(E):
+        for name, (K, N) in (("gate", (H, F)), ("up", (H, F)), ("down", (F, H))):
+            c, s = inputs.w4_weights(rng, K, N, G)
+            W[name + "_codes"].append(c)
+            W[name + "_scales"].append(s)
+    W = {k: np.stack(v) for k, v in W.items()}
+    sz_gu, sz_d = tf.packed_bytes(H, 2 * F, G), tf.packed_bytes(F, H, G)
+    gu = torch.empty(E * sz_gu, dtype=torch.uint8, device="cuda")
+    dn = torch.empty(E * sz_d, dtype=torch.uint8, device="cuda")
+    for e in range(E):
+        c = np.concatenate([W["gate_codes"][e], W["up_codes"][e]])
+        s = np.concatenate([W["gate_scales"][e], W["up_scales"][e]])
+        tf.pack_w4(dev_u8(c), dev_bits16(s), G, gate_up=True, out=gu[e * sz_gu:(e + 1) * sz_gu])
+        tf.pack_w4(dev_u8(W["down_codes"][e]), dev_bits16(W["down_scales"][e]), G, out=dn[e * sz_d:(e + 1) * sz_d])
+    return W, tf.MoeLayer(gu, dn, H, F, E, top_k, G)
+
+
+def run_moe(tf, layer, x, z):
+    return tf.moe_w4(layer, dev_bits16(x), torch.from_numpy(z).cuda()).cpu().numpy()
+
+
+@pytest.mark.parametrize("R", [1, 3, 16])
+def test_small_moe_matches_oracle(tf, R):
+    rng = inputs.rng_for(301, R)
+    E, H, F, G, k = 8, 256, 128, 32, 2
+    W, layer = make_moe(tf, rng, E, H, F, G, k)
+    x = inputs.bf16_normal(rng, (R, H))
+    z = inputs.router_logits(rng, R, E)
+    out = run_moe(tf, layer, x, z)
+    ref, *_ = omoe.moe(x, z, W, G, top_k=k)
+    assert_close_rows(out, ref)
+
+
+@pytest.fixture(scope="module")
+def moe30b(tf):
+    rng = inputs.rng_for(4)
+    cfg = inputs.CONFIGS["moe30b"]
+    W, layer = make_moe(tf, rng, cfg["n_experts"], cfg["hidden"], cfg["ffn"], cfg["group"], cfg["top_k"])
+    x = inputs.bf16_normal(rng, (16, cfg["hidden"]))
+    z = inputs.router_logits(rng, 16, cfg["n_experts"])
+    return cfg, W, layer, x, z
+
+
+@pytest.mark.parametrize("R", [1, 4, 8, 16])
+def test_moe30b_matches_oracle(tf, moe30b, R):
+    cfg, W, layer, x, z = moe30b
+    out = run_moe(tf, layer, x[:R], z[:R])
+    ref, *_ = omoe.moe(x[:R], z[:R], W, cfg["group"], top_k=cfg["top_k"])
+    assert_close_rows(out, ref)
+
+
+def test_moe30b_rows_invariant_to_R(tf, moe30b):
+    cfg, W, layer, x, z = moe30b
+    single = np.stack([run_moe(tf, layer, x[r:r + 1], z[r:r + 1])[0] for r in range(16)])
+    for R in (4, 8, 16):
+        out = run_moe(tf, layer, x[:R], z[:R])
+        assert np.array_equal(out.view(np.uint32), single[:R].view(np.uint32))
+
+
+# ---------------------------------------------------------------- decoder
+def tiny_weights(seed=401, V=3000, H=256, F=512, n_blocks=2, G=64):
+    rng = inputs.rng_for(seed)
+    blocks = []
+    for _ in range(n_blocks):
+        gc, gs = inputs.w4_weights(rng, H, F, G)
+        uc, us = inputs.w4_weights(rng, H, F, G)
+        dc, ds = inputs.w4_weights(rng, F, H, G)
+        blocks.append(dict(gate_codes=gc, gate_scales=gs, up_codes=uc, up_scales=us, down_codes=dc, down_scales=ds))
+    lc, ls = inputs.w4_weights(rng, H, V, G)
+    return dict(emb=inputs.bf16_normal(rng, (V, H), 0.02), blocks=blocks, lm_codes=lc, lm_scales=ls, group=G)
+
+
+@pytest.fixture(scope="module")
+def tiny_decoder(tf):
+    from w4_gemm_keyed_gb300 import decode
+    w = tiny_weights()
+    model = decode.upload_model(w)
+    return w, model, decode.Decoder(model, keep_logits=True)
+
+
+def test_decoder_logits_match_oracle_teacher_forced(tf, tiny_decoder):
+    w, model, dec = tiny_decoder
+    toks = [5, 17, 2999, 0, 42, 42, 7, 1234]
+    dec.reset(toks[0], 1)
+    a, t = dec.step(8, toks[1:], 0.7, 20, 0.95, 1234)
+    lg = dec.logits[:8].cpu().numpy()
+    ref = odec.logits(w, toks)
+    assert_close_rows(lg, ref)
+    # identical logits -> identical tokens (oracle sampler on the GPU's logits)
+    for i in range(8):
+        tok, gap = osamp.sample_row(lg[i], 0.7, 20, 0.95, 1234, 1 + i)
+        assert tok == t[i] or gap < 1e-9
+    # acceptance of this pass
+    from oracle import accept as oacc
+    assert (a, t[a]) == oacc.accept(toks[1:], t)
+
+
+@pytest.mark.parametrize("R,p_match", [(8, 0.75), (4, 1.0), (16, 0.3)])
+def test_decoder_drafted_equals_serial(tf, tiny_decoder, R, p_match):
+    from w4_gemm_keyed_gb300 import decode
+    w, model, dec = tiny_decoder
+    T, k, p, seed, n = 0.7, 20, 0.95, 1234, 40
+    serial = decode.serial_decode(dec, 11, n, T, k, p, seed)
+    rng = inputs.rng_for(402, R)
+    future = np.array(serial + [0] * (R + 1))
+    drafted, lens = decode.drafted_decode(
+        dec, 11, n, R, T, k, p, seed, lambda pos0, m: inputs.noisy_drafts(rng, future[pos0 - 1: pos0 - 1 + m], p_match, 3000))
+    assert decode.token_sha(drafted) == decode.token_sha(serial)
+    if p_match == 1.0:
+        assert all(a == R - 1 for a in lens[:-1])
+    assert tf.workspace_status(dec.ws) == tf.TF_DEV_OK
+
+
+def test_decoder_serial_matches_oracle_free_running(tf, tiny_decoder):
+    from w4_gemm_keyed_gb300 import decode
+    w, model, dec = tiny_decoder
+    T, k, p, seed, n = 0.7, 20, 0.95, 1235, 16
+    gpu = decode.serial_decode(dec, 11, n, T, k, p, seed)
+    ref = odec.serial_decode(w, 11, n, T, k, p, seed)
+    assert gpu == ref
+
+
+def test_decoder_bad_token_sets_status(tf, tiny_decoder):
+    w, model, dec = tiny_decoder
+    dec.reset(5, 1)
+    dec.step(3, [1, 999999], 0.0, 0, 1.0, 1)
+    assert tf.workspace_status(dec.ws) == tf.TF_DEV_BAD_TOKEN

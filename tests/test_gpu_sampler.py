@@ -1,0 +1,124 @@
+"""Keyed sampler and acceptance on the GPU against the oracle.
+
+Given identical logits the token ids must be identical; a mismatch is only
+tolerated as a logged near-tie (oracle score gap < 1e-9, where the fp64 log /
+exp of the two sides may round differently).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import accept as oacc
+from oracle import sampling as osamp
+from w4_gemm_keyed_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+SETTINGS = [(0.0, 0, 1.0), (0.6, 20, 0.95), (1.0, 50, 0.8), (0.7, 20, 0.95), (1.3, 64, 0.99), (0.9, 7, 1.0),
+            (0.5, 33, 0.3)]
+
+
+def gpu_sample(tf, logits, T, k, p, seed, pos):
+    t = tf.keyed_sample(torch.from_numpy(logits).cuda(), T, k, p, seed, torch.from_numpy(pos).cuda())
+    return t.cpu().numpy()
+
+
+def check_tokens(gpu, logits, T, k, p, seed, pos):
+    ref, gaps = osamp.sample(logits, T, k, p, seed, pos)
+    for r in range(len(ref)):
+        if gpu[r] != ref[r]:
+            assert gaps[r] < 1e-9, f"row {r}: gpu {gpu[r]} oracle {ref[r]} gap {gaps[r]}"
+            print(f"near-tie row {r}: gap {gaps[r]:.3e}")
+
+
+@pytest.mark.parametrize("T,k,p", SETTINGS)
+@pytest.mark.parametrize("V", [1024, 151936, 8193])
+def test_tokens_match_oracle(tf, V, T, k, p):
+    rng = inputs.rng_for(201, V, int(T * 10), k)
+    R = 16
+    logits = inputs.logits_normal(rng, R, V, std=2.0)
+    seed = int(inputs.seeds_u64(rng, 1)[0])
+    pos = inputs.positions(rng, R)
+    check_tokens(gpu_sample(tf, logits, T, k, p, seed, pos), logits, T, k, p, seed, pos)
+
+
+@pytest.mark.parametrize("T,k,p", SETTINGS)
+def test_ties_follow_the_lower_id(tf, T, k, p):
+    rng = inputs.rng_for(202, k)
+    R, V = 16, 5000
+    logits = rng.integers(-3, 2, size=(R, V)).astype(np.float32)   # massive ties
+    logits[3, :] = 0.0
+    logits[4, ::2] = -0.0                                            # signed zeros tie with +0
+    seed = 1234
+    pos = np.arange(R, dtype=np.int64)
+    check_tokens(gpu_sample(tf, logits, T, k, p, seed, pos), logits, T, k, p, seed, pos)
+
+
+@pytest.mark.parametrize("V", [1, 2, 5, 63, 64, 4096, 4097])
+def test_small_and_ragged_vocabularies(tf, V):
+    rng = inputs.rng_for(203, V)
+    R = 4
+    logits = inputs.logits_normal(rng, R, V, std=1.0)
+    pos = inputs.positions(rng, R)
+    for T, k, p in [(0.0, 0, 1.0), (0.8, 0 if V <= 64 else 64, 0.9), (1.0, 3, 0.5)]:
+        check_tokens(gpu_sample(tf, logits, T, k, p, 77, pos), logits, T, k, p, 77, pos)
+
+
+def test_nonfinite_logits_flag_the_row(tf):
+    R, V = 3, 3000
+    logits = np.zeros((R, V), np.float32)
+    logits[1, 2999] = np.nan
+    logits[2, 5] = np.inf
+    ws = tf.workspace(tf.keyed_sample_workspace_bytes(R, V))
+    t = tf.keyed_sample(torch.from_numpy(logits).cuda(), 0.7, 20, 0.9, 5,
+                        torch.zeros(R, dtype=torch.int64, device="cuda"), ws=ws).cpu().numpy()
+    assert t[1] == -1 and t[2] == -1 and t[0] >= 0
+    assert tf.workspace_status(ws) == tf.TF_DEV_NONFINITE_LOGIT
+    # the workspace is clean again: a finite call reports OK
+    tf.keyed_sample(torch.zeros((R, V), device="cuda"), 0.7, 20, 0.9, 5,
+                    torch.zeros(R, dtype=torch.int64, device="cuda"), ws=ws)
+    assert tf.workspace_status(ws) == tf.TF_DEV_OK
+
+
+def test_unsupported_candidate_count(tf):
+    with pytest.raises(tf.TFError) as e:
+        tf.keyed_sample(torch.zeros((1, 1000), device="cuda"), 0.7, 0, 0.9, 5,
+                        torch.zeros(1, dtype=torch.int64, device="cuda"))
+    assert e.value.status == tf.TF_ERR_UNSUPPORTED
+
+
+def test_rows_independent_of_R(tf):
+    rng = inputs.rng_for(204)
+    V = 151936
+    logits = inputs.logits_normal(rng, 16, V, std=2.0)
+    pos = inputs.positions(rng, 16)
+    full = gpu_sample(tf, logits, 0.6, 20, 0.95, 99, pos)
+    for r in (0, 7, 15):
+        one = gpu_sample(tf, logits[r:r + 1], 0.6, 20, 0.95, 99, pos[r:r + 1])
+        assert one[0] == full[r]
+
+
+def test_accept_brute_force(tf):
+    import itertools
+    for R in range(1, 5):
+        for V in range(1, 4):
+            combos_t = list(itertools.product(range(V), repeat=R))
+            combos_d = list(itertools.product(range(V), repeat=R - 1))
+            for t in combos_t:
+                for d in combos_d:
+                    dd = torch.tensor(list(d) or [0], dtype=torch.int32, device="cuda")
+                    tt = torch.tensor(list(t), dtype=torch.int32, device="cuda")
+                    a, b = tf.accept(dd, tt)
+                    assert (int(a.item()), int(b.item())) == oacc.accept(d, t)
+
+
+def test_accept_sixteen_rows(tf):
+    rng = np.random.default_rng(5)
+    for _ in range(50):
+        t = rng.integers(0, 3, 16)
+        d = np.where(rng.random(15) < 0.8, t[:15], rng.integers(0, 3, 15))
+        a, b = tf.accept(torch.from_numpy(d.astype(np.int32)).cuda(), torch.from_numpy(t.astype(np.int32)).cuda())
+        assert (int(a.item()), int(b.item())) == oacc.accept(d, t)

@@ -1,0 +1,29 @@
+// MoE routing / combine and synthetic-decoder glue kernels: declarations.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tfk {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxRouteK = 8;
+
+// Per row: experts ranked by (router logit desc, id asc), first top_k kept,
+// renormalised weights computed in fp64 and stored as fp32.
+cudaError_t launch_route(const float *router, int R, int E, int top_k, int32_t *ids, float *w, int *err,
+                         cudaStream_t s);
+// Touched experts in ascending id: expert_ids[0..U), *n_problems = U,
+// slot_of[r][j] = index u of ids[r][j].
+cudaError_t launch_expert_list(const int32_t *ids, int R, int E, int top_k, int32_t *expert_ids,
+                               int32_t *n_problems, int32_t *slot_of, cudaStream_t s);
+// out[r][n] = sum_j w[r][j] * Y[slot_of[r][j]][r][n], j ascending (fp32 FMA chain).
+cudaError_t launch_combine(const float *Y, const int32_t *slot_of, const float *w, int R, int H, int top_k,
+                           float *out, cudaStream_t s);
+
+// x[r][:] = emb[token_r][:] (bf16 -> fp32); token_0 = *last_token, token_r = drafts[r-1].
+cudaError_t launch_embed(const uint16_t *emb, int V, int H, const int32_t *last_token, const int32_t *drafts,
+                         int R, float *x, int *err, cudaStream_t s);
+// out[r][:] = bf16(x[r][:] / sqrt(mean(x[r]^2) + eps)), fixed-order fp32 reduction per row.
+cudaError_t launch_rmsnorm_bf16(const float *x, int R, int H, float eps, uint16_t *out, cudaStream_t s);
+
+}  // namespace tfk

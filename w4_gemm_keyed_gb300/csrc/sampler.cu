@@ -1,0 +1,360 @@
+// Keyed Gumbel-max sampling over top-k / top-p candidates, and acceptance.
+//
+// TensorFold README, "Every token is the model's own sample": the token at
+// position p is the argmax over the top-k/top-p candidates of
+// logit/T + g(seed, p, token), g Gumbel noise from a hash of (seed, p, token);
+// "--temperature 0" is greedy.  Acceptance: a draft is accepted exactly when it
+// equals the token serial decoding samples there.
+//
+// Two launches per call:
+//   1. topk_partial: grid (ceil(V/4096), R).  Each CTA keeps 16 logits per
+//      thread in registers (coalesced loads), finds its chunk's k-th largest
+//      (logit, -id) key with a 4-pass 8-bit radix select over a shared
+//      histogram, breaks ties at the threshold by a second radix select on the
+//      ids, and writes its <= k candidates.  It also flags non-finite logits.
+//   2. finalize: one CTA per row merges the <= 64 * chunks candidates with the
+//      same select, orders the k' survivors by (logit desc, id asc), computes
+//      the top-p prefix in fp64 left to right, then the Gumbel argmax.
+// Every decision depends on the row's own logits only, so a row's token is the
+// same whatever R is.
+#include <cuda_runtime.h>
+
+#include "sampler.cuh"
+#include "tf_ptx.cuh"
+
+namespace tfk {
+
+namespace {
+
+constexpr int kE1 = kSampleChunk / kSampleThreads;  // 16 logits per thread in a chunk
+constexpr int kE2 = 32;                             // pool entries per thread in finalize
+constexpr int kMaxChunks = kE2 * kSampleThreads / kMaxTopK;  // 128
+
+// Order-preserving key: larger float -> larger key; -0 and +0 share a key.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t b = __float_as_uint(f);
+    if (b == 0x80000000u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// SplitMix64 output function (Steele, Lea & Flood 2014): advance by the golden
+// gamma, then the two xor-shift-multiply rounds and a final xor-shift.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t z) {
+    z += 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+__device__ __forceinline__ double gumbel(uint64_t seed, int64_t pos, int32_t token) {
+    uint64_t h = splitmix64(seed);
+    h = splitmix64(h ^ static_cast<uint64_t>(pos));
+    h = splitmix64(h ^ static_cast<uint64_t>(static_cast<uint32_t>(token)));
+    const double u = (__ull2double_rn(h >> 11) + 0.5) * (1.0 / 9007199254740992.0);
+    return -log(-log(u));
+}
+
+struct Sel {
+    uint32_t thr;  // key of the k-th largest element
+    int need;      // how many elements equal to thr belong to the top k
+    int n_eq;      // how many elements equal thr
+};
+
+// Block-wide: k-th largest of the valid keys (k >= 1 and <= number of valid).
+template <int E>
+__device__ Sel radix_select(const uint32_t (&key)[E], uint32_t valid, int k, uint32_t *hist, int *sh) {
+    uint32_t prefix = 0, mask = 0;
+    int remaining = k, n_eq = 0;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            if (((valid >> e) & 1u) && (key[e] & mask) == prefix) atomicAdd(&hist[(key[e] >> shift) & 0xFFu], 1u);
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            uint32_t c[8], s = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                c[j] = hist[255 - lane * 8 - j];
+                s += c[j];
+            }
+            uint32_t incl = s;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const uint32_t excl = incl - s;
+            if (excl < uint32_t(remaining) && uint32_t(remaining) <= incl) {
+                uint32_t run = excl;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (run + c[j] >= uint32_t(remaining)) {
+                        sh[0] = 255 - lane * 8 - j;
+                        sh[1] = int(run);
+                        sh[2] = int(c[j]);
+                        break;
+                    }
+                    run += c[j];
+                }
+            }
+        }
+        __syncthreads();
+        const uint32_t d = uint32_t(sh[0]);
+        remaining -= sh[1];
+        n_eq = sh[2];
+        prefix |= d << shift;
+        mask |= 0xFFu << shift;
+        __syncthreads();
+    }
+    return Sel{prefix, remaining, n_eq};
+}
+
+// Selects the top-k by (key desc, id asc) among valid entries; returns, per
+// entry, whether it is selected (bit mask).
+template <int E>
+__device__ uint32_t select_top(const uint32_t (&key)[E], const int32_t (&id)[E], uint32_t valid, int k,
+                               uint32_t *hist, int *sh) {
+    const Sel s = radix_select<E>(key, valid, k, hist, sh);
+    uint32_t id_max = 0xFFFFFFFFu;  // ties at the threshold are taken up to this id
+    if (s.need < s.n_eq) {
+        uint32_t key2[E];
+        uint32_t v2 = 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            key2[e] = ~uint32_t(id[e]);  // larger key2 = smaller id
+            if (((valid >> e) & 1u) && key[e] == s.thr) v2 |= 1u << e;
+        }
+        const Sel s2 = radix_select<E>(key2, v2, s.need, hist, sh);
+        id_max = ~s2.thr;
+    }
+    uint32_t chosen = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        if (!((valid >> e) & 1u)) continue;
+        if (key[e] > s.thr || (key[e] == s.thr && uint32_t(id[e]) <= id_max)) chosen |= 1u << e;
+    }
+    return chosen;
+}
+
+__global__ void __launch_bounds__(kSampleThreads) topk_partial_kernel(const SampleArgs a) {
+    __shared__ uint32_t hist[256];
+    __shared__ int sh[4];
+    __shared__ int s_cnt, s_bad;
+    const int c = blockIdx.x, r = blockIdx.y;
+    const float *row = a.logits + (long long)r * a.ldl;
+    const int base = c * kSampleChunk;
+    uint32_t key[kE1];
+    int32_t id[kE1];
+    uint32_t valid = 0;
+    bool bad = false;
+#pragma unroll
+    for (int e = 0; e < kE1; ++e) {
+        const int idx = base + e * kSampleThreads + threadIdx.x;
+        id[e] = idx;
+        key[e] = 0;
+        if (idx < a.V) {
+            const float f = row[idx];
+            bad |= !isfinite(f);
+            key[e] = order_key(f);
+            valid |= 1u << e;
+        }
+    }
+    if (threadIdx.x == 0) {
+        s_cnt = 0;
+        s_bad = 0;
+    }
+    __syncthreads();
+    if (bad) atomicOr(&s_bad, 1);
+    __syncthreads();
+    const int slot0 = r * a.n_chunks + c;
+    if (s_bad) {
+        if (threadIdx.x == 0) {
+            atomicOr(&a.row_bad[r], 1);
+            set_error(a.err, 2);
+            a.cand_cnt[slot0] = 0;
+        }
+        return;
+    }
+    const int n_valid = min(kSampleChunk, a.V - base);
+    const int k = min(a.k_eff, n_valid);
+    const uint32_t chosen = select_top<kE1>(key, id, valid, k, hist, sh);
+#pragma unroll
+    for (int e = 0; e < kE1; ++e) {
+        if ((chosen >> e) & 1u) {
+            const int s = atomicAdd(&s_cnt, 1);
+            if (s < kMaxTopK) {
+                a.cand_val[(long long)slot0 * kMaxTopK + s] = key_value(key[e]);
+                a.cand_id[(long long)slot0 * kMaxTopK + s] = id[e];
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) a.cand_cnt[slot0] = min(s_cnt, kMaxTopK);
+}
+
+__global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleArgs a) {
+    __shared__ uint32_t hist[256];
+    __shared__ int sh[4];
+    __shared__ int s_cnt, s_m;
+    __shared__ float sel_val[kMaxTopK], srt_val[kMaxTopK];
+    __shared__ int32_t sel_id[kMaxTopK], srt_id[kMaxTopK];
+    __shared__ double ex[kMaxTopK], score[kMaxTopK];
+    const int r = blockIdx.x;
+    const int tid = threadIdx.x;
+    uint32_t key[kE2];
+    int32_t id[kE2];
+    uint32_t valid = 0;
+    int n_total = 0;
+    for (int c = 0; c < a.n_chunks; ++c) n_total += a.cand_cnt[r * a.n_chunks + c];
+#pragma unroll
+    for (int e = 0; e < kE2; ++e) {
+        const int p = e * kSampleThreads + tid;
+        const int c = p / kMaxTopK, s = p % kMaxTopK;
+        key[e] = 0;
+        id[e] = 0;
+        if (c < a.n_chunks && s < a.cand_cnt[r * a.n_chunks + c]) {
+            const long long q = (long long)(r * a.n_chunks + c) * kMaxTopK + s;
+            key[e] = order_key(a.cand_val[q]);
+            id[e] = a.cand_id[q];
+            valid |= 1u << e;
+        }
+    }
+    if (tid == 0) s_cnt = 0;
+    __syncthreads();
+    const bool bad = a.row_bad[r] != 0;
+    if (bad || n_total == 0) {
+        __syncthreads();
+        if (tid == 0) {
+            a.tokens[r] = -1;
+            a.row_bad[r] = 0;  // leave the workspace clean for the next call
+        }
+        return;
+    }
+    const int k = min(a.k_eff, n_total);
+    const uint32_t chosen = select_top<kE2>(key, id, valid, k, hist, sh);
+#pragma unroll
+    for (int e = 0; e < kE2; ++e) {
+        if ((chosen >> e) & 1u) {
+            const int s = atomicAdd(&s_cnt, 1);
+            if (s < kMaxTopK) {
+                sel_val[s] = key_value(key[e]);
+                sel_id[s] = id[e];
+            }
+        }
+    }
+    __syncthreads();
+    const int n_sel = min(s_cnt, kMaxTopK);
+    if (tid < n_sel) {  // rank sort by (logit desc, id asc)
+        const uint32_t ki = order_key(sel_val[tid]);
+        int rank = 0;
+        for (int j = 0; j < n_sel; ++j) {
+            const uint32_t kj = order_key(sel_val[j]);
+            rank += (kj > ki) || (kj == ki && sel_id[j] < sel_id[tid]);
+        }
+        srt_val[rank] = sel_val[tid];
+        srt_id[rank] = sel_id[tid];
+    }
+    __syncthreads();
+    if (a.temperature == 0.0f) {
+        if (tid == 0) a.tokens[r] = srt_id[0];
+        return;
+    }
+    const double T = double(a.temperature);
+    const double p = double(a.top_p);
+    const int64_t pos = a.pos ? a.pos[r] : (*a.pos_base + r);
+    if (p < 1.0) {
+        if (tid < n_sel) ex[tid] = exp((double(srt_val[tid]) - double(srt_val[0])) / T);
+        __syncthreads();
+        if (tid == 0) {
+            double Z = 0.0;
+            for (int i = 0; i < n_sel; ++i) Z += ex[i];
+            double S = 0.0;
+            int m = n_sel;
+            for (int i = 0; i < n_sel; ++i) {
+                S += ex[i] / Z;
+                if (S >= p) {
+                    m = i + 1;
+                    break;
+                }
+            }
+            s_m = m;
+        }
+    } else if (tid == 0) {
+        s_m = n_sel;
+    }
+    __syncthreads();
+    const int m = s_m;
+    if (tid < m) score[tid] = double(srt_val[tid]) / T + gumbel(a.seed, pos, srt_id[tid]);
+    __syncthreads();
+    if (tid == 0) {
+        int best = 0;
+        for (int i = 1; i < m; ++i)
+            if (score[i] > score[best] || (score[i] == score[best] && srt_id[i] < srt_id[best])) best = i;
+        a.tokens[r] = srt_id[best];
+    }
+}
+
+__global__ void accept_kernel(const int32_t *drafts, const int32_t *sampled, int R, int32_t *accepted,
+                              int32_t *bonus, int64_t *pos) {
+    const int lane = threadIdx.x;
+    const bool mismatch = lane < R - 1 && drafts[lane] != sampled[lane];
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, mismatch);
+    const int acc = m ? __ffs(m) - 1 : R - 1;
+    if (lane == 0) {
+        const int32_t t = sampled[acc];
+        if (accepted) *accepted = acc;
+        if (bonus) *bonus = t;
+        if (pos) *pos += acc + 1;
+    }
+}
+
+}  // namespace
+
+static int n_chunks_of(int V) { return (V + kSampleChunk - 1) / kSampleChunk; }
+
+// Region layout: row_bad flags first, at a fixed offset and sized for the
+// largest R, so a workspace reused by calls with different R never sees stale
+// flags; the candidate arrays that follow are always written before read.
+size_t sample_workspace_bytes(int R, int V) {
+    const size_t nc = size_t(n_chunks_of(V));
+    size_t b = 256;  // row_bad[kMaxRows]
+    b += size_t(R) * nc * kMaxTopK * (sizeof(float) + sizeof(int32_t));
+    b += size_t(R) * nc * sizeof(int32_t);
+    return (b + 255) / 256 * 256;
+}
+
+void sample_bind_workspace(SampleArgs &a, void *ws_region, int R, int V) {
+    const size_t nc = size_t(n_chunks_of(V));
+    char *p = static_cast<char *>(ws_region);
+    a.row_bad = reinterpret_cast<int32_t *>(p);
+    p += 256;
+    a.cand_val = reinterpret_cast<float *>(p);
+    p += size_t(R) * nc * kMaxTopK * sizeof(float);
+    a.cand_id = reinterpret_cast<int32_t *>(p);
+    p += size_t(R) * nc * kMaxTopK * sizeof(int32_t);
+    a.cand_cnt = reinterpret_cast<int32_t *>(p);
+    a.n_chunks = int(nc);
+}
+
+cudaError_t launch_keyed_sample(const SampleArgs &a, cudaStream_t s) {
+    if (a.n_chunks > kMaxChunks) return cudaErrorInvalidValue;
+    topk_partial_kernel<<<dim3(a.n_chunks, a.R), kSampleThreads, 0, s>>>(a);
+    finalize_kernel<<<a.R, kSampleThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_accept(const int32_t *drafts, const int32_t *sampled, int R, int32_t *accepted, int32_t *bonus,
+                          int64_t *pos, cudaStream_t s) {
+    accept_kernel<<<1, 32, 0, s>>>(drafts, sampled, R, accepted, bonus, pos);
+    return cudaGetLastError();
+}
+
+int sample_max_vocab() { return kMaxChunks * kSampleChunk; }
+
+}  // namespace tfk

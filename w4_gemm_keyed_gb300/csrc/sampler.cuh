@@ -1,0 +1,42 @@
+// Keyed sampler and acceptance: declarations shared with the C ABI layer.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tfk {
+
+constexpr int kSampleChunk = 4096;     // vocabulary entries per top-k CTA
+constexpr int kSampleThreads = 256;
+constexpr int kMaxTopK = 64;
+
+struct SampleArgs {
+    const float *logits;
+    int ldl;
+    int R, V;
+    int k_eff;            // 1 for greedy, else k' = min(top_k or V, V) <= 64
+    float temperature;
+    float top_p;
+    uint64_t seed;
+    const int64_t *pos;   // dev [R] (or pos_base when pos_scalar)
+    const int64_t *pos_base;  // dev [1]: row r at *pos_base + r (used when pos == nullptr)
+    int32_t *tokens;
+    // workspace
+    float *cand_val;      // [R][n_chunks][64]
+    int32_t *cand_id;     // [R][n_chunks][64]
+    int32_t *cand_cnt;    // [R][n_chunks]
+    int32_t *row_bad;     // [R]
+    int *err;
+    int n_chunks;
+};
+
+size_t sample_workspace_bytes(int R, int V);
+void sample_bind_workspace(SampleArgs &a, void *ws_region, int R, int V);
+cudaError_t launch_keyed_sample(const SampleArgs &a, cudaStream_t s);
+int sample_max_vocab();
+// Acceptance; if last_token / pos are non-null also writes the bonus to
+// *last_token and advances *pos by a + 1 (device-side chaining of steps).
+cudaError_t launch_accept(const int32_t *drafts, const int32_t *sampled, int R, int32_t *accepted,
+                          int32_t *bonus, int64_t *pos, cudaStream_t s);
+
+}  // namespace tfk

@@ -1,0 +1,467 @@
+// extern "C" entry points of libtf: argument validation, workspace layout and
+// launch sequencing.  Every step of the verify pass runs in this library's own
+// kernels (w4_gemm.cu, sampler.cu, glue.cu); nothing here computes on the host.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/tf.h"
+#include "glue.cuh"
+#include "sampler.cuh"
+#include "w4_gemm.cuh"
+
+using namespace tfk;
+
+namespace {
+
+thread_local std::string g_error;
+
+tf_status fail(tf_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_error = buf;
+    return st;
+}
+
+tf_status ok() {
+    g_error.clear();
+    return TF_OK;
+}
+
+tf_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(TF_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+constexpr int kGroupedPv = 16;  // virtual CTAs per MoE expert problem
+
+int dense_pv(int T, int Kc) {
+    const long long tot = (long long)T * Kc;
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 1;
+    return int(tot < sms ? tot : sms);
+}
+
+int grouped_pv(int T, int Kc) {
+    const long long tot = (long long)T * Kc;
+    return int(tot < kGroupedPv ? tot : kGroupedPv);
+}
+
+tf_status check_matrix(const tf_w4_matrix *W, const char *name) {
+    if (!W) return fail(TF_ERR_INVALID_ARG, "%s: null matrix", name);
+    if (!W->packed) return fail(TF_ERR_INVALID_ARG, "%s: null packed pointer", name);
+    if (!aligned(W->packed, 256)) return fail(TF_ERR_INVALID_ARG, "%s: packed pointer not 256-B aligned", name);
+    if (W->group != 32 && W->group != 64) return fail(TF_ERR_UNSUPPORTED, "%s: group %d not in {32, 64}", name, W->group);
+    if (W->K <= 0 || W->K % kKChunk) return fail(TF_ERR_UNSUPPORTED, "%s: K=%d is not a positive multiple of 64", name, W->K);
+    if (W->N <= 0) return fail(TF_ERR_INVALID_ARG, "%s: N=%d must be >= 1", name, W->N);
+    return TF_OK;
+}
+
+tf_status check_ws(const void *ws, size_t ws_bytes, size_t need) {
+    if (!ws) return fail(TF_ERR_WORKSPACE, "null workspace");
+    if (!aligned(ws, 256)) return fail(TF_ERR_WORKSPACE, "workspace not 256-B aligned");
+    if (ws_bytes < need) return fail(TF_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+    return TF_OK;
+}
+
+tf_status check_sampling(const tf_sampling *p, int V, int *k_eff) {
+    if (!p) return fail(TF_ERR_INVALID_ARG, "null sampling parameters");
+    if (!std::isfinite(p->temperature) || p->temperature < 0.f)
+        return fail(TF_ERR_INVALID_ARG, "temperature must be finite and >= 0");
+    if (std::isnan(p->top_p)) return fail(TF_ERR_INVALID_ARG, "top_p is NaN");
+    if (p->temperature == 0.f) {
+        *k_eff = 1;
+        return TF_OK;
+    }
+    const int kk = (p->top_k <= 0 || p->top_k >= V) ? V : p->top_k;
+    if (kk > kMaxTopK)
+        return fail(TF_ERR_UNSUPPORTED, "candidate count k'=%d exceeds %d (set top_k <= %d)", kk, kMaxTopK, kMaxTopK);
+    *k_eff = kk;
+    return TF_OK;
+}
+
+GemmArgs dense_args(const tf_w4_matrix &W, const uint16_t *x, int ldx, int R, void *y, int ldy, int mode) {
+    GemmArgs a{};
+    a.w = static_cast<const uint8_t *>(W.packed);
+    a.x = x;
+    a.ldx = ldx;
+    a.y = y;
+    a.ldy = ldy;
+    a.mode = mode;
+    a.F = W.N / 2;
+    a.R = R;
+    a.K = W.K;
+    a.N = W.N;
+    a.G = W.group;
+    a.T = (W.N + kTileN - 1) / kTileN;
+    a.Kc = W.K / kKChunk;
+    a.Pv = dense_pv(a.T, a.Kc);
+    return a;
+}
+
+size_t dense_gemm_ws(const tf_w4_matrix &W) {
+    const int T = (W.N + kTileN - 1) / kTileN;
+    return gemm_workspace_bytes(W.K, W.N, W.group, 1, dense_pv(T, W.K / kKChunk));
+}
+
+// ---- MoE workspace layout ----
+struct MoeLayout {
+    size_t gemm, ids, w, expert_ids, nprob, slot_of, h, Y, total;
+    int u_max;
+};
+
+MoeLayout moe_layout(const tf_moe_layer &L, int R) {
+    MoeLayout m{};
+    m.u_max = L.n_experts < L.top_k * R ? L.n_experts : L.top_k * R;
+    const int Tgu = (2 * L.ffn + kTileN - 1) / kTileN, Td = (L.hidden + kTileN - 1) / kTileN;
+    const size_t g1 = gemm_workspace_bytes(L.hidden, 2 * L.ffn, L.group, m.u_max, grouped_pv(Tgu, L.hidden / kKChunk));
+    const size_t g2 = gemm_workspace_bytes(L.ffn, L.hidden, L.group, m.u_max, grouped_pv(Td, L.ffn / kKChunk));
+    size_t off = round256(g1 > g2 ? g1 : g2);
+    m.gemm = 0;
+    m.ids = off;
+    off += round256(size_t(R) * kMaxRouteK * 4);
+    m.w = off;
+    off += round256(size_t(R) * kMaxRouteK * 4);
+    m.expert_ids = off;
+    off += round256(size_t(kMaxExperts) * 4);
+    m.nprob = off;
+    off += 256;
+    m.slot_of = off;
+    off += round256(size_t(R) * kMaxRouteK * 4);
+    m.h = off;
+    off += round256(size_t(m.u_max) * R * L.ffn * 2);
+    m.Y = off;
+    off += round256(size_t(m.u_max) * R * L.hidden * 4);
+    m.total = off;
+    return m;
+}
+
+tf_status check_moe(const tf_moe_layer *L) {
+    if (!L) return fail(TF_ERR_INVALID_ARG, "null MoE layer");
+    if (!L->gate_up || !L->down) return fail(TF_ERR_INVALID_ARG, "null MoE weights");
+    if (!aligned(L->gate_up, 256) || !aligned(L->down, 256))
+        return fail(TF_ERR_INVALID_ARG, "MoE weights not 256-B aligned");
+    if (L->group != 32 && L->group != 64) return fail(TF_ERR_UNSUPPORTED, "group %d not in {32, 64}", L->group);
+    if (L->hidden <= 0 || L->hidden % kKChunk || L->ffn <= 0 || L->ffn % kKChunk)
+        return fail(TF_ERR_UNSUPPORTED, "hidden and ffn must be positive multiples of 64");
+    if (L->n_experts < 1 || L->n_experts > kMaxExperts)
+        return fail(TF_ERR_UNSUPPORTED, "n_experts must be in [1, %d]", kMaxExperts);
+    if (L->top_k < 1 || L->top_k > kMaxRouteK || L->top_k > L->n_experts)
+        return fail(TF_ERR_UNSUPPORTED, "top_k must be in [1, min(8, n_experts)]");
+    return TF_OK;
+}
+
+// ---- verify-step workspace layout ----
+struct StepLayout {
+    size_t gemm, sample, x, n, h, logits, total;
+};
+
+StepLayout step_layout(const tf_model &m, int R) {
+    StepLayout s{};
+    size_t g = dense_gemm_ws(m.lm_head);
+    for (int b = 0; b < m.n_blocks; ++b) {
+        const size_t g1 = dense_gemm_ws(m.gate_up[b]), g2 = dense_gemm_ws(m.down[b]);
+        g = g1 > g ? g1 : g;
+        g = g2 > g ? g2 : g;
+    }
+    size_t off = round256(g);
+    s.gemm = 0;
+    s.sample = off;
+    off += round256(sample_workspace_bytes(R, m.vocab));
+    s.x = off;
+    off += round256(size_t(R) * m.hidden * 4);
+    s.n = off;
+    off += round256(size_t(R) * m.hidden * 2);
+    s.h = off;
+    off += round256(size_t(R) * m.ffn * 2);
+    s.logits = off;
+    off += round256(size_t(R) * m.vocab * 4);
+    s.total = off;
+    return s;
+}
+
+tf_status check_model(const tf_model *m) {
+    if (!m) return fail(TF_ERR_INVALID_ARG, "null model");
+    if (!m->embedding || !m->gate_up || !m->down) return fail(TF_ERR_INVALID_ARG, "null model pointer");
+    if (m->n_blocks < 0) return fail(TF_ERR_INVALID_ARG, "n_blocks < 0");
+    if (m->vocab < 1 || m->vocab > sample_max_vocab())
+        return fail(TF_ERR_UNSUPPORTED, "vocab must be in [1, %d]", sample_max_vocab());
+    if (!(m->rms_eps >= 0.f) || !std::isfinite(m->rms_eps)) return fail(TF_ERR_INVALID_ARG, "bad rms_eps");
+    for (int b = 0; b < m->n_blocks; ++b) {
+        tf_status st = check_matrix(&m->gate_up[b], "gate_up");
+        if (st) return st;
+        if ((st = check_matrix(&m->down[b], "down"))) return st;
+        if (m->gate_up[b].K != m->hidden || m->gate_up[b].N != 2 * m->ffn || m->down[b].K != m->ffn ||
+            m->down[b].N != m->hidden || m->gate_up[b].group != m->group || m->down[b].group != m->group)
+            return fail(TF_ERR_INVALID_ARG, "block %d: matrix shapes do not match the model", b);
+    }
+    tf_status st = check_matrix(&m->lm_head, "lm_head");
+    if (st) return st;
+    if (m->lm_head.K != m->hidden || m->lm_head.N != m->vocab)
+        return fail(TF_ERR_INVALID_ARG, "lm_head shape does not match the model");
+    if (m->hidden % kKChunk || m->ffn % kKChunk) return fail(TF_ERR_UNSUPPORTED, "hidden, ffn must be multiples of 64");
+    return TF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *tf_last_error(void) { return g_error.c_str(); }
+
+const char *tf_status_string(tf_status s) {
+    switch (s) {
+        case TF_OK: return "ok";
+        case TF_ERR_INVALID_ARG: return "invalid argument";
+        case TF_ERR_UNSUPPORTED: return "unsupported";
+        case TF_ERR_CUDA: return "CUDA error";
+        case TF_ERR_TIMEOUT: return "device wait timed out";
+        case TF_ERR_WORKSPACE: return "bad workspace";
+    }
+    return "unknown status";
+}
+
+int tf_version(void) { return 100; }
+
+int32_t tf_device_sm_count(void) { return device_sm_count(); }
+
+tf_status tf_workspace_status(void *ws, void *stream, int32_t *code) {
+    if (!ws || !code) return fail(TF_ERR_INVALID_ARG, "null argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof v, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "tf_workspace_status");
+    *code = v;
+    return ok();
+}
+
+size_t tf_w4_packed_bytes(int32_t K, int32_t N, int32_t group) { return packed_bytes(K, N, group); }
+
+static tf_status pack_common(const uint8_t *codes, const uint16_t *scales, int32_t K, int32_t N, int32_t group,
+                             void *packed, size_t bytes, void *stream, bool inter) {
+    if (!codes || !scales || !packed) return fail(TF_ERR_INVALID_ARG, "null pointer");
+    if (!packed_shape_ok(K, N, group)) return fail(TF_ERR_UNSUPPORTED, "unsupported shape K=%d N=%d group=%d", K, N, group);
+    if (inter && N % 2) return fail(TF_ERR_INVALID_ARG, "gate/up matrix needs an even N");
+    if (!aligned(packed, 256)) return fail(TF_ERR_INVALID_ARG, "packed pointer not 256-B aligned");
+    if (bytes < packed_bytes(K, N, group)) return fail(TF_ERR_INVALID_ARG, "packed buffer too small");
+    cudaError_t e = launch_pack_w4(codes, scales, K, N, group, packed, inter, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_pack_w4");
+    return ok();
+}
+
+tf_status tf_pack_w4(const uint8_t *codes, const uint16_t *scales, int32_t K, int32_t N, int32_t group, void *packed,
+                     size_t packed_bytes_, void *stream) {
+    return pack_common(codes, scales, K, N, group, packed, packed_bytes_, stream, false);
+}
+
+tf_status tf_pack_w4_gate_up(const uint8_t *codes, const uint16_t *scales, int32_t K, int32_t ffn, int32_t group,
+                             void *packed, size_t packed_bytes_, void *stream) {
+    if (ffn <= 0) return fail(TF_ERR_INVALID_ARG, "ffn must be >= 1");
+    return pack_common(codes, scales, K, 2 * ffn, group, packed, packed_bytes_, stream, true);
+}
+
+size_t tf_lane_gemm_workspace_bytes(int32_t K, int32_t N, int32_t group) {
+    if (!packed_shape_ok(K, N, group)) return 0;
+    tf_w4_matrix W{nullptr, K, N, group};
+    return dense_gemm_ws(W);
+}
+
+tf_status tf_lane_gemm_w4(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R, float *y, int32_t ldy,
+                          void *ws, size_t ws_bytes, void *stream) {
+    tf_status st = check_matrix(W, "W");
+    if (st) return st;
+    if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
+    if (!x || !aligned(x, 16)) return fail(TF_ERR_INVALID_ARG, "x must be non-null and 16-B aligned");
+    if (ldx < W->K || ldx % 8) return fail(TF_ERR_INVALID_ARG, "ldx=%d must be >= K and a multiple of 8", ldx);
+    if (!y || !aligned(y, 4)) return fail(TF_ERR_INVALID_ARG, "y must be non-null and 4-B aligned");
+    if (ldy < W->N) return fail(TF_ERR_INVALID_ARG, "ldy=%d must be >= N", ldy);
+    if ((st = check_ws(ws, ws_bytes, dense_gemm_ws(*W)))) return st;
+    GemmArgs a = dense_args(*W, x, ldx, R, y, ldy, kStoreF32);
+    gemm_bind_workspace(a, ws, 1);
+    cudaError_t e = launch_w4_gemm(a, 1, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_lane_gemm_w4");
+    return ok();
+}
+
+size_t tf_keyed_sample_workspace_bytes(int32_t R, int32_t V) {
+    if (R < 1 || V < 1) return 0;
+    return 256 + sample_workspace_bytes(R, V);
+}
+
+tf_status tf_keyed_sample(const float *logits, int32_t ldl, int32_t R, int32_t V, const tf_sampling *p, uint64_t seed,
+                          const int64_t *pos, int32_t *tokens, void *ws, size_t ws_bytes, void *stream) {
+    if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
+    if (V < 1) return fail(TF_ERR_INVALID_ARG, "V must be >= 1");
+    if (V > sample_max_vocab()) return fail(TF_ERR_UNSUPPORTED, "V=%d exceeds %d", V, sample_max_vocab());
+    if (!logits || !aligned(logits, 4)) return fail(TF_ERR_INVALID_ARG, "logits must be non-null");
+    if (ldl < V) return fail(TF_ERR_INVALID_ARG, "ldl must be >= V");
+    if (!tokens) return fail(TF_ERR_INVALID_ARG, "tokens must be non-null");
+    int k_eff = 0;
+    tf_status st = check_sampling(p, V, &k_eff);
+    if (st) return st;
+    if (p->temperature > 0.f && !pos) return fail(TF_ERR_INVALID_ARG, "pos must be non-null when T > 0");
+    if ((st = check_ws(ws, ws_bytes, tf_keyed_sample_workspace_bytes(R, V)))) return st;
+    SampleArgs a{};
+    a.logits = logits;
+    a.ldl = ldl;
+    a.R = R;
+    a.V = V;
+    a.k_eff = k_eff;
+    a.temperature = p->temperature;
+    a.top_p = p->top_p;
+    a.seed = seed;
+    a.pos = pos;
+    a.pos_base = nullptr;
+    a.tokens = tokens;
+    a.err = static_cast<int *>(ws);
+    sample_bind_workspace(a, static_cast<char *>(ws) + 256, R, V);
+    if (!a.pos) {  // greedy without positions: never read
+        a.pos = reinterpret_cast<const int64_t *>(ws);
+    }
+    cudaError_t e = launch_keyed_sample(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_keyed_sample");
+    return ok();
+}
+
+tf_status tf_accept(const int32_t *drafts, const int32_t *sampled, int32_t R, int32_t *accepted, int32_t *bonus,
+                    void *stream) {
+    if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
+    if (R > 1 && !drafts) return fail(TF_ERR_INVALID_ARG, "drafts must be non-null when R > 1");
+    if (!sampled || !accepted || !bonus) return fail(TF_ERR_INVALID_ARG, "null pointer");
+    cudaError_t e = launch_accept(drafts, sampled, R, accepted, bonus, nullptr, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_accept");
+    return ok();
+}
+
+size_t tf_moe_workspace_bytes(const tf_moe_layer *L, int32_t R) {
+    if (!L || R < 1 || R > TF_MAX_ROWS || L->n_experts < 1 || L->top_k < 1 || L->hidden <= 0 || L->ffn <= 0)
+        return 0;
+    return moe_layout(*L, R).total;
+}
+
+tf_status tf_moe_w4(const tf_moe_layer *L, const uint16_t *x, const float *router_logits, int32_t R, float *out,
+                    void *ws, size_t ws_bytes, void *stream) {
+    tf_status st = check_moe(L);
+    if (st) return st;
+    if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
+    if (!x || !aligned(x, 16) || !router_logits || !out) return fail(TF_ERR_INVALID_ARG, "null or misaligned pointer");
+    const MoeLayout m = moe_layout(*L, R);
+    if ((st = check_ws(ws, ws_bytes, m.total))) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *base = static_cast<char *>(ws);
+    int32_t *ids = reinterpret_cast<int32_t *>(base + m.ids);
+    float *w = reinterpret_cast<float *>(base + m.w);
+    int32_t *expert_ids = reinterpret_cast<int32_t *>(base + m.expert_ids);
+    int32_t *nprob = reinterpret_cast<int32_t *>(base + m.nprob);
+    int32_t *slot_of = reinterpret_cast<int32_t *>(base + m.slot_of);
+    uint16_t *h = reinterpret_cast<uint16_t *>(base + m.h);
+    float *Y = reinterpret_cast<float *>(base + m.Y);
+    int *err = reinterpret_cast<int *>(base);
+
+    cudaError_t e = launch_route(router_logits, R, L->n_experts, L->top_k, ids, w, err, s);
+    if (e == cudaSuccess) e = launch_expert_list(ids, R, L->n_experts, L->top_k, expert_ids, nprob, slot_of, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tf_moe_w4 routing");
+
+    // gate/up (+ SwiGLU) for every touched expert, all R rows
+    tf_w4_matrix Wgu{L->gate_up, L->hidden, 2 * L->ffn, L->group};
+    GemmArgs g1 = dense_args(Wgu, x, L->hidden, R, h, L->ffn, kSwiGluBf16);
+    g1.Pv = grouped_pv(g1.T, g1.Kc);
+    g1.w_stride = (long long)packed_bytes(L->hidden, 2 * L->ffn, L->group);
+    g1.expert_ids = expert_ids;
+    g1.n_problems = nprob;
+    g1.x_stride = 0;
+    g1.y_stride = (long long)R * L->ffn;
+    gemm_bind_workspace(g1, ws, m.u_max);
+    e = launch_w4_gemm(g1, m.u_max, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tf_moe_w4 gate/up");
+
+    tf_w4_matrix Wd{L->down, L->ffn, L->hidden, L->group};
+    GemmArgs g2 = dense_args(Wd, h, L->ffn, R, Y, L->hidden, kStoreF32);
+    g2.Pv = grouped_pv(g2.T, g2.Kc);
+    g2.w_stride = (long long)packed_bytes(L->ffn, L->hidden, L->group);
+    g2.expert_ids = expert_ids;
+    g2.n_problems = nprob;
+    g2.x_stride = (long long)R * L->ffn;
+    g2.y_stride = (long long)R * L->hidden;
+    gemm_bind_workspace(g2, ws, m.u_max);
+    e = launch_w4_gemm(g2, m.u_max, s);
+    if (e == cudaSuccess) e = launch_combine(Y, slot_of, w, R, L->hidden, L->top_k, out, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tf_moe_w4 down/combine");
+    return ok();
+}
+
+size_t tf_verify_step_workspace_bytes(const tf_model *m, int32_t R) {
+    if (R < 1 || R > TF_MAX_ROWS || check_model(m) != TF_OK) return 0;
+    return step_layout(*m, R).total;
+}
+
+tf_status tf_verify_step(const tf_model *m, int32_t R, int32_t *last_token, int64_t *pos, const int32_t *drafts,
+                         const tf_sampling *p, uint64_t seed, int32_t *tokens, int32_t *accepted, float *logits,
+                         void *ws, size_t ws_bytes, void *stream) {
+    tf_status st = check_model(m);
+    if (st) return st;
+    if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
+    if (!last_token || !pos || !tokens || !accepted) return fail(TF_ERR_INVALID_ARG, "null pointer");
+    if (R > 1 && !drafts) return fail(TF_ERR_INVALID_ARG, "drafts must be non-null when R > 1");
+    int k_eff = 0;
+    if ((st = check_sampling(p, m->vocab, &k_eff))) return st;
+    const StepLayout L = step_layout(*m, R);
+    if ((st = check_ws(ws, ws_bytes, L.total))) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *base = static_cast<char *>(ws);
+    int *err = reinterpret_cast<int *>(base);
+    float *x = reinterpret_cast<float *>(base + L.x);
+    uint16_t *n = reinterpret_cast<uint16_t *>(base + L.n);
+    uint16_t *h = reinterpret_cast<uint16_t *>(base + L.h);
+    float *lg = logits ? logits : reinterpret_cast<float *>(base + L.logits);
+
+    cudaError_t e = launch_embed(m->embedding, m->vocab, m->hidden, last_token, drafts, R, x, err, s);
+    for (int b = 0; b < m->n_blocks && e == cudaSuccess; ++b) {
+        e = launch_rmsnorm_bf16(x, R, m->hidden, m->rms_eps, n, s);
+        if (e != cudaSuccess) break;
+        GemmArgs g1 = dense_args(m->gate_up[b], n, m->hidden, R, h, m->ffn, kSwiGluBf16);
+        gemm_bind_workspace(g1, ws, 1);
+        e = launch_w4_gemm(g1, 1, s);
+        if (e != cudaSuccess) break;
+        GemmArgs g2 = dense_args(m->down[b], h, m->ffn, R, x, m->hidden, kAccumulateF32);
+        gemm_bind_workspace(g2, ws, 1);
+        e = launch_w4_gemm(g2, 1, s);
+    }
+    if (e == cudaSuccess) e = launch_rmsnorm_bf16(x, R, m->hidden, m->rms_eps, n, s);
+    if (e == cudaSuccess) {
+        GemmArgs g = dense_args(m->lm_head, n, m->hidden, R, lg, m->vocab, kStoreF32);
+        gemm_bind_workspace(g, ws, 1);
+        e = launch_w4_gemm(g, 1, s);
+    }
+    if (e == cudaSuccess) {
+        SampleArgs a{};
+        a.logits = lg;
+        a.ldl = m->vocab;
+        a.R = R;
+        a.V = m->vocab;
+        a.k_eff = k_eff;
+        a.temperature = p->temperature;
+        a.top_p = p->top_p;
+        a.seed = seed;
+        a.pos = nullptr;
+        a.pos_base = pos;
+        a.tokens = tokens;
+        a.err = err;
+        sample_bind_workspace(a, base + L.sample, R, m->vocab);
+        e = launch_keyed_sample(a, s);
+    }
+    if (e == cudaSuccess) e = launch_accept(drafts, tokens, R, accepted, last_token, pos, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tf_verify_step");
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,263 @@
+"""Thin Python binding of libtf (the C ABI in include/tf.h).
+
+Argument marshalling only: every step of the verify pass runs in the
+library's CUDA kernels.  PyTorch supplies device memory and the current
+stream.  If the shared library is missing the functions raise -- there is
+no CPU fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtf.so")
+
+TF_OK, TF_ERR_INVALID_ARG, TF_ERR_UNSUPPORTED, TF_ERR_CUDA, TF_ERR_TIMEOUT, TF_ERR_WORKSPACE = range(6)
+TF_DEV_OK, TF_DEV_TIMEOUT, TF_DEV_NONFINITE_LOGIT, TF_DEV_BAD_TOKEN = range(4)
+MAX_ROWS = 16
+MAX_TOP_K = 64
+
+P = ctypes.c_void_p
+I32 = ctypes.c_int32
+SZ = ctypes.c_size_t
+
+
+class TFError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"tf status {status}: {message}")
+        self.status = status
+
+
+class W4MatrixC(ctypes.Structure):
+    _fields_ = [("packed", P), ("K", I32), ("N", I32), ("group", I32)]
+
+
+class SamplingC(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", I32), ("top_p", ctypes.c_float)]
+
+
+class MoeLayerC(ctypes.Structure):
+    _fields_ = [("gate_up", P), ("down", P), ("hidden", I32), ("ffn", I32), ("n_experts", I32),
+                ("top_k", I32), ("group", I32)]
+
+
+class ModelC(ctypes.Structure):
+    _fields_ = [("vocab", I32), ("hidden", I32), ("ffn", I32), ("n_blocks", I32), ("group", I32),
+                ("rms_eps", ctypes.c_float), ("embedding", P), ("gate_up", ctypes.POINTER(W4MatrixC)),
+                ("down", ctypes.POINTER(W4MatrixC)), ("lm_head", W4MatrixC)]
+
+
+# (name, restype, argtypes) of every exported symbol
+SIGNATURES = [
+    ("tf_last_error", ctypes.c_char_p, []),
+    ("tf_status_string", ctypes.c_char_p, [ctypes.c_int]),
+    ("tf_version", ctypes.c_int, []),
+    ("tf_device_sm_count", I32, []),
+    ("tf_workspace_status", ctypes.c_int, [P, P, ctypes.POINTER(I32)]),
+    ("tf_w4_packed_bytes", SZ, [I32, I32, I32]),
+    ("tf_pack_w4", ctypes.c_int, [P, P, I32, I32, I32, P, SZ, P]),
+    ("tf_pack_w4_gate_up", ctypes.c_int, [P, P, I32, I32, I32, P, SZ, P]),
+    ("tf_lane_gemm_workspace_bytes", SZ, [I32, I32, I32]),
+    ("tf_lane_gemm_w4", ctypes.c_int, [ctypes.POINTER(W4MatrixC), P, I32, I32, P, I32, P, SZ, P]),
+    ("tf_keyed_sample_workspace_bytes", SZ, [I32, I32]),
+    ("tf_keyed_sample", ctypes.c_int, [P, I32, I32, I32, ctypes.POINTER(SamplingC), ctypes.c_uint64, P, P, P, SZ, P]),
+    ("tf_accept", ctypes.c_int, [P, P, I32, P, P, P]),
+    ("tf_moe_workspace_bytes", SZ, [ctypes.POINTER(MoeLayerC), I32]),
+    ("tf_moe_w4", ctypes.c_int, [ctypes.POINTER(MoeLayerC), P, P, I32, P, P, SZ, P]),
+    ("tf_verify_step_workspace_bytes", SZ, [ctypes.POINTER(ModelC), I32]),
+    ("tf_verify_step", ctypes.c_int, [ctypes.POINTER(ModelC), I32, P, P, P, ctypes.POINTER(SamplingC),
+                                      ctypes.c_uint64, P, P, P, P, SZ, P]),
+]
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libtf.so (built by ``w4_gemm_keyed_gb300.build``); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise FileNotFoundError(f"{path} is missing: run __graft_entry__.build() first (no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        for name, res, args in SIGNATURES:
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != TF_OK:
+        raise TFError(status, load().tf_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """Zero-filled device scratch (the caching allocator aligns to >= 256 B)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def workspace_status(ws: torch.Tensor, stream=None) -> int:
+    code = I32(0)
+    _check(load().tf_workspace_status(_ptr(ws), _stream(stream), ctypes.byref(code)))
+    return int(code.value)
+
+
+# ---------------------------------------------------------------- weights
+class W4Matrix:
+    """A packed W4 matrix living on the device."""
+
+    def __init__(self, packed: torch.Tensor, K: int, N: int, group: int, gate_up: bool = False):
+        self.packed, self.K, self.N, self.group, self.gate_up = packed, K, N, group, gate_up
+
+    def c(self) -> W4MatrixC:
+        return W4MatrixC(self.packed.data_ptr(), self.K, self.N, self.group)
+
+
+def packed_bytes(K: int, N: int, group: int) -> int:
+    return int(load().tf_w4_packed_bytes(K, N, group))
+
+
+def pack_w4(codes: torch.Tensor, scales: torch.Tensor, group: int, gate_up: bool = False,
+            out: torch.Tensor = None, stream=None) -> W4Matrix:
+    """codes uint8 [N][K/2] and scales fp16 (or int16/uint16 bits) [N][K/group], on the device."""
+    lib = load()
+    N, K2 = codes.shape
+    K = 2 * K2
+    nbytes = packed_bytes(K, N, group)
+    if nbytes == 0:
+        raise TFError(TF_ERR_UNSUPPORTED, f"unsupported shape K={K} N={N} group={group}")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=codes.device)
+    codes = codes.contiguous()
+    scales = scales.contiguous()
+    if gate_up:
+        _check(lib.tf_pack_w4_gate_up(_ptr(codes), _ptr(scales), K, N // 2, group, _ptr(out), nbytes, _stream(stream)))
+    else:
+        _check(lib.tf_pack_w4(_ptr(codes), _ptr(scales), K, N, group, _ptr(out), nbytes, _stream(stream)))
+    return W4Matrix(out, K, N, group, gate_up)
+
+
+# ---------------------------------------------------------------- linear
+def lane_gemm_workspace_bytes(K: int, N: int, group: int) -> int:
+    return int(load().tf_lane_gemm_workspace_bytes(K, N, group))
+
+
+def lane_gemm_w4(W: W4Matrix, x: torch.Tensor, y: torch.Tensor = None, ws: torch.Tensor = None,
+                 stream=None) -> torch.Tensor:
+    """y[R][N] fp32 = W4 linear of bf16 rows x[R][K] (x may be bf16 or int16 bits)."""
+    lib = load()
+    R = x.shape[0]
+    if y is None:
+        y = torch.empty((R, W.N), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(lane_gemm_workspace_bytes(W.K, W.N, W.group), x.device)
+    wc = W.c()
+    _check(lib.tf_lane_gemm_w4(ctypes.byref(wc), _ptr(x), x.stride(0), R, _ptr(y), y.stride(0), _ptr(ws),
+                               ws.numel(), _stream(stream)))
+    return y
+
+
+# ---------------------------------------------------------------- sampling
+def keyed_sample_workspace_bytes(R: int, V: int) -> int:
+    return int(load().tf_keyed_sample_workspace_bytes(R, V))
+
+
+def keyed_sample(logits: torch.Tensor, temperature: float, top_k: int, top_p: float, seed: int,
+                 pos: torch.Tensor = None, tokens: torch.Tensor = None, ws: torch.Tensor = None,
+                 stream=None) -> torch.Tensor:
+    lib = load()
+    R, V = logits.shape
+    if tokens is None:
+        tokens = torch.empty(R, dtype=torch.int32, device=logits.device)
+    if ws is None:
+        ws = workspace(keyed_sample_workspace_bytes(R, V), logits.device)
+    sp = SamplingC(temperature, top_k, top_p)
+    _check(lib.tf_keyed_sample(_ptr(logits), logits.stride(0), R, V, ctypes.byref(sp), ctypes.c_uint64(seed & (2**64 - 1)),
+                               _ptr(pos), _ptr(tokens), _ptr(ws), ws.numel(), _stream(stream)))
+    return tokens
+
+
+def accept(drafts: torch.Tensor, sampled: torch.Tensor, accepted: torch.Tensor = None,
+           bonus: torch.Tensor = None, stream=None):
+    lib = load()
+    R = sampled.shape[0]
+    dev = sampled.device
+    if accepted is None:
+        accepted = torch.empty(1, dtype=torch.int32, device=dev)
+    if bonus is None:
+        bonus = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(lib.tf_accept(_ptr(drafts) if R > 1 else None, _ptr(sampled), R, _ptr(accepted), _ptr(bonus),
+                         _stream(stream)))
+    return accepted, bonus
+
+
+# ---------------------------------------------------------------- MoE
+class MoeLayer:
+    def __init__(self, gate_up: torch.Tensor, down: torch.Tensor, hidden: int, ffn: int, n_experts: int,
+                 top_k: int, group: int):
+        self.gate_up, self.down = gate_up, down
+        self.hidden, self.ffn, self.n_experts, self.top_k, self.group = hidden, ffn, n_experts, top_k, group
+
+    def c(self) -> MoeLayerC:
+        return MoeLayerC(self.gate_up.data_ptr(), self.down.data_ptr(), self.hidden, self.ffn, self.n_experts,
+                         self.top_k, self.group)
+
+
+def moe_workspace_bytes(layer: MoeLayer, R: int) -> int:
+    lc = layer.c()
+    return int(load().tf_moe_workspace_bytes(ctypes.byref(lc), R))
+
+
+def moe_w4(layer: MoeLayer, x: torch.Tensor, router: torch.Tensor, out: torch.Tensor = None,
+           ws: torch.Tensor = None, stream=None) -> torch.Tensor:
+    lib = load()
+    R = x.shape[0]
+    if out is None:
+        out = torch.empty((R, layer.hidden), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(moe_workspace_bytes(layer, R), x.device)
+    lc = layer.c()
+    _check(lib.tf_moe_w4(ctypes.byref(lc), _ptr(x), _ptr(router), R, _ptr(out), _ptr(ws), ws.numel(),
+                         _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------- synthetic decoder
+class Model:
+    """Device weights of the attention-free synthetic decoder."""
+
+    def __init__(self, embedding: torch.Tensor, gate_up, down, lm_head: W4Matrix, vocab: int, hidden: int,
+                 ffn: int, group: int, rms_eps: float = 1e-6):
+        self.embedding, self.gate_up, self.down, self.lm_head = embedding, list(gate_up), list(down), lm_head
+        self.vocab, self.hidden, self.ffn, self.group, self.rms_eps = vocab, hidden, ffn, group, rms_eps
+        n = len(self.gate_up)
+        self._gu = (W4MatrixC * max(n, 1))(*[m.c() for m in self.gate_up])
+        self._dn = (W4MatrixC * max(n, 1))(*[m.c() for m in self.down])
+        self._c = ModelC(vocab, hidden, ffn, n, group, rms_eps, embedding.data_ptr(), self._gu, self._dn,
+                         lm_head.c())
+
+    def workspace_bytes(self, R: int) -> int:
+        return int(load().tf_verify_step_workspace_bytes(ctypes.byref(self._c), R))
+
+    def verify_step(self, R: int, last_token: torch.Tensor, pos: torch.Tensor, drafts: torch.Tensor,
+                    temperature: float, top_k: int, top_p: float, seed: int, tokens: torch.Tensor,
+                    accepted: torch.Tensor, ws: torch.Tensor, logits: torch.Tensor = None, stream=None):
+        sp = SamplingC(temperature, top_k, top_p)
+        _check(load().tf_verify_step(ctypes.byref(self._c), R, _ptr(last_token), _ptr(pos),
+                                     _ptr(drafts) if R > 1 else None, ctypes.byref(sp),
+                                     ctypes.c_uint64(seed & (2**64 - 1)), _ptr(tokens), _ptr(accepted),
+                                     _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)))
