@@ -246,6 +246,27 @@ TF_API tf_status tf_verify_step(const tf_model *m, int32_t R, int32_t *last_toke
                          const int32_t *drafts, const tf_sampling *p, uint64_t seed, int32_t *tokens,
                          int32_t *accepted, float *logits, void *ws, size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Pieces of the synthetic decoder (the steps tf_verify_step chains), public so
+ * a caller can compose or check them one layer at a time.
+ * ------------------------------------------------------------------------
+ * tf_embed_rows: x[r][:] = float(embedding[token_r][:]) with token_0 =
+ *   *last_token and token_r = drafts[r-1]; x dev fp32 [R][hidden].  An id
+ *   outside [0, vocab) records TF_DEV_BAD_TOKEN in ws and uses id 0.
+ * tf_rmsnorm_bf16: out[r][:] = bf16(x[r][:] / sqrt(mean(x[r]^2) + eps)), one
+ *   fixed-order fp32 reduction per row; x dev fp32 [R][H], out dev bf16 [R][H].
+ * tf_decoder_block: one residual SwiGLU block b of the model, in place on the
+ *   fp32 residual x [R][hidden]:  n = bf16(rms(x)); h = bf16(silu(n Wg) * (n Wu));
+ *   x += h Wd.  n_out (dev bf16 [R][hidden]) and h_out (dev bf16 [R][ffn]) receive
+ *   the block's intermediate activations.  ws: tf_decoder_block_workspace_bytes.
+ */
+TF_API tf_status tf_embed_rows(const tf_model *m, const int32_t *last_token, const int32_t *drafts, int32_t R,
+                               float *x, void *ws, void *stream);
+TF_API tf_status tf_rmsnorm_bf16(const float *x, int32_t R, int32_t H, float eps, uint16_t *out, void *stream);
+TF_API size_t tf_decoder_block_workspace_bytes(const tf_model *m);
+TF_API tf_status tf_decoder_block(const tf_model *m, int32_t block, float *x, int32_t R, uint16_t *n_out,
+                                  uint16_t *h_out, void *ws, size_t ws_bytes, void *stream);
+
 /* Number of SMs the split-K decomposition is sized for on the current device. */
 TF_API int32_t tf_device_sm_count(void);
 

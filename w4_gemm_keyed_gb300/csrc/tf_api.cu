@@ -144,6 +144,12 @@ MoeLayout moe_layout(const tf_moe_layer &L, int R) {
 
 tf_status check_moe(const tf_moe_layer *L) {
     if (!L) return fail(TF_ERR_INVALID_ARG, "null MoE layer");
+    {
+        const size_t T = size_t((2 * size_t(L->ffn > 0 ? L->ffn : 0) + kTileN - 1) / kTileN) +
+                         size_t((L->hidden > 0 ? L->hidden : 0) + kTileN - 1) / kTileN;
+        if (T * kBlocks * size_t(kMaxExperts) > kMaxCounters)
+            return fail(TF_ERR_UNSUPPORTED, "MoE layer too large for the split-K counter region");
+    }
     if (!L->gate_up || !L->down) return fail(TF_ERR_INVALID_ARG, "null MoE weights");
     if (!aligned(L->gate_up, 256) || !aligned(L->down, 256))
         return fail(TF_ERR_INVALID_ARG, "MoE weights not 256-B aligned");
@@ -206,7 +212,33 @@ tf_status check_model(const tf_model *m) {
     if (m->lm_head.K != m->hidden || m->lm_head.N != m->vocab)
         return fail(TF_ERR_INVALID_ARG, "lm_head shape does not match the model");
     if (m->hidden % kKChunk || m->ffn % kKChunk) return fail(TF_ERR_UNSUPPORTED, "hidden, ffn must be multiples of 64");
+    if (size_t((m->vocab + kTileN - 1) / kTileN) * kBlocks > kMaxCounters ||
+        size_t((2 * size_t(m->ffn) + kTileN - 1) / kTileN) * kBlocks > kMaxCounters)
+        return fail(TF_ERR_UNSUPPORTED, "model too large for the split-K counter region");
     return TF_OK;
+}
+
+cudaError_t run_block(const tf_model &m, int b, float *x, int R, uint16_t *n, uint16_t *h, void *ws,
+                      cudaStream_t s) {
+    cudaError_t e = launch_rmsnorm_bf16(x, R, m.hidden, m.rms_eps, n, s);
+    if (e != cudaSuccess) return e;
+    GemmArgs g1 = dense_args(m.gate_up[b], n, m.hidden, R, h, m.ffn, kSwiGluBf16);
+    gemm_bind_workspace(g1, ws, 1);
+    e = launch_w4_gemm(g1, 1, s);
+    if (e != cudaSuccess) return e;
+    GemmArgs g2 = dense_args(m.down[b], h, m.ffn, R, x, m.hidden, kAccumulateF32);
+    gemm_bind_workspace(g2, ws, 1);
+    return launch_w4_gemm(g2, 1, s);
+}
+
+size_t block_gemm_ws(const tf_model &m) {
+    size_t g = 256;
+    for (int b = 0; b < m.n_blocks; ++b) {
+        const size_t g1 = dense_gemm_ws(m.gate_up[b]), g2 = dense_gemm_ws(m.down[b]);
+        g = g1 > g ? g1 : g;
+        g = g2 > g ? g2 : g;
+    }
+    return g;
 }
 
 }  // namespace
@@ -285,6 +317,8 @@ tf_status tf_lane_gemm_w4(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx,
     if (!y || !aligned(y, 4)) return fail(TF_ERR_INVALID_ARG, "y must be non-null and 4-B aligned");
     if (ldy < W->N) return fail(TF_ERR_INVALID_ARG, "ldy=%d must be >= N", ldy);
     if ((st = check_ws(ws, ws_bytes, dense_gemm_ws(*W)))) return st;
+    if (size_t((W->N + kTileN - 1) / kTileN) * kBlocks > kMaxCounters)
+        return fail(TF_ERR_UNSUPPORTED, "N=%d too large for the split-K counter region", W->N);
     GemmArgs a = dense_args(*W, x, ldx, R, y, ldy, kStoreF32);
     gemm_bind_workspace(a, ws, 1);
     cudaError_t e = launch_w4_gemm(a, 1, static_cast<cudaStream_t>(stream));
@@ -425,17 +459,7 @@ tf_status tf_verify_step(const tf_model *m, int32_t R, int32_t *last_token, int6
     float *lg = logits ? logits : reinterpret_cast<float *>(base + L.logits);
 
     cudaError_t e = launch_embed(m->embedding, m->vocab, m->hidden, last_token, drafts, R, x, err, s);
-    for (int b = 0; b < m->n_blocks && e == cudaSuccess; ++b) {
-        e = launch_rmsnorm_bf16(x, R, m->hidden, m->rms_eps, n, s);
-        if (e != cudaSuccess) break;
-        GemmArgs g1 = dense_args(m->gate_up[b], n, m->hidden, R, h, m->ffn, kSwiGluBf16);
-        gemm_bind_workspace(g1, ws, 1);
-        e = launch_w4_gemm(g1, 1, s);
-        if (e != cudaSuccess) break;
-        GemmArgs g2 = dense_args(m->down[b], h, m->ffn, R, x, m->hidden, kAccumulateF32);
-        gemm_bind_workspace(g2, ws, 1);
-        e = launch_w4_gemm(g2, 1, s);
-    }
+    for (int b = 0; b < m->n_blocks && e == cudaSuccess; ++b) e = run_block(*m, b, x, R, n, h, ws, s);
     if (e == cudaSuccess) e = launch_rmsnorm_bf16(x, R, m->hidden, m->rms_eps, n, s);
     if (e == cudaSuccess) {
         GemmArgs g = dense_args(m->lm_head, n, m->hidden, R, lg, m->vocab, kStoreF32);
@@ -461,6 +485,47 @@ tf_status tf_verify_step(const tf_model *m, int32_t R, int32_t *last_token, int6
     }
     if (e == cudaSuccess) e = launch_accept(drafts, tokens, R, accepted, last_token, pos, s);
     if (e != cudaSuccess) return cuda_fail(e, "tf_verify_step");
+    return ok();
+}
+
+tf_status tf_embed_rows(const tf_model *m, const int32_t *last_token, const int32_t *drafts, int32_t R, float *x,
+                        void *ws, void *stream) {
+    if (!m || !m->embedding) return fail(TF_ERR_INVALID_ARG, "null model");
+    if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
+    if (!last_token || !x || (R > 1 && !drafts)) return fail(TF_ERR_INVALID_ARG, "null pointer");
+    tf_status st = check_ws(ws, 256, 256);
+    if (st) return st;
+    cudaError_t e = launch_embed(m->embedding, m->vocab, m->hidden, last_token, drafts, R, x, static_cast<int *>(ws),
+                                 static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_embed_rows");
+    return ok();
+}
+
+tf_status tf_rmsnorm_bf16(const float *x, int32_t R, int32_t H, float eps, uint16_t *out, void *stream) {
+    if (!x || !out) return fail(TF_ERR_INVALID_ARG, "null pointer");
+    if (R < 1 || H < 1) return fail(TF_ERR_INVALID_ARG, "R and H must be >= 1");
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(TF_ERR_INVALID_ARG, "bad eps");
+    cudaError_t e = launch_rmsnorm_bf16(x, R, H, eps, out, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_rmsnorm_bf16");
+    return ok();
+}
+
+size_t tf_decoder_block_workspace_bytes(const tf_model *m) {
+    if (check_model(m) != TF_OK) return 0;
+    return block_gemm_ws(*m);
+}
+
+tf_status tf_decoder_block(const tf_model *m, int32_t block, float *x, int32_t R, uint16_t *n_out, uint16_t *h_out,
+                           void *ws, size_t ws_bytes, void *stream) {
+    tf_status st = check_model(m);
+    if (st) return st;
+    if (block < 0 || block >= m->n_blocks) return fail(TF_ERR_INVALID_ARG, "block %d outside the model", block);
+    if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
+    if (!x || !n_out || !h_out) return fail(TF_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(n_out, 16) || !aligned(h_out, 16)) return fail(TF_ERR_INVALID_ARG, "n_out / h_out not 16-B aligned");
+    if ((st = check_ws(ws, ws_bytes, block_gemm_ws(*m)))) return st;
+    cudaError_t e = run_block(*m, block, x, R, n_out, h_out, ws, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_decoder_block");
     return ok();
 }
 

@@ -460,20 +460,17 @@ cudaError_t launch_pack_g(const uint8_t *codes, const uint16_t *scales, int K, i
 
 size_t gemm_workspace_bytes(int K, int N, int G, int u_max, int Pv) {
     (void)K;
+    (void)N;
     (void)G;
-    const size_t T = (size_t(N) + kTileN - 1) / kTileN;
-    size_t ctr = T * size_t(u_max) * kBlocks * sizeof(unsigned);
-    ctr = (ctr + 255) / 256 * 256;
-    return 256 + ctr + size_t(u_max) * size_t(Pv) * 2 * kSlotBytes;
+    return 256 + kCounterBytes + size_t(u_max) * size_t(Pv) * 2 * kSlotBytes;
 }
 
 void gemm_bind_workspace(GemmArgs &a, void *ws, int u_max) {
+    (void)u_max;
     char *base = static_cast<char *>(ws);
     a.err = reinterpret_cast<int *>(base);
     a.counters = reinterpret_cast<unsigned *>(base + 256);
-    size_t ctr = size_t(a.T) * size_t(u_max) * kBlocks * sizeof(unsigned);
-    ctr = (ctr + 255) / 256 * 256;
-    a.partials = reinterpret_cast<float4 *>(base + 256 + ctr);
+    a.partials = reinterpret_cast<float4 *>(base + 256 + kCounterBytes);
 }
 
 cudaError_t launch_w4_gemm(const GemmArgs &a, int u_max, cudaStream_t s) {

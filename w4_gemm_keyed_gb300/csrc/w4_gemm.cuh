@@ -84,6 +84,13 @@ struct GemmArgs {
     int *err;
 };
 
+// GEMM workspace: [0, 256) status word | [256, 256 + kCounterBytes) split-K
+// counters | partial tiles.  The counter region has a fixed size so that every
+// GEMM sharing one workspace (the launches of a verify step, the two MoE
+// projections) finds its counters at the same place, left zero by the last
+// launch; partial tiles are always written before they are read.
+constexpr size_t kCounterBytes = size_t(1) << 18;      // 65536 counters
+constexpr size_t kMaxCounters = kCounterBytes / sizeof(unsigned);
 size_t gemm_workspace_bytes(int K, int N, int G, int u_max, int Pv);
 // Fills counters/partials pointers inside `a` from a workspace region.
 void gemm_bind_workspace(GemmArgs &a, void *ws, int u_max);

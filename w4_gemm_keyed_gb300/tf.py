@@ -69,6 +69,10 @@ SIGNATURES = [
     ("tf_moe_workspace_bytes", SZ, [ctypes.POINTER(MoeLayerC), I32]),
     ("tf_moe_w4", ctypes.c_int, [ctypes.POINTER(MoeLayerC), P, P, I32, P, P, SZ, P]),
     ("tf_verify_step_workspace_bytes", SZ, [ctypes.POINTER(ModelC), I32]),
+    ("tf_embed_rows", ctypes.c_int, [ctypes.POINTER(ModelC), P, P, I32, P, P, P]),
+    ("tf_rmsnorm_bf16", ctypes.c_int, [P, I32, I32, ctypes.c_float, P, P]),
+    ("tf_decoder_block_workspace_bytes", SZ, [ctypes.POINTER(ModelC)]),
+    ("tf_decoder_block", ctypes.c_int, [ctypes.POINTER(ModelC), I32, P, I32, P, P, P, SZ, P]),
     ("tf_verify_step", ctypes.c_int, [ctypes.POINTER(ModelC), I32, P, P, P, ctypes.POINTER(SamplingC),
                                       ctypes.c_uint64, P, P, P, P, SZ, P]),
 ]
@@ -205,6 +209,15 @@ def accept(drafts: torch.Tensor, sampled: torch.Tensor, accepted: torch.Tensor =
     return accepted, bonus
 
 
+def rmsnorm_bf16(x: torch.Tensor, eps: float, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """bf16 bits (int16 tensor) of x / sqrt(mean(x^2) + eps), per row of fp32 x [R][H]."""
+    R, H = x.shape
+    if out is None:
+        out = torch.empty((R, H), dtype=torch.int16, device=x.device)
+    _check(load().tf_rmsnorm_bf16(_ptr(x), R, H, eps, _ptr(out), _stream(stream)))
+    return out
+
+
 # ---------------------------------------------------------------- MoE
 class MoeLayer:
     def __init__(self, gate_up: torch.Tensor, down: torch.Tensor, hidden: int, ffn: int, n_experts: int,
@@ -252,6 +265,19 @@ class Model:
 
     def workspace_bytes(self, R: int) -> int:
         return int(load().tf_verify_step_workspace_bytes(ctypes.byref(self._c), R))
+
+    def embed_rows(self, last_token, drafts, R: int, x: torch.Tensor, ws: torch.Tensor, stream=None):
+        _check(load().tf_embed_rows(ctypes.byref(self._c), _ptr(last_token), _ptr(drafts) if R > 1 else None, R,
+                                    _ptr(x), _ptr(ws), _stream(stream)))
+
+    def block_workspace_bytes(self) -> int:
+        return int(load().tf_decoder_block_workspace_bytes(ctypes.byref(self._c)))
+
+    def block(self, b: int, x: torch.Tensor, n_out: torch.Tensor, h_out: torch.Tensor, ws: torch.Tensor,
+              stream=None):
+        """In place on the fp32 residual x [R][hidden]; n_out/h_out receive the bf16 intermediates."""
+        _check(load().tf_decoder_block(ctypes.byref(self._c), b, _ptr(x), x.shape[0], _ptr(n_out), _ptr(h_out),
+                                       _ptr(ws), ws.numel(), _stream(stream)))
 
     def verify_step(self, R: int, last_token: torch.Tensor, pos: torch.Tensor, drafts: torch.Tensor,
                     temperature: float, top_k: int, top_p: float, seed: int, tokens: torch.Tensor,
