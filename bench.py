@@ -463,6 +463,8 @@ def main():
     ap.add_argument("--impl", default="tf", choices=["tf", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the LM-head / MoE / decoder side measurements")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--only", choices=["lmhead", "dense", "moe", "decoder"],
+                    help="run one workload briefly and print its timings (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -472,6 +474,18 @@ def main():
     world, rank, local = dist_env()
     import torch
     torch.cuda.set_device(local)
+    if args.only:
+        from w4_gemm_keyed_gb300 import tf
+        tf.load()
+        if args.only == "dense":
+            mats = setup_dense(tf, torch, rank)
+            secs, steps, lps = time_dense(tf, torch, mats, args.steps, args.warmup)
+            out = {"dense_gbs": STEP_BYTES * steps / secs / 1e9}
+        else:
+            fn = {"lmhead": extra_lmhead, "moe": extra_moe, "decoder": extra_decoder}[args.only]
+            out = fn(tf, torch, steps=args.steps)
+        print(json.dumps({"only": args.only, "result": out}))
+        return 0
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")

@@ -119,6 +119,20 @@ def assert_bf16_close(gpu_bits, ref_bits, max_frac=0.01):
     assert diff.mean() <= max_frac, f"{diff.mean():.3%} of bf16 values differ"
 
 
+def assert_rounded_close(gpu_bits, exact, rel=1e-4):
+    """bf16 values computed from fp32 GEMM outputs, against the exact (fp64) value.
+
+    Allowed: half a bf16 ulp of rounding plus the fp32 GEMM error carried
+    through the activation, bounded by rel * rms of the row (the GEMM itself
+    is held to 1e-3 * rms; its measured error is ~1e-6 * rms)."""
+    g = (np.asarray(gpu_bits).view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ex = np.asarray(exact, dtype=np.float64)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(ex))[1] - 8)
+    rms = np.sqrt(np.mean(ex ** 2, axis=-1, keepdims=True))
+    bad = np.abs(g - ex) > 0.5 * ulp + rel * rms
+    assert not bad.any(), f"{int(bad.sum())} bf16 values off by more than rounding + {rel} * rms"
+
+
 def test_decoder_layers_teacher_forced(tf, tiny_decoder):
     """Each layer of the GPU decoder against the oracle fed the GPU's own inputs."""
     from oracle import numerics as onum
@@ -141,7 +155,7 @@ def test_decoder_layers_teacher_forced(tf, tiny_decoder):
         assert_bf16_close(n_g, onum.bf16_bits_of(onum.bf16_round(onum.rms_norm(x_in, 1e-6))))
         g = oracle.w4_linear(blk["gate_codes"], blk["gate_scales"], n_g, G)
         u = oracle.w4_linear(blk["up_codes"], blk["up_scales"], n_g, G)
-        assert_bf16_close(h_g, onum.bf16_bits_of(onum.bf16_round(onum.silu(g) * u)))
+        assert_rounded_close(h_g, onum.silu(g) * u)
         x_ref = x_in + oracle.w4_linear(blk["down_codes"], blk["down_scales"], h_g, G)
         assert_close_rows(x.cpu().numpy(), x_ref)
     n_fin = tf.rmsnorm_bf16(x, 1e-6)

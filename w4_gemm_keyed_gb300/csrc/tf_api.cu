@@ -86,11 +86,9 @@ tf_status check_sampling(const tf_sampling *p, int V, int *k_eff) {
     return TF_OK;
 }
 
-GemmArgs dense_args(const tf_w4_matrix &W, const uint16_t *x, int ldx, int R, void *y, int ldy, int mode) {
+GemmArgs dense_args(const tf_w4_matrix &W, int R, void *y, int ldy, int mode) {
     GemmArgs a{};
     a.w = static_cast<const uint8_t *>(W.packed);
-    a.x = x;
-    a.ldx = ldx;
     a.y = y;
     a.ldy = ldy;
     a.mode = mode;
@@ -103,6 +101,14 @@ GemmArgs dense_args(const tf_w4_matrix &W, const uint16_t *x, int ldx, int R, vo
     a.Kc = W.K / kKChunk;
     a.Pv = dense_pv(a.T, a.Kc);
     return a;
+}
+
+// Binds the workspace, encodes the activation tensor map and launches.
+cudaError_t bind_and_launch(GemmArgs &a, const uint16_t *x, int ldx, long long x_stride, int u_max, void *ws,
+                            cudaStream_t s, const char **why) {
+    gemm_bind_workspace(a, ws, u_max);
+    if (!gemm_encode_x(a, x, ldx, x_stride, u_max, why)) return cudaErrorInvalidValue;
+    return launch_w4_gemm(a, u_max, s);
 }
 
 size_t dense_gemm_ws(const tf_w4_matrix &W) {
@@ -147,7 +153,7 @@ tf_status check_moe(const tf_moe_layer *L) {
     {
         const size_t T = size_t((2 * size_t(L->ffn > 0 ? L->ffn : 0) + kTileN - 1) / kTileN) +
                          size_t((L->hidden > 0 ? L->hidden : 0) + kTileN - 1) / kTileN;
-        if (T * kBlocks * size_t(kMaxExperts) > kMaxCounters)
+        if (T * kDequantWarps * size_t(kMaxExperts) > kMaxCounters)
             return fail(TF_ERR_UNSUPPORTED, "MoE layer too large for the split-K counter region");
     }
     if (!L->gate_up || !L->down) return fail(TF_ERR_INVALID_ARG, "null MoE weights");
@@ -212,23 +218,21 @@ tf_status check_model(const tf_model *m) {
     if (m->lm_head.K != m->hidden || m->lm_head.N != m->vocab)
         return fail(TF_ERR_INVALID_ARG, "lm_head shape does not match the model");
     if (m->hidden % kKChunk || m->ffn % kKChunk) return fail(TF_ERR_UNSUPPORTED, "hidden, ffn must be multiples of 64");
-    if (size_t((m->vocab + kTileN - 1) / kTileN) * kBlocks > kMaxCounters ||
-        size_t((2 * size_t(m->ffn) + kTileN - 1) / kTileN) * kBlocks > kMaxCounters)
+    if (size_t((m->vocab + kTileN - 1) / kTileN) * kDequantWarps > kMaxCounters ||
+        size_t((2 * size_t(m->ffn) + kTileN - 1) / kTileN) * kDequantWarps > kMaxCounters)
         return fail(TF_ERR_UNSUPPORTED, "model too large for the split-K counter region");
     return TF_OK;
 }
 
 cudaError_t run_block(const tf_model &m, int b, float *x, int R, uint16_t *n, uint16_t *h, void *ws,
-                      cudaStream_t s) {
+                      cudaStream_t s, const char **why) {
     cudaError_t e = launch_rmsnorm_bf16(x, R, m.hidden, m.rms_eps, n, s);
     if (e != cudaSuccess) return e;
-    GemmArgs g1 = dense_args(m.gate_up[b], n, m.hidden, R, h, m.ffn, kSwiGluBf16);
-    gemm_bind_workspace(g1, ws, 1);
-    e = launch_w4_gemm(g1, 1, s);
+    GemmArgs g1 = dense_args(m.gate_up[b], R, h, m.ffn, kSwiGluBf16);
+    e = bind_and_launch(g1, n, m.hidden, 0, 1, ws, s, why);
     if (e != cudaSuccess) return e;
-    GemmArgs g2 = dense_args(m.down[b], h, m.ffn, R, x, m.hidden, kAccumulateF32);
-    gemm_bind_workspace(g2, ws, 1);
-    return launch_w4_gemm(g2, 1, s);
+    GemmArgs g2 = dense_args(m.down[b], R, x, m.hidden, kAccumulateF32);
+    return bind_and_launch(g2, h, m.ffn, 0, 1, ws, s, why);
 }
 
 size_t block_gemm_ws(const tf_model &m) {
@@ -317,12 +321,12 @@ tf_status tf_lane_gemm_w4(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx,
     if (!y || !aligned(y, 4)) return fail(TF_ERR_INVALID_ARG, "y must be non-null and 4-B aligned");
     if (ldy < W->N) return fail(TF_ERR_INVALID_ARG, "ldy=%d must be >= N", ldy);
     if ((st = check_ws(ws, ws_bytes, dense_gemm_ws(*W)))) return st;
-    if (size_t((W->N + kTileN - 1) / kTileN) * kBlocks > kMaxCounters)
+    if (size_t((W->N + kTileN - 1) / kTileN) * kDequantWarps > kMaxCounters)
         return fail(TF_ERR_UNSUPPORTED, "N=%d too large for the split-K counter region", W->N);
-    GemmArgs a = dense_args(*W, x, ldx, R, y, ldy, kStoreF32);
-    gemm_bind_workspace(a, ws, 1);
-    cudaError_t e = launch_w4_gemm(a, 1, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "tf_lane_gemm_w4");
+    GemmArgs a = dense_args(*W, R, y, ldy, kStoreF32);
+    const char *why = "";
+    cudaError_t e = bind_and_launch(a, x, ldx, 0, 1, ws, static_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess) return fail(TF_ERR_CUDA, "tf_lane_gemm_w4: %s (%s)", cudaGetErrorString(e), why);
     return ok();
 }
 
@@ -406,30 +410,27 @@ tf_status tf_moe_w4(const tf_moe_layer *L, const uint16_t *x, const float *route
     if (e != cudaSuccess) return cuda_fail(e, "tf_moe_w4 routing");
 
     // gate/up (+ SwiGLU) for every touched expert, all R rows
+    const char *why = "";
     tf_w4_matrix Wgu{L->gate_up, L->hidden, 2 * L->ffn, L->group};
-    GemmArgs g1 = dense_args(Wgu, x, L->hidden, R, h, L->ffn, kSwiGluBf16);
+    GemmArgs g1 = dense_args(Wgu, R, h, L->ffn, kSwiGluBf16);
     g1.Pv = grouped_pv(g1.T, g1.Kc);
     g1.w_stride = (long long)packed_bytes(L->hidden, 2 * L->ffn, L->group);
     g1.expert_ids = expert_ids;
     g1.n_problems = nprob;
-    g1.x_stride = 0;
     g1.y_stride = (long long)R * L->ffn;
-    gemm_bind_workspace(g1, ws, m.u_max);
-    e = launch_w4_gemm(g1, m.u_max, s);
-    if (e != cudaSuccess) return cuda_fail(e, "tf_moe_w4 gate/up");
+    e = bind_and_launch(g1, x, L->hidden, 0, m.u_max, ws, s, &why);
+    if (e != cudaSuccess) return fail(TF_ERR_CUDA, "tf_moe_w4 gate/up: %s (%s)", cudaGetErrorString(e), why);
 
     tf_w4_matrix Wd{L->down, L->ffn, L->hidden, L->group};
-    GemmArgs g2 = dense_args(Wd, h, L->ffn, R, Y, L->hidden, kStoreF32);
+    GemmArgs g2 = dense_args(Wd, R, Y, L->hidden, kStoreF32);
     g2.Pv = grouped_pv(g2.T, g2.Kc);
     g2.w_stride = (long long)packed_bytes(L->ffn, L->hidden, L->group);
     g2.expert_ids = expert_ids;
     g2.n_problems = nprob;
-    g2.x_stride = (long long)R * L->ffn;
     g2.y_stride = (long long)R * L->hidden;
-    gemm_bind_workspace(g2, ws, m.u_max);
-    e = launch_w4_gemm(g2, m.u_max, s);
+    e = bind_and_launch(g2, h, L->ffn, (long long)R * L->ffn, m.u_max, ws, s, &why);
     if (e == cudaSuccess) e = launch_combine(Y, slot_of, w, R, L->hidden, L->top_k, out, s);
-    if (e != cudaSuccess) return cuda_fail(e, "tf_moe_w4 down/combine");
+    if (e != cudaSuccess) return fail(TF_ERR_CUDA, "tf_moe_w4 down/combine: %s (%s)", cudaGetErrorString(e), why);
     return ok();
 }
 
@@ -458,13 +459,13 @@ tf_status tf_verify_step(const tf_model *m, int32_t R, int32_t *last_token, int6
     uint16_t *h = reinterpret_cast<uint16_t *>(base + L.h);
     float *lg = logits ? logits : reinterpret_cast<float *>(base + L.logits);
 
+    const char *why = "";
     cudaError_t e = launch_embed(m->embedding, m->vocab, m->hidden, last_token, drafts, R, x, err, s);
-    for (int b = 0; b < m->n_blocks && e == cudaSuccess; ++b) e = run_block(*m, b, x, R, n, h, ws, s);
+    for (int b = 0; b < m->n_blocks && e == cudaSuccess; ++b) e = run_block(*m, b, x, R, n, h, ws, s, &why);
     if (e == cudaSuccess) e = launch_rmsnorm_bf16(x, R, m->hidden, m->rms_eps, n, s);
     if (e == cudaSuccess) {
-        GemmArgs g = dense_args(m->lm_head, n, m->hidden, R, lg, m->vocab, kStoreF32);
-        gemm_bind_workspace(g, ws, 1);
-        e = launch_w4_gemm(g, 1, s);
+        GemmArgs g = dense_args(m->lm_head, R, lg, m->vocab, kStoreF32);
+        e = bind_and_launch(g, n, m->hidden, 0, 1, ws, s, &why);
     }
     if (e == cudaSuccess) {
         SampleArgs a{};
@@ -484,7 +485,7 @@ tf_status tf_verify_step(const tf_model *m, int32_t R, int32_t *last_token, int6
         e = launch_keyed_sample(a, s);
     }
     if (e == cudaSuccess) e = launch_accept(drafts, tokens, R, accepted, last_token, pos, s);
-    if (e != cudaSuccess) return cuda_fail(e, "tf_verify_step");
+    if (e != cudaSuccess) return fail(TF_ERR_CUDA, "tf_verify_step: %s %s", cudaGetErrorString(e), why);
     return ok();
 }
 
@@ -524,8 +525,9 @@ tf_status tf_decoder_block(const tf_model *m, int32_t block, float *x, int32_t R
     if (!x || !n_out || !h_out) return fail(TF_ERR_INVALID_ARG, "null pointer");
     if (!aligned(n_out, 16) || !aligned(h_out, 16)) return fail(TF_ERR_INVALID_ARG, "n_out / h_out not 16-B aligned");
     if ((st = check_ws(ws, ws_bytes, block_gemm_ws(*m)))) return st;
-    cudaError_t e = run_block(*m, block, x, R, n_out, h_out, ws, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "tf_decoder_block");
+    const char *why = "";
+    cudaError_t e = run_block(*m, block, x, R, n_out, h_out, ws, static_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess) return fail(TF_ERR_CUDA, "tf_decoder_block: %s %s", cudaGetErrorString(e), why);
     return ok();
 }
 

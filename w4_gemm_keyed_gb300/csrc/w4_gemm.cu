@@ -1,27 +1,38 @@
-// W4 lane GEMM for the speculative-decoding verify pass (sm_103a).
+// W4 lane GEMM for the speculative-decoding verify pass (sm_103a, tcgen05).
 //
 // TensorFold README, "A row of a multi-row verify pass gets the same bits as a
 // one-row step": up to 16 drafted rows share one launch that streams every
 // 4-bit weight once, and row r's bits never depend on how many rows there are.
 //
-// Structure of one CTA (9 warps, one CTA per SM):
-//   * warp 8 (producer): one elected lane streams, per iteration (tile t,
-//     k-slice kc), the contiguous packed weight stage with a bulk TMA copy
-//     (L2 evict-first) plus the R activation rows of that k-slice, into a
-//     14-deep shared-memory ring guarded by full/empty mbarriers;
-//   * warps 0-7 (consumers): warp (kg, b) handles feature block b of the tile
-//     for the iterations of parity kg.  Per 16-wide k step it turns one 32-bit
-//     packed word into the m16n8k16 A fragment with one LOP3 + one bf16x2 FMA
-//     per register (exact: integer codes -8..7), loads the activation B
-//     fragment with ldmatrix and issues one mma per 8 rows.  Each quantisation
-//     group's partial sum is formed in a fresh fp32 fragment and folded into the
-//     running sum as  acc = fma(scale, partial, acc).
-// Row invariance: rows are MMA columns; a column's result depends only on its
-// own activations, the rows 8..15 MMA is simply skipped when R <= 8, and the
-// stream-K cut, the k-group parity split and the fixed-order partial sums all
-// depend on (T, Kc, Pv) only.
+// One CTA per SM, 10 warps:
+//   warp 0  producer: per pipeline stage (up to 4 consecutive 64-wide k slices
+//           of one 256-feature tile, never crossing a tile boundary) lane 0
+//           issues ONE bulk TMA copy of the packed weights (~35 KB, L2
+//           evict-first) and ONE 4-D tensor TMA of the activation slices
+//           ([16 rows][64 k] bf16 each, 128-byte swizzled, rows >= R
+//           zero-filled by the copy engine's out-of-bounds fill).
+//   warp 1  MMA issuer (lane 0) and TMEM owner.  For each slice and M-tile it
+//           issues tcgen05.mma kind::f16, M=128 (weight rows), N=16 (verify
+//           rows), K=16, A from tensor memory, B (activations) from shared
+//           memory, fp32 accumulator in tensor memory.
+//   warps 2-9  two warpgroups, one per 128-row M-tile.  Each thread owns one
+//           weight row: it turns the row's 64 packed codes of a slice into
+//           bf16 (16 + u, u = code + 8; exact) with one shift + LOP3 per pair, stores
+//           them to tensor memory as the MMA's A operand, and later reads back
+//           the group's fp32 partial sums (tcgen05.ld) and folds them in as
+//           acc = fma(scale, partial, acc).
+// Exactness: the A operand holds 16 + u; for every k step a second MMA adds
+// (-24) x the same activations from a constant A block, so the tensor core
+// accumulates  sum (16 + u - 24) x = sum code * x  of the group; every product
+// is exact and the partial carries only the fp32 accumulation error (the bias
+// of 24 is the smallest this OR-into-the-mantissa conversion allows: u sits in
+// mantissa bits 3..6 under the implicit leading one of 16).
+// Row invariance: rows are MMA columns (N = 16 for every R); the cut of the
+// iteration space, the stage schedule and the fixed-order split-K sums depend
+// on (T, Kc, Pv) only.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cudaTypedefs.h>
 
 #include "tf_ptx.cuh"
 #include "w4_gemm.cuh"
@@ -30,143 +41,142 @@ namespace tfk {
 
 namespace {
 
-constexpr uint32_t kBf16One2 = 0x3F803F80u;    // (1.0, 1.0)
-constexpr uint32_t kBf16Neg136x2 = 0xC308C308u; // (-136, -136)
-constexpr uint32_t kNibMask = 0x000F000Fu;
-constexpr uint32_t kBf16Magic = 0x43004300u;    // (128, 128): OR-ing u in gives 128 + u
+constexpr uint32_t kNibMask = 0x00780078u;    // mantissa bits 3..6 of both bf16 halves
+constexpr uint32_t kBf16Magic = 0x41804180u;  // (16, 16): u in mantissa bits 3..6 gives 16 + u
+constexpr uint32_t kBf16Neg24x2 = 0xC1C0C1C0u;  // (-24, -24)
+// tcgen05 instruction descriptor, kind::f16: D fp32, A bf16, B bf16, both
+// K-major, N = 16, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t(kRows) >> 3) << 17) |
+                            ((uint32_t(kMTile) >> 4) << 24);
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColA = 0;        // A buffers: [mt][2] x 32 columns
+constexpr uint32_t kColConst = 128;  // 8 columns of -24
+constexpr uint32_t kColD = 160;      // D buffers: [mt][2*NG] x 16 columns
 
-__device__ __forceinline__ uint32_t word_of(const uint4 &q, int j) {
-    return j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
+__device__ __forceinline__ float half_at(const uint8_t *p) {
+    return __half2float(*reinterpret_cast<const __half *>(p));
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+// Shared-memory descriptor of a [16 rows][64 k] bf16 slice, K-major, 128-byte
+// swizzle (8-row atoms of 1024 B), starting `koff` bytes into each row.
+__device__ __forceinline__ uint64_t x_desc(uint32_t slice_smem, uint32_t koff) {
+    const uint32_t start = (slice_smem + koff) >> 4;
+    return uint64_t(start & 0x3FFFu) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) |
+           (uint64_t(2) << 61);
 }
 
-__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))); }
-__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+struct Sync {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t a_full[kMTiles][2];
+    uint64_t a_free[kMTiles][2];
+    uint64_t d_full[kMTiles][4];
+    uint64_t d_free[kMTiles][4];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+};
 
-// One 64-wide k slice of one 64-feature block for this warp.
-template <int G>
-__device__ __forceinline__ void consume_stage(const uint8_t *cb, uint32_t xaddr, int lane, int gq, bool hi,
-                                              float (&acc)[4][2][4]) {
-    constexpr int NG = kKChunk / G;
-    constexpr int KS = G / 16;
-    uint4 q[4];
+// Bounded wait that gives up at once after any wait of this CTA timed out.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Sync *sy, int *err) {
+    for (uint32_t i = 0; i < kSpinPolls; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 1023u) == 1023u && *reinterpret_cast<volatile int *>(&sy->abort)) return false;
+    }
+    *reinterpret_cast<volatile int *>(&sy->abort) = 1;
+    set_error(err, 1);
+    return false;
+}
+
+// Iteration-space walker shared by every role so all agree on the schedule:
+// segments end at tile boundaries, stages are runs of <= kStageIters
+// iterations from the segment start.
+struct Walk {
+    long long gi;     // global iteration index (tile * Kc + kc)
+    long long seg_b, seg_e;
+    int pos;          // position inside the stage
+    int st;           // stage counter
+    int n_in_stage;
+};
+
+__device__ __forceinline__ void walk_begin(Walk &w, long long i0, long long i1, int Kc) {
+    w.gi = i0;
+    w.seg_b = i0;
+    w.seg_e = min(i1, (i0 / Kc + 1) * (long long)Kc);
+    w.pos = 0;
+    w.st = 0;
+    w.n_in_stage = int(min((long long)kStageIters, w.seg_e - w.seg_b));
+}
+
+__device__ __forceinline__ void walk_next(Walk &w, long long i1, int Kc) {
+    ++w.gi;
+    if (w.gi == w.seg_e) {
+        w.seg_b = w.gi;
+        w.seg_e = min(i1, (w.gi / Kc + 1) * (long long)Kc);
+    }
+    const int pos = int((w.gi - w.seg_b) % kStageIters);
+    if (pos == 0) {
+        ++w.st;
+        w.n_in_stage = int(min((long long)kStageIters, w.seg_e - w.gi));
+    }
+    w.pos = pos;
+}
+
+__device__ __forceinline__ void dequant_slice(const uint4 &c0, const uint4 &c1, uint32_t (&v)[32]) {
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) q[mt] = *reinterpret_cast<const uint4 *>(cb + (mt * 32 + lane) * 16);
+    for (int e = 0; e < 8; ++e) {
+        // pair p (bits 4p / 16+4p) moves to mantissa bits 3..6 of each half
+        v[4 * e + 0] = lop3_and_or(w[e] << 3, kNibMask, kBf16Magic);
 #pragma unroll
-    for (int grp = 0; grp < NG; ++grp) {
-        const uint4 sv = *reinterpret_cast<const uint4 *>(cb + 2048 + grp * 128 + gq * 16);
-        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-        float part[4][2][4];
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) part[mt][n][c] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            const int j = grp * KS + kk;
-            uint32_t b0, b1, b2 = 0, b3 = 0;
-            if (hi)
-                ldsm_x4(xaddr + j * 32, b0, b1, b2, b3);
-            else
-                ldsm_x2(xaddr + j * 32, b0, b1);
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                const uint32_t w = word_of(q[mt], j);
-                uint32_t af[4];
-                af[0] = fma_bf16x2(lop3_and_or(w, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
-                af[1] = fma_bf16x2(lop3_and_or(w >> 4, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
-                af[2] = fma_bf16x2(lop3_and_or(w >> 8, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
-                af[3] = fma_bf16x2(lop3_and_or(w >> 12, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
-                mma_bf16_16816(part[mt][0], af, b0, b1);
-                if (hi) mma_bf16_16816(part[mt][1], af, b2, b3);
-            }
-        }
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-            const float s_lo = half_lo(sw[mt]);   // feature mt*16 + g
-            const float s_hi = half_hi(sw[mt]);   // feature mt*16 + g + 8
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                if (n == 1 && !hi) continue;
-                acc[mt][n][0] = fmaf(s_lo, part[mt][n][0], acc[mt][n][0]);
-                acc[mt][n][1] = fmaf(s_lo, part[mt][n][1], acc[mt][n][1]);
-                acc[mt][n][2] = fmaf(s_hi, part[mt][n][2], acc[mt][n][2]);
-                acc[mt][n][3] = fmaf(s_hi, part[mt][n][3], acc[mt][n][3]);
-            }
-        }
+        for (int p = 1; p < 4; ++p) v[4 * e + p] = lop3_and_or(w[e] >> (4 * p - 3), kNibMask, kBf16Magic);
     }
 }
 
-__device__ __forceinline__ void put(const GemmArgs &a, void *yb, int r, int f, float v) {
-    float *y = static_cast<float *>(yb) + (long long)r * a.ldy + f;
-    if (a.mode == kAccumulateF32)
-        *y = *y + v;
-    else
-        *y = v;
-}
-
-__device__ __forceinline__ void store_tile(const GemmArgs &a, void *yb, int t, int b, int gq, int tq, bool hi,
-                                           const float (&v)[4][2][4]) {
+// Writes one thread's 16 results (its weight row, verify rows 0..15).
+__device__ __forceinline__ void store_row(const GemmArgs &a, void *yb, int t, int mt, int quarter, int lane,
+                                          const float (&v)[kRows]) {
     if (a.mode == kSwiGluBf16) {
-        // sub-tiles (0,1) and (2,3) are (gate, up) of the same 16 h columns
+        // lanes 0-15 hold gate rows, lanes 16-31 the matching up rows
+        const int j = t * (kTileN / 2) + mt * (kMTile / 2) + quarter * 16 + (lane & 15);
+        __nv_bfloat16 *h = static_cast<__nv_bfloat16 *>(yb);
 #pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                if (n == 1 && !hi) continue;
-                const int j = t * (kTileN / 2) + b * 32 + pr * 16 + gq;
-                const int r = n * 8 + tq * 2;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int jj = j + (c >= 2 ? 8 : 0);
-                    const int rr = r + (c & 1);
-                    if (jj < a.F && rr < a.R) {
-                        const float g = v[2 * pr][n][c];
-                        const float up = v[2 * pr + 1][n][c];
-                        const float h = g / (1.0f + expf(-g)) * up;
-                        static_cast<__nv_bfloat16 *>(yb)[(long long)rr * a.ldy + jj] = __float2bfloat16_rn(h);
-                    }
-                }
+        for (int r = 0; r < kRows; ++r) {
+            const float up = __shfl_down_sync(0xFFFFFFFFu, v[r], 16);
+            if (lane < 16 && j < a.F && r < a.R) {
+                const float g = v[r];
+                h[(long long)r * a.ldy + j] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * up);
             }
         }
         return;
     }
-    const int f0 = t * kTileN + b * 64;
+    const int f = t * kTileN + mt * kMTile + quarter * 32 + lane;
+    if (f >= a.N) return;
+    float *y = static_cast<float *>(yb);
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
-            if (n == 1 && !hi) continue;
-            const int f = f0 + mt * 16 + gq;
-            const int r = n * 8 + tq * 2;
-            if (f < a.N) {
-                if (r < a.R) put(a, yb, r, f, v[mt][n][0]);
-                if (r + 1 < a.R) put(a, yb, r + 1, f, v[mt][n][1]);
-            }
-            if (f + 8 < a.N) {
-                if (r < a.R) put(a, yb, r, f + 8, v[mt][n][2]);
-                if (r + 1 < a.R) put(a, yb, r + 1, f + 8, v[mt][n][3]);
-            }
+    for (int r = 0; r < kRows; ++r) {
+        if (r < a.R) {
+            float *p = y + (long long)r * a.ldy + f;
+            *p = a.mode == kAccumulateF32 ? *p + v[r] : v[r];
         }
     }
 }
 
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_constant__ GemmArgs a) {
+    constexpr int NG = kKChunk / G;   // quantisation groups per slice
+    constexpr int KS = G / 16;        // k16 steps per group
+    constexpr int MB = mtile_bytes(G);
     constexpr int CB = chunk_bytes(G);
-    constexpr int SWB = stage_w_bytes(G);
+    constexpr int STW = kStageIters * CB;
 
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *sw = smem;
-    uint8_t *sx = sw + kStages * SWB;
-    float *red = reinterpret_cast<float *>(sx + kStages * kXStageBytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(red + kBlocks * kWarpAccFloats);
-    uint64_t *empty = full + kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sx = smem;                                  // [kStages][kXStageBytes], 1024-B aligned
+    uint8_t *sw = sx + kStages * kXStageBytes;           // [kStages][STW]
+    Sync *sy = reinterpret_cast<Sync *>(sw + kStages * STW);
 
     const int u = blockIdx.y;
     const int nprob = a.n_problems ? *a.n_problems : 1;
@@ -176,135 +186,162 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     const long long i0 = (long long)vp * tot / a.Pv;
     const long long i1 = (long long)(vp + 1) * tot / a.Pv;
     if (i0 >= i1) return;
+    const int n_it = int(i1 - i0);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < kStages * kXStageBytes / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(sx)[i] = make_uint4(0u, 0u, 0u, 0u);  // rows >= R stay zero
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kBlocks);
+            mbar_init(&sy->full[s], 1);
+            mbar_init(&sy->empty[s], kDequantWarps + 1);
         }
+        for (int m = 0; m < kMTiles; ++m) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&sy->a_full[m][b], 4);
+                mbar_init(&sy->a_free[m][b], 1);
+            }
+            for (int b = 0; b < 4; ++b) {
+                mbar_init(&sy->d_full[m][b], 1);
+                mbar_init(&sy->d_free[m][b], 4);
+            }
+        }
+        mbar_init(&sy->done, 1);
+        sy->abort = 0;
         fence_mbar_init();
     }
-    fence_proxy_async_smem();
+    if (warp == 1) {
+        tmem_alloc(&sy->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = sy->tmem_base;
 
     const int e = a.expert_ids ? a.expert_ids[u] : u;
     const uint8_t *wb = a.w + (long long)e * a.w_stride;
-    const uint16_t *xb = a.x + (long long)u * a.x_stride;
-    const int R = a.R;
 
-    if (warp == kConsumerWarps) {
+    if (warp == 0) {
         // ---------------- producer ----------------
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            const uint32_t tx = SWB + R * 128;
-            long long n_issued = 0;
-            for (long long i = i0; i < i1; ++i) {
-                const int it = int(i - i0);
-                const int s = it % kStages;
-                if (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1)) {
-                    set_error(a.err, 1);
+            Walk w;
+            walk_begin(w, i0, i1, a.Kc);
+            int issued = 0;
+            for (int j = 0; j < n_it; ++j, walk_next(w, i1, a.Kc)) {
+                if (w.pos != 0) continue;
+                const int s = w.st % kStages;
+                if (w.st >= kStages && !wait_bar(&sy->empty[s], uint32_t((w.st / kStages) - 1) & 1, sy, a.err))
                     break;
-                }
-                const int kc = int(i % a.Kc);
-                mbar_arrive_expect_tx(&full[s], tx);
-                bulk_g2s_hint(sw + s * SWB, wb + i * SWB, SWB, &full[s], pol);
-                const uint16_t *xs = xb + kc * kKChunk;
-                for (int r = 0; r < R; ++r)
-                    bulk_g2s(sx + s * kXStageBytes + r * kXRowStride, xs + (long long)r * a.ldx, 128, &full[s]);
-                ++n_issued;
+                mbar_arrive_expect_tx(&sy->full[s], uint32_t(w.n_in_stage * CB + kXStageBytes));
+                bulk_g2s_hint(sw + s * STW, wb + w.gi * CB, uint32_t(w.n_in_stage * CB), &sy->full[s], pol);
+                tma_load_4d(sx + s * kXStageBytes, &a.xmap, 0, 0, int(w.gi % a.Kc), a.x_per_problem ? u : 0,
+                            &sy->full[s]);
+                issued = w.st + 1;
             }
-            // Leave only once every issued copy has landed (bounded).
-            for (long long k = (n_issued > kStages ? n_issued - kStages : 0); k < n_issued; ++k)
-                mbar_wait(&full[k % kStages], uint32_t(k / kStages) & 1);
+            // leave only once every issued copy has landed (bounded)
+            for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
+                wait_bar(&sy->full[k % kStages], uint32_t(k / kStages) & 1, sy, a.err);
         }
-        return;
-    }
-
-    // ---------------- consumers ----------------
-    const int kg = warp / kBlocks;
-    const int b = warp % kBlocks;
-    const int gq = lane >> 2, tq = lane & 3;
-    const bool hi = R > 8;
-    const int lrow = (lane & 7) + ((lane >> 4) << 3);
-    const int lcol = (lane >> 3) & 1;
-    const uint32_t sx_lane = smem_u32(sx) + lrow * kXRowStride + lcol * 16;
-    const size_t ysz = a.mode == kSwiGluBf16 ? sizeof(__nv_bfloat16) : sizeof(float);
-    void *yb = static_cast<char *>(a.y) + (long long)u * a.y_stride * (long long)ysz;
-    float *rb = red + b * kWarpAccFloats;
-    bool failed = false;
-
-    long long i = i0;
-    while (i < i1) {
-        const int t = int(i / a.Kc);
-        const long long seg_b = i;
-        const long long seg_e = min(i1, (long long)(t + 1) * a.Kc);
-        float acc[4][2][4];
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            Walk w;
+            walk_begin(w, i0, i1, a.Kc);
+            bool ok = true;
+            for (int j = 0; j < n_it && ok; ++j, walk_next(w, i1, a.Kc)) {
+                const int s = w.st % kStages;
+                if (w.pos == 0) ok = wait_bar(&sy->full[s], uint32_t(w.st / kStages) & 1, sy, a.err);
+                const uint32_t slice = smem_u32(sx + s * kXStageBytes + w.pos * kXSliceBytes);
+                for (int m = 0; m < kMTiles && ok; ++m) {
+                    ok = wait_bar(&sy->a_full[m][j & 1], uint32_t(j >> 1) & 1, sy, a.err);
+                    tc_fence_after();
+                    const uint32_t acol = tbase + kColA + uint32_t(m * 2 + (j & 1)) * 32;
+                    for (int g = 0; g < NG && ok; ++g) {
+                        const int gi = j * NG + g;
+                        const int db = gi % (2 * NG);
+                        if (gi >= 2 * NG)
+                            ok = wait_bar(&sy->d_free[m][db], uint32_t(gi / (2 * NG) - 1) & 1, sy, a.err);
+                        tc_fence_after();
+                        const uint32_t dcol = tbase + kColD + uint32_t(m * 2 * NG + db) * 16;
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[mt][n][c] = 0.f;
-
-        if (!failed) {
-            for (long long j = seg_b; j < seg_e; ++j) {
-                const int it = int(j - i0);
-                if ((it & 1) != kg) continue;
-                const int s = it % kStages;
-                if (!mbar_wait(&full[s], uint32_t(it / kStages) & 1)) {
-                    set_error(a.err, 1);
-                    failed = true;
-                    break;
-                }
-                consume_stage<G>(sw + s * SWB + b * CB, sx_lane + s * kXStageBytes, lane, gq, hi, acc);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-            }
-        }
-
-        // Combine the two k-parity groups in a fixed order (group 0 + group 1).
-        named_bar_sync(1, kConsumerWarps * 32);
-        if (kg == 1) {
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                for (int n = 0; n < 2; ++n)
-                    reinterpret_cast<float4 *>(rb)[(mt * 2 + n) * 32 + lane] =
-                        make_float4(acc[mt][n][0], acc[mt][n][1], acc[mt][n][2], acc[mt][n][3]);
-        }
-        named_bar_sync(1, kConsumerWarps * 32);
-        if (kg == 0) {
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                for (int n = 0; n < 2; ++n) {
-                    const float4 o = reinterpret_cast<const float4 *>(rb)[(mt * 2 + n) * 32 + lane];
-                    acc[mt][n][0] += o.x;
-                    acc[mt][n][1] += o.y;
-                    acc[mt][n][2] += o.z;
-                    acc[mt][n][3] += o.w;
-                }
-            const long long tb = (long long)t * a.Kc;
-            const long long te = tb + a.Kc;
-            if (seg_b == tb && seg_e == te) {
-                store_tile(a, yb, t, b, gq, tq, hi, acc);
-            } else {
-                // Stream-K partial: publish, count, and let the last arriver sum
-                // every segment of this tile in k order.
-                const int which = (t == int(i0 / a.Kc)) ? 0 : 1;
-                float4 *slot = a.partials + ((((long long)u * a.Pv + vp) * 2 + which) * kBlocks + b) * 256;
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                    for (int n = 0; n < 2; ++n) {
-                        if (n == 1 && !hi) continue;
-                        __stcg(slot + (mt * 2 + n) * 32 + lane,
-                               make_float4(acc[mt][n][0], acc[mt][n][1], acc[mt][n][2], acc[mt][n][3]));
+                        for (int kk = 0; kk < KS; ++kk) {
+                            const int ks = g * KS + kk;
+                            const uint64_t bd = x_desc(slice, uint32_t(ks) * 32);
+                            umma_tmem_a(dcol, acol + uint32_t(ks) * 8, bd, kIdesc, kk > 0 ? 1u : 0u);
+                            umma_tmem_a(dcol, tbase + kColConst, bd, kIdesc, 1u);
+                        }
+                        umma_commit(&sy->d_full[m][db]);
                     }
+                    umma_commit(&sy->a_free[m][j & 1]);
+                }
+                if (w.pos == w.n_in_stage - 1) umma_commit(&sy->empty[s]);
+            }
+            // every MMA has completed before TMEM is released (bounded)
+            umma_commit(&sy->done);
+            wait_bar(&sy->done, 0, sy, a.err);
+        }
+    } else {
+        // ---------------- dequant + epilogue warpgroups ----------------
+        const int wid = warp - 2;                 // 0..7
+        const int mt = wid / 4;                   // M-tile of this warpgroup
+        const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+        const int row = quarter * 32 + lane;      // weight row within the M-tile
+        const uint32_t tl = uint32_t(quarter * 32) << 16;
+        const size_t ysz = a.mode == kSwiGluBf16 ? sizeof(__nv_bfloat16) : sizeof(float);
+        void *yb = static_cast<char *>(a.y) + (long long)u * a.y_stride * (long long)ysz;
+
+        if (mt == 0) {  // the constant A block: -24 in every lane
+            uint32_t cv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cv[i] = kBf16Neg24x2;
+            tmem_st_x8(tbase + tl + kColConst, cv);
+            tmem_wait_st();
+        }
+
+        float acc[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) acc[r] = 0.f;
+        float sc_prev[NG];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) sc_prev[g] = 0.f;
+        long long prev_gi = -1, prev_seg_b = 0, prev_seg_e = 0;
+        bool ok = true;
+
+        // Reads back the group partials of iteration jj.
+        auto readback = [&](int jj) {
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+                const int gi = jj * NG + g;
+                const int db = gi % (2 * NG);
+                if (ok) ok = wait_bar(&sy->d_full[mt][db], uint32_t(gi / (2 * NG)) & 1, sy, a.err);
+                tc_fence_after();
+                uint32_t d[16];
+                tmem_ld_x16(tbase + tl + kColD + uint32_t(mt * 2 * NG + db) * 16, d);
+                tmem_wait_ld();
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) acc[r] = fmaf(sc_prev[g], __uint_as_float(d[r]), acc[r]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sy->d_free[mt][db]);
+            }
+        };
+
+        // Publishes the segment ending with iteration gi_last.
+        auto finish_segment = [&](long long gi_last, long long sb, long long se) {
+            const int t = int(gi_last / a.Kc);
+            const long long tb = (long long)t * a.Kc, te = tb + a.Kc;
+            if (sb == tb && se == te) {
+                store_row(a, yb, t, mt, quarter, lane, acc);
+            } else {
+                // stream-K partial: publish; the last arriver sums every
+                // segment of this tile in ascending k order
+                const int which = (t == int(i0 / a.Kc)) ? 0 : 1;
+                float4 *slot = a.partials +
+                               ((((long long)u * a.Pv + vp) * 2 + which) * kDequantWarps + wid) * 128 + lane * 4;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    __stcg(slot + q, make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
                 __threadfence();
                 __syncwarp();
                 const int p_lo = int(((tb + 1) * a.Pv - 1) / tot);
@@ -312,122 +349,172 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 int nseg = 0;
                 for (int p2 = p_lo; p2 <= p_hi; ++p2)
                     if ((long long)p2 * tot / a.Pv < (long long)(p2 + 1) * tot / a.Pv) ++nseg;
-                unsigned *ctr = a.counters + ((long long)u * a.T + t) * kBlocks + b;
+                unsigned *ctr = a.counters + ((long long)u * a.T + t) * kDequantWarps + wid;
                 unsigned old = 0;
                 if (lane == 0) old = atomicAdd(ctr, 1u);
                 old = __shfl_sync(0xFFFFFFFFu, old, 0);
                 if (old == unsigned(nseg - 1)) {
                     __threadfence();
-                    float sum[4][2][4];
+                    float sum[kRows];
 #pragma unroll
-                    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                        for (int n = 0; n < 2; ++n)
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) sum[mt][n][c] = 0.f;
-                    for (int p2 = p_lo; p2 <= p_hi; ++p2) {
-                        const long long r0 = (long long)p2 * tot / a.Pv;
-                        const long long r1 = (long long)(p2 + 1) * tot / a.Pv;
-                        if (r0 >= r1) continue;
-                        const int which2 = (t == int(r0 / a.Kc)) ? 0 : 1;
-                        const float4 *src =
-                            a.partials + ((((long long)u * a.Pv + p2) * 2 + which2) * kBlocks + b) * 256;
-#pragma unroll
-                        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                            for (int n = 0; n < 2; ++n) {
-                                if (n == 1 && !hi) continue;
-                                const float4 v = __ldcg(src + (mt * 2 + n) * 32 + lane);
-                                sum[mt][n][0] += v.x;
-                                sum[mt][n][1] += v.y;
-                                sum[mt][n][2] += v.z;
-                                sum[mt][n][3] += v.w;
+                    for (int r = 0; r < kRows; ++r) sum[r] = 0.f;
+                    int p2 = p_lo;
+                    while (p2 <= p_hi) {
+                        // up to 4 segments' loads in flight, summed in k order
+                        const float4 *src[4];
+                        int ns = 0;
+                        while (ns < 4 && p2 <= p_hi) {
+                            const long long r0 = (long long)p2 * tot / a.Pv;
+                            const long long r1 = (long long)(p2 + 1) * tot / a.Pv;
+                            if (r0 < r1) {
+                                const int w2 = (t == int(r0 / a.Kc)) ? 0 : 1;
+                                src[ns++] = a.partials +
+                                            ((((long long)u * a.Pv + p2) * 2 + w2) * kDequantWarps + wid) * 128 +
+                                            lane * 4;
                             }
+                            ++p2;
+                        }
+                        float4 v[4][4];
+#pragma unroll
+                        for (int s2 = 0; s2 < 4; ++s2)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                v[s2][q] = s2 < ns ? __ldcg(src[s2] + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                        for (int s2 = 0; s2 < 4; ++s2) {
+                            if (s2 >= ns) continue;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                sum[4 * q] += v[s2][q].x;
+                                sum[4 * q + 1] += v[s2][q].y;
+                                sum[4 * q + 2] += v[s2][q].z;
+                                sum[4 * q + 3] += v[s2][q].w;
+                            }
+                        }
                     }
                     if (lane == 0) *ctr = 0u;  // leave the counter zero for the next launch
-                    store_tile(a, yb, t, b, gq, tq, hi, sum);
+                    store_row(a, yb, t, mt, quarter, lane, sum);
                 }
             }
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) acc[r] = 0.f;
+        };
+
+        Walk w;
+        walk_begin(w, i0, i1, a.Kc);
+        for (int j = 0; j < n_it; ++j, walk_next(w, i1, a.Kc)) {
+            const int s = w.st % kStages;
+            if (w.pos == 0 && ok) ok = wait_bar(&sy->full[s], uint32_t(w.st / kStages) & 1, sy, a.err);
+            const uint8_t *blk = sw + s * STW + w.pos * CB + mt * MB;
+            const uint4 c0 = *reinterpret_cast<const uint4 *>(blk + row * 16);
+            const uint4 c1 = *reinterpret_cast<const uint4 *>(blk + 2048 + row * 16);
+            float sc[NG];
+#pragma unroll
+            for (int g = 0; g < NG; ++g) sc[g] = half_at(blk + 4096 + (row * NG + g) * 2);
+            __syncwarp();
+            if (w.pos == w.n_in_stage - 1 && lane == 0) mbar_arrive(&sy->empty[s]);
+            uint32_t v[32];
+            dequant_slice(c0, c1, v);
+            if (j >= 2 && ok) ok = wait_bar(&sy->a_free[mt][j & 1], uint32_t((j >> 1) - 1) & 1, sy, a.err);
+            tc_fence_after();
+            tmem_st_x32(tbase + tl + kColA + uint32_t(mt * 2 + (j & 1)) * 32, v);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sy->a_full[mt][j & 1]);
+            // software pipeline: fold in the previous slice while this one multiplies
+            if (j > 0) {
+                readback(j - 1);
+                if (prev_gi + 1 == prev_seg_e) finish_segment(prev_gi, prev_seg_b, prev_seg_e);
+            }
+#pragma unroll
+            for (int g = 0; g < NG; ++g) sc_prev[g] = sc[g];
+            prev_gi = w.gi;
+            prev_seg_b = w.seg_b;
+            prev_seg_e = w.seg_e;
         }
-        i = seg_e;
+        readback(n_it - 1);
+        finish_segment(prev_gi, prev_seg_b, prev_seg_e);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, kTmemCols);
     }
 }
 
 // ---- load-time repack: canonical [N][K/2] nibbles + [N][K/G] fp16 -> kernel layout
-// Canonical row of packed feature p (interleave: gate/up pairs per 32 features).
+// Canonical row of packed feature p (interleave: per 32-row warp slice, 16 gate
+// rows then the 16 matching up rows).
 __device__ __forceinline__ long long canonical_row(long long p, int N, bool inter) {
     if (!inter) return p < N ? p : -1;
     const int F = N / 2;
     const long long t = p / kTileN;
-    const int w = int(p % kTileN);
-    const int b = w / 64, mt = (w % 64) / 16, row = w % 16;
-    const long long j = t * (kTileN / 2) + b * 32 + (mt >> 1) * 16 + row;
+    const int wtile = int(p % kTileN);
+    const int mt = wtile / kMTile, row = wtile % kMTile;
+    const int quarter = row / 32, lane = row % 32;
+    const long long j = t * (kTileN / 2) + mt * (kMTile / 2) + quarter * 16 + (lane & 15);
     if (j >= F) return -1;
-    return (mt & 1) ? F + j : j;
+    return lane < 16 ? j : F + j;
 }
 
 template <int G>
 __global__ void pack_codes_kernel(const uint8_t *codes, int K, int N, uint8_t *out, long long n_entries, int Kc,
                                   bool inter) {
+    constexpr int MB = mtile_bytes(G);
     constexpr int CB = chunk_bytes(G);
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= n_entries) return;
-    const int lane = int(idx % 32);
-    long long r = idx / 32;
-    const int mt = int(r % 4);
-    r /= 4;
-    const int b = int(r % kBlocks);
-    r /= kBlocks;
+    const int row = int(idx % kMTile);
+    long long r = idx / kMTile;
+    const int half = int(r % 2);
+    r /= 2;
+    const int mt = int(r % kMTiles);
+    r /= kMTiles;
     const int kc = int(r % Kc);
     const long long t = r / Kc;
-    const int gq = lane >> 2, tq = lane & 3;
+    const long long f = canonical_row(t * kTileN + mt * kMTile + row, N, inter);
     uint32_t words[4];
-    for (int j = 0; j < 4; ++j) {
+    for (int e = 0; e < 4; ++e) {
         uint32_t w = 0;
-        for (int i = 0; i < 4; ++i)
-            for (int h = 0; h < 2; ++h) {
-                const long long f =
-                    canonical_row(t * kTileN + b * 64 + mt * 16 + gq + ((i & 1) ? 8 : 0), N, inter);
-                const int k = kc * kKChunk + j * 16 + 2 * tq + h + ((i & 2) ? 8 : 0);
-                uint32_t nib = 0;  // code 0
-                if (f >= 0) {
-                    const uint8_t byte = codes[f * (K / 2) + k / 2];
-                    nib = (k & 1) ? (byte >> 4) : (byte & 0xF);
-                }
-                w |= ((nib ^ 8u) & 0xFu) << (4 * i + 16 * h);   // two's complement -> offset binary
+        for (int q = 0; q < 8; ++q) {
+            const int k = kc * kKChunk + half * 32 + e * 8 + q;
+            uint32_t nib = 0;  // code 0
+            if (f >= 0) {
+                const uint8_t byte = codes[f * (K / 2) + k / 2];
+                nib = (k & 1) ? (byte >> 4) : (byte & 0xF);
             }
-        words[j] = w;
+            w |= ((nib ^ 8u) & 0xFu) << (4 * (q / 2) + 16 * (q % 2));   // two's complement -> offset binary
+        }
+        words[e] = w;
     }
-    uint8_t *dst = out + ((t * Kc + kc) * kBlocks + b) * (long long)CB + (mt * 32 + lane) * 16;
+    uint8_t *dst = out + (t * Kc + kc) * (long long)CB + mt * MB + half * 2048 + row * 16;
     *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
 }
 
 template <int G>
 __global__ void pack_scales_kernel(const uint16_t *scales, int K, int N, uint8_t *out, long long n_entries, int Kc,
                                    bool inter) {
+    constexpr int MB = mtile_bytes(G);
     constexpr int CB = chunk_bytes(G);
     constexpr int NG = kKChunk / G;
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= n_entries) return;
-    const int mt = int(idx % 4);
-    long long r = idx / 4;
-    const int g = int(r % 8);
-    r /= 8;
-    const int grp = int(r % NG);
-    r /= NG;
-    const int b = int(r % kBlocks);
-    r /= kBlocks;
+    const int g = int(idx % NG);
+    long long r = idx / NG;
+    const int row = int(r % kMTile);
+    r /= kMTile;
+    const int mt = int(r % kMTiles);
+    r /= kMTiles;
     const int kc = int(r % Kc);
     const long long t = r / Kc;
-    const long long p = t * kTileN + b * 64 + mt * 16 + g;
-    const long long f_lo = canonical_row(p, N, inter);
-    const long long f_hi = canonical_row(p + 8, N, inter);
-    const int gi = kc * NG + grp;
+    const long long f = canonical_row(t * kTileN + mt * kMTile + row, N, inter);
     const int ngroups = K / G;
-    const uint32_t lo = f_lo >= 0 ? scales[f_lo * ngroups + gi] : 0u;
-    const uint32_t hi = f_hi >= 0 ? scales[f_hi * ngroups + gi] : 0u;
-    uint8_t *dst = out + ((t * Kc + kc) * kBlocks + b) * (long long)CB + 2048 + grp * 128 + g * 16 + mt * 4;
-    *reinterpret_cast<uint32_t *>(dst) = lo | (hi << 16);
+    const uint16_t v = f >= 0 ? scales[f * ngroups + kc * NG + g] : uint16_t(0);
+    uint8_t *dst = out + (t * Kc + kc) * (long long)CB + mt * MB + 4096 + (row * NG + g) * 2;
+    *reinterpret_cast<uint16_t *>(dst) = v;
 }
 
 template <int G>
@@ -446,14 +533,27 @@ cudaError_t launch_pack_g(const uint8_t *codes, const uint16_t *scales, int K, i
                           cudaStream_t s) {
     const int T = (N + kTileN - 1) / kTileN;
     const int Kc = K / kKChunk;
-    const long long n_codes = (long long)T * Kc * kBlocks * 4 * 32;
-    const long long n_scales = (long long)T * Kc * kBlocks * (kKChunk / G) * 8 * 4;
+    const long long n_codes = (long long)T * Kc * kMTiles * 2 * kMTile;
+    const long long n_scales = (long long)T * Kc * kMTiles * kMTile * (kKChunk / G);
     const int th = 256;
-    pack_codes_kernel<G><<<unsigned((n_codes + th - 1) / th), th, 0, s>>>(codes, K, N, (uint8_t *)packed, n_codes, Kc,
-                                                                                        inter);
-    pack_scales_kernel<G><<<unsigned((n_scales + th - 1) / th), th, 0, s>>>(scales, K, N, (uint8_t *)packed, n_scales,
-                                                                           Kc, inter);
+    pack_codes_kernel<G><<<unsigned((n_codes + th - 1) / th), th, 0, s>>>(codes, K, N, (uint8_t *)packed, n_codes,
+                                                                        Kc, inter);
+    pack_scales_kernel<G><<<unsigned((n_scales + th - 1) / th), th, 0, s>>>(scales, K, N, (uint8_t *)packed,
+                                                                          n_scales, Kc, inter);
     return cudaGetLastError();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
 }
 
 }  // namespace
@@ -471,6 +571,30 @@ void gemm_bind_workspace(GemmArgs &a, void *ws, int u_max) {
     a.err = reinterpret_cast<int *>(base);
     a.counters = reinterpret_cast<unsigned *>(base + 256);
     a.partials = reinterpret_cast<float4 *>(base + 256 + kCounterBytes);
+}
+
+bool gemm_encode_x(GemmArgs &a, const uint16_t *x, int ldx, long long x_stride, int u_max, const char **why) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) {
+        *why = "cuTensorMapEncodeTiled is unavailable";
+        return false;
+    }
+    const bool per = x_stride != 0 && u_max > 1;
+    // dims (innermost first): k within a 64-wide slice, row, slice, problem
+    cuuint64_t dims[4] = {cuuint64_t(kKChunk), cuuint64_t(a.R), cuuint64_t(a.Kc), cuuint64_t(per ? u_max : 1)};
+    cuuint64_t strides[3] = {cuuint64_t(ldx) * 2, cuuint64_t(kKChunk) * 2,
+                             per ? cuuint64_t(x_stride) * 2 : cuuint64_t(ldx) * 2 * cuuint64_t(a.R)};
+    cuuint32_t box[4] = {cuuint32_t(kKChunk), cuuint32_t(kRows), cuuint32_t(kStageIters), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(&a.xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(x), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    a.x_per_problem = per ? 1 : 0;
+    if (r != CUDA_SUCCESS) {
+        *why = "cuTensorMapEncodeTiled rejected the activation layout";
+        return false;
+    }
+    return true;
 }
 
 cudaError_t launch_w4_gemm(const GemmArgs &a, int u_max, cudaStream_t s) {

@@ -2,44 +2,44 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace tfk {
 
 // ---- packed weight layout --------------------------------------------------
-// A "tile" is 256 output features = 4 feature blocks of 64.  For every tile t
-// and every 64-wide slice kc of the input features there is one contiguous
-// "stage" of 4 chunks (one per feature block).  A chunk holds
-//   codes : [mt 0..3][lane 0..31][4 x u32]   2048 B
-//   scales: [grp][g 0..7][mt 0..3] half2     128 B per group (64/G groups)
-// Lane (g = lane/4, q = lane%4) of a warp owns, for the 16-feature sub-tile mt
-// and the 16-wide k step j, the 32-bit word j of its 16-byte entry.  Its nibble
-// i (bits 4i..4i+3) / 16+4i.. holds, as offset-binary (code + 8):
-//   i=0: (f=g,   k=2q | 2q+1)      i=1: (f=g+8, k=2q | 2q+1)
-//   i=2: (f=g,   k=2q+8 | 2q+9)    i=3: (f=g+8, k=2q+8 | 2q+9)
-// low half = the even k, high half = the odd k: exactly the m16n8k16 A
-// fragment, so one LOP3 per register turns it into bf16 (128 + u).
-constexpr int kBlocks = 4;                 // feature blocks per tile
-constexpr int kTileN = 64 * kBlocks;       // 256
-constexpr int kKChunk = 64;                // k per stage
-constexpr int kKGroups = 2;                // consumer warp groups splitting the stages
-constexpr int kConsumerWarps = kBlocks * kKGroups;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one producer warp
-constexpr int kStages = 14;
-constexpr int kXRowStride = 144;           // staged activation row: 128 B + 16 B pad (conflict-free ldmatrix)
-constexpr int kXStageBytes = 16 * kXRowStride;
-constexpr int kMaxRows = 16;
+// Output features are grouped in tiles of 256 = two "M-tiles" of 128 rows (one
+// tcgen05 MMA's M).  For every tile t and every 64-wide slice kc of the input
+// features there is one contiguous "chunk", and consecutive kc of a tile are
+// consecutive in memory, so any run of iterations of one tile is one bulk copy.
+// A chunk is two M-tile blocks; an M-tile block holds
+//   codes : [half 0..1][row 0..127][16 B]   4096 B   row's k = 32*half .. +31
+//   scales: [row 0..127][64/G] fp16          256 B per group
+// Inside a row's 16 bytes, word e (k = 32*half + 8*e .. +7, e = 0..3) keeps the
+// code of k offset q (0..7) as offset binary (code + 8) at bits
+// 4*(q/2) + 16*(q%2): one shift + LOP3 per pair turns it into bf16 (16 + u).
+constexpr int kMTile = 128;                // rows per tcgen05 MMA (M)
+constexpr int kMTiles = 2;                 // M-tiles per tile
+constexpr int kTileN = kMTile * kMTiles;   // 256 output features per tile
+constexpr int kKChunk = 64;                // k per iteration
+constexpr int kRows = 16;                  // MMA N: verify rows, zero-padded
+constexpr int kStageIters = 4;             // iterations per pipeline stage (one weight copy of ~35 KB)
+constexpr int kStages = 4;
+constexpr int kDequantWarps = 8;           // two warpgroups, one per M-tile
+constexpr int kThreads = 32 * (2 + kDequantWarps);  // producer + MMA + dequant/epilogue warps
+constexpr int kXSliceBytes = kRows * kKChunk * 2;   // [16 rows][64 k] bf16, 128-byte swizzled
+constexpr int kXStageBytes = kStageIters * kXSliceBytes;
 
-__host__ __device__ constexpr int chunk_bytes(int G) { return 2048 + 128 * (kKChunk / G); }
-__host__ __device__ constexpr int stage_w_bytes(int G) { return kBlocks * chunk_bytes(G); }
-// Per consumer warp: 4 sub-tiles x 2 row-halves x 32 lanes x float4.
-constexpr int kWarpAccFloats = 4 * 2 * 32 * 4;
-constexpr size_t kSlotBytes = size_t(kBlocks) * kWarpAccFloats * 4;   // one partial tile, 16 KB
+__host__ __device__ constexpr int mtile_bytes(int G) { return 4096 + 256 * (kKChunk / G); }
+__host__ __device__ constexpr int chunk_bytes(int G) { return kMTiles * mtile_bytes(G); }
+// One partial tile of the split-K fixup: 8 warps x 32 lanes x 16 floats.
+constexpr size_t kSlotBytes = size_t(kDequantWarps) * 32 * kRows * 4;
 
 inline size_t gemm_smem_bytes(int G) {
-    return size_t(kStages) * (stage_w_bytes(G) + kXStageBytes)   // weight + activation stages
-           + size_t(kBlocks) * kWarpAccFloats * 4                 // cross-group reduction buffer
-           + size_t(2 * kStages) * 8;                             // full / empty barriers
+    return 1024                                                         // alignment slack
+           + size_t(kStages) * kXStageBytes                             // activation slices (1024-B aligned)
+           + size_t(kStages) * kStageIters * chunk_bytes(G)            // weight stages
+           + 256;                                                       // barriers, TMEM base
 }
 
 inline bool packed_shape_ok(int K, int N, int G) {
@@ -48,16 +48,16 @@ inline bool packed_shape_ok(int K, int N, int G) {
 inline size_t packed_bytes(int K, int N, int G) {
     if (!packed_shape_ok(K, N, G)) return 0;
     size_t T = (size_t(N) + kTileN - 1) / kTileN;
-    return T * size_t(K / kKChunk) * size_t(stage_w_bytes(G));
+    return T * size_t(K / kKChunk) * size_t(chunk_bytes(G));
 }
 
 // ---- launch description ------------------------------------------------------
 // A launch runs U problems (U = 1 for a plain linear layer; U = touched experts
 // for the MoE layer).  Problem u uses weights at w + expert(u) * w_stride,
-// activations x + u * x_stride and writes y + u * y_stride.  Each problem's
-// tile x k-slice iteration space is cut into Pv contiguous ranges ("virtual
-// CTAs", stream-K style); the cut depends only on (T, Kc, Pv).
-// Epilogue of a launch.
+// activations from the tensor map (problem coordinate u when x_per_problem)
+// and writes y + u * y_stride.  Each problem's tile x k-slice iteration space
+// is cut into Pv contiguous ranges ("virtual CTAs", stream-K style); the cut
+// depends only on (T, Kc, Pv).
 enum EpilogueMode : int {
     kStoreF32 = 0,      // y (fp32) = result
     kAccumulateF32 = 1, // y (fp32) += result          (residual update)
@@ -65,13 +65,12 @@ enum EpilogueMode : int {
 };
 
 struct GemmArgs {
+    CUtensorMap xmap;          // activations: dims {64, R, K/64, U}, box {64, 16, kStageIters, 1}, 128B swizzle
     const uint8_t *w;
     long long w_stride;        // bytes between experts
     const int *expert_ids;     // dev [U_max] or nullptr (expert = u)
     const int *n_problems;     // dev count or nullptr (1)
-    const uint16_t *x;
-    long long x_stride;        // elements between problems
-    int ldx;
+    int x_per_problem;         // activations differ per problem (use coordinate u)
     void *y;                   // fp32, or bf16 for kSwiGluBf16
     long long y_stride;        // elements between problems
     int ldy;
@@ -79,8 +78,8 @@ struct GemmArgs {
     int F;                     // kSwiGluBf16: width of h (N = 2F)
     int R, K, N, G;
     int T, Kc, Pv;
-    unsigned *counters;        // [U_max][T][kBlocks], zero between launches
-    float4 *partials;          // [U_max][Pv][2][kBlocks][8][32]
+    unsigned *counters;        // [U_max][T][kDequantWarps], zero between launches
+    float4 *partials;          // [U_max][Pv][2][kDequantWarps][32][4]
     int *err;
 };
 
@@ -92,12 +91,15 @@ struct GemmArgs {
 constexpr size_t kCounterBytes = size_t(1) << 18;      // 65536 counters
 constexpr size_t kMaxCounters = kCounterBytes / sizeof(unsigned);
 size_t gemm_workspace_bytes(int K, int N, int G, int u_max, int Pv);
-// Fills counters/partials pointers inside `a` from a workspace region.
 void gemm_bind_workspace(GemmArgs &a, void *ws, int u_max);
+// Encodes a.xmap for activations x (bf16) [U][R][ldx] with problem stride
+// x_stride elements (0: shared by all problems).  Returns false (with a message)
+// if the driver rejects the description.
+bool gemm_encode_x(GemmArgs &a, const uint16_t *x, int ldx, long long x_stride, int u_max, const char **why);
 cudaError_t launch_w4_gemm(const GemmArgs &a, int u_max, cudaStream_t s);
 // interleave_gate_up: rows [0, N/2) are gate rows, [N/2, N) up rows; they are
-// packed so that each 32-feature group holds 16 gate rows then the 16 matching
-// up rows (the layout kSwiGluBf16 expects).
+// packed so that lanes 0-15 of every 32-row warp slice hold 16 gate rows and
+// lanes 16-31 the matching up rows (the layout kSwiGluBf16 expects).
 cudaError_t launch_pack_w4(const uint8_t *codes, const uint16_t *scales, int K, int N, int G, void *packed,
                            bool interleave_gate_up, cudaStream_t s);
 int device_sm_count();
