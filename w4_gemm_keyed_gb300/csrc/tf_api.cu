@@ -153,7 +153,7 @@ tf_status check_moe(const tf_moe_layer *L) {
     {
         const size_t T = size_t((2 * size_t(L->ffn > 0 ? L->ffn : 0) + kTileN - 1) / kTileN) +
                          size_t((L->hidden > 0 ? L->hidden : 0) + kTileN - 1) / kTileN;
-        if (T * kDequantWarps * size_t(kMaxExperts) > kMaxCounters)
+        if (T * kFeatWarps * size_t(kMaxExperts) > kMaxCounters)
             return fail(TF_ERR_UNSUPPORTED, "MoE layer too large for the split-K counter region");
     }
     if (!L->gate_up || !L->down) return fail(TF_ERR_INVALID_ARG, "null MoE weights");
@@ -218,8 +218,8 @@ tf_status check_model(const tf_model *m) {
     if (m->lm_head.K != m->hidden || m->lm_head.N != m->vocab)
         return fail(TF_ERR_INVALID_ARG, "lm_head shape does not match the model");
     if (m->hidden % kKChunk || m->ffn % kKChunk) return fail(TF_ERR_UNSUPPORTED, "hidden, ffn must be multiples of 64");
-    if (size_t((m->vocab + kTileN - 1) / kTileN) * kDequantWarps > kMaxCounters ||
-        size_t((2 * size_t(m->ffn) + kTileN - 1) / kTileN) * kDequantWarps > kMaxCounters)
+    if (size_t((m->vocab + kTileN - 1) / kTileN) * kFeatWarps > kMaxCounters ||
+        size_t((2 * size_t(m->ffn) + kTileN - 1) / kTileN) * kFeatWarps > kMaxCounters)
         return fail(TF_ERR_UNSUPPORTED, "model too large for the split-K counter region");
     return TF_OK;
 }
@@ -321,7 +321,7 @@ tf_status tf_lane_gemm_w4(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx,
     if (!y || !aligned(y, 4)) return fail(TF_ERR_INVALID_ARG, "y must be non-null and 4-B aligned");
     if (ldy < W->N) return fail(TF_ERR_INVALID_ARG, "ldy=%d must be >= N", ldy);
     if ((st = check_ws(ws, ws_bytes, dense_gemm_ws(*W)))) return st;
-    if (size_t((W->N + kTileN - 1) / kTileN) * kDequantWarps > kMaxCounters)
+    if (size_t((W->N + kTileN - 1) / kTileN) * kFeatWarps > kMaxCounters)
         return fail(TF_ERR_UNSUPPORTED, "N=%d too large for the split-K counter region", W->N);
     GemmArgs a = dense_args(*W, R, y, ldy, kStoreF32);
     const char *why = "";

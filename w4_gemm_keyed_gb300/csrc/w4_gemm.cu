@@ -1,35 +1,34 @@
-// W4 lane GEMM for the speculative-decoding verify pass (sm_103a, tcgen05).
+// W4 lane GEMM for the speculative-decoding verify pass (sm_103a).
 //
 // TensorFold README, "A row of a multi-row verify pass gets the same bits as a
 // one-row step": up to 16 drafted rows share one launch that streams every
 // 4-bit weight once, and row r's bits never depend on how many rows there are.
 //
-// One CTA per SM, 10 warps:
-//   warp 0  producer: per pipeline stage (up to 4 consecutive 64-wide k slices
-//           of one 256-feature tile, never crossing a tile boundary) lane 0
+// One CTA per SM, 17 warps:
+//   warp 16 producer: per pipeline stage (up to 4 consecutive 64-wide k slices
+//           of one 256-feature tile, never crossing a tile boundary) one lane
 //           issues ONE bulk TMA copy of the packed weights (~35 KB, L2
-//           evict-first) and ONE 4-D tensor TMA of the activation slices
+//           evict-first; the bulk engine only reaches HBM rate with copies of
+//           this size) and ONE 4-D tensor TMA of the activation slices
 //           ([16 rows][64 k] bf16 each, 128-byte swizzled, rows >= R
 //           zero-filled by the copy engine's out-of-bounds fill).
-//   warp 1  MMA issuer (lane 0) and TMEM owner.  For each slice and M-tile it
-//           issues tcgen05.mma kind::f16, M=128 (weight rows), N=16 (verify
-//           rows), K=16, A from tensor memory, B (activations) from shared
-//           memory, fp32 accumulator in tensor memory.
-//   warps 2-9  two warpgroups, one per 128-row M-tile.  Each thread owns one
-//           weight row: it turns the row's 64 packed codes of a slice into
-//           bf16 (16 + u, u = code + 8; exact) with one shift + LOP3 per pair, stores
-//           them to tensor memory as the MMA's A operand, and later reads back
-//           the group's fp32 partial sums (tcgen05.ld) and folds them in as
+//   warps 0-15 consumers: warp (kg, fw) owns the 32 weight rows of feature
+//           block fw and the iterations of parity kg.  Per 16-wide k step it
+//           turns one packed 32-bit word per 16-row sub-tile into the m16n8k16
+//           A fragment (shift + LOP3 + bf16x2 FMA per register: exact integer
+//           codes -8..7), loads the activation B fragment with a swizzle-aware
+//           ldmatrix and issues one mma.sync per 8 rows.  Each quantisation
+//           group's partial is formed in a fresh fp32 fragment and folded in as
 //           acc = fma(scale, partial, acc).
-// Exactness: the A operand holds 16 + u; for every k step a second MMA adds
-// (-24) x the same activations from a constant A block, so the tensor core
-// accumulates  sum (16 + u - 24) x = sum code * x  of the group; every product
-// is exact and the partial carries only the fp32 accumulation error (the bias
-// of 24 is the smallest this OR-into-the-mantissa conversion allows: u sits in
-// mantissa bits 3..6 under the implicit leading one of 16).
-// Row invariance: rows are MMA columns (N = 16 for every R); the cut of the
-// iteration space, the stage schedule and the fixed-order split-K sums depend
-// on (T, Kc, Pv) only.
+// Why mma.sync and not tcgen05: the verify pass multiplies a weight tile by at
+// most 16 rows, so the MMA's N is 16.  A tcgen05.mma (M=128, K=16) was measured
+// on this part at ~153 cycles per instruction whatever its N (16..256), i.e.
+// ~13 weights/cycle/SM at N=16 against the ~45 the HBM stream delivers; the
+// register-operand m16n8k16 path processes ~68 weights/cycle/SM.
+// Row invariance: rows are MMA columns (a column's result depends only on its
+// own activations; the rows 8..15 MMA is skipped when R <= 8), and the cut of
+// the iteration space, the stage schedule, the k-parity split and the
+// fixed-order split-K sums depend on (T, Kc, Pv) only.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
@@ -41,43 +40,30 @@ namespace tfk {
 
 namespace {
 
-constexpr uint32_t kNibMask = 0x00780078u;    // mantissa bits 3..6 of both bf16 halves
-constexpr uint32_t kBf16Magic = 0x41804180u;  // (16, 16): u in mantissa bits 3..6 gives 16 + u
-constexpr uint32_t kBf16Neg24x2 = 0xC1C0C1C0u;  // (-24, -24)
-// tcgen05 instruction descriptor, kind::f16: D fp32, A bf16, B bf16, both
-// K-major, N = 16, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t(kRows) >> 3) << 17) |
-                            ((uint32_t(kMTile) >> 4) << 24);
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColA = 0;        // A buffers: [mt][2] x 32 columns
-constexpr uint32_t kColConst = 128;  // 8 columns of -24
-constexpr uint32_t kColD = 160;      // D buffers: [mt][2*NG] x 16 columns
+constexpr uint32_t kBf16One2 = 0x3F803F80u;     // (1.0, 1.0)
+constexpr uint32_t kBf16Neg136x2 = 0xC308C308u; // (-136, -136)
+constexpr uint32_t kNibMask = 0x000F000Fu;
+constexpr uint32_t kBf16Magic = 0x43004300u;    // (128, 128): OR-ing u in gives 128 + u
 
-__device__ __forceinline__ float half_at(const uint8_t *p) {
-    return __half2float(*reinterpret_cast<const __half *>(p));
+__device__ __forceinline__ uint32_t word_of(const uint4 &q, int j) {
+    return j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
 }
 
-// Shared-memory descriptor of a [16 rows][64 k] bf16 slice, K-major, 128-byte
-// swizzle (8-row atoms of 1024 B), starting `koff` bytes into each row.
-__device__ __forceinline__ uint64_t x_desc(uint32_t slice_smem, uint32_t koff) {
-    const uint32_t start = (slice_smem + koff) >> 4;
-    return uint64_t(start & 0x3FFFu) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) |
-           (uint64_t(2) << 61);
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
+
+__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))); }
+__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
 
 struct Sync {
     uint64_t full[kStages];
     uint64_t empty[kStages];
-    uint64_t a_full[kMTiles][2];
-    uint64_t a_free[kMTiles][2];
-    uint64_t d_full[kMTiles][4];
-    uint64_t d_free[kMTiles][4];
-    uint64_t done;
-    uint32_t tmem_base;
     int abort;
 };
 
-// Bounded wait that gives up at once after any wait of this CTA timed out.
+// Bounded wait: non-suspending polls for short hand-offs, then try_wait; gives
+// up at once after any wait of this CTA timed out.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Sync *sy, int *err) {
     for (uint32_t i = 0; i < kSpinPolls; ++i)
         if (mbar_test_wait(bar, parity)) return true;
@@ -90,85 +76,117 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Sync *s
     return false;
 }
 
-// Iteration-space walker shared by every role so all agree on the schedule:
-// segments end at tile boundaries, stages are runs of <= kStageIters
-// iterations from the segment start.
-struct Walk {
-    long long gi;     // global iteration index (tile * Kc + kc)
-    long long seg_b, seg_e;
-    int pos;          // position inside the stage
-    int st;           // stage counter
-    int n_in_stage;
-};
-
-__device__ __forceinline__ void walk_begin(Walk &w, long long i0, long long i1, int Kc) {
-    w.gi = i0;
-    w.seg_b = i0;
-    w.seg_e = min(i1, (i0 / Kc + 1) * (long long)Kc);
-    w.pos = 0;
-    w.st = 0;
-    w.n_in_stage = int(min((long long)kStageIters, w.seg_e - w.seg_b));
-}
-
-__device__ __forceinline__ void walk_next(Walk &w, long long i1, int Kc) {
-    ++w.gi;
-    if (w.gi == w.seg_e) {
-        w.seg_b = w.gi;
-        w.seg_e = min(i1, (w.gi / Kc + 1) * (long long)Kc);
-    }
-    const int pos = int((w.gi - w.seg_b) % kStageIters);
-    if (pos == 0) {
-        ++w.st;
-        w.n_in_stage = int(min((long long)kStageIters, w.seg_e - w.gi));
-    }
-    w.pos = pos;
-}
-
-__device__ __forceinline__ void dequant_slice(const uint4 &c0, const uint4 &c1, uint32_t (&v)[32]) {
-    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+// One 64-wide k slice of one 32-row feature block for this warp.
+template <int G>
+__device__ __forceinline__ void consume_slice(const uint8_t *blk, uint32_t xslice, int lane, int gq, int lrow,
+                                              int lcol, bool hi, float (&acc)[2][2][4]) {
+    constexpr int NG = kKChunk / G;
+    constexpr int KS = G / 16;
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + lane * 16);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 512 + lane * 16);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        // pair p (bits 4p / 16+4p) moves to mantissa bits 3..6 of each half
-        v[4 * e + 0] = lop3_and_or(w[e] << 3, kNibMask, kBf16Magic);
+    for (int grp = 0; grp < NG; ++grp) {
+        const uint2 sv = *reinterpret_cast<const uint2 *>(blk + 1024 + grp * 64 + gq * 8);
+        float part[2][2][4];
 #pragma unroll
-        for (int p = 1; p < 4; ++p) v[4 * e + p] = lop3_and_or(w[e] >> (4 * p - 3), kNibMask, kBf16Magic);
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) part[mt][n][c] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            const int j = grp * KS + kk;
+            // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
+            const uint32_t xa = xslice + lrow * 128 + ((((2 * j + lcol) ^ (lrow & 7))) << 4);
+            uint32_t b0, b1, b2 = 0, b3 = 0;
+            if (hi)
+                ldsm_x4(xa, b0, b1, b2, b3);
+            else
+                ldsm_x2(xa, b0, b1);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const uint32_t w = word_of(mt ? q1 : q0, j);
+                uint32_t af[4];
+                af[0] = fma_bf16x2(lop3_and_or(w, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
+                af[1] = fma_bf16x2(lop3_and_or(w >> 4, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
+                af[2] = fma_bf16x2(lop3_and_or(w >> 8, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
+                af[3] = fma_bf16x2(lop3_and_or(w >> 12, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
+                mma_bf16_16816(part[mt][0], af, b0, b1);
+                if (hi) mma_bf16_16816(part[mt][1], af, b2, b3);
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            const uint32_t sw = mt ? sv.y : sv.x;
+            const float s_lo = half_lo(sw);   // row mt*16 + g
+            const float s_hi = half_hi(sw);   // row mt*16 + g + 8
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                if (n == 1 && !hi) continue;
+                acc[mt][n][0] = fmaf(s_lo, part[mt][n][0], acc[mt][n][0]);
+                acc[mt][n][1] = fmaf(s_lo, part[mt][n][1], acc[mt][n][1]);
+                acc[mt][n][2] = fmaf(s_hi, part[mt][n][2], acc[mt][n][2]);
+                acc[mt][n][3] = fmaf(s_hi, part[mt][n][3], acc[mt][n][3]);
+            }
+        }
     }
 }
 
-// Writes one thread's 16 results (its weight row, verify rows 0..15).
-__device__ __forceinline__ void store_row(const GemmArgs &a, void *yb, int t, int mt, int quarter, int lane,
-                                          const float (&v)[kRows]) {
+__device__ __forceinline__ void put(const GemmArgs &a, void *yb, int r, int f, float v) {
+    float *y = static_cast<float *>(yb) + (long long)r * a.ldy + f;
+    if (a.mode == kAccumulateF32)
+        *y = *y + v;
+    else
+        *y = v;
+}
+
+// Stores a lane's 16 results: element (mt, n, c) is weight row mt*16 + g (+8
+// for c >= 2) of the feature block and verify row n*8 + 2q + (c & 1).
+__device__ __forceinline__ void store_block(const GemmArgs &a, void *yb, int t, int fw, int gq, int tq, bool hi,
+                                            const float (&v)[2][2][4]) {
     if (a.mode == kSwiGluBf16) {
-        // lanes 0-15 hold gate rows, lanes 16-31 the matching up rows
-        const int j = t * (kTileN / 2) + mt * (kMTile / 2) + quarter * 16 + (lane & 15);
+        // sub-tile 0 holds gate rows, sub-tile 1 the matching up rows
         __nv_bfloat16 *h = static_cast<__nv_bfloat16 *>(yb);
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-            const float up = __shfl_down_sync(0xFFFFFFFFu, v[r], 16);
-            if (lane < 16 && j < a.F && r < a.R) {
-                const float g = v[r];
-                h[(long long)r * a.ldy + j] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * up);
+        for (int n = 0; n < 2; ++n) {
+            if (n == 1 && !hi) continue;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int j = t * (kTileN / 2) + fw * 16 + gq + (c >= 2 ? 8 : 0);
+                const int r = n * 8 + tq * 2 + (c & 1);
+                if (j < a.F && r < a.R) {
+                    const float g = v[0][n][c];
+                    const float up = v[1][n][c];
+                    h[(long long)r * a.ldy + j] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * up);
+                }
             }
         }
         return;
     }
-    const int f = t * kTileN + mt * kMTile + quarter * 32 + lane;
-    if (f >= a.N) return;
-    float *y = static_cast<float *>(yb);
+    const int f0 = t * kTileN + fw * kBlockRows;
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-        if (r < a.R) {
-            float *p = y + (long long)r * a.ldy + f;
-            *p = a.mode == kAccumulateF32 ? *p + v[r] : v[r];
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            if (n == 1 && !hi) continue;
+            const int f = f0 + mt * 16 + gq;
+            const int r = n * 8 + tq * 2;
+            if (f < a.N) {
+                if (r < a.R) put(a, yb, r, f, v[mt][n][0]);
+                if (r + 1 < a.R) put(a, yb, r + 1, f, v[mt][n][1]);
+            }
+            if (f + 8 < a.N) {
+                if (r < a.R) put(a, yb, r, f + 8, v[mt][n][2]);
+                if (r + 1 < a.R) put(a, yb, r + 1, f + 8, v[mt][n][3]);
+            }
         }
     }
 }
 
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_constant__ GemmArgs a) {
-    constexpr int NG = kKChunk / G;   // quantisation groups per slice
-    constexpr int KS = G / 16;        // k16 steps per group
-    constexpr int MB = mtile_bytes(G);
+    constexpr int BB = block_bytes(G);
     constexpr int CB = chunk_bytes(G);
     constexpr int STW = kStageIters * CB;
 
@@ -176,7 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sx = smem;                                  // [kStages][kXStageBytes], 1024-B aligned
     uint8_t *sw = sx + kStages * kXStageBytes;           // [kStages][STW]
-    Sync *sy = reinterpret_cast<Sync *>(sw + kStages * STW);
+    float *red = reinterpret_cast<float *>(sw + kStages * STW);   // [kFeatWarps][32][16]
+    Sync *sy = reinterpret_cast<Sync *>(red + kFeatWarps * 32 * kLaneAcc);
 
     const int u = blockIdx.y;
     const int nprob = a.n_problems ? *a.n_problems : 1;
@@ -193,155 +212,121 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sy->full[s], 1);
-            mbar_init(&sy->empty[s], kDequantWarps + 1);
+            mbar_init(&sy->empty[s], kConsumerWarps);
         }
-        for (int m = 0; m < kMTiles; ++m) {
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(&sy->a_full[m][b], 4);
-                mbar_init(&sy->a_free[m][b], 1);
-            }
-            for (int b = 0; b < 4; ++b) {
-                mbar_init(&sy->d_full[m][b], 1);
-                mbar_init(&sy->d_free[m][b], 4);
-            }
-        }
-        mbar_init(&sy->done, 1);
         sy->abort = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
-        tmem_alloc(&sy->tmem_base, kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = sy->tmem_base;
 
     const int e = a.expert_ids ? a.expert_ids[u] : u;
     const uint8_t *wb = a.w + (long long)e * a.w_stride;
 
-    if (warp == 0) {
+    if (warp == kConsumerWarps) {
         // ---------------- producer ----------------
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            Walk w;
-            walk_begin(w, i0, i1, a.Kc);
-            int issued = 0;
-            for (int j = 0; j < n_it; ++j, walk_next(w, i1, a.Kc)) {
-                if (w.pos != 0) continue;
-                const int s = w.st % kStages;
-                if (w.st >= kStages && !wait_bar(&sy->empty[s], uint32_t((w.st / kStages) - 1) & 1, sy, a.err))
-                    break;
-                mbar_arrive_expect_tx(&sy->full[s], uint32_t(w.n_in_stage * CB + kXStageBytes));
-                bulk_g2s_hint(sw + s * STW, wb + w.gi * CB, uint32_t(w.n_in_stage * CB), &sy->full[s], pol);
-                tma_load_4d(sx + s * kXStageBytes, &a.xmap, 0, 0, int(w.gi % a.Kc), a.x_per_problem ? u : 0,
-                            &sy->full[s]);
-                issued = w.st + 1;
+            int st = 0;
+            bool ok = true;
+            for (int j = 0; j < n_it && ok;) {
+                const long long gi = i0 + j;
+                const int kc0 = int(gi % a.Kc);
+                const int seg_len = min(n_it - j, a.Kc - kc0);
+                for (int sj = 0; sj < seg_len; sj += kStageIters, ++st) {
+                    const int n_here = min(kStageIters, seg_len - sj);
+                    const int s = st % kStages;
+                    if (st >= kStages && !wait_bar(&sy->empty[s], uint32_t(st / kStages - 1) & 1, sy, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sy->full[s], uint32_t(n_here * CB + kXStageBytes));
+                    bulk_g2s_hint(sw + s * STW, wb + (gi + sj) * CB, uint32_t(n_here * CB), &sy->full[s], pol);
+                    tma_load_4d(sx + s * kXStageBytes, &a.xmap, 0, 0, kc0 + sj, a.x_per_problem ? u : 0, &sy->full[s]);
+                }
+                j += seg_len;
             }
+            const int issued = st;
             // leave only once every issued copy has landed (bounded)
             for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
                 wait_bar(&sy->full[k % kStages], uint32_t(k / kStages) & 1, sy, a.err);
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            Walk w;
-            walk_begin(w, i0, i1, a.Kc);
-            bool ok = true;
-            for (int j = 0; j < n_it && ok; ++j, walk_next(w, i1, a.Kc)) {
-                const int s = w.st % kStages;
-                if (w.pos == 0) ok = wait_bar(&sy->full[s], uint32_t(w.st / kStages) & 1, sy, a.err);
-                const uint32_t slice = smem_u32(sx + s * kXStageBytes + w.pos * kXSliceBytes);
-                for (int m = 0; m < kMTiles && ok; ++m) {
-                    ok = wait_bar(&sy->a_full[m][j & 1], uint32_t(j >> 1) & 1, sy, a.err);
-                    tc_fence_after();
-                    const uint32_t acol = tbase + kColA + uint32_t(m * 2 + (j & 1)) * 32;
-                    for (int g = 0; g < NG && ok; ++g) {
-                        const int gi = j * NG + g;
-                        const int db = gi % (2 * NG);
-                        if (gi >= 2 * NG)
-                            ok = wait_bar(&sy->d_free[m][db], uint32_t(gi / (2 * NG) - 1) & 1, sy, a.err);
-                        tc_fence_after();
-                        const uint32_t dcol = tbase + kColD + uint32_t(m * 2 * NG + db) * 16;
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int kg = warp / kFeatWarps;   // iterations of parity kg
+    const int fw = warp % kFeatWarps;   // feature block
+    const int gq = lane >> 2, tq = lane & 3;
+    const bool hi = a.R > 8;
+    const int lrow = (lane & 7) + ((lane >> 4) << 3);
+    const int lcol = (lane >> 3) & 1;
+    const size_t ysz = a.mode == kSwiGluBf16 ? sizeof(__nv_bfloat16) : sizeof(float);
+    void *yb = static_cast<char *>(a.y) + (long long)u * a.y_stride * (long long)ysz;
+    float4 *rb = reinterpret_cast<float4 *>(red) + fw * 32 * 4 + lane * 4;
+    bool ok = true;
+
+    float acc[2][2][4];
 #pragma unroll
-                        for (int kk = 0; kk < KS; ++kk) {
-                            const int ks = g * KS + kk;
-                            const uint64_t bd = x_desc(slice, uint32_t(ks) * 32);
-                            umma_tmem_a(dcol, acol + uint32_t(ks) * 8, bd, kIdesc, kk > 0 ? 1u : 0u);
-                            umma_tmem_a(dcol, tbase + kColConst, bd, kIdesc, 1u);
-                        }
-                        umma_commit(&sy->d_full[m][db]);
-                    }
-                    umma_commit(&sy->a_free[m][j & 1]);
-                }
-                if (w.pos == w.n_in_stage - 1) umma_commit(&sy->empty[s]);
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[mt][n][c] = 0.f;
+
+    int st = 0;  // stage counter, identical to the producer's
+    for (int j = 0; j < n_it;) {
+        const long long gi = i0 + j;
+        const int t = int(gi / a.Kc);
+        const int kc0 = int(gi % a.Kc);
+        const int seg_len = min(n_it - j, a.Kc - kc0);
+        for (int sj = 0; sj < seg_len; sj += kStageIters, ++st) {
+            const int n_here = min(kStageIters, seg_len - sj);
+            const int s = st % kStages;
+            if (ok) ok = wait_bar(&sy->full[s], uint32_t(st / kStages) & 1, sy, a.err);
+            if (ok) {
+                const uint8_t *stage_w = sw + s * STW + fw * BB;
+                const uint32_t stage_x = smem_u32(sx + s * kXStageBytes);
+                // slices of this stage whose global parity is kg
+                for (int p = ((j + sj) & 1) == kg ? 0 : 1; p < n_here; p += 2)
+                    consume_slice<G>(stage_w + p * CB, stage_x + p * kXSliceBytes, lane, gq, lrow, lcol, hi, acc);
             }
-            // every MMA has completed before TMEM is released (bounded)
-            umma_commit(&sy->done);
-            wait_bar(&sy->done, 0, sy, a.err);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sy->empty[s]);
         }
-    } else {
-        // ---------------- dequant + epilogue warpgroups ----------------
-        const int wid = warp - 2;                 // 0..7
-        const int mt = wid / 4;                   // M-tile of this warpgroup
-        const int quarter = warp & 3;             // TMEM lane quarter this warp may access
-        const int row = quarter * 32 + lane;      // weight row within the M-tile
-        const uint32_t tl = uint32_t(quarter * 32) << 16;
-        const size_t ysz = a.mode == kSwiGluBf16 ? sizeof(__nv_bfloat16) : sizeof(float);
-        void *yb = static_cast<char *>(a.y) + (long long)u * a.y_stride * (long long)ysz;
+        const long long seg_b = gi, seg_e = gi + seg_len;
+        j += seg_len;
 
-        if (mt == 0) {  // the constant A block: -24 in every lane
-            uint32_t cv[8];
+        // ---- segment end: combine the k-parity groups in a fixed order (0 + 1)
+        named_bar_sync(1, kConsumerWarps * 32);
+        if (kg == 1) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) cv[i] = kBf16Neg24x2;
-            tmem_st_x8(tbase + tl + kColConst, cv);
-            tmem_wait_st();
+            for (int q = 0; q < 4; ++q)
+                rb[q] = make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1], acc[q >> 1][q & 1][2],
+                                    acc[q >> 1][q & 1][3]);
         }
-
-        float acc[kRows];
+        named_bar_sync(1, kConsumerWarps * 32);
+        if (kg == 0) {
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) acc[r] = 0.f;
-        float sc_prev[NG];
-#pragma unroll
-        for (int g = 0; g < NG; ++g) sc_prev[g] = 0.f;
-        long long prev_gi = -1, prev_seg_b = 0, prev_seg_e = 0;
-        bool ok = true;
-
-        // Reads back the group partials of iteration jj.
-        auto readback = [&](int jj) {
-#pragma unroll
-            for (int g = 0; g < NG; ++g) {
-                const int gi = jj * NG + g;
-                const int db = gi % (2 * NG);
-                if (ok) ok = wait_bar(&sy->d_full[mt][db], uint32_t(gi / (2 * NG)) & 1, sy, a.err);
-                tc_fence_after();
-                uint32_t d[16];
-                tmem_ld_x16(tbase + tl + kColD + uint32_t(mt * 2 * NG + db) * 16, d);
-                tmem_wait_ld();
-#pragma unroll
-                for (int r = 0; r < kRows; ++r) acc[r] = fmaf(sc_prev[g], __uint_as_float(d[r]), acc[r]);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sy->d_free[mt][db]);
+            for (int q = 0; q < 4; ++q) {
+                const float4 o = rb[q];
+                acc[q >> 1][q & 1][0] += o.x;
+                acc[q >> 1][q & 1][1] += o.y;
+                acc[q >> 1][q & 1][2] += o.z;
+                acc[q >> 1][q & 1][3] += o.w;
             }
-        };
-
-        // Publishes the segment ending with iteration gi_last.
-        auto finish_segment = [&](long long gi_last, long long sb, long long se) {
-            const int t = int(gi_last / a.Kc);
             const long long tb = (long long)t * a.Kc, te = tb + a.Kc;
-            if (sb == tb && se == te) {
-                store_row(a, yb, t, mt, quarter, lane, acc);
+            if (seg_b == tb && seg_e == te) {
+                store_block(a, yb, t, fw, gq, tq, hi, acc);
             } else {
                 // stream-K partial: publish; the last arriver sums every
                 // segment of this tile in ascending k order
                 const int which = (t == int(i0 / a.Kc)) ? 0 : 1;
-                float4 *slot = a.partials +
-                               ((((long long)u * a.Pv + vp) * 2 + which) * kDequantWarps + wid) * 128 + lane * 4;
+                float4 *slot = a.partials + ((((long long)u * a.Pv + vp) * 2 + which) * kFeatWarps + fw) * 128 +
+                               lane * 4;
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    __stcg(slot + q, make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
+                    __stcg(slot + q, make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
+                                                 acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3]));
                 __threadfence();
                 __syncwarp();
                 const int p_lo = int(((tb + 1) * a.Pv - 1) / tot);
@@ -349,172 +334,150 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 int nseg = 0;
                 for (int p2 = p_lo; p2 <= p_hi; ++p2)
                     if ((long long)p2 * tot / a.Pv < (long long)(p2 + 1) * tot / a.Pv) ++nseg;
-                unsigned *ctr = a.counters + ((long long)u * a.T + t) * kDequantWarps + wid;
+                unsigned *ctr = a.counters + ((long long)u * a.T + t) * kFeatWarps + fw;
                 unsigned old = 0;
                 if (lane == 0) old = atomicAdd(ctr, 1u);
                 old = __shfl_sync(0xFFFFFFFFu, old, 0);
                 if (old == unsigned(nseg - 1)) {
                     __threadfence();
-                    float sum[kRows];
+                    float sum[2][2][4];
 #pragma unroll
-                    for (int r = 0; r < kRows; ++r) sum[r] = 0.f;
-                    int p2 = p_lo;
-                    while (p2 <= p_hi) {
-                        // up to 4 segments' loads in flight, summed in k order
-                        const float4 *src[4];
-                        int ns = 0;
-                        while (ns < 4 && p2 <= p_hi) {
-                            const long long r0 = (long long)p2 * tot / a.Pv;
-                            const long long r1 = (long long)(p2 + 1) * tot / a.Pv;
+                    for (int q = 0; q < 16; ++q) sum[q >> 3][(q >> 2) & 1][q & 3] = 0.f;
+                    // segments in ascending k order, two loads in flight at a time
+                    auto seg_src = [&](int &p) -> const float4 * {
+                        while (p <= p_hi) {
+                            const long long r0 = (long long)p * tot / a.Pv;
+                            const long long r1 = (long long)(p + 1) * tot / a.Pv;
+                            const int pp = p++;
                             if (r0 < r1) {
                                 const int w2 = (t == int(r0 / a.Kc)) ? 0 : 1;
-                                src[ns++] = a.partials +
-                                            ((((long long)u * a.Pv + p2) * 2 + w2) * kDequantWarps + wid) * 128 +
-                                            lane * 4;
+                                return a.partials + ((((long long)u * a.Pv + pp) * 2 + w2) * kFeatWarps + fw) * 128 +
+                                       lane * 4;
                             }
-                            ++p2;
                         }
-                        float4 v[4][4];
+                        return nullptr;
+                    };
+                    int p2 = p_lo;
+                    while (p2 <= p_hi) {
+                        const float4 *s0 = seg_src(p2);
+                        const float4 *s1 = seg_src(p2);
+                        float4 v0[4], v1[4];
 #pragma unroll
-                        for (int s2 = 0; s2 < 4; ++s2)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                v[s2][q] = s2 < ns ? __ldcg(src[s2] + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                        for (int s2 = 0; s2 < 4; ++s2) {
-                            if (s2 >= ns) continue;
+                        for (int q = 0; q < 4; ++q) {
+                            v0[q] = s0 ? __ldcg(s0 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            v1[q] = s1 ? __ldcg(s1 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                        if (s0) {
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
-                                sum[4 * q] += v[s2][q].x;
-                                sum[4 * q + 1] += v[s2][q].y;
-                                sum[4 * q + 2] += v[s2][q].z;
-                                sum[4 * q + 3] += v[s2][q].w;
+                                sum[q >> 1][q & 1][0] += v0[q].x;
+                                sum[q >> 1][q & 1][1] += v0[q].y;
+                                sum[q >> 1][q & 1][2] += v0[q].z;
+                                sum[q >> 1][q & 1][3] += v0[q].w;
+                            }
+                        }
+                        if (s1) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                sum[q >> 1][q & 1][0] += v1[q].x;
+                                sum[q >> 1][q & 1][1] += v1[q].y;
+                                sum[q >> 1][q & 1][2] += v1[q].z;
+                                sum[q >> 1][q & 1][3] += v1[q].w;
                             }
                         }
                     }
                     if (lane == 0) *ctr = 0u;  // leave the counter zero for the next launch
-                    store_row(a, yb, t, mt, quarter, lane, sum);
+                    store_block(a, yb, t, fw, gq, tq, hi, sum);
                 }
             }
-#pragma unroll
-            for (int r = 0; r < kRows; ++r) acc[r] = 0.f;
-        };
-
-        Walk w;
-        walk_begin(w, i0, i1, a.Kc);
-        for (int j = 0; j < n_it; ++j, walk_next(w, i1, a.Kc)) {
-            const int s = w.st % kStages;
-            if (w.pos == 0 && ok) ok = wait_bar(&sy->full[s], uint32_t(w.st / kStages) & 1, sy, a.err);
-            const uint8_t *blk = sw + s * STW + w.pos * CB + mt * MB;
-            const uint4 c0 = *reinterpret_cast<const uint4 *>(blk + row * 16);
-            const uint4 c1 = *reinterpret_cast<const uint4 *>(blk + 2048 + row * 16);
-            float sc[NG];
-#pragma unroll
-            for (int g = 0; g < NG; ++g) sc[g] = half_at(blk + 4096 + (row * NG + g) * 2);
-            __syncwarp();
-            if (w.pos == w.n_in_stage - 1 && lane == 0) mbar_arrive(&sy->empty[s]);
-            uint32_t v[32];
-            dequant_slice(c0, c1, v);
-            if (j >= 2 && ok) ok = wait_bar(&sy->a_free[mt][j & 1], uint32_t((j >> 1) - 1) & 1, sy, a.err);
-            tc_fence_after();
-            tmem_st_x32(tbase + tl + kColA + uint32_t(mt * 2 + (j & 1)) * 32, v);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sy->a_full[mt][j & 1]);
-            // software pipeline: fold in the previous slice while this one multiplies
-            if (j > 0) {
-                readback(j - 1);
-                if (prev_gi + 1 == prev_seg_e) finish_segment(prev_gi, prev_seg_b, prev_seg_e);
-            }
-#pragma unroll
-            for (int g = 0; g < NG; ++g) sc_prev[g] = sc[g];
-            prev_gi = w.gi;
-            prev_seg_b = w.seg_b;
-            prev_seg_e = w.seg_e;
         }
-        readback(n_it - 1);
-        finish_segment(prev_gi, prev_seg_b, prev_seg_e);
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tbase, kTmemCols);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[mt][n][c] = 0.f;
     }
 }
 
 // ---- load-time repack: canonical [N][K/2] nibbles + [N][K/G] fp16 -> kernel layout
-// Canonical row of packed feature p (interleave: per 32-row warp slice, 16 gate
-// rows then the 16 matching up rows).
+// Canonical row of packed feature p (interleave: per 32-row feature block, 16
+// gate rows then the 16 matching up rows).
 __device__ __forceinline__ long long canonical_row(long long p, int N, bool inter) {
     if (!inter) return p < N ? p : -1;
     const int F = N / 2;
     const long long t = p / kTileN;
-    const int wtile = int(p % kTileN);
-    const int mt = wtile / kMTile, row = wtile % kMTile;
-    const int quarter = row / 32, lane = row % 32;
-    const long long j = t * (kTileN / 2) + mt * (kMTile / 2) + quarter * 16 + (lane & 15);
+    const int fw = int(p % kTileN) / kBlockRows;
+    const int r32 = int(p % kBlockRows);
+    const long long j = t * (kTileN / 2) + fw * 16 + (r32 & 15);
     if (j >= F) return -1;
-    return lane < 16 ? j : F + j;
+    return r32 < 16 ? j : F + j;
 }
 
 template <int G>
 __global__ void pack_codes_kernel(const uint8_t *codes, int K, int N, uint8_t *out, long long n_entries, int Kc,
                                   bool inter) {
-    constexpr int MB = mtile_bytes(G);
+    constexpr int BB = block_bytes(G);
     constexpr int CB = chunk_bytes(G);
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= n_entries) return;
-    const int row = int(idx % kMTile);
-    long long r = idx / kMTile;
-    const int half = int(r % 2);
+    const int lane = int(idx % 32);
+    long long r = idx / 32;
+    const int mt = int(r % 2);
     r /= 2;
-    const int mt = int(r % kMTiles);
-    r /= kMTiles;
+    const int fw = int(r % kFeatWarps);
+    r /= kFeatWarps;
     const int kc = int(r % Kc);
     const long long t = r / Kc;
-    const long long f = canonical_row(t * kTileN + mt * kMTile + row, N, inter);
+    const int gq = lane >> 2, tq = lane & 3;
     uint32_t words[4];
-    for (int e = 0; e < 4; ++e) {
+    for (int j = 0; j < 4; ++j) {
         uint32_t w = 0;
-        for (int q = 0; q < 8; ++q) {
-            const int k = kc * kKChunk + half * 32 + e * 8 + q;
-            uint32_t nib = 0;  // code 0
-            if (f >= 0) {
-                const uint8_t byte = codes[f * (K / 2) + k / 2];
-                nib = (k & 1) ? (byte >> 4) : (byte & 0xF);
+        for (int i = 0; i < 4; ++i)
+            for (int h = 0; h < 2; ++h) {
+                const long long f = canonical_row(
+                    t * kTileN + fw * kBlockRows + mt * 16 + gq + ((i & 1) ? 8 : 0), N, inter);
+                const int k = kc * kKChunk + j * 16 + 2 * tq + h + ((i & 2) ? 8 : 0);
+                uint32_t nib = 0;  // code 0
+                if (f >= 0) {
+                    const uint8_t byte = codes[f * (K / 2) + k / 2];
+                    nib = (k & 1) ? (byte >> 4) : (byte & 0xF);
+                }
+                w |= ((nib ^ 8u) & 0xFu) << (4 * i + 16 * h);   // two's complement -> offset binary
             }
-            w |= ((nib ^ 8u) & 0xFu) << (4 * (q / 2) + 16 * (q % 2));   // two's complement -> offset binary
-        }
-        words[e] = w;
+        words[j] = w;
     }
-    uint8_t *dst = out + (t * Kc + kc) * (long long)CB + mt * MB + half * 2048 + row * 16;
+    uint8_t *dst = out + (t * Kc + kc) * (long long)CB + fw * BB + mt * 512 + lane * 16;
     *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
 }
 
 template <int G>
 __global__ void pack_scales_kernel(const uint16_t *scales, int K, int N, uint8_t *out, long long n_entries, int Kc,
                                    bool inter) {
-    constexpr int MB = mtile_bytes(G);
+    constexpr int BB = block_bytes(G);
     constexpr int CB = chunk_bytes(G);
     constexpr int NG = kKChunk / G;
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= n_entries) return;
-    const int g = int(idx % NG);
-    long long r = idx / NG;
-    const int row = int(r % kMTile);
-    r /= kMTile;
-    const int mt = int(r % kMTiles);
-    r /= kMTiles;
+    const int mt = int(idx % 2);
+    long long r = idx / 2;
+    const int g = int(r % 8);
+    r /= 8;
+    const int grp = int(r % NG);
+    r /= NG;
+    const int fw = int(r % kFeatWarps);
+    r /= kFeatWarps;
     const int kc = int(r % Kc);
     const long long t = r / Kc;
-    const long long f = canonical_row(t * kTileN + mt * kMTile + row, N, inter);
+    const long long p = t * kTileN + fw * kBlockRows + mt * 16 + g;
+    const long long f_lo = canonical_row(p, N, inter);
+    const long long f_hi = canonical_row(p + 8, N, inter);
+    const int gi = kc * NG + grp;
     const int ngroups = K / G;
-    const uint16_t v = f >= 0 ? scales[f * ngroups + kc * NG + g] : uint16_t(0);
-    uint8_t *dst = out + (t * Kc + kc) * (long long)CB + mt * MB + 4096 + (row * NG + g) * 2;
-    *reinterpret_cast<uint16_t *>(dst) = v;
+    const uint32_t lo = f_lo >= 0 ? scales[f_lo * ngroups + gi] : 0u;
+    const uint32_t hi = f_hi >= 0 ? scales[f_hi * ngroups + gi] : 0u;
+    uint8_t *dst = out + (t * Kc + kc) * (long long)CB + fw * BB + 1024 + grp * 64 + g * 8 + mt * 4;
+    *reinterpret_cast<uint32_t *>(dst) = lo | (hi << 16);
 }
 
 template <int G>
@@ -533,8 +496,8 @@ cudaError_t launch_pack_g(const uint8_t *codes, const uint16_t *scales, int K, i
                           cudaStream_t s) {
     const int T = (N + kTileN - 1) / kTileN;
     const int Kc = K / kKChunk;
-    const long long n_codes = (long long)T * Kc * kMTiles * 2 * kMTile;
-    const long long n_scales = (long long)T * Kc * kMTiles * kMTile * (kKChunk / G);
+    const long long n_codes = (long long)T * Kc * kFeatWarps * 2 * 32;
+    const long long n_scales = (long long)T * Kc * kFeatWarps * (kKChunk / G) * 8 * 2;
     const int th = 256;
     pack_codes_kernel<G><<<unsigned((n_codes + th - 1) / th), th, 0, s>>>(codes, K, N, (uint8_t *)packed, n_codes,
                                                                         Kc, inter);

@@ -8,38 +8,44 @@
 namespace tfk {
 
 // ---- packed weight layout --------------------------------------------------
-// Output features are grouped in tiles of 256 = two "M-tiles" of 128 rows (one
-// tcgen05 MMA's M).  For every tile t and every 64-wide slice kc of the input
-// features there is one contiguous "chunk", and consecutive kc of a tile are
-// consecutive in memory, so any run of iterations of one tile is one bulk copy.
-// A chunk is two M-tile blocks; an M-tile block holds
-//   codes : [half 0..1][row 0..127][16 B]   4096 B   row's k = 32*half .. +31
-//   scales: [row 0..127][64/G] fp16          256 B per group
-// Inside a row's 16 bytes, word e (k = 32*half + 8*e .. +7, e = 0..3) keeps the
-// code of k offset q (0..7) as offset binary (code + 8) at bits
-// 4*(q/2) + 16*(q%2): one shift + LOP3 per pair turns it into bf16 (16 + u).
-constexpr int kMTile = 128;                // rows per tcgen05 MMA (M)
-constexpr int kMTiles = 2;                 // M-tiles per tile
-constexpr int kTileN = kMTile * kMTiles;   // 256 output features per tile
+// Output features are grouped in tiles of 256 = 8 "feature blocks" of 32 rows
+// (one consumer warp each).  For every tile t and every 64-wide slice kc of the
+// input features there is one contiguous "chunk", and consecutive kc of a tile
+// are consecutive in memory, so any run of iterations of one tile is one bulk
+// copy.  A chunk is 8 feature blocks; a block holds
+//   codes : [mt 0..1][lane 0..31][16 B]       1024 B
+//   scales: [grp][g 0..7][mt 0..1] half2      64 B per quantisation group
+// Lane (g = lane/4, q = lane%4) of the warp owns, for the 16-row sub-tile mt and
+// the 16-wide k step j, word j of its 16-byte entry.  Its nibble pairs
+// (bits 4i / 16+4i, offset binary code + 8) are the m16n8k16 A fragment:
+//   i=0: (row g,   k 2q | 2q+1)      i=1: (row g+8, k 2q | 2q+1)
+//   i=2: (row g,   k 2q+8 | 2q+9)    i=3: (row g+8, k 2q+8 | 2q+9)
+// and the half2 (s[row g], s[row g+8]) of each sub-tile are the lane's scales.
+constexpr int kBlockRows = 32;             // weight rows per consumer warp
+constexpr int kFeatWarps = 8;              // feature blocks per tile
+constexpr int kTileN = kBlockRows * kFeatWarps;   // 256 output features per tile
 constexpr int kKChunk = 64;                // k per iteration
-constexpr int kRows = 16;                  // MMA N: verify rows, zero-padded
+constexpr int kRows = 16;                  // verify rows (MMA columns), zero-padded
+constexpr int kKGroups = 2;                // consumer warp groups splitting the iterations by parity
+constexpr int kConsumerWarps = kFeatWarps * kKGroups;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
 constexpr int kStageIters = 4;             // iterations per pipeline stage (one weight copy of ~35 KB)
 constexpr int kStages = 4;
-constexpr int kDequantWarps = 8;           // two warpgroups, one per M-tile
-constexpr int kThreads = 32 * (2 + kDequantWarps);  // producer + MMA + dequant/epilogue warps
-constexpr int kXSliceBytes = kRows * kKChunk * 2;   // [16 rows][64 k] bf16, 128-byte swizzled
+constexpr int kXSliceBytes = kRows * kKChunk * 2;     // [16 rows][64 k] bf16, 128-byte swizzled
 constexpr int kXStageBytes = kStageIters * kXSliceBytes;
+constexpr int kLaneAcc = 16;               // fp32 accumulators per lane: 2 sub-tiles x 2 row-halves x 4
 
-__host__ __device__ constexpr int mtile_bytes(int G) { return 4096 + 256 * (kKChunk / G); }
-__host__ __device__ constexpr int chunk_bytes(int G) { return kMTiles * mtile_bytes(G); }
-// One partial tile of the split-K fixup: 8 warps x 32 lanes x 16 floats.
-constexpr size_t kSlotBytes = size_t(kDequantWarps) * 32 * kRows * 4;
+__host__ __device__ constexpr int block_bytes(int G) { return 1024 + 64 * (kKChunk / G); }
+__host__ __device__ constexpr int chunk_bytes(int G) { return kFeatWarps * block_bytes(G); }
+// One partial tile of the split-K fixup: 8 feature warps x 32 lanes x 16 floats.
+constexpr size_t kSlotBytes = size_t(kFeatWarps) * 32 * kLaneAcc * 4;
 
 inline size_t gemm_smem_bytes(int G) {
     return 1024                                                         // alignment slack
            + size_t(kStages) * kXStageBytes                             // activation slices (1024-B aligned)
            + size_t(kStages) * kStageIters * chunk_bytes(G)            // weight stages
-           + 256;                                                       // barriers, TMEM base
+           + size_t(kFeatWarps) * 32 * kLaneAcc * 4                     // k-group combine buffer
+           + 256;                                                       // barriers
 }
 
 inline bool packed_shape_ok(int K, int N, int G) {
@@ -78,8 +84,8 @@ struct GemmArgs {
     int F;                     // kSwiGluBf16: width of h (N = 2F)
     int R, K, N, G;
     int T, Kc, Pv;
-    unsigned *counters;        // [U_max][T][kDequantWarps], zero between launches
-    float4 *partials;          // [U_max][Pv][2][kDequantWarps][32][4]
+    unsigned *counters;        // [U_max][T][kFeatWarps], zero between launches
+    float4 *partials;          // [U_max][Pv][2][kFeatWarps][32][4]
     int *err;
 };
 
@@ -98,8 +104,8 @@ void gemm_bind_workspace(GemmArgs &a, void *ws, int u_max);
 bool gemm_encode_x(GemmArgs &a, const uint16_t *x, int ldx, long long x_stride, int u_max, const char **why);
 cudaError_t launch_w4_gemm(const GemmArgs &a, int u_max, cudaStream_t s);
 // interleave_gate_up: rows [0, N/2) are gate rows, [N/2, N) up rows; they are
-// packed so that lanes 0-15 of every 32-row warp slice hold 16 gate rows and
-// lanes 16-31 the matching up rows (the layout kSwiGluBf16 expects).
+// packed so that each 32-row feature block holds 16 gate rows (sub-tile 0) and
+// the 16 matching up rows (sub-tile 1), the layout kSwiGluBf16 expects.
 cudaError_t launch_pack_w4(const uint8_t *codes, const uint16_t *scales, int K, int N, int G, void *packed,
                            bool interleave_gate_up, cudaStream_t s);
 int device_sm_count();
