@@ -53,8 +53,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))); }
-__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
 
 struct Sync {
     uint64_t full[kStages];
@@ -76,10 +74,12 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Sync *s
     return false;
 }
 
-// One 64-wide k slice of one 32-row feature block for this warp.
-template <int G>
+// One 64-wide k slice of one 32-row feature block for this warp.  HI: the
+// launch has more than 8 rows (a second n8 MMA per sub-tile); rows 0..7 run the
+// identical instruction sequence in both instantiations.
+template <int G, bool HI>
 __device__ __forceinline__ void consume_slice(const uint8_t *blk, uint32_t xslice, int lane, int gq, int lrow,
-                                              int lcol, bool hi, float (&acc)[2][2][4]) {
+                                              int lcol, float (&acc)[2][2][4]) {
     constexpr int NG = kKChunk / G;
     constexpr int KS = G / 16;
     const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + lane * 16);
@@ -89,18 +89,12 @@ __device__ __forceinline__ void consume_slice(const uint8_t *blk, uint32_t xslic
         const uint2 sv = *reinterpret_cast<const uint2 *>(blk + 1024 + grp * 64 + gq * 8);
         float part[2][2][4];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) part[mt][n][c] = 0.f;
-#pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
             const int j = grp * KS + kk;
             // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
             const uint32_t xa = xslice + lrow * 128 + ((((2 * j + lcol) ^ (lrow & 7))) << 4);
             uint32_t b0, b1, b2 = 0, b3 = 0;
-            if (hi)
+            if (HI)
                 ldsm_x4(xa, b0, b1, b2, b3);
             else
                 ldsm_x2(xa, b0, b1);
@@ -112,22 +106,25 @@ __device__ __forceinline__ void consume_slice(const uint8_t *blk, uint32_t xslic
                 af[1] = fma_bf16x2(lop3_and_or(w >> 4, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
                 af[2] = fma_bf16x2(lop3_and_or(w >> 8, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
                 af[3] = fma_bf16x2(lop3_and_or(w >> 12, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
-                mma_bf16_16816(part[mt][0], af, b0, b1);
-                if (hi) mma_bf16_16816(part[mt][1], af, b2, b3);
+                if (kk == 0) {
+                    mma_bf16_16816_zero(part[mt][0], af, b0, b1);
+                    if (HI) mma_bf16_16816_zero(part[mt][1], af, b2, b3);
+                } else {
+                    mma_bf16_16816(part[mt][0], af, b0, b1);
+                    if (HI) mma_bf16_16816(part[mt][1], af, b2, b3);
+                }
             }
         }
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
-            const uint32_t sw = mt ? sv.y : sv.x;
-            const float s_lo = half_lo(sw);   // row mt*16 + g
-            const float s_hi = half_hi(sw);   // row mt*16 + g + 8
+            const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(mt ? &sv.y : &sv.x));
+            // sc.x: row mt*16 + g, sc.y: row mt*16 + g + 8
 #pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                if (n == 1 && !hi) continue;
-                acc[mt][n][0] = fmaf(s_lo, part[mt][n][0], acc[mt][n][0]);
-                acc[mt][n][1] = fmaf(s_lo, part[mt][n][1], acc[mt][n][1]);
-                acc[mt][n][2] = fmaf(s_hi, part[mt][n][2], acc[mt][n][2]);
-                acc[mt][n][3] = fmaf(s_hi, part[mt][n][3], acc[mt][n][3]);
+            for (int n = 0; n < (HI ? 2 : 1); ++n) {
+                acc[mt][n][0] = fmaf(sc.x, part[mt][n][0], acc[mt][n][0]);
+                acc[mt][n][1] = fmaf(sc.x, part[mt][n][1], acc[mt][n][1]);
+                acc[mt][n][2] = fmaf(sc.y, part[mt][n][2], acc[mt][n][2]);
+                acc[mt][n][3] = fmaf(sc.y, part[mt][n][3], acc[mt][n][3]);
             }
         }
     }
@@ -184,7 +181,7 @@ __device__ __forceinline__ void store_block(const GemmArgs &a, void *yb, int t, 
     }
 }
 
-template <int G>
+template <int G, bool HI>
 __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_constant__ GemmArgs a) {
     constexpr int BB = block_bytes(G);
     constexpr int CB = chunk_bytes(G);
@@ -226,7 +223,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
         // ---------------- producer ----------------
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            int st = 0;
+            // Weights are read-only model data: the first kStages stages are
+            // requested before waiting for the preceding grid (programmatic
+            // dependent launch), their activation slices only after it.
+            int st = 0, x_issued = 0;
+            int stage_kc[kStages];
             bool ok = true;
             for (int j = 0; j < n_it && ok;) {
                 const long long gi = i0 + j;
@@ -235,15 +236,32 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 for (int sj = 0; sj < seg_len; sj += kStageIters, ++st) {
                     const int n_here = min(kStageIters, seg_len - sj);
                     const int s = st % kStages;
+                    if (st == kStages) {
+                        grid_dependency_wait();
+                        for (; x_issued < kStages; ++x_issued)
+                            tma_load_4d(sx + x_issued * kXStageBytes, &a.xmap, 0, 0, stage_kc[x_issued],
+                                        a.x_per_problem ? u : 0, &sy->full[x_issued]);
+                    }
                     if (st >= kStages && !wait_bar(&sy->empty[s], uint32_t(st / kStages - 1) & 1, sy, a.err)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&sy->full[s], uint32_t(n_here * CB + kXStageBytes));
                     bulk_g2s_hint(sw + s * STW, wb + (gi + sj) * CB, uint32_t(n_here * CB), &sy->full[s], pol);
-                    tma_load_4d(sx + s * kXStageBytes, &a.xmap, 0, 0, kc0 + sj, a.x_per_problem ? u : 0, &sy->full[s]);
+                    if (st < kStages) {
+                        stage_kc[st] = kc0 + sj;
+                    } else {
+                        tma_load_4d(sx + s * kXStageBytes, &a.xmap, 0, 0, kc0 + sj, a.x_per_problem ? u : 0,
+                                    &sy->full[s]);
+                    }
                 }
                 j += seg_len;
+            }
+            if (x_issued < min(st, kStages)) {  // short ranges: fewer than kStages stages
+                grid_dependency_wait();
+                for (; x_issued < min(st, kStages); ++x_issued)
+                    tma_load_4d(sx + x_issued * kXStageBytes, &a.xmap, 0, 0, stage_kc[x_issued],
+                                a.x_per_problem ? u : 0, &sy->full[x_issued]);
             }
             const int issued = st;
             // leave only once every issued copy has landed (bounded)
@@ -257,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     const int kg = warp / kFeatWarps;   // iterations of parity kg
     const int fw = warp % kFeatWarps;   // feature block
     const int gq = lane >> 2, tq = lane & 3;
-    const bool hi = a.R > 8;
+    constexpr bool hi = HI;
     const int lrow = (lane & 7) + ((lane >> 4) << 3);
     const int lcol = (lane >> 3) & 1;
     const size_t ysz = a.mode == kSwiGluBf16 ? sizeof(__nv_bfloat16) : sizeof(float);
@@ -273,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[mt][n][c] = 0.f;
 
+    grid_dependency_wait();  // activations, workspace and outputs come from earlier grids
     int st = 0;  // stage counter, identical to the producer's
     for (int j = 0; j < n_it;) {
         const long long gi = i0 + j;
@@ -288,23 +307,25 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 const uint32_t stage_x = smem_u32(sx + s * kXStageBytes);
                 // slices of this stage whose global parity is kg
                 for (int p = ((j + sj) & 1) == kg ? 0 : 1; p < n_here; p += 2)
-                    consume_slice<G>(stage_w + p * CB, stage_x + p * kXSliceBytes, lane, gq, lrow, lcol, hi, acc);
+                    consume_slice<G, HI>(stage_w + p * CB, stage_x + p * kXSliceBytes, lane, gq, lrow, lcol, acc);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sy->empty[s]);
         }
         const long long seg_b = gi, seg_e = gi + seg_len;
         j += seg_len;
+        if (j == n_it && warp == 0 && lane == 0) grid_launch_dependents();  // main loop done: let the next grid start
 
-        // ---- segment end: combine the k-parity groups in a fixed order (0 + 1)
-        named_bar_sync(1, kConsumerWarps * 32);
+        // ---- segment end: combine the k-parity groups in a fixed order (0 + 1);
+        // warps fw and fw + 8 pair up through their own named barrier
+        named_bar_sync(1 + fw, 64);
         if (kg == 1) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 rb[q] = make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1], acc[q >> 1][q & 1][2],
                                     acc[q >> 1][q & 1][3]);
         }
-        named_bar_sync(1, kConsumerWarps * 32);
+        named_bar_sync(1 + fw, 64);
         if (kg == 0) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -318,17 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
             if (seg_b == tb && seg_e == te) {
                 store_block(a, yb, t, fw, gq, tq, hi, acc);
             } else {
-                // stream-K partial: publish; the last arriver sums every
-                // segment of this tile in ascending k order
+                // stream-K partial.  The last segment to finish sums every
+                // segment of this tile in ascending k order.  A warp that finds
+                // all other segments already published is last: it skips
+                // publishing its own and reads the others directly.
                 const int which = (t == int(i0 / a.Kc)) ? 0 : 1;
-                float4 *slot = a.partials + ((((long long)u * a.Pv + vp) * 2 + which) * kFeatWarps + fw) * 128 +
-                               lane * 4;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    __stcg(slot + q, make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
-                                                 acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3]));
-                __threadfence();
-                __syncwarp();
                 const int p_lo = int(((tb + 1) * a.Pv - 1) / tot);
                 const int p_hi = int((te * a.Pv - 1) / tot);
                 int nseg = 0;
@@ -336,20 +351,43 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                     if ((long long)p2 * tot / a.Pv < (long long)(p2 + 1) * tot / a.Pv) ++nseg;
                 unsigned *ctr = a.counters + ((long long)u * a.T + t) * kFeatWarps + fw;
                 unsigned old = 0;
-                if (lane == 0) old = atomicAdd(ctr, 1u);
+                if (lane == 0) old = ld_acquire_gpu(ctr);
                 old = __shfl_sync(0xFFFFFFFFu, old, 0);
-                if (old == unsigned(nseg - 1)) {
+                const bool own_in_regs = old == unsigned(nseg - 1);
+                if (!own_in_regs) {
+                    float4 *slot = a.partials +
+                                   ((((long long)u * a.Pv + vp) * 2 + which) * kFeatWarps + fw) * 128 + lane * 4;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        __stcg(slot + q, make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
+                                                     acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3]));
                     __threadfence();
+                    __syncwarp();
+                    if (lane == 0) old = atomicAdd(ctr, 1u);
+                    old = __shfl_sync(0xFFFFFFFFu, old, 0);
+                }
+                if (old == unsigned(nseg - 1)) {
+                    __syncwarp();     // order every lane's reads after lane 0's acquire / atomic
+                    __threadfence();
+                    const int me = vp;
                     float sum[2][2][4];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) sum[q >> 3][(q >> 2) & 1][q & 3] = 0.f;
                     // segments in ascending k order, two loads in flight at a time
+                    // nullptr = "this CTA's own segment, still in registers" when
+                    // own_in_regs; segments are visited in ascending k order
+                    bool own_next = false;
                     auto seg_src = [&](int &p) -> const float4 * {
+                        own_next = false;
                         while (p <= p_hi) {
                             const long long r0 = (long long)p * tot / a.Pv;
                             const long long r1 = (long long)(p + 1) * tot / a.Pv;
                             const int pp = p++;
                             if (r0 < r1) {
+                                if (own_in_regs && pp == me) {
+                                    own_next = true;
+                                    return nullptr;
+                                }
                                 const int w2 = (t == int(r0 / a.Kc)) ? 0 : 1;
                                 return a.partials + ((((long long)u * a.Pv + pp) * 2 + w2) * kFeatWarps + fw) * 128 +
                                        lane * 4;
@@ -360,14 +398,22 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                     int p2 = p_lo;
                     while (p2 <= p_hi) {
                         const float4 *s0 = seg_src(p2);
+                        const bool own0 = own_next;
                         const float4 *s1 = seg_src(p2);
+                        const bool own1 = own_next;
                         float4 v0[4], v1[4];
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            v0[q] = s0 ? __ldcg(s0 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-                            v1[q] = s1 ? __ldcg(s1 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            v0[q] = s0 ? __ldcg(s0 + q)
+                                       : own0 ? make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
+                                                            acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3])
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                            v1[q] = s1 ? __ldcg(s1 + q)
+                                       : own1 ? make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
+                                                            acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3])
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
-                        if (s0) {
+                        if (s0 || own0) {
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
                                 sum[q >> 1][q & 1][0] += v0[q].x;
@@ -376,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                                 sum[q >> 1][q & 1][3] += v0[q].w;
                             }
                         }
-                        if (s1) {
+                        if (s1 || own1) {
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
                                 sum[q >> 1][q & 1][0] += v1[q].x;
@@ -480,15 +526,23 @@ __global__ void pack_scales_kernel(const uint16_t *scales, int K, int N, uint8_t
     *reinterpret_cast<uint32_t *>(dst) = lo | (hi << 16);
 }
 
-template <int G>
+template <int G, bool HI>
 cudaError_t launch_gemm_g(const GemmArgs &a, int u_max, cudaStream_t s) {
     const size_t smem = gemm_smem_bytes(G);
-    cudaError_t err = cudaFuncSetAttribute(w4_lane_gemm_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(w4_lane_gemm_kernel<G, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            int(smem));
     if (err != cudaSuccess) return err;
-    dim3 grid(a.Pv, u_max);
-    w4_lane_gemm_kernel<G><<<grid, kThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.Pv, u_max);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, w4_lane_gemm_kernel<G, HI>, a);
 }
 
 template <int G>
@@ -561,7 +615,8 @@ bool gemm_encode_x(GemmArgs &a, const uint16_t *x, int ldx, long long x_stride, 
 }
 
 cudaError_t launch_w4_gemm(const GemmArgs &a, int u_max, cudaStream_t s) {
-    return a.G == 64 ? launch_gemm_g<64>(a, u_max, s) : launch_gemm_g<32>(a, u_max, s);
+    if (a.R > 8) return a.G == 64 ? launch_gemm_g<64, true>(a, u_max, s) : launch_gemm_g<32, true>(a, u_max, s);
+    return a.G == 64 ? launch_gemm_g<64, false>(a, u_max, s) : launch_gemm_g<32, false>(a, u_max, s);
 }
 
 cudaError_t launch_pack_w4(const uint8_t *codes, const uint16_t *scales, int K, int N, int G, void *packed,
