@@ -147,6 +147,37 @@ TF_API tf_status tf_lane_gemm_w4(const tf_w4_matrix *W, const uint16_t *x, int32
                           float *y, int32_t ldy, void *ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * tf_lane_gemm_w4_noalloc -- tf_lane_gemm_w4 without a caller workspace
+ * ------------------------------------------------------------------------
+ * No counterpart in the pages: an integration convenience.  Same operation,
+ * arguments (minus ws / ws_bytes), layouts and bits as tf_lane_gemm_w4.
+ *
+ * For callers that cannot hand in device memory: code that runs inside an
+ * allocator or an out-of-memory handler (allocating there would re-enter the
+ * allocator or fail), and hosts that own no device memory pool and must not
+ * call cudaMalloc, which can synchronise the device.  This call allocates
+ * nothing: its split-K scratch is a fixed 8 MiB array inside libtf, one copy
+ * per device.
+ *
+ * - The first call on a device (made with that device current) looks up the
+ *   array's address; make that first call before any stream capture.
+ * - A launch whose scratch need exceeds the array (it grows with the device's
+ *   SM count: 256 B + 256 KiB + 32 KiB per SM) returns TF_ERR_UNSUPPORTED and
+ *   launches nothing.
+ * - Every call on a device shares the one array, which keeps what the last call
+ *   left; each call clears the parts that must start at zero on `stream`
+ *   before its kernel.  Calls that can overlap in time on one device (different
+ *   streams, or several host threads) race on the array and give undefined
+ *   results: serialise them, or use tf_lane_gemm_w4 with one workspace each.
+ * status  dev int32 or NULL.  When given (zeroed by the caller), the kernel
+ *         records there the first device-side error of this call
+ *         (TF_DEV_TIMEOUT); when NULL, such an error goes to the shared array
+ *         and is cleared, unread, by the next call.
+ */
+TF_API tf_status tf_lane_gemm_w4_noalloc(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R,
+                                         float *y, int32_t ldy, int32_t *status, void *stream);
+
+/* ------------------------------------------------------------------------
  * tf_keyed_sample -- keyed Gumbel-max sampling over top-k / top-p
  * ------------------------------------------------------------------------
  * README, "Every token is the model's own sample", and the CLI table

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "../../include/tf.h"
@@ -327,6 +328,76 @@ tf_status tf_lane_gemm_w4(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx,
     const char *why = "";
     cudaError_t e = bind_and_launch(a, x, ldx, 0, 1, ws, static_cast<cudaStream_t>(stream), &why);
     if (e != cudaSuccess) return fail(TF_ERR_CUDA, "tf_lane_gemm_w4: %s (%s)", cudaGetErrorString(e), why);
+    return ok();
+}
+
+// ---- tf_lane_gemm_w4_noalloc: the lane GEMM on library-owned scratch ----
+// The split-K status word, counters and partial tiles live in one fixed array
+// of this module instead of a caller workspace.  Each device has its own copy
+// of the array; its address is looked up once per device (with that device
+// current) and then reused.  All calls on a device share the copy.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+constexpr int kNoAllocMaxDevices = 64;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kNoAllocMaxDevices];
+
+tf_status noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "tf_lane_gemm_w4_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return fail(TF_ERR_UNSUPPORTED, "tf_lane_gemm_w4_noalloc: device %d (at most %d devices)", dev,
+                    kNoAllocMaxDevices);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "tf_lane_gemm_w4_noalloc: cudaGetSymbolAddress");
+        if (!p || !aligned(p, 256)) return fail(TF_ERR_CUDA, "tf_lane_gemm_w4_noalloc: scratch address unusable");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return TF_OK;
+}
+}  // namespace
+
+tf_status tf_lane_gemm_w4_noalloc(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R, float *y,
+                                  int32_t ldy, int32_t *status, void *stream) {
+    tf_status st = check_matrix(W, "W");
+    if (st) return st;
+    if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
+    if (!x || !aligned(x, 16)) return fail(TF_ERR_INVALID_ARG, "x must be non-null and 16-B aligned");
+    if (ldx < W->K || ldx % 8) return fail(TF_ERR_INVALID_ARG, "ldx=%d must be >= K and a multiple of 8", ldx);
+    if (!y || !aligned(y, 4)) return fail(TF_ERR_INVALID_ARG, "y must be non-null and 4-B aligned");
+    if (ldy < W->N) return fail(TF_ERR_INVALID_ARG, "ldy=%d must be >= N", ldy);
+    if (status && !aligned(status, 4)) return fail(TF_ERR_INVALID_ARG, "status must be 4-B aligned");
+    if (size_t((W->N + kTileN - 1) / kTileN) * kFeatWarps > kMaxCounters)
+        return fail(TF_ERR_UNSUPPORTED, "N=%d too large for the split-K counter region", W->N);
+    GemmArgs a = dense_args(*W, R, y, ldy, kStoreF32);
+    const size_t need = gemm_workspace_bytes(a.K, a.N, a.G, 1, a.Pv);
+    if (need > kNoAllocScratchBytes)
+        return fail(TF_ERR_UNSUPPORTED,
+                    "tf_lane_gemm_w4_noalloc: this launch needs %zu bytes of scratch, the built-in array holds %zu "
+                    "(use tf_lane_gemm_w4 with a workspace)",
+                    need, kNoAllocScratchBytes);
+    void *scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch))) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The array keeps whatever the previous call left.  The status word and this
+    // launch's split-K counters must start at zero; partial tiles are always
+    // written before they are read.
+    cudaError_t e = cudaMemsetAsync(scratch, 0, 256 + size_t(a.T) * kFeatWarps * sizeof(unsigned), s);
+    if (e != cudaSuccess) return cuda_fail(e, "tf_lane_gemm_w4_noalloc: clearing scratch");
+    gemm_bind_workspace(a, scratch, 1);
+    if (status) a.err = status;
+    const char *why = "";
+    if (!gemm_encode_x(a, x, ldx, 0, 1, &why))
+        return fail(TF_ERR_CUDA, "tf_lane_gemm_w4_noalloc: %s", why);
+    e = launch_w4_gemm(a, 1, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tf_lane_gemm_w4_noalloc");
     return ok();
 }
 

@@ -63,6 +63,7 @@ SIGNATURES = [
     ("tf_pack_w4_gate_up", ctypes.c_int, [P, P, I32, I32, I32, P, SZ, P]),
     ("tf_lane_gemm_workspace_bytes", SZ, [I32, I32, I32]),
     ("tf_lane_gemm_w4", ctypes.c_int, [ctypes.POINTER(W4MatrixC), P, I32, I32, P, I32, P, SZ, P]),
+    ("tf_lane_gemm_w4_noalloc", ctypes.c_int, [ctypes.POINTER(W4MatrixC), P, I32, I32, P, I32, P, P]),
     ("tf_keyed_sample_workspace_bytes", SZ, [I32, I32]),
     ("tf_keyed_sample", ctypes.c_int, [P, I32, I32, I32, ctypes.POINTER(SamplingC), ctypes.c_uint64, P, P, P, SZ, P]),
     ("tf_accept", ctypes.c_int, [P, P, I32, P, P, P]),
@@ -172,6 +173,19 @@ def lane_gemm_w4(W: W4Matrix, x: torch.Tensor, y: torch.Tensor = None, ws: torch
     wc = W.c()
     _check(lib.tf_lane_gemm_w4(ctypes.byref(wc), _ptr(x), x.stride(0), R, _ptr(y), y.stride(0), _ptr(ws),
                                ws.numel(), _stream(stream)))
+    return y
+
+
+def lane_gemm_w4_noalloc(W: W4Matrix, x: torch.Tensor, y: torch.Tensor, status: torch.Tensor = None,
+                         stream=None) -> torch.Tensor:
+    """lane_gemm_w4 on the library's built-in scratch: the call allocates no device
+    memory, so the output y[R][N] fp32 must be given.  status: optional device int32
+    (zeroed by the caller) that receives a device-side error code."""
+    lib = load()
+    R = x.shape[0]
+    wc = W.c()
+    _check(lib.tf_lane_gemm_w4_noalloc(ctypes.byref(wc), _ptr(x), x.stride(0), R, _ptr(y), y.stride(0),
+                                       _ptr(status), _stream(stream)))
     return y
 
 
