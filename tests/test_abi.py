@@ -89,30 +89,38 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.tf_last_error() != b""
 
 
-def _cta_of(i, Pv, tot):
-    return ((i + 1) * Pv - 1) // tot
+def _start(p, q, rem):
+    return p * q + min(p, rem)
+
+
+def _owner(i, q, rem):
+    big = rem * (q + 1)
+    return i // (q + 1) if i < big else rem + (i - big) // q
 
 
 @pytest.mark.parametrize("T,Kc,Pv", [(4, 4, 16), (68, 80, 152), (20, 272, 152), (594, 80, 152), (6, 32, 16),
-                                     (8, 12, 16), (1, 1, 1), (3, 5, 11)])
+                                     (8, 12, 16), (1, 1, 1), (3, 5, 11), (7, 9, 63)])
 def test_stream_k_cut_formulas(T, Kc, Pv):
-    """The split-K cut used by the GEMM kernel: ranges tile the iteration space,
-    cta_of() inverts them, and every tile's segment slots are distinct."""
+    """The split-K cut used by the GEMM kernel: Pv = min(Pv, T*Kc) contiguous
+    ranges whose sizes differ by at most one tile the iteration space, owner()
+    inverts them, and every tile's segment slots are distinct."""
     tot = T * Kc
     Pv = min(Pv, tot)
-    b = [p * tot // Pv for p in range(Pv + 1)]
-    assert b[0] == 0 and b[-1] == tot and all(b[p] < b[p + 1] for p in range(Pv))
+    q, rem = divmod(tot, Pv)
+    b = [_start(p, q, rem) for p in range(Pv + 1)]
+    assert b[0] == 0 and b[-1] == tot and all(q <= b[p + 1] - b[p] <= q + 1 for p in range(Pv))
     for i in range(tot):
-        p = _cta_of(i, Pv, tot)
+        p = _owner(i, q, rem)
         assert b[p] <= i < b[p + 1]
     slots = set()
     for t in range(T):
-        lo, hi = _cta_of(t * Kc, Pv, tot), _cta_of((t + 1) * Kc - 1, Pv, tot)
-        segs = [p for p in range(lo, hi + 1) if b[p] < b[p + 1]]
-        covered = sum(min(b[p + 1], (t + 1) * Kc) - max(b[p], t * Kc) for p in segs)
-        assert covered == Kc
+        tb, te = t * Kc, (t + 1) * Kc
+        lo, hi = _owner(tb, q, rem), _owner(te - 1, q, rem)
+        segs = list(range(lo, hi + 1))
+        covered = sum(min(b[p + 1], te) - max(b[p], tb) for p in segs)
+        assert covered == Kc and all(min(b[p + 1], te) > max(b[p], tb) for p in segs)
         if len(segs) > 1:
             for p in segs:
-                which = 0 if t == b[p] // Kc else 1
+                which = 0 if b[p] >= tb else 1
                 assert (p, which) not in slots
                 slots.add((p, which))

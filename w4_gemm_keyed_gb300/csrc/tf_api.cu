@@ -61,6 +61,8 @@ tf_status check_matrix(const tf_w4_matrix *W, const char *name) {
     if (W->group != 32 && W->group != 64) return fail(TF_ERR_UNSUPPORTED, "%s: group %d not in {32, 64}", name, W->group);
     if (W->K <= 0 || W->K % kKChunk) return fail(TF_ERR_UNSUPPORTED, "%s: K=%d is not a positive multiple of 64", name, W->K);
     if (W->N <= 0) return fail(TF_ERR_INVALID_ARG, "%s: N=%d must be >= 1", name, W->N);
+    if ((long long)((W->N + kTileN - 1) / kTileN) * (W->K / kKChunk) > 0x7FFFFFFFLL)
+        return fail(TF_ERR_UNSUPPORTED, "%s: K x N too large for the split-K index space", name);
     return TF_OK;
 }
 

@@ -74,6 +74,18 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Sync *s
     return false;
 }
 
+// Balanced split of a problem's tot = T * Kc iterations into Pv contiguous
+// ranges: the first rem ranges hold q + 1 iterations, the others q
+// (q = tot / Pv, rem = tot % Pv, Pv <= tot).  Range p starts at p*q + min(p, rem).
+struct Split {
+    unsigned q, rem;
+    __device__ __forceinline__ unsigned start(unsigned p) const { return p * q + (p < rem ? p : rem); }
+    __device__ __forceinline__ unsigned owner(unsigned i) const {
+        const unsigned big = rem * (q + 1);
+        return i < big ? i / (q + 1) : rem + (i - big) / q;
+    }
+};
+
 // One 64-wide k slice of one 32-row feature block for this warp.  HI: the
 // launch has more than 8 rows (a second n8 MMA per sub-tile); rows 0..7 run the
 // identical instruction sequence in both instantiations.
@@ -195,14 +207,18 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     Sync *sy = reinterpret_cast<Sync *>(red + kFeatWarps * 32 * kLaneAcc);
 
     const int u = blockIdx.y;
+    // Grouped launches take their problem list from the preceding grid.
+    if (a.n_problems || a.expert_ids) grid_dependency_wait();
     const int nprob = a.n_problems ? *a.n_problems : 1;
     if (u >= nprob) return;
-    const long long tot = (long long)a.T * a.Kc;
+    const unsigned tot = unsigned(a.T) * unsigned(a.Kc);
+    const Split split{tot / unsigned(a.Pv), tot % unsigned(a.Pv)};
     const int vp = blockIdx.x;
-    const long long i0 = (long long)vp * tot / a.Pv;
-    const long long i1 = (long long)(vp + 1) * tot / a.Pv;
+    const unsigned i0 = split.start(vp);
+    const unsigned i1 = split.start(vp + 1);
     if (i0 >= i1) return;
     const int n_it = int(i1 - i0);
+    const unsigned Kc = unsigned(a.Kc);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -230,8 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
             int stage_kc[kStages];
             bool ok = true;
             for (int j = 0; j < n_it && ok;) {
-                const long long gi = i0 + j;
-                const int kc0 = int(gi % a.Kc);
+                const unsigned gi = i0 + unsigned(j);
+                const int kc0 = int(gi % Kc);
                 const int seg_len = min(n_it - j, a.Kc - kc0);
                 for (int sj = 0; sj < seg_len; sj += kStageIters, ++st) {
                     const int n_here = min(kStageIters, seg_len - sj);
@@ -247,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                         break;
                     }
                     mbar_arrive_expect_tx(&sy->full[s], uint32_t(n_here * CB + kXStageBytes));
-                    bulk_g2s_hint(sw + s * STW, wb + (gi + sj) * CB, uint32_t(n_here * CB), &sy->full[s], pol);
+                    bulk_g2s_hint(sw + s * STW, wb + (long long)(gi + sj) * CB, uint32_t(n_here * CB), &sy->full[s],
+                                  pol);
                     if (st < kStages) {
                         stage_kc[st] = kc0 + sj;
                     } else {
@@ -294,9 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     grid_dependency_wait();  // activations, workspace and outputs come from earlier grids
     int st = 0;  // stage counter, identical to the producer's
     for (int j = 0; j < n_it;) {
-        const long long gi = i0 + j;
-        const int t = int(gi / a.Kc);
-        const int kc0 = int(gi % a.Kc);
+        const unsigned gi = i0 + unsigned(j);
+        const int t = int(gi / Kc);
+        const int kc0 = int(gi - unsigned(t) * Kc);
         const int seg_len = min(n_it - j, a.Kc - kc0);
         for (int sj = 0; sj < seg_len; sj += kStageIters, ++st) {
             const int n_here = min(kStageIters, seg_len - sj);
@@ -312,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
             __syncwarp();
             if (lane == 0) mbar_arrive(&sy->empty[s]);
         }
-        const long long seg_b = gi, seg_e = gi + seg_len;
+        const unsigned seg_b = gi, seg_e = gi + unsigned(seg_len);
         j += seg_len;
         if (j == n_it && warp == 0 && lane == 0) grid_launch_dependents();  // main loop done: let the next grid start
 
@@ -335,32 +352,38 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 acc[q >> 1][q & 1][2] += o.z;
                 acc[q >> 1][q & 1][3] += o.w;
             }
-            const long long tb = (long long)t * a.Kc, te = tb + a.Kc;
+            const unsigned tb = unsigned(t) * Kc, te = tb + Kc;
             if (seg_b == tb && seg_e == te) {
                 store_block(a, yb, t, fw, gq, tq, hi, acc);
             } else {
                 // stream-K partial.  The last segment to finish sums every
                 // segment of this tile in ascending k order.  A warp that finds
                 // all other segments already published is last: it skips
-                // publishing its own and reads the others directly.
-                const int which = (t == int(i0 / a.Kc)) ? 0 : 1;
-                const int p_lo = int(((tb + 1) * a.Pv - 1) / tot);
-                const int p_hi = int((te * a.Pv - 1) / tot);
-                int nseg = 0;
-                for (int p2 = p_lo; p2 <= p_hi; ++p2)
-                    if ((long long)p2 * tot / a.Pv < (long long)(p2 + 1) * tot / a.Pv) ++nseg;
+                // publishing its own and reads the others directly.  Rows 8..15
+                // (accumulator half n = 1) travel only when the launch has them.
+                constexpr int NQ = HI ? 4 : 2;   // float4 per lane and segment
+                constexpr int NB = HI ? 2 : 4;   // segments loaded per round
+                const int p_lo = int(split.owner(tb));
+                const int p_hi = int(split.owner(te - 1));
+                const int nseg = p_hi - p_lo + 1;
+                // slot of segment p: index 0 if the tile is the first of p's range, else 1
+                auto slot_of = [&](int p) -> float4 * {
+                    const int which = split.start(unsigned(p)) >= tb ? 0 : 1;
+                    return a.partials + ((((long long)u * a.Pv + p) * 2 + which) * kFeatWarps + fw) * 128 + lane * 4;
+                };
                 unsigned *ctr = a.counters + ((long long)u * a.T + t) * kFeatWarps + fw;
                 unsigned old = 0;
                 if (lane == 0) old = ld_acquire_gpu(ctr);
                 old = __shfl_sync(0xFFFFFFFFu, old, 0);
                 const bool own_in_regs = old == unsigned(nseg - 1);
                 if (!own_in_regs) {
-                    float4 *slot = a.partials +
-                                   ((((long long)u * a.Pv + vp) * 2 + which) * kFeatWarps + fw) * 128 + lane * 4;
+                    float4 *slot = slot_of(vp);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
+                    for (int jq = 0; jq < NQ; ++jq) {
+                        const int q = HI ? jq : 2 * jq;
                         __stcg(slot + q, make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
                                                      acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3]));
+                    }
                     __threadfence();
                     __syncwarp();
                     if (lane == 0) old = atomicAdd(ctr, 1u);
@@ -369,66 +392,35 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 if (old == unsigned(nseg - 1)) {
                     __syncwarp();     // order every lane's reads after lane 0's acquire / atomic
                     __threadfence();
-                    const int me = vp;
                     float sum[2][2][4];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) sum[q >> 3][(q >> 2) & 1][q & 3] = 0.f;
-                    // segments in ascending k order, two loads in flight at a time
-                    // nullptr = "this CTA's own segment, still in registers" when
-                    // own_in_regs; segments are visited in ascending k order
-                    bool own_next = false;
-                    auto seg_src = [&](int &p) -> const float4 * {
-                        own_next = false;
-                        while (p <= p_hi) {
-                            const long long r0 = (long long)p * tot / a.Pv;
-                            const long long r1 = (long long)(p + 1) * tot / a.Pv;
-                            const int pp = p++;
-                            if (r0 < r1) {
-                                if (own_in_regs && pp == me) {
-                                    own_next = true;
-                                    return nullptr;
-                                }
-                                const int w2 = (t == int(r0 / a.Kc)) ? 0 : 1;
-                                return a.partials + ((((long long)u * a.Pv + pp) * 2 + w2) * kFeatWarps + fw) * 128 +
-                                       lane * 4;
+                    for (int pb = p_lo; pb <= p_hi; pb += NB) {
+                        float4 v[NB][NQ];
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) {
+                            const int p = pb + b;
+                            const bool mine = own_in_regs && p == vp;
+                            const float4 *src = (p <= p_hi && !mine) ? slot_of(p) : nullptr;
+#pragma unroll
+                            for (int jq = 0; jq < NQ; ++jq) {
+                                const int q = HI ? jq : 2 * jq;
+                                v[b][jq] = src ? __ldcg(src + q)
+                                               : make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
+                                                             acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3]);
                             }
                         }
-                        return nullptr;
-                    };
-                    int p2 = p_lo;
-                    while (p2 <= p_hi) {
-                        const float4 *s0 = seg_src(p2);
-                        const bool own0 = own_next;
-                        const float4 *s1 = seg_src(p2);
-                        const bool own1 = own_next;
-                        float4 v0[4], v1[4];
+                        // add in ascending k order
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            v0[q] = s0 ? __ldcg(s0 + q)
-                                       : own0 ? make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
-                                                            acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3])
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
-                            v1[q] = s1 ? __ldcg(s1 + q)
-                                       : own1 ? make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
-                                                            acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3])
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-                        if (s0 || own0) {
+                        for (int b = 0; b < NB; ++b) {
+                            if (pb + b > p_hi) break;
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                sum[q >> 1][q & 1][0] += v0[q].x;
-                                sum[q >> 1][q & 1][1] += v0[q].y;
-                                sum[q >> 1][q & 1][2] += v0[q].z;
-                                sum[q >> 1][q & 1][3] += v0[q].w;
-                            }
-                        }
-                        if (s1 || own1) {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                sum[q >> 1][q & 1][0] += v1[q].x;
-                                sum[q >> 1][q & 1][1] += v1[q].y;
-                                sum[q >> 1][q & 1][2] += v1[q].z;
-                                sum[q >> 1][q & 1][3] += v1[q].w;
+                            for (int jq = 0; jq < NQ; ++jq) {
+                                const int q = HI ? jq : 2 * jq;
+                                sum[q >> 1][q & 1][0] += v[b][jq].x;
+                                sum[q >> 1][q & 1][1] += v[b][jq].y;
+                                sum[q >> 1][q & 1][2] += v[b][jq].z;
+                                sum[q >> 1][q & 1][3] += v[b][jq].w;
                             }
                         }
                     }
