@@ -90,8 +90,8 @@ struct Split {
 // launch has more than 8 rows (a second n8 MMA per sub-tile); rows 0..7 run the
 // identical instruction sequence in both instantiations.
 template <int G, bool HI>
-__device__ __forceinline__ void consume_slice(const uint8_t *blk, uint32_t xslice, int lane, int gq, int lrow,
-                                              int lcol, float (&acc)[2][2][4]) {
+__device__ __forceinline__ void consume_slice(const uint8_t *blk, uint32_t xslice, int lane, int gq,
+                                              const uint32_t (&xoff)[4], float (&acc)[2][2][4]) {
     constexpr int NG = kKChunk / G;
     constexpr int KS = G / 16;
     const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + lane * 16);
@@ -103,8 +103,7 @@ __device__ __forceinline__ void consume_slice(const uint8_t *blk, uint32_t xslic
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
             const int j = grp * KS + kk;
-            // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
-            const uint32_t xa = xslice + lrow * 128 + ((((2 * j + lcol) ^ (lrow & 7))) << 4);
+            const uint32_t xa = xslice + xoff[j];
             uint32_t b0, b1, b2 = 0, b3 = 0;
             if (HI)
                 ldsm_x4(xa, b0, b1, b2, b3);
@@ -200,7 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     constexpr int STW = kStageIters * CB;
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-B aligned start, derived by pointer arithmetic so that the compiler
+    // keeps every access below in the shared state space
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sx = smem;                                  // [kStages][kXStageBytes], 1024-B aligned
     uint8_t *sw = sx + kStages * kXStageBytes;           // [kStages][STW]
     float *red = reinterpret_cast<float *>(sw + kStages * STW);   // [kFeatWarps][32][16]
@@ -293,8 +294,16 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     const int fw = warp % kFeatWarps;   // feature block
     const int gq = lane >> 2, tq = lane & 3;
     constexpr bool hi = HI;
-    const int lrow = (lane & 7) + ((lane >> 4) << 3);
-    const int lcol = (lane >> 3) & 1;
+    // ldmatrix row addresses: lane l supplies row (l & 7) + 8 * (l >> 4), 16-byte
+    // chunk (l >> 3) & 1 of k step j; with the 128-byte swizzle, chunk c of row r
+    // sits at chunk c ^ (r % 8)
+    uint32_t xoff[4];
+    {
+        const int lrow = (lane & 7) + ((lane >> 4) << 3);
+        const int lcol = (lane >> 3) & 1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) xoff[j] = uint32_t(lrow * 128 + (((2 * j + lcol) ^ (lrow & 7)) << 4));
+    }
     const size_t ysz = a.mode == kSwiGluBf16 ? sizeof(__nv_bfloat16) : sizeof(float);
     void *yb = static_cast<char *>(a.y) + (long long)u * a.y_stride * (long long)ysz;
     float4 *rb = reinterpret_cast<float4 *>(red) + fw * 32 * 4 + lane * 4;
@@ -323,8 +332,16 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 const uint8_t *stage_w = sw + s * STW + fw * BB;
                 const uint32_t stage_x = smem_u32(sx + s * kXStageBytes);
                 // slices of this stage whose global parity is kg
-                for (int p = ((j + sj) & 1) == kg ? 0 : 1; p < n_here; p += 2)
-                    consume_slice<G, HI>(stage_w + p * CB, stage_x + p * kXSliceBytes, lane, gq, lrow, lcol, acc);
+                const int p0 = ((j + sj) & 1) == kg ? 0 : 1;
+                if (!HI && n_here == kStageIters) {
+#pragma unroll
+                    for (int p = 0; p < kStageIters; p += 2)
+                        consume_slice<G, HI>(stage_w + (p0 + p) * CB, stage_x + (p0 + p) * kXSliceBytes, lane, gq,
+                                             xoff, acc);
+                } else {
+                    for (int p = p0; p < n_here; p += 2)
+                        consume_slice<G, HI>(stage_w + p * CB, stage_x + p * kXSliceBytes, lane, gq, xoff, acc);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sy->empty[s]);
