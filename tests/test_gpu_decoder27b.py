@@ -1,0 +1,53 @@
+"""The 27B-class synthetic decoder at full size: drafted decoding writes the
+same tokens as serial decoding.
+
+bf16 embedding 151936 x 5120 N(0, 0.02); 8 residual blocks of RMSNorm + W4
+group-64 SwiGLU MLP 5120 -> 17408 -> 5120; W4 LM head 5120 -> 151936.  For
+seeds 1234..1238: 64 tokens decoded one row per step, and the same 64 tokens
+decoded by verify passes of R = 8 rows whose drafts copy the serial tokens
+with probability 0.75 (else a uniform token); token_sha must be equal, and
+the device status must stay clean.
+"""
+
+import numpy as np
+import pytest
+
+from w4_gemm_keyed_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+V, H, F, N_BLOCKS, G = 151936, 5120, 17408, 8, 64
+
+
+@pytest.fixture(scope="module")
+def decoder27b(tf):
+    from w4_gemm_keyed_gb300 import decode
+    rng = inputs.rng_for(5)
+    blocks = []
+    for _ in range(N_BLOCKS):
+        gc, gs = inputs.w4_weights(rng, H, F, G)
+        uc, us = inputs.w4_weights(rng, H, F, G)
+        dc, ds = inputs.w4_weights(rng, F, H, G)
+        blocks.append(dict(gate_codes=gc, gate_scales=gs, up_codes=uc, up_scales=us, down_codes=dc, down_scales=ds))
+    lc, ls = inputs.w4_weights(rng, H, V, G)
+    weights = dict(emb=inputs.bf16_normal(rng, (V, H), 0.02), blocks=blocks, lm_codes=lc, lm_scales=ls, group=G)
+    model = decode.upload_model(weights)
+    del weights, blocks
+    return model, decode.Decoder(model)
+
+
+@pytest.mark.parametrize("seed", [1234, 1235, 1236, 1237, 1238])
+def test_drafted_equals_serial(tf, decoder27b, seed):
+    from w4_gemm_keyed_gb300 import decode
+    model, dec = decoder27b
+    T, k, p, n, R, prompt = 0.7, 20, 0.95, 64, 8, 11
+    serial = decode.serial_decode(dec, prompt, n, T, k, p, seed)
+    assert tf.workspace_status(dec.ws) == tf.TF_DEV_OK
+    rng = inputs.rng_for(502, seed)
+    future = np.array(serial + [0] * (R + 1))
+    drafted, lens = decode.drafted_decode(
+        dec, prompt, n, R, T, k, p, seed,
+        lambda pos0, m: inputs.noisy_drafts(rng, future[pos0 - 1: pos0 - 1 + m], 0.75, V))
+    assert decode.token_sha(drafted) == decode.token_sha(serial)
+    assert len(lens) < n  # the drafts were used
+    assert tf.workspace_status(dec.ws) == tf.TF_DEV_OK
