@@ -551,7 +551,7 @@ def main():
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "traffic": recorded_traffic(), "kernel": "w4_lane_gemm_kernel<64>"},
+                         "traffic": recorded_traffic(), "kernel": "w4_lane_gemm_kernel<64,HI>"},
             "per_launch": per_R,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": steps * launches_per_step,
