@@ -209,23 +209,35 @@ def time_per_launch(tf, torch, mats, reps=20):
 
 
 def time_dense_e2e(tf, torch, mats, steps, warmup):
-    """Same step through the C ABI with host buffers: H2D of x and D2H of y every step."""
+    """Same step through the C ABI with host buffers.  Every step copies all of
+    its inputs host->device in one pinned copy, runs the ten launches on slices
+    of the device buffers (leading dimensions through the ABI) and reads all
+    outputs back device->host in one copy."""
     stream = torch.cuda.current_stream()
     launches = dense_launches()
-    hx = {k: torch.from_numpy(m["x_host"].view(np.int16)).pin_memory() for k, m in mats.items()}
-    hy = {(K, N, R): torch.empty((R, N), dtype=torch.float32).pin_memory() for K, N, R in launches}
-    h2d = sum(R * K * 2 for K, N, R in launches)
-    d2h = sum(R * N * 4 for K, N, R in launches)
+    x_off, y_off, xo, yo = [], [], 0, 0
+    for K, N, R in launches:
+        x_off.append(xo)
+        y_off.append(yo)
+        xo += R * K
+        yo += R * N
+    hx = torch.empty(xo, dtype=torch.int16).pin_memory()
+    for (K, N, R), o in zip(launches, x_off):
+        hx[o:o + R * K] = torch.from_numpy(mats[(K, N)]["x_host"][:R].reshape(-1).view(np.int16))
+    hy = torch.empty(yo, dtype=torch.float32).pin_memory()
+    dx = torch.empty(xo, dtype=torch.int16, device="cuda")
+    dy = torch.empty(yo, dtype=torch.float32, device="cuda")
+    h2d, d2h = xo * 2, yo * 4
     counter = [0]
 
     def step():
-        for K, N, R in launches:
+        dx.copy_(hx, non_blocking=True)
+        for (K, N, R), xo_, yo_ in zip(launches, x_off, y_off):
             m = mats[(K, N)]
-            m["x"][:R].copy_(hx[(K, N)][:R], non_blocking=True)
             W = m["copies"][counter[0] % len(m["copies"])]
             counter[0] += 1
-            tf.lane_gemm_w4(W, m["x"][:R], y=m["y"][:R], ws=m["ws"])
-            hy[(K, N, R)].copy_(m["y"][:R], non_blocking=True)
+            tf.lane_gemm_w4(W, dx[xo_:xo_ + R * K].view(R, K), y=dy[yo_:yo_ + R * N].view(R, N), ws=m["ws"])
+        hy.copy_(dy, non_blocking=True)
 
     for _ in range(warmup):
         step()

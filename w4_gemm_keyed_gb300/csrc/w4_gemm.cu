@@ -197,15 +197,17 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     constexpr int BB = block_bytes(G);
     constexpr int CB = chunk_bytes(G);
     constexpr int STW = kStageIters * CB;
+    constexpr int NS = kStages;
+    constexpr int NQ = lane_vals(HI) / 4;   // float4 per lane in the combine and the fixup
 
     extern __shared__ uint8_t smem_raw[];
     // 1024-B aligned start, derived by pointer arithmetic so that the compiler
     // keeps every access below in the shared state space
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t *sx = smem;                                  // [kStages][kXStageBytes], 1024-B aligned
-    uint8_t *sw = sx + kStages * kXStageBytes;           // [kStages][STW]
-    float *red = reinterpret_cast<float *>(sw + kStages * STW);   // [kFeatWarps][32][16]
-    Sync *sy = reinterpret_cast<Sync *>(red + kFeatWarps * 32 * kLaneAcc);
+    uint8_t *sx = smem;                                  // [NS][kXStageBytes], 1024-B aligned
+    uint8_t *sw = sx + NS * kXStageBytes;                // [NS][STW]
+    float *red = reinterpret_cast<float *>(sw + NS * STW);   // [kFeatWarps][32][4 * NQ]
+    Sync *sy = reinterpret_cast<Sync *>(red + kFeatWarps * 32 * 4 * NQ);
 
     const int u = blockIdx.y;
     // Grouped launches take their problem list from the preceding grid.
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&sy->full[s], 1);
             mbar_init(&sy->empty[s], kConsumerWarps);
         }
@@ -240,11 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
         // ---------------- producer ----------------
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            // Weights are read-only model data: the first kStages stages are
+            // Weights are read-only model data: the first NS stages are
             // requested before waiting for the preceding grid (programmatic
             // dependent launch), their activation slices only after it.
             int st = 0, x_issued = 0;
-            int stage_kc[kStages];
+            int stage_kc[NS];
             bool ok = true;
             for (int j = 0; j < n_it && ok;) {
                 const unsigned gi = i0 + unsigned(j);
@@ -252,21 +254,21 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 const int seg_len = min(n_it - j, a.Kc - kc0);
                 for (int sj = 0; sj < seg_len; sj += kStageIters, ++st) {
                     const int n_here = min(kStageIters, seg_len - sj);
-                    const int s = st % kStages;
-                    if (st == kStages) {
+                    const int s = st % NS;
+                    if (st == NS) {
                         grid_dependency_wait();
-                        for (; x_issued < kStages; ++x_issued)
+                        for (; x_issued < NS; ++x_issued)
                             tma_load_4d(sx + x_issued * kXStageBytes, &a.xmap, 0, 0, stage_kc[x_issued],
                                         a.x_per_problem ? u : 0, &sy->full[x_issued]);
                     }
-                    if (st >= kStages && !wait_bar(&sy->empty[s], uint32_t(st / kStages - 1) & 1, sy, a.err)) {
+                    if (st >= NS && !wait_bar(&sy->empty[s], uint32_t(st / NS - 1) & 1, sy, a.err)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&sy->full[s], uint32_t(n_here * CB + kXStageBytes));
                     bulk_g2s_hint(sw + s * STW, wb + (long long)(gi + sj) * CB, uint32_t(n_here * CB), &sy->full[s],
                                   pol);
-                    if (st < kStages) {
+                    if (st < NS) {
                         stage_kc[st] = kc0 + sj;
                     } else {
                         tma_load_4d(sx + s * kXStageBytes, &a.xmap, 0, 0, kc0 + sj, a.x_per_problem ? u : 0,
@@ -275,16 +277,16 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 }
                 j += seg_len;
             }
-            if (x_issued < min(st, kStages)) {  // short ranges: fewer than kStages stages
+            if (x_issued < min(st, NS)) {  // short ranges: fewer than NS stages
                 grid_dependency_wait();
-                for (; x_issued < min(st, kStages); ++x_issued)
+                for (; x_issued < min(st, NS); ++x_issued)
                     tma_load_4d(sx + x_issued * kXStageBytes, &a.xmap, 0, 0, stage_kc[x_issued],
                                 a.x_per_problem ? u : 0, &sy->full[x_issued]);
             }
             const int issued = st;
             // leave only once every issued copy has landed (bounded)
-            for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
-                wait_bar(&sy->full[k % kStages], uint32_t(k / kStages) & 1, sy, a.err);
+            for (int k = (issued > NS ? issued - NS : 0); k < issued; ++k)
+                wait_bar(&sy->full[k % NS], uint32_t(k / NS) & 1, sy, a.err);
         }
         return;
     }
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     }
     const size_t ysz = a.mode == kSwiGluBf16 ? sizeof(__nv_bfloat16) : sizeof(float);
     void *yb = static_cast<char *>(a.y) + (long long)u * a.y_stride * (long long)ysz;
-    float4 *rb = reinterpret_cast<float4 *>(red) + fw * 32 * 4 + lane * 4;
+    float4 *rb = reinterpret_cast<float4 *>(red) + (fw * 32 + lane) * NQ;
     bool ok = true;
 
     float acc[2][2][4];
@@ -326,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
         const int seg_len = min(n_it - j, a.Kc - kc0);
         for (int sj = 0; sj < seg_len; sj += kStageIters, ++st) {
             const int n_here = min(kStageIters, seg_len - sj);
-            const int s = st % kStages;
-            if (ok) ok = wait_bar(&sy->full[s], uint32_t(st / kStages) & 1, sy, a.err);
+            const int s = st % NS;
+            if (ok) ok = wait_bar(&sy->full[s], uint32_t(st / NS) & 1, sy, a.err);
             if (ok) {
                 const uint8_t *stage_w = sw + s * STW + fw * BB;
                 const uint32_t stage_x = smem_u32(sx + s * kXStageBytes);
@@ -355,15 +357,18 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
         named_bar_sync(1 + fw, 64);
         if (kg == 1) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                rb[q] = make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1], acc[q >> 1][q & 1][2],
-                                    acc[q >> 1][q & 1][3]);
+            for (int jq = 0; jq < NQ; ++jq) {
+                const int q = HI ? jq : 2 * jq;
+                rb[jq] = make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1], acc[q >> 1][q & 1][2],
+                                     acc[q >> 1][q & 1][3]);
+            }
         }
         named_bar_sync(1 + fw, 64);
         if (kg == 0) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 o = rb[q];
+            for (int jq = 0; jq < NQ; ++jq) {
+                const int q = HI ? jq : 2 * jq;
+                const float4 o = rb[jq];
                 acc[q >> 1][q & 1][0] += o.x;
                 acc[q >> 1][q & 1][1] += o.y;
                 acc[q >> 1][q & 1][2] += o.z;
@@ -378,7 +383,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 // all other segments already published is last: it skips
                 // publishing its own and reads the others directly.  Rows 8..15
                 // (accumulator half n = 1) travel only when the launch has them.
-                constexpr int NQ = HI ? 4 : 2;   // float4 per lane and segment
                 constexpr int NB = HI ? 2 : 4;   // segments loaded per round
                 const int p_lo = int(split.owner(tb));
                 const int p_hi = int(split.owner(te - 1));
@@ -537,7 +541,7 @@ __global__ void pack_scales_kernel(const uint16_t *scales, int K, int N, uint8_t
 
 template <int G, bool HI>
 cudaError_t launch_gemm_g(const GemmArgs &a, int u_max, cudaStream_t s) {
-    const size_t smem = gemm_smem_bytes(G);
+    const size_t smem = gemm_smem_bytes(G, HI);
     cudaError_t err = cudaFuncSetAttribute(w4_lane_gemm_kernel<G, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            int(smem));
     if (err != cudaSuccess) return err;

@@ -31,20 +31,24 @@ constexpr int kConsumerWarps = kFeatWarps * kKGroups;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
 constexpr int kStageIters = 4;             // iterations per pipeline stage (one weight copy of ~35 KB)
 constexpr int kStages = 4;
+
 constexpr int kXSliceBytes = kRows * kKChunk * 2;     // [16 rows][64 k] bf16, 128-byte swizzled
 constexpr int kXStageBytes = kStageIters * kXSliceBytes;
-constexpr int kLaneAcc = 16;               // fp32 accumulators per lane: 2 sub-tiles x 2 row-halves x 4
+constexpr int kLaneAccHi = 16;             // fp32 accumulators per lane: 2 sub-tiles x 2 row-halves x 4
+// fp32 values per lane exchanged by the k-group combine and the split-K fixup:
+// rows 8..15 (accumulator half n = 1) only when the launch has them
+__host__ __device__ constexpr int lane_vals(bool hi) { return hi ? kLaneAccHi : kLaneAccHi / 2; }
 
 __host__ __device__ constexpr int block_bytes(int G) { return 1024 + 64 * (kKChunk / G); }
 __host__ __device__ constexpr int chunk_bytes(int G) { return kFeatWarps * block_bytes(G); }
 // One partial tile of the split-K fixup: 8 feature warps x 32 lanes x 16 floats.
-constexpr size_t kSlotBytes = size_t(kFeatWarps) * 32 * kLaneAcc * 4;
+constexpr size_t kSlotBytes = size_t(kFeatWarps) * 32 * kLaneAccHi * 4;
 
-inline size_t gemm_smem_bytes(int G) {
+inline size_t gemm_smem_bytes(int G, bool hi) {
     return 1024                                                         // alignment slack
            + size_t(kStages) * kXStageBytes                             // activation slices (1024-B aligned)
            + size_t(kStages) * kStageIters * chunk_bytes(G)            // weight stages
-           + size_t(kFeatWarps) * 32 * kLaneAcc * 4                     // k-group combine buffer
+           + size_t(kFeatWarps) * 32 * lane_vals(hi) * 4                // k-group combine buffer
            + 256;                                                       // barriers
 }
 
