@@ -17,80 +17,94 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 // MoE routing (TensorFold README: MoE kernels over 4-bit group-32 weights; the
-// 30B-A3B class routes each token to its top-8 of 128 experts).
-__global__ void route_kernel(const float *router, int E, int top_k, int32_t *ids, float *w, int *err) {
-    __shared__ unsigned long long s_best[32];
-    __shared__ int s_sel[kMaxRouteK];
-    __shared__ int s_bad;
-    const int r = blockIdx.x, tid = threadIdx.x;
-    const float z = tid < E ? router[(long long)r * E + tid] : 0.f;
-    if (tid == 0) s_bad = 0;
-    __syncthreads();
-    if (tid < E && !isfinite(z)) atomicOr(&s_bad, 1);
-    __syncthreads();
-    if (s_bad) {
-        if (tid == 0) set_error(err, 2);
-        if (tid < top_k) {
-            ids[r * kMaxRouteK + tid] = tid;
-            w[r * kMaxRouteK + tid] = 0.f;
-        }
-        return;
-    }
-    // composite key: (logit desc, id asc); distinct for distinct ids
-    unsigned long long key =
-        tid < E ? ((unsigned long long)order_key(z) << 32) | (0xFFFFFFFFull - (unsigned)tid) : 0ull;
-    for (int j = 0; j < top_k; ++j) {
-        unsigned long long m = key;
-        for (int o = 16; o > 0; o >>= 1) {
-            const unsigned long long v = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-            m = v > m ? v : m;
-        }
-        if ((tid & 31) == 0) s_best[tid >> 5] = m;
-        __syncthreads();
-        if (tid == 0) {
-            unsigned long long b = 0;
-            for (int i = 0; i < int(blockDim.x + 31) / 32; ++i) b = s_best[i] > b ? s_best[i] : b;
-            s_sel[j] = int(0xFFFFFFFFull - (b & 0xFFFFFFFFull));
-        }
-        __syncthreads();
-        if (tid == s_sel[j]) key = 0ull;  // remove the chosen expert
-    }
-    if (tid == 0) {
-        double e[kMaxRouteK];
-        const double z0 = double(router[(long long)r * E + s_sel[0]]);
-        double tot = 0.0;
-        for (int j = 0; j < top_k; ++j) {
-            e[j] = exp(double(router[(long long)r * E + s_sel[j]]) - z0);
-            tot += e[j];
-        }
-        for (int j = 0; j < top_k; ++j) {
-            ids[r * kMaxRouteK + j] = s_sel[j];
-            w[r * kMaxRouteK + j] = float(e[j] / tot);
-        }
-    }
-}
-
-__global__ void expert_list_kernel(const int32_t *ids, int R, int E, int top_k, int32_t *expert_ids,
-                                   int32_t *n_problems, int32_t *slot_of) {
+// 30B-A3B class routes each token to its top-8 of 128 experts), followed by the
+// list of touched experts, in one CTA: warp r routes row r, then warp 0 numbers
+// the touched experts in ascending id.
+__global__ void route_list_kernel(const float *router, int R, int E, int top_k, int32_t *ids, float *w,
+                                  int32_t *expert_ids, int32_t *n_problems, int32_t *slot_of, int *err) {
+    constexpr int KE = kMaxExperts / 32;   // experts per lane
     __shared__ int touched[kMaxExperts];
     __shared__ int pos[kMaxExperts];
-    const int tid = threadIdx.x;
+    __shared__ int s_ids[kMaxRows][kMaxRouteK];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int e = tid; e < kMaxExperts; e += blockDim.x) touched[e] = 0;
     __syncthreads();
-    for (int i = tid; i < R * top_k; i += blockDim.x) touched[ids[(i / top_k) * kMaxRouteK + i % top_k]] = 1;
-    __syncthreads();
-    if (tid == 0) {
-        int n = 0;
-        for (int e = 0; e < E; ++e) {
-            pos[e] = n;
-            if (touched[e]) expert_ids[n++] = e;
+    if (warp < R) {
+        const int r = warp;
+        const float *z = router + (long long)r * E;
+        // composite key (logit desc, id asc), distinct for distinct ids; 0 = absent
+        unsigned long long key[KE];
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < KE; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) {
+                const float v = z[e];
+                bad |= !isfinite(v);
+                key[i] = ((unsigned long long)order_key(v) << 32) | (0xFFFFFFFFull - (unsigned)e);
+            } else {
+                key[i] = 0ull;
+            }
         }
-        *n_problems = n;
+        if (__any_sync(0xFFFFFFFFu, bad)) {
+            if (lane == 0) set_error(err, 2);
+            if (lane < top_k) {
+                s_ids[r][lane] = lane;
+                ids[r * kMaxRouteK + lane] = lane;
+                w[r * kMaxRouteK + lane] = 0.f;
+            }
+        } else {
+            for (int j = 0; j < top_k; ++j) {
+                unsigned long long m = key[0];
+#pragma unroll
+                for (int i = 1; i < KE; ++i) m = key[i] > m ? key[i] : m;
+                for (int o = 16; o > 0; o >>= 1) {
+                    const unsigned long long v = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+                    m = v > m ? v : m;
+                }
+                const int sel = int(0xFFFFFFFFull - (m & 0xFFFFFFFFull));
+#pragma unroll
+                for (int i = 0; i < KE; ++i)
+                    if (lane + 32 * i == sel) key[i] = 0ull;   // remove the chosen expert
+                if (lane == 0) s_ids[r][j] = sel;
+            }
+            __syncwarp();
+            // renormalised weights over the kept experts: fp64, summed in rank order
+            double ej = 0.0;
+            if (lane < top_k) ej = exp(double(z[s_ids[r][lane]]) - double(z[s_ids[r][0]]));
+            double e_all[kMaxRouteK];
+#pragma unroll
+            for (int j = 0; j < kMaxRouteK; ++j) e_all[j] = __shfl_sync(0xFFFFFFFFu, ej, j);
+            if (lane == 0) {
+                double tot = 0.0;
+                for (int j = 0; j < top_k; ++j) tot += e_all[j];
+                for (int j = 0; j < top_k; ++j) {
+                    ids[r * kMaxRouteK + j] = s_ids[r][j];
+                    w[r * kMaxRouteK + j] = float(e_all[j] / tot);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane < top_k) touched[s_ids[r][lane]] = 1;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int base = 0;
+        for (int c = 0; c < KE; ++c) {
+            const int e = c * 32 + lane;
+            const int f = e < E ? touched[e] : 0;
+            const unsigned b = __ballot_sync(0xFFFFFFFFu, f);
+            const int before = __popc(b & ((1u << lane) - 1u));
+            pos[e] = base + before;
+            if (f) expert_ids[base + before] = e;
+            base += __popc(b);
+        }
+        if (lane == 0) *n_problems = base;
     }
     __syncthreads();
     for (int i = tid; i < R * top_k; i += blockDim.x) {
         const int r = i / top_k, j = i % top_k;
-        slot_of[r * kMaxRouteK + j] = pos[ids[r * kMaxRouteK + j]];
+        slot_of[r * kMaxRouteK + j] = pos[s_ids[r][j]];
     }
 }
 
@@ -144,15 +158,9 @@ __global__ void rmsnorm_bf16_kernel(const float *x, int H, float eps, uint16_t *
 
 }  // namespace
 
-cudaError_t launch_route(const float *router, int R, int E, int top_k, int32_t *ids, float *w, int *err,
-                         cudaStream_t s) {
-    route_kernel<<<R, kMaxExperts, 0, s>>>(router, E, top_k, ids, w, err);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_expert_list(const int32_t *ids, int R, int E, int top_k, int32_t *expert_ids,
-                               int32_t *n_problems, int32_t *slot_of, cudaStream_t s) {
-    expert_list_kernel<<<1, 256, 0, s>>>(ids, R, E, top_k, expert_ids, n_problems, slot_of);
+cudaError_t launch_route_list(const float *router, int R, int E, int top_k, int32_t *ids, float *w,
+                              int32_t *expert_ids, int32_t *n_problems, int32_t *slot_of, int *err, cudaStream_t s) {
+    route_list_kernel<<<1, 32 * R, 0, s>>>(router, R, E, top_k, ids, w, expert_ids, n_problems, slot_of, err);
     return cudaGetLastError();
 }
 

@@ -8,14 +8,13 @@ namespace tfk {
 constexpr int kMaxExperts = 256;
 constexpr int kMaxRouteK = 8;
 
+constexpr int kMaxRows = 16;
 // Per row: experts ranked by (router logit desc, id asc), first top_k kept,
-// renormalised weights computed in fp64 and stored as fp32.
-cudaError_t launch_route(const float *router, int R, int E, int top_k, int32_t *ids, float *w, int *err,
-                         cudaStream_t s);
-// Touched experts in ascending id: expert_ids[0..U), *n_problems = U,
-// slot_of[r][j] = index u of ids[r][j].
-cudaError_t launch_expert_list(const int32_t *ids, int R, int E, int top_k, int32_t *expert_ids,
-                               int32_t *n_problems, int32_t *slot_of, cudaStream_t s);
+// renormalised weights computed in fp64 and stored as fp32; then the touched
+// experts in ascending id: expert_ids[0..U), *n_problems = U, and
+// slot_of[r][j] = index u of ids[r][j].  One CTA, R <= kMaxRows.
+cudaError_t launch_route_list(const float *router, int R, int E, int top_k, int32_t *ids, float *w,
+                              int32_t *expert_ids, int32_t *n_problems, int32_t *slot_of, int *err, cudaStream_t s);
 // out[r][n] = sum_j w[r][j] * Y[slot_of[r][j]][r][n], j ascending (fp32 FMA chain).
 cudaError_t launch_combine(const float *Y, const int32_t *slot_of, const float *w, int R, int H, int top_k,
                            float *out, cudaStream_t s);

@@ -478,8 +478,8 @@ tf_status tf_moe_w4(const tf_moe_layer *L, const uint16_t *x, const float *route
     float *Y = reinterpret_cast<float *>(base + m.Y);
     int *err = reinterpret_cast<int *>(base);
 
-    cudaError_t e = launch_route(router_logits, R, L->n_experts, L->top_k, ids, w, err, s);
-    if (e == cudaSuccess) e = launch_expert_list(ids, R, L->n_experts, L->top_k, expert_ids, nprob, slot_of, s);
+    cudaError_t e = launch_route_list(router_logits, R, L->n_experts, L->top_k, ids, w, expert_ids, nprob,
+                                      slot_of, err, s);
     if (e != cudaSuccess) return cuda_fail(e, "tf_moe_w4 routing");
 
     // gate/up (+ SwiGLU) for every touched expert, all R rows

@@ -209,18 +209,15 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     float *red = reinterpret_cast<float *>(sw + NS * STW);   // [kFeatWarps][32][4 * NQ]
     Sync *sy = reinterpret_cast<Sync *>(red + kFeatWarps * 32 * 4 * NQ);
 
-    const int u = blockIdx.y;
-    // Grouped launches take their problem list from the preceding grid.
+    // Work items are (problem u, range vp) pairs, u-major; CTA b takes items
+    // b, b + gridDim.x, ...  Grouped launches take their problem list from the
+    // preceding grid.
     if (a.n_problems || a.expert_ids) grid_dependency_wait();
     const int nprob = a.n_problems ? *a.n_problems : 1;
-    if (u >= nprob) return;
+    const int n_items = nprob * a.Pv;
+    if (int(blockIdx.x) >= n_items) return;
     const unsigned tot = unsigned(a.T) * unsigned(a.Kc);
-    const Split split{tot / unsigned(a.Pv), tot % unsigned(a.Pv)};
-    const int vp = blockIdx.x;
-    const unsigned i0 = split.start(vp);
-    const unsigned i1 = split.start(vp + 1);
-    if (i0 >= i1) return;
-    const int n_it = int(i1 - i0);
+    const Split split{tot / unsigned(a.Pv), tot % unsigned(a.Pv)};   // Pv <= tot: no empty range
     const unsigned Kc = unsigned(a.Kc);
 
     const int warp = threadIdx.x >> 5;
@@ -235,9 +232,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     }
     __syncthreads();
 
-    const int e = a.expert_ids ? a.expert_ids[u] : u;
-    const uint8_t *wb = a.w + (long long)e * a.w_stride;
-
     if (warp == kConsumerWarps) {
         // ---------------- producer ----------------
         if (lane == 0) {
@@ -246,8 +240,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
             // requested before waiting for the preceding grid (programmatic
             // dependent launch), their activation slices only after it.
             int st = 0, x_issued = 0;
-            int stage_kc[NS];
+            int stage_kc[NS], stage_u[NS];
             bool ok = true;
+            for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const int u = item / a.Pv, vp = item - u * a.Pv;
+            const int xu = a.x_per_problem ? u : 0;
+            const uint8_t *wb = a.w + (long long)(a.expert_ids ? a.expert_ids[u] : u) * a.w_stride;
+            const unsigned i0 = split.start(vp);
+            const int n_it = int(split.start(vp + 1) - i0);
             for (int j = 0; j < n_it && ok;) {
                 const unsigned gi = i0 + unsigned(j);
                 const int kc0 = int(gi % Kc);
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                         grid_dependency_wait();
                         for (; x_issued < NS; ++x_issued)
                             tma_load_4d(sx + x_issued * kXStageBytes, &a.xmap, 0, 0, stage_kc[x_issued],
-                                        a.x_per_problem ? u : 0, &sy->full[x_issued]);
+                                        stage_u[x_issued], &sy->full[x_issued]);
                     }
                     if (st >= NS && !wait_bar(&sy->empty[s], uint32_t(st / NS - 1) & 1, sy, a.err)) {
                         ok = false;
@@ -270,18 +270,19 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                                   pol);
                     if (st < NS) {
                         stage_kc[st] = kc0 + sj;
+                        stage_u[st] = xu;
                     } else {
-                        tma_load_4d(sx + s * kXStageBytes, &a.xmap, 0, 0, kc0 + sj, a.x_per_problem ? u : 0,
-                                    &sy->full[s]);
+                        tma_load_4d(sx + s * kXStageBytes, &a.xmap, 0, 0, kc0 + sj, xu, &sy->full[s]);
                     }
                 }
                 j += seg_len;
             }
+            }
             if (x_issued < min(st, NS)) {  // short ranges: fewer than NS stages
                 grid_dependency_wait();
                 for (; x_issued < min(st, NS); ++x_issued)
-                    tma_load_4d(sx + x_issued * kXStageBytes, &a.xmap, 0, 0, stage_kc[x_issued],
-                                a.x_per_problem ? u : 0, &sy->full[x_issued]);
+                    tma_load_4d(sx + x_issued * kXStageBytes, &a.xmap, 0, 0, stage_kc[x_issued], stage_u[x_issued],
+                                &sy->full[x_issued]);
             }
             const int issued = st;
             // leave only once every issued copy has landed (bounded)
@@ -307,7 +308,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
         for (int j = 0; j < 4; ++j) xoff[j] = uint32_t(lrow * 128 + (((2 * j + lcol) ^ (lrow & 7)) << 4));
     }
     const size_t ysz = a.mode == kSwiGluBf16 ? sizeof(__nv_bfloat16) : sizeof(float);
-    void *yb = static_cast<char *>(a.y) + (long long)u * a.y_stride * (long long)ysz;
     float4 *rb = reinterpret_cast<float4 *>(red) + (fw * 32 + lane) * NQ;
     bool ok = true;
 
@@ -321,6 +321,12 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
 
     grid_dependency_wait();  // activations, workspace and outputs come from earlier grids
     int st = 0;  // stage counter, identical to the producer's
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int u = item / a.Pv, vp = item - u * a.Pv;
+    const bool last_item = item + int(gridDim.x) >= n_items;
+    void *yb = static_cast<char *>(a.y) + (long long)u * a.y_stride * (long long)ysz;
+    const unsigned i0 = split.start(vp);
+    const int n_it = int(split.start(vp + 1) - i0);
     for (int j = 0; j < n_it;) {
         const unsigned gi = i0 + unsigned(j);
         const int t = int(gi / Kc);
@@ -350,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
         }
         const unsigned seg_b = gi, seg_e = gi + unsigned(seg_len);
         j += seg_len;
-        if (j == n_it && warp == 0 && lane == 0) grid_launch_dependents();  // main loop done: let the next grid start
+        if (j == n_it && last_item && warp == 0 && lane == 0) grid_launch_dependents();  // let the next grid start
 
         // ---- segment end: combine the k-parity groups in a fixed order (0 + 1);
         // warps fw and fw + 8 pair up through their own named barrier
@@ -457,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[mt][n][c] = 0.f;
     }
+    }
 }
 
 // ---- load-time repack: canonical [N][K/2] nibbles + [N][K/G] fp16 -> kernel layout
@@ -546,7 +553,11 @@ cudaError_t launch_gemm_g(const GemmArgs &a, int u_max, cudaStream_t s) {
                                            int(smem));
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.Pv, u_max);
+    // persistent over work items: at most one CTA per SM
+    const long long items = (long long)a.Pv * u_max;
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 1;
+    cfg.gridDim = dim3(unsigned(items < sms ? items : sms));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
