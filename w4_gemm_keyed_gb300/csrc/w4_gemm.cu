@@ -411,14 +411,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                         __stcg(slot + q, make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
                                                      acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3]));
                     }
-                    __threadfence();
+                    // the warp barrier orders every lane's stores before lane 0's
+                    // release; the acquire half orders the reads below
                     __syncwarp();
-                    if (lane == 0) old = atomicAdd(ctr, 1u);
+                    if (lane == 0) old = atom_add_acq_rel_gpu(ctr, 1u);
                     old = __shfl_sync(0xFFFFFFFFu, old, 0);
                 }
                 if (old == unsigned(nseg - 1)) {
-                    __syncwarp();     // order every lane's reads after lane 0's acquire / atomic
-                    __threadfence();
+                    __syncwarp();     // every lane's reads after lane 0's acquire
                     float sum[2][2][4];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) sum[q >> 3][(q >> 2) & 1][q & 3] = 0.f;
