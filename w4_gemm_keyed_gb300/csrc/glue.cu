@@ -22,6 +22,8 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 // the touched experts in ascending id.
 __global__ void route_list_kernel(const float *router, int R, int E, int top_k, int32_t *ids, float *w,
                                   int32_t *expert_ids, int32_t *n_problems, int32_t *slot_of, int *err) {
+    grid_dependency_wait();     // inputs come from the preceding grid
+    grid_launch_dependents();
     constexpr int KE = kMaxExperts / 32;   // experts per lane
     __shared__ int touched[kMaxExperts];
     __shared__ int pos[kMaxExperts];
@@ -110,6 +112,8 @@ __global__ void route_list_kernel(const float *router, int R, int E, int top_k, 
 
 __global__ void combine_kernel(const float *Y, const int32_t *slot_of, const float *w, int R, int H, int top_k,
                                float *out) {
+    grid_dependency_wait();     // inputs come from the preceding grid
+    grid_launch_dependents();
     const int r = blockIdx.y;
     const int n = blockIdx.x * blockDim.x + threadIdx.x;
     if (n >= H) return;
@@ -123,6 +127,8 @@ __global__ void combine_kernel(const float *Y, const int32_t *slot_of, const flo
 
 __global__ void embed_kernel(const uint16_t *emb, int V, int H, const int32_t *last_token, const int32_t *drafts,
                              float *x, int *err) {
+    grid_dependency_wait();     // inputs come from the preceding grid
+    grid_launch_dependents();
     const int r = blockIdx.x;
     int tok = r == 0 ? *last_token : drafts[r - 1];
     if (tok < 0 || tok >= V) {
@@ -135,6 +141,8 @@ __global__ void embed_kernel(const uint16_t *emb, int V, int H, const int32_t *l
 }
 
 __global__ void rmsnorm_bf16_kernel(const float *x, int H, float eps, uint16_t *out) {
+    grid_dependency_wait();     // inputs come from the preceding grid
+    grid_launch_dependents();
     __shared__ float s_part[32];
     const int r = blockIdx.x, tid = threadIdx.x;
     const float *xr = x + (long long)r * H;
@@ -160,25 +168,22 @@ __global__ void rmsnorm_bf16_kernel(const float *x, int H, float eps, uint16_t *
 
 cudaError_t launch_route_list(const float *router, int R, int E, int top_k, int32_t *ids, float *w,
                               int32_t *expert_ids, int32_t *n_problems, int32_t *slot_of, int *err, cudaStream_t s) {
-    route_list_kernel<<<1, 32 * R, 0, s>>>(router, R, E, top_k, ids, w, expert_ids, n_problems, slot_of, err);
-    return cudaGetLastError();
+    return launch_pdl(route_list_kernel, dim3(1), dim3(32 * R), 0, s, router, R, E, top_k, ids, w, expert_ids, n_problems,
+                      slot_of, err);
 }
 
 cudaError_t launch_combine(const float *Y, const int32_t *slot_of, const float *w, int R, int H, int top_k,
                            float *out, cudaStream_t s) {
-    combine_kernel<<<dim3((H + 255) / 256, R), 256, 0, s>>>(Y, slot_of, w, R, H, top_k, out);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3((H + 255) / 256, R), dim3(256), 0, s, Y, slot_of, w, R, H, top_k, out);
 }
 
 cudaError_t launch_embed(const uint16_t *emb, int V, int H, const int32_t *last_token, const int32_t *drafts,
                          int R, float *x, int *err, cudaStream_t s) {
-    embed_kernel<<<R, 256, 0, s>>>(emb, V, H, last_token, drafts, x, err);
-    return cudaGetLastError();
+    return launch_pdl(embed_kernel, dim3(R), dim3(256), 0, s, emb, V, H, last_token, drafts, x, err);
 }
 
 cudaError_t launch_rmsnorm_bf16(const float *x, int R, int H, float eps, uint16_t *out, cudaStream_t s) {
-    rmsnorm_bf16_kernel<<<R, 256, 0, s>>>(x, H, eps, out);
-    return cudaGetLastError();
+    return launch_pdl(rmsnorm_bf16_kernel, dim3(R), dim3(256), 0, s, x, H, eps, out);
 }
 
 }  // namespace tfk

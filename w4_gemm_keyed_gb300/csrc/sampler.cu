@@ -143,6 +143,8 @@ __device__ uint32_t select_top(const uint32_t (&key)[E], const int32_t (&id)[E],
 }
 
 __global__ void __launch_bounds__(kSampleThreads) topk_partial_kernel(const SampleArgs a) {
+    grid_dependency_wait();     // inputs come from the preceding grid
+    grid_launch_dependents();
     __shared__ uint32_t hist[256];
     __shared__ int sh[4];
     __shared__ int s_cnt, s_bad;
@@ -199,6 +201,8 @@ __global__ void __launch_bounds__(kSampleThreads) topk_partial_kernel(const Samp
 }
 
 __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleArgs a) {
+    grid_dependency_wait();     // inputs come from the preceding grid
+    grid_launch_dependents();
     __shared__ uint32_t hist[256];
     __shared__ int sh[4];
     __shared__ int s_cnt, s_m;
@@ -302,6 +306,8 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleAr
 
 __global__ void accept_kernel(const int32_t *drafts, const int32_t *sampled, int R, int32_t *accepted,
                               int32_t *bonus, int64_t *pos) {
+    grid_dependency_wait();     // inputs come from the preceding grid
+    grid_launch_dependents();
     const int lane = threadIdx.x;
     const bool mismatch = lane < R - 1 && drafts[lane] != sampled[lane];
     const uint32_t m = __ballot_sync(0xFFFFFFFFu, mismatch);
@@ -344,15 +350,14 @@ void sample_bind_workspace(SampleArgs &a, void *ws_region, int R, int V) {
 
 cudaError_t launch_keyed_sample(const SampleArgs &a, cudaStream_t s) {
     if (a.n_chunks > kMaxChunks) return cudaErrorInvalidValue;
-    topk_partial_kernel<<<dim3(a.n_chunks, a.R), kSampleThreads, 0, s>>>(a);
-    finalize_kernel<<<a.R, kSampleThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(topk_partial_kernel, dim3(a.n_chunks, a.R), dim3(kSampleThreads), 0, s, a);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(finalize_kernel, dim3(a.R), dim3(kSampleThreads), 0, s, a);
 }
 
 cudaError_t launch_accept(const int32_t *drafts, const int32_t *sampled, int R, int32_t *accepted, int32_t *bonus,
                           int64_t *pos, cudaStream_t s) {
-    accept_kernel<<<1, 32, 0, s>>>(drafts, sampled, R, accepted, bonus, pos);
-    return cudaGetLastError();
+    return launch_pdl(accept_kernel, dim3(1), dim3(32), 0, s, drafts, sampled, R, accepted, bonus, pos);
 }
 
 int sample_max_vocab() { return kMaxChunks * kSampleChunk; }

@@ -244,6 +244,27 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
     return v;
 }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// before the preceding grid in the stream finishes.  Every kernel launched this
+// way calls grid_dependency_wait() before it reads anything an earlier grid
+// wrote and before it finishes, so that ordering stays transitive along the
+// stream.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 // Record the first device-side error of a launch in the workspace status word.
 __device__ __forceinline__ void set_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
