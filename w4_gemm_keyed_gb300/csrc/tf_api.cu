@@ -42,10 +42,14 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 constexpr int kGroupedPv = 16;  // virtual CTAs per MoE expert problem
 
+// Ranges of a dense launch.  When the tiles nearly fill the SMs, each CTA takes
+// whole tiles and no tile is split (no split-K fixup); otherwise a stream-K
+// split over all SMs.  The choice depends on the shape only, never on R.
 int dense_pv(int T, int Kc) {
     const long long tot = (long long)T * Kc;
     int sms = device_sm_count();
     if (sms <= 0) sms = 1;
+    if (T <= sms && 8LL * T >= 7LL * sms) return T;
     return int(tot < sms ? tot : sms);
 }
 
