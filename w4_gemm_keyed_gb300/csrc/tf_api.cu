@@ -40,7 +40,7 @@ tf_status cuda_fail(cudaError_t e, const char *what) {
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-constexpr int kGroupedPv = 16;  // virtual CTAs per MoE expert problem
+constexpr int kGroupedPv = 8;   // ranges per MoE expert problem (fixed: bits must not depend on R)
 
 // Ranges of a dense launch.  When the tiles nearly fill the SMs, each CTA takes
 // whole tiles and no tile is split (no split-K fixup); otherwise a stream-K
