@@ -419,6 +419,22 @@ def host_mats():
 
 
 # ----------------------------------------------------------------------------- main
+def max_over_ranks(value: float, world: int, device: str) -> float:
+    """The largest value over all ranks: the whole job's time is its slowest rank's."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, world: int, secs: float) -> float:
+    """Replicas (weak scaling): every rank streams its own copy of the step's bytes."""
+    return bytes_per_step * steps * world / secs / 1e9
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -517,12 +533,8 @@ def main():
     with ClockSampler(local) as clk:
         secs, steps, launches_per_step = time_dense(tf, torch, mats, args.steps, args.warmup)
     barrier()
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([secs], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = float(t.item())
-    value = STEP_BYTES * steps * world / secs / 1e9
+    secs = max_over_ranks(secs, world, "cuda")
+    value = whole_job_gbs(STEP_BYTES, steps, world, secs)
     peak, peak_kind = peaks()
     # every launch of the step streams the same number of bytes; the average
     # launch duration over the timed region includes the inter-kernel gaps
@@ -536,8 +548,12 @@ def main():
                                   "frac": bytes_per_launch(K, N) / (ms * 1e-3) / 1e9 / peak}
 
     # ---- end to end through the C ABI with host buffers
-    e2e_secs, h2d, d2h = time_dense_e2e(tf, torch, mats, max(10, args.steps // 4), args.warmup)
-    e2e_value = STEP_BYTES * max(10, args.steps // 4) * world / e2e_secs / 1e9
+    e2e_steps = max(10, args.steps // 4)
+    barrier()
+    e2e_secs, h2d, d2h = time_dense_e2e(tf, torch, mats, e2e_steps, args.warmup)
+    barrier()
+    e2e_secs = max_over_ranks(e2e_secs, world, "cuda")
+    e2e_value = whole_job_gbs(STEP_BYTES, e2e_steps, world, e2e_secs)
 
     extra = {}
     if rank == 0 and not args.no_extra:
