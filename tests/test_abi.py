@@ -51,7 +51,7 @@ def test_only_declared_symbols_are_exported(lib):
 
 def test_packed_size_and_status_strings(lib):
     from w4_gemm_keyed_gb300 import tf
-    # 256-feature tiles x 64-wide k slices; G=64 -> 4*(2048+128) bytes per stage
+    # 128-feature tiles x 64-wide k slices (N padded to a multiple of 128)
     assert tf.packed_bytes(5120, 17408, 64) == 68 * 80 * 4 * 2176
     assert tf.packed_bytes(256, 1000, 64) == 4 * 4 * 4 * 2176         # N padded to 1024
     assert tf.packed_bytes(2048, 1536, 32) == 6 * 32 * 4 * 2304

@@ -42,14 +42,16 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 constexpr int kGroupedPv = 8;   // ranges per MoE expert problem (fixed: bits must not depend on R)
 
-// Ranges of a dense launch.  When the tiles nearly fill the SMs, each CTA takes
-// whole tiles and no tile is split (no split-K fixup); otherwise a stream-K
-// split over all SMs.  The choice depends on the shape only, never on R.
+// Ranges of a dense launch.  When an even share of m whole tiles per CTA
+// (m = 1..4) nearly fills the SMs, no tile is split (no split-K fixup);
+// otherwise a stream-K split over all SMs.  The choice depends on the shape
+// only, never on R.
 int dense_pv(int T, int Kc) {
     const long long tot = (long long)T * Kc;
     int sms = device_sm_count();
     if (sms <= 0) sms = 1;
-    if (T <= sms && 8LL * T >= 7LL * sms) return T;
+    for (int m = 1; m <= 4; ++m)
+        if (T % m == 0 && T / m <= sms && 8LL * (T / m) >= 7LL * sms) return T / m;
     return int(tot < sms ? tot : sms);
 }
 

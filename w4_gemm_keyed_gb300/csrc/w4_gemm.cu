@@ -198,16 +198,18 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     constexpr int CB = chunk_bytes(G);
     constexpr int STW = kStageIters * CB;
     constexpr int NS = kStages;
+    constexpr int XSL = x_slice_bytes(HI);
+    constexpr int XST = x_stage_bytes(HI);
     constexpr int NQ = lane_vals(HI) / 4;   // float4 per lane in the combine and the fixup
 
     extern __shared__ uint8_t smem_raw[];
     // 1024-B aligned start, derived by pointer arithmetic so that the compiler
     // keeps every access below in the shared state space
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t *sx = smem;                                  // [NS][kXStageBytes], 1024-B aligned
-    uint8_t *sw = sx + NS * kXStageBytes;                // [NS][STW]
-    float *red = reinterpret_cast<float *>(sw + NS * STW);   // [kFeatWarps][32][4 * NQ]
-    Sync *sy = reinterpret_cast<Sync *>(red + kFeatWarps * 32 * 4 * NQ);
+    uint8_t *sx = smem;                                  // [NS][XST], 1024-B aligned
+    uint8_t *sw = sx + NS * XST;                         // [NS][STW]
+    float *red = reinterpret_cast<float *>(sw + NS * STW);   // [2][kFeatWarps][32][4 * NQ]
+    Sync *sy = reinterpret_cast<Sync *>(red + 2 * kFeatWarps * 32 * 4 * NQ);
 
     // Work items are (problem u, range vp) pairs, u-major; CTA b takes items
     // b, b + gridDim.x, ...  Grouped launches take their problem list from the
@@ -258,21 +260,21 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                     if (st == NS) {
                         grid_dependency_wait();
                         for (; x_issued < NS; ++x_issued)
-                            tma_load_4d(sx + x_issued * kXStageBytes, &a.xmap, 0, 0, stage_kc[x_issued],
+                            tma_load_4d(sx + x_issued * XST, &a.xmap, 0, 0, stage_kc[x_issued],
                                         stage_u[x_issued], &sy->full[x_issued]);
                     }
                     if (st >= NS && !wait_bar(&sy->empty[s], uint32_t(st / NS - 1) & 1, sy, a.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&sy->full[s], uint32_t(n_here * CB + kXStageBytes));
+                    mbar_arrive_expect_tx(&sy->full[s], uint32_t(n_here * CB + XST));
                     bulk_g2s_hint(sw + s * STW, wb + (long long)(gi + sj) * CB, uint32_t(n_here * CB), &sy->full[s],
                                   pol);
                     if (st < NS) {
                         stage_kc[st] = kc0 + sj;
                         stage_u[st] = xu;
                     } else {
-                        tma_load_4d(sx + s * kXStageBytes, &a.xmap, 0, 0, kc0 + sj, xu, &sy->full[s]);
+                        tma_load_4d(sx + s * XST, &a.xmap, 0, 0, kc0 + sj, xu, &sy->full[s]);
                     }
                 }
                 j += seg_len;
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
             if (x_issued < min(st, NS)) {  // short ranges: fewer than NS stages
                 grid_dependency_wait();
                 for (; x_issued < min(st, NS); ++x_issued)
-                    tma_load_4d(sx + x_issued * kXStageBytes, &a.xmap, 0, 0, stage_kc[x_issued], stage_u[x_issued],
+                    tma_load_4d(sx + x_issued * XST, &a.xmap, 0, 0, stage_kc[x_issued], stage_u[x_issued],
                                 &sy->full[x_issued]);
             }
             const int issued = st;
@@ -308,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
         for (int j = 0; j < 4; ++j) xoff[j] = uint32_t(lrow * 128 + (((2 * j + lcol) ^ (lrow & 7)) << 4));
     }
     const size_t ysz = a.mode == kSwiGluBf16 ? sizeof(__nv_bfloat16) : sizeof(float);
-    float4 *rb = reinterpret_cast<float4 *>(red) + (fw * 32 + lane) * NQ;
+    float4 *rb_a = reinterpret_cast<float4 *>(red) + (fw * 32 + lane) * NQ;
+    float4 *rb_b = rb_a + kFeatWarps * 32 * NQ;
     bool ok = true;
 
     float acc[2][2][4];
@@ -338,17 +341,17 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
             if (ok) ok = wait_bar(&sy->full[s], uint32_t(st / NS) & 1, sy, a.err);
             if (ok) {
                 const uint8_t *stage_w = sw + s * STW + fw * BB;
-                const uint32_t stage_x = smem_u32(sx + s * kXStageBytes);
-                // slices of this stage whose global parity is kg
-                const int p0 = ((j + sj) & 1) == kg ? 0 : 1;
+                const uint32_t stage_x = smem_u32(sx + s * XST);
+                // slices of this stage whose index within the range is kg mod kKGroups
+                const int p0 = (kg - (j + sj)) & (kKGroups - 1);
                 if (!HI && n_here == kStageIters) {
 #pragma unroll
-                    for (int p = 0; p < kStageIters; p += 2)
-                        consume_slice<G, HI>(stage_w + (p0 + p) * CB, stage_x + (p0 + p) * kXSliceBytes, lane, gq,
+                    for (int p = 0; p < kStageIters; p += kKGroups)
+                        consume_slice<G, HI>(stage_w + (p0 + p) * CB, stage_x + (p0 + p) * XSL, lane, gq,
                                              xoff, acc);
                 } else {
-                    for (int p = p0; p < n_here; p += 2)
-                        consume_slice<G, HI>(stage_w + p * CB, stage_x + p * kXSliceBytes, lane, gq, xoff, acc);
+                    for (int p = p0; p < n_here; p += kKGroups)
+                        consume_slice<G, HI>(stage_w + p * CB, stage_x + p * XSL, lane, gq, xoff, acc);
                 }
             }
             __syncwarp();
@@ -358,19 +361,17 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
         j += seg_len;
         if (j == n_it && last_item && warp == 0 && lane == 0) grid_launch_dependents();  // let the next grid start
 
-        // ---- segment end: combine the k-parity groups in a fixed order (0 + 1);
-        // warps fw and fw + 8 pair up through their own named barrier
-        named_bar_sync(1 + fw, 64);
-        if (kg == 1) {
+        // ---- segment end: combine the k-groups in a fixed order, (0 + 1) + (2 + 3);
+        // the four warps of feature block fw meet at their own named barrier
+        auto put_rb = [&](float4 *rb) {
 #pragma unroll
             for (int jq = 0; jq < NQ; ++jq) {
                 const int q = HI ? jq : 2 * jq;
                 rb[jq] = make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1], acc[q >> 1][q & 1][2],
                                      acc[q >> 1][q & 1][3]);
             }
-        }
-        named_bar_sync(1 + fw, 64);
-        if (kg == 0) {
+        };
+        auto add_rb = [&](const float4 *rb) {
 #pragma unroll
             for (int jq = 0; jq < NQ; ++jq) {
                 const int q = HI ? jq : 2 * jq;
@@ -380,6 +381,19 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 acc[q >> 1][q & 1][2] += o.z;
                 acc[q >> 1][q & 1][3] += o.w;
             }
+        };
+        named_bar_sync(1 + fw, 32 * kKGroups);
+        if (kg == 1) put_rb(rb_a);
+        if (kg == 3) put_rb(rb_b);
+        named_bar_sync(1 + fw, 32 * kKGroups);
+        if (kg == 0) add_rb(rb_a);          // 0 + 1
+        if (kg == 2) {
+            add_rb(rb_b);                   // 2 + 3, written back over the slot it came from
+            put_rb(rb_b);
+        }
+        named_bar_sync(1 + fw, 32 * kKGroups);
+        if (kg == 0) {
+            add_rb(rb_b);                   // (0 + 1) + (2 + 3)
             const unsigned tb = unsigned(t) * Kc, te = tb + Kc;
             if (seg_b == tb && seg_e == te) {
                 store_block(a, yb, t, fw, gq, tq, hi, acc);
@@ -625,7 +639,7 @@ bool gemm_encode_x(GemmArgs &a, const uint16_t *x, int ldx, long long x_stride, 
     cuuint64_t dims[4] = {cuuint64_t(kKChunk), cuuint64_t(a.R), cuuint64_t(a.Kc), cuuint64_t(per ? u_max : 1)};
     cuuint64_t strides[3] = {cuuint64_t(ldx) * 2, cuuint64_t(kKChunk) * 2,
                              per ? cuuint64_t(x_stride) * 2 : cuuint64_t(ldx) * 2 * cuuint64_t(a.R)};
-    cuuint32_t box[4] = {cuuint32_t(kKChunk), cuuint32_t(kRows), cuuint32_t(kStageIters), 1};
+    cuuint32_t box[4] = {cuuint32_t(kKChunk), cuuint32_t(x_rows(a.R > 8)), cuuint32_t(kStageIters), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUresult r = fn(&a.xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(x), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

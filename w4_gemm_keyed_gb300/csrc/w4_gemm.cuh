@@ -8,11 +8,11 @@
 namespace tfk {
 
 // ---- packed weight layout --------------------------------------------------
-// Output features are grouped in tiles of 256 = 8 "feature blocks" of 32 rows
-// (one consumer warp each).  For every tile t and every 64-wide slice kc of the
-// input features there is one contiguous "chunk", and consecutive kc of a tile
-// are consecutive in memory, so any run of iterations of one tile is one bulk
-// copy.  A chunk is 8 feature blocks; a block holds
+// Output features are grouped in tiles of 128 = 4 "feature blocks" of 32 rows
+// (one consumer warp per k-group each).  For every tile t and every 64-wide
+// slice kc of the input features there is one contiguous "chunk", and
+// consecutive kc of a tile are consecutive in memory, so any run of iterations
+// of one tile is one bulk copy.  A chunk is 4 feature blocks; a block holds
 //   codes : [mt 0..1][lane 0..31][16 B]       1024 B
 //   scales: [grp][g 0..7][mt 0..1] half2      64 B per quantisation group
 // Lane (g = lane/4, q = lane%4) of the warp owns, for the 16-row sub-tile mt and
@@ -22,18 +22,21 @@ namespace tfk {
 //   i=2: (row g,   k 2q+8 | 2q+9)    i=3: (row g+8, k 2q+8 | 2q+9)
 // and the half2 (s[row g], s[row g+8]) of each sub-tile are the lane's scales.
 constexpr int kBlockRows = 32;             // weight rows per consumer warp
-constexpr int kFeatWarps = 8;              // feature blocks per tile
-constexpr int kTileN = kBlockRows * kFeatWarps;   // 256 output features per tile
+constexpr int kFeatWarps = 4;              // feature blocks per tile
+constexpr int kTileN = kBlockRows * kFeatWarps;   // 128 output features per tile
 constexpr int kKChunk = 64;                // k per iteration
 constexpr int kRows = 16;                  // verify rows (MMA columns), zero-padded
-constexpr int kKGroups = 2;                // consumer warp groups splitting the iterations by parity
+constexpr int kKGroups = 4;                // consumer warp groups taking every fourth k slice
 constexpr int kConsumerWarps = kFeatWarps * kKGroups;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
-constexpr int kStageIters = 4;             // iterations per pipeline stage (one weight copy of ~35 KB)
+constexpr int kStageIters = 8;             // iterations per pipeline stage (one weight copy of ~35 KB)
 constexpr int kStages = 4;
 
-constexpr int kXSliceBytes = kRows * kKChunk * 2;     // [16 rows][64 k] bf16, 128-byte swizzled
-constexpr int kXStageBytes = kStageIters * kXSliceBytes;
+// Activation slice in shared memory: [rows][64 k] bf16, 128-byte swizzled; 16
+// rows when the launch has more than 8, else 8 (rows >= R are zero-filled).
+__host__ __device__ constexpr int x_rows(bool hi) { return hi ? kRows : kRows / 2; }
+__host__ __device__ constexpr int x_slice_bytes(bool hi) { return x_rows(hi) * kKChunk * 2; }
+__host__ __device__ constexpr int x_stage_bytes(bool hi) { return kStageIters * x_slice_bytes(hi); }
 constexpr int kLaneAccHi = 16;             // fp32 accumulators per lane: 2 sub-tiles x 2 row-halves x 4
 // fp32 values per lane exchanged by the k-group combine and the split-K fixup:
 // rows 8..15 (accumulator half n = 1) only when the launch has them
@@ -41,14 +44,14 @@ __host__ __device__ constexpr int lane_vals(bool hi) { return hi ? kLaneAccHi : 
 
 __host__ __device__ constexpr int block_bytes(int G) { return 1024 + 64 * (kKChunk / G); }
 __host__ __device__ constexpr int chunk_bytes(int G) { return kFeatWarps * block_bytes(G); }
-// One partial tile of the split-K fixup: 8 feature warps x 32 lanes x 16 floats.
+// One partial tile of the split-K fixup: 4 feature warps x 32 lanes x 16 floats.
 constexpr size_t kSlotBytes = size_t(kFeatWarps) * 32 * kLaneAccHi * 4;
 
 inline size_t gemm_smem_bytes(int G, bool hi) {
     return 1024                                                         // alignment slack
-           + size_t(kStages) * kXStageBytes                             // activation slices (1024-B aligned)
+           + size_t(kStages) * x_stage_bytes(hi)                        // activation slices (1024-B aligned)
            + size_t(kStages) * kStageIters * chunk_bytes(G)            // weight stages
-           + size_t(kFeatWarps) * 32 * lane_vals(hi) * 4                // k-group combine buffer
+           + 2 * size_t(kFeatWarps) * 32 * lane_vals(hi) * 4            // k-group combine buffers
            + 256;                                                       // barriers
 }
 
