@@ -95,7 +95,7 @@ TF_API tf_status tf_workspace_status(void *ws, void *stream, int32_t *code);
  *   w[n][k] = code(n, k) * scale(n, k / G)   (symmetric, no zero point).
  * The kernels read a private "packed" layout produced on the device by
  * tf_pack_w4 (a load-time step).  Its size is tf_w4_packed_bytes(); N is padded
- * up to a multiple of 256 with zero weights inside it.
+ * up to a multiple of 128 with zero weights inside it.
  */
 typedef struct tf_w4_matrix {
     const void *packed;   /* dev, tf_w4_packed_bytes(K, N, group) bytes, 256-B aligned */
@@ -162,7 +162,7 @@ TF_API tf_status tf_lane_gemm_w4(const tf_w4_matrix *W, const uint16_t *x, int32
  * - The first call on a device (made with that device current) looks up the
  *   array's address; make that first call before any stream capture.
  * - A launch whose scratch need exceeds the array (it grows with the device's
- *   SM count: 256 B + 256 KiB + 32 KiB per SM) returns TF_ERR_UNSUPPORTED and
+ *   SM count: 256 B + 256 KiB + 16 KiB per SM) returns TF_ERR_UNSUPPORTED and
  *   launches nothing.
  * - Every call on a device shares the one array, which keeps what the last call
  *   left; each call clears the parts that must start at zero on `stream`
