@@ -6,15 +6,20 @@
 // "--temperature 0" is greedy.  Acceptance: a draft is accepted exactly when it
 // equals the token serial decoding samples there.
 //
-// Two launches per call:
+// Two launches per call.  Candidates are ordered by the composite key
+// (logit desc, id asc), unique per token.
 //   1. topk_partial: grid (ceil(V/4096), R).  Each CTA keeps 16 logits per
-//      thread in registers (coalesced loads), finds its chunk's k-th largest
-//      (logit, -id) key with a 4-pass 8-bit radix select over a shared
-//      histogram, breaks ties at the threshold by a second radix select on the
-//      ids, and writes its <= k candidates.  It also flags non-finite logits.
-//   2. finalize: one CTA per row merges the <= 64 * chunks candidates with the
-//      same select, orders the k' survivors by (logit desc, id asc), computes
-//      the top-p prefix in fp64 left to right, then the Gumbel argmax.
+//      thread in registers (coalesced loads).  The k-th largest of the 256
+//      per-thread maxima bounds the chunk's k-th largest from below (k threads
+//      hold an element at or above it), so only the few elements at or above it
+//      survive; each survivor's rank among them gives the chunk's top k in
+//      order.  When ties leave too many survivors, a 4-pass 8-bit radix select
+//      over a shared histogram (ties at the threshold broken by a second select
+//      on the ids) picks them instead.  Non-finite logits flag the row.
+//   2. finalize: one CTA per row.  The largest of the chunks' k-th best keys
+//      bounds the row's k-th best from below; the candidates at or above it are
+//      ranked the same way (radix select as the fallback), giving the k' best in
+//      order; then the top-p prefix in fp64 left to right and the Gumbel argmax.
 // Every decision depends on the row's own logits only, so a row's token is the
 // same whatever R is.
 #include <cuda_runtime.h>
@@ -29,6 +34,12 @@ namespace {
 constexpr int kE1 = kSampleChunk / kSampleThreads;  // 16 logits per thread in a chunk
 constexpr int kE2 = 32;                             // pool entries per thread in finalize
 constexpr int kMaxChunks = kE2 * kSampleThreads / kMaxTopK;  // 128
+constexpr int kSurvMax = 1024;                      // survivors ranked directly (else radix select)
+
+__device__ __forceinline__ uint64_t composite(uint32_t key, int32_t id) {
+    return (uint64_t(key) << 32) | uint64_t(0xFFFFFFFFu - uint32_t(id));
+}
+__device__ __forceinline__ int32_t composite_id(uint64_t c) { return int32_t(0xFFFFFFFFu - uint32_t(c)); }
 
 // Order-preserving key: larger float -> larger key; -0 and +0 share a key.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -185,19 +196,77 @@ __global__ void __launch_bounds__(kSampleThreads) topk_partial_kernel(const Samp
     }
     const int n_valid = min(kSampleChunk, a.V - base);
     const int k = min(a.k_eff, n_valid);
-    const uint32_t chosen = select_top<kE1>(key, id, valid, k, hist, sh);
+    float *out_val = a.cand_val + (long long)slot0 * kMaxTopK;
+    int32_t *out_id = a.cand_id + (long long)slot0 * kMaxTopK;
+
+    // lower bound: the k-th largest per-thread maximum (0 when fewer than k threads hold one)
+    __shared__ uint64_t s_tmax[kSampleThreads];
+    __shared__ uint64_t s_surv[kSurvMax];
+    __shared__ uint64_t s_L;
+    __shared__ int s_ns;
+    uint64_t ck[kE1];
+    uint64_t tmax = 0;
 #pragma unroll
     for (int e = 0; e < kE1; ++e) {
-        if ((chosen >> e) & 1u) {
-            const int s = atomicAdd(&s_cnt, 1);
-            if (s < kMaxTopK) {
-                a.cand_val[(long long)slot0 * kMaxTopK + s] = key_value(key[e]);
-                a.cand_id[(long long)slot0 * kMaxTopK + s] = id[e];
-            }
-        }
+        ck[e] = ((valid >> e) & 1u) ? composite(key[e], id[e]) : 0ull;
+        tmax = ck[e] > tmax ? ck[e] : tmax;
+    }
+    s_tmax[threadIdx.x] = tmax;
+    if (threadIdx.x == 0) {
+        s_L = 0ull;
+        s_ns = 0;
     }
     __syncthreads();
-    if (threadIdx.x == 0) a.cand_cnt[slot0] = min(s_cnt, kMaxTopK);
+    if (tmax != 0ull) {
+        int above = 0;
+        for (int j = 0; j < kSampleThreads; ++j) above += s_tmax[j] > tmax;
+        if (above == k - 1) s_L = tmax;
+    }
+    __syncthreads();
+    const uint64_t L = s_L;
+#pragma unroll
+    for (int e = 0; e < kE1; ++e)
+        if (ck[e] != 0ull && ck[e] >= L) {
+            const int q = atomicAdd(&s_ns, 1);
+            if (q < kSurvMax) s_surv[q] = ck[e];
+        }
+    __syncthreads();
+    const int ns = s_ns;
+    if (ns <= kSurvMax) {
+        // the k best survivors, written in order
+        for (int i = threadIdx.x; i < ns; i += kSampleThreads) {
+            const uint64_t v = s_surv[i];
+            int rank = 0;
+            for (int j = 0; j < ns; ++j) rank += s_surv[j] > v;
+            if (rank < k) {
+                out_val[rank] = key_value(uint32_t(v >> 32));
+                out_id[rank] = composite_id(v);
+                if (rank == k - 1) a.cand_kth[slot0] = k == a.k_eff ? v : 0ull;
+            }
+        }
+    } else {
+        const uint32_t chosen = select_top<kE1>(key, id, valid, k, hist, sh);
+        uint64_t kmin = ~0ull;
+#pragma unroll
+        for (int e = 0; e < kE1; ++e) {
+            if ((chosen >> e) & 1u) {
+                const int q = atomicAdd(&s_cnt, 1);
+                if (q < kMaxTopK) {
+                    out_val[q] = key_value(key[e]);
+                    out_id[q] = id[e];
+                }
+                kmin = ck[e] < kmin ? ck[e] : kmin;
+            }
+        }
+        // the k-th best is the smallest chosen key
+        __shared__ unsigned long long s_kmin;
+        if (threadIdx.x == 0) s_kmin = ~0ull;
+        __syncthreads();
+        if (kmin != ~0ull) atomicMin(&s_kmin, (unsigned long long)kmin);
+        __syncthreads();
+        if (threadIdx.x == 0) a.cand_kth[slot0] = k == a.k_eff ? uint64_t(s_kmin) : 0ull;
+    }
+    if (threadIdx.x == 0) a.cand_cnt[slot0] = k;
 }
 
 __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleArgs a) {
@@ -211,29 +280,31 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleAr
     __shared__ double ex[kMaxTopK], score[kMaxTopK];
     const int r = blockIdx.x;
     const int tid = threadIdx.x;
-    uint32_t key[kE2];
-    int32_t id[kE2];
-    uint32_t valid = 0;
-    int n_total = 0;
-    for (int c = 0; c < a.n_chunks; ++c) n_total += a.cand_cnt[r * a.n_chunks + c];
-#pragma unroll
-    for (int e = 0; e < kE2; ++e) {
-        const int p = e * kSampleThreads + tid;
-        const int c = p / kMaxTopK, s = p % kMaxTopK;
-        key[e] = 0;
-        id[e] = 0;
-        if (c < a.n_chunks && s < a.cand_cnt[r * a.n_chunks + c]) {
-            const long long q = (long long)(r * a.n_chunks + c) * kMaxTopK + s;
-            key[e] = order_key(a.cand_val[q]);
-            id[e] = a.cand_id[q];
-            valid |= 1u << e;
-        }
+    const int nc = a.n_chunks;
+    __shared__ int s_ccnt[kMaxChunks];
+    __shared__ unsigned long long s_L;
+    __shared__ int s_total, s_ns;
+    __shared__ uint64_t s_surv[kSurvMax];
+    __shared__ uint64_t s_tmax[kSampleThreads];
+    if (tid == 0) {
+        s_L = 0ull;
+        s_total = 0;
+        s_ns = 0;
+        s_cnt = 0;
     }
-    if (tid == 0) s_cnt = 0;
     __syncthreads();
+    // chunk counts, their total, and the bound: the largest chunk k-th best
+    for (int c = tid; c < nc; c += kSampleThreads) {
+        const int cnt = a.cand_cnt[r * nc + c];
+        s_ccnt[c] = cnt;
+        atomicAdd(&s_total, cnt);
+        const unsigned long long kth = a.cand_kth[r * nc + c];
+        if (kth) atomicMax(&s_L, kth);
+    }
+    __syncthreads();
+    const int n_total = s_total;
     const bool bad = a.row_bad[r] != 0;
     if (bad || n_total == 0) {
-        __syncthreads();
         if (tid == 0) {
             a.tokens[r] = -1;
             a.row_bad[r] = 0;  // leave the workspace clean for the next call
@@ -241,30 +312,82 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleAr
         return;
     }
     const int k = min(a.k_eff, n_total);
-    const uint32_t chosen = select_top<kE2>(key, id, valid, k, hist, sh);
+    uint64_t ck[kE2];
+    uint64_t tmax = 0ull;
 #pragma unroll
     for (int e = 0; e < kE2; ++e) {
-        if ((chosen >> e) & 1u) {
-            const int s = atomicAdd(&s_cnt, 1);
-            if (s < kMaxTopK) {
-                sel_val[s] = key_value(key[e]);
-                sel_id[s] = id[e];
+        const int p = e * kSampleThreads + tid;
+        const int c = p / kMaxTopK, s = p % kMaxTopK;
+        ck[e] = 0ull;
+        if (c < nc && s < s_ccnt[c]) {
+            const long long q = (long long)(r * nc + c) * kMaxTopK + s;
+            ck[e] = composite(order_key(a.cand_val[q]), a.cand_id[q]);
+        }
+        tmax = ck[e] > tmax ? ck[e] : tmax;
+    }
+    // a second bound, as in topk_partial: the k-th largest per-thread maximum
+    s_tmax[tid] = tmax;
+    __syncthreads();
+    if (tmax != 0ull) {
+        int above = 0;
+        for (int j = 0; j < kSampleThreads; ++j) above += s_tmax[j] > tmax;
+        if (above == k - 1) atomicMax(&s_L, (unsigned long long)tmax);
+    }
+    __syncthreads();
+    const uint64_t L = s_L;
+    // candidates at or above the bounds
+#pragma unroll
+    for (int e = 0; e < kE2; ++e)
+        if (ck[e] != 0ull && ck[e] >= L) {
+            const int q = atomicAdd(&s_ns, 1);
+            if (q < kSurvMax) s_surv[q] = ck[e];
+        }
+    __syncthreads();
+    const int ns = s_ns;
+    if (ns <= kSurvMax) {
+        for (int i = tid; i < ns; i += kSampleThreads) {
+            const uint64_t v = s_surv[i];
+            int rank = 0;
+            for (int j = 0; j < ns; ++j) rank += s_surv[j] > v;
+            if (rank < k) {
+                srt_val[rank] = key_value(uint32_t(v >> 32));
+                srt_id[rank] = composite_id(v);
             }
+        }
+        if (tid == 0) s_cnt = k;
+    } else {
+        uint32_t key[kE2];
+        int32_t id[kE2];
+        uint32_t valid = 0;
+#pragma unroll
+        for (int e = 0; e < kE2; ++e) {
+            key[e] = uint32_t(ck[e] >> 32);
+            id[e] = composite_id(ck[e]);
+            if (ck[e] != 0ull) valid |= 1u << e;
+        }
+        const uint32_t chosen = select_top<kE2>(key, id, valid, k, hist, sh);
+#pragma unroll
+        for (int e = 0; e < kE2; ++e) {
+            if ((chosen >> e) & 1u) {
+                const int q = atomicAdd(&s_cnt, 1);
+                if (q < kMaxTopK) {
+                    sel_val[q] = key_value(key[e]);
+                    sel_id[q] = id[e];
+                }
+            }
+        }
+        __syncthreads();
+        const int n_sel = min(s_cnt, kMaxTopK);
+        if (tid < n_sel) {  // rank sort by (logit desc, id asc)
+            const uint64_t ki = composite(order_key(sel_val[tid]), sel_id[tid]);
+            int rank = 0;
+            for (int j = 0; j < n_sel; ++j) rank += composite(order_key(sel_val[j]), sel_id[j]) > ki;
+            srt_val[rank] = sel_val[tid];
+            srt_id[rank] = sel_id[tid];
         }
     }
     __syncthreads();
     const int n_sel = min(s_cnt, kMaxTopK);
-    if (tid < n_sel) {  // rank sort by (logit desc, id asc)
-        const uint32_t ki = order_key(sel_val[tid]);
-        int rank = 0;
-        for (int j = 0; j < n_sel; ++j) {
-            const uint32_t kj = order_key(sel_val[j]);
-            rank += (kj > ki) || (kj == ki && sel_id[j] < sel_id[tid]);
-        }
-        srt_val[rank] = sel_val[tid];
-        srt_id[rank] = sel_id[tid];
-    }
-    __syncthreads();
     if (a.temperature == 0.0f) {
         if (tid == 0) a.tokens[r] = srt_id[0];
         return;
@@ -273,15 +396,22 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleAr
     const double p = double(a.top_p);
     const int64_t pos = a.pos ? a.pos[r] : (*a.pos_base + r);
     if (p < 1.0) {
+        __shared__ double s_Z;
         if (tid < n_sel) ex[tid] = exp((double(srt_val[tid]) - double(srt_val[0])) / T);
         __syncthreads();
         if (tid == 0) {
             double Z = 0.0;
             for (int i = 0; i < n_sel; ++i) Z += ex[i];
+            s_Z = Z;
+        }
+        __syncthreads();
+        if (tid < n_sel) score[tid] = ex[tid] / s_Z;   // q_i, each term on its own thread
+        __syncthreads();
+        if (tid == 0) {
             double S = 0.0;
             int m = n_sel;
-            for (int i = 0; i < n_sel; ++i) {
-                S += ex[i] / Z;
+            for (int i = 0; i < n_sel; ++i) {   // renormalised mass summed left to right
+                S += score[i];
                 if (S >= p) {
                     m = i + 1;
                     break;
@@ -294,13 +424,28 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleAr
     }
     __syncthreads();
     const int m = s_m;
+    // Gumbel-max over the m candidates (ties to the lower id): one score per
+    // thread, then a shuffle reduction in warp 0
     if (tid < m) score[tid] = double(srt_val[tid]) / T + gumbel(a.seed, pos, srt_id[tid]);
     __syncthreads();
-    if (tid == 0) {
-        int best = 0;
-        for (int i = 1; i < m; ++i)
-            if (score[i] > score[best] || (score[i] == score[best] && srt_id[i] < srt_id[best])) best = i;
-        a.tokens[r] = srt_id[best];
+    if (tid < 32) {
+        double best = -1.0 / 0.0;
+        int best_id = 0x7FFFFFFF;
+        for (int i = tid; i < m; i += 32) {
+            if (score[i] > best || (score[i] == best && srt_id[i] < best_id)) {
+                best = score[i];
+                best_id = srt_id[i];
+            }
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            const double ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+            const int oid = __shfl_xor_sync(0xFFFFFFFFu, best_id, o);
+            if (ob > best || (ob == best && oid < best_id)) {
+                best = ob;
+                best_id = oid;
+            }
+        }
+        if (tid == 0) a.tokens[r] = best_id;
     }
 }
 
@@ -330,6 +475,7 @@ static int n_chunks_of(int V) { return (V + kSampleChunk - 1) / kSampleChunk; }
 size_t sample_workspace_bytes(int R, int V) {
     const size_t nc = size_t(n_chunks_of(V));
     size_t b = 256;  // row_bad[kMaxRows]
+    b += size_t(R) * nc * sizeof(uint64_t);
     b += size_t(R) * nc * kMaxTopK * (sizeof(float) + sizeof(int32_t));
     b += size_t(R) * nc * sizeof(int32_t);
     return (b + 255) / 256 * 256;
@@ -340,6 +486,8 @@ void sample_bind_workspace(SampleArgs &a, void *ws_region, int R, int V) {
     char *p = static_cast<char *>(ws_region);
     a.row_bad = reinterpret_cast<int32_t *>(p);
     p += 256;
+    a.cand_kth = reinterpret_cast<uint64_t *>(p);
+    p += size_t(R) * nc * sizeof(uint64_t);
     a.cand_val = reinterpret_cast<float *>(p);
     p += size_t(R) * nc * kMaxTopK * sizeof(float);
     a.cand_id = reinterpret_cast<int32_t *>(p);

@@ -25,6 +25,7 @@ struct SampleArgs {
     float *cand_val;      // [R][n_chunks][64]
     int32_t *cand_id;     // [R][n_chunks][64]
     int32_t *cand_cnt;    // [R][n_chunks]
+    uint64_t *cand_kth;   // [R][n_chunks]: (key, id) of the chunk's k-th best when it kept k_eff, else 0
     int32_t *row_bad;     // [R]
     int *err;
     int n_chunks;
