@@ -105,3 +105,19 @@ def test_strided_activations_and_outputs(tf):
     yb = ybig.cpu().numpy()
     assert np.all(yb[:, N:] == 7.0)
     assert_close_rows(yb[:, :N], oracle.w4_linear(codes, scales, x, G))
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 4])
+def test_whole_tile_ranges_match_oracle_and_are_row_invariant(tf, m):
+    """Shapes whose tiles split evenly into nearly one share per SM take whole
+    tiles per CTA (no split-K): 140 * m tiles of 128 features."""
+    K, G = 128, 64
+    N = 128 * 140 * m
+    rng = inputs.rng_for(104, m)
+    codes, scales = inputs.w4_weights(rng, K, N, G)
+    x = inputs.bf16_normal(rng, (16, K))
+    W = pack(tf, codes, scales, G)
+    y16 = run(tf, W, x)
+    assert_close_rows(y16[:3], oracle.w4_linear(codes, scales, x[:3], G))
+    y1 = run(tf, W, x[:1])
+    assert np.array_equal(y1.view(np.uint32), y16[:1].view(np.uint32))

@@ -4,22 +4,23 @@
 // one-row step": up to 16 drafted rows share one launch that streams every
 // 4-bit weight once, and row r's bits never depend on how many rows there are.
 //
-// One CTA per SM, 17 warps:
-//   warp 16 producer: per pipeline stage (up to 4 consecutive 64-wide k slices
-//           of one 256-feature tile, never crossing a tile boundary) one lane
+// At most one CTA per SM, 17 warps, persistent over work items (problem,
+// range of the tile x k-slice iteration space):
+//   warp 16 producer: per pipeline stage (up to 8 consecutive 64-wide k slices
+//           of one 128-feature tile, never crossing a tile boundary) one lane
 //           issues ONE bulk TMA copy of the packed weights (~35 KB, L2
 //           evict-first; the bulk engine only reaches HBM rate with copies of
 //           this size) and ONE 4-D tensor TMA of the activation slices
-//           ([16 rows][64 k] bf16 each, 128-byte swizzled, rows >= R
+//           ([8 or 16 rows][64 k] bf16 each, 128-byte swizzled, rows >= R
 //           zero-filled by the copy engine's out-of-bounds fill).
 //   warps 0-15 consumers: warp (kg, fw) owns the 32 weight rows of feature
-//           block fw and the iterations of parity kg.  Per 16-wide k step it
-//           turns one packed 32-bit word per 16-row sub-tile into the m16n8k16
-//           A fragment (shift + LOP3 + bf16x2 FMA per register: exact integer
-//           codes -8..7), loads the activation B fragment with a swizzle-aware
-//           ldmatrix and issues one mma.sync per 8 rows.  Each quantisation
-//           group's partial is formed in a fresh fp32 fragment and folded in as
-//           acc = fma(scale, partial, acc).
+//           block fw and every fourth k slice (k-group kg).  Per 16-wide k step
+//           it turns one packed 32-bit word per 16-row sub-tile into the
+//           m16n8k16 A fragment (shift + LOP3 + bf16x2 FMA per register: exact
+//           integer codes -8..7), loads the activation B fragment with a
+//           swizzle-aware ldmatrix and issues one mma.sync per 8 rows.  Each
+//           quantisation group's partial is formed in a fresh fp32 fragment and
+//           folded in as acc = fma(scale, partial, acc).
 // Why mma.sync and not tcgen05: the verify pass multiplies a weight tile by at
 // most 16 rows, so the MMA's N is 16.  A tcgen05.mma (M=128, K=16) was measured
 // on this part at ~153 cycles per instruction whatever its N (16..256), i.e.
@@ -27,8 +28,8 @@
 // register-operand m16n8k16 path processes ~68 weights/cycle/SM.
 // Row invariance: rows are MMA columns (a column's result depends only on its
 // own activations; the rows 8..15 MMA is skipped when R <= 8), and the cut of
-// the iteration space, the stage schedule, the k-parity split and the
-// fixed-order split-K sums depend on (T, Kc, Pv) only.
+// the iteration space, the stage schedule, the k-group split, the fixed-order
+// k-group combine and the fixed-order split-K sums depend on (T, Kc, Pv) only.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     }
 
     // ---------------- consumers ----------------
-    const int kg = warp / kFeatWarps;   // iterations of parity kg
+    const int kg = warp / kFeatWarps;   // k-group: slices kg, kg + 4, ... of each stage
     const int fw = warp % kFeatWarps;   // feature block
     const int gq = lane >> 2, tq = lane & 3;
     constexpr bool hi = HI;
