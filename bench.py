@@ -228,15 +228,17 @@ def time_dense_e2e(tf, torch, mats, steps, warmup):
     dx = torch.empty(xo, dtype=torch.int16, device="cuda")
     dy = torch.empty(yo, dtype=torch.float32, device="cuda")
     h2d, d2h = xo * 2, yo * 4
+    # per launch: the weight copies it rotates over and its slices of the device buffers
+    plan = [(mats[(K, N)]["copies"], dx[xo_:xo_ + R * K].view(R, K), dy[yo_:yo_ + R * N].view(R, N), mats[(K, N)]["ws"])
+            for (K, N, R), xo_, yo_ in zip(launches, x_off, y_off)]
     counter = [0]
 
     def step():
         dx.copy_(hx, non_blocking=True)
-        for (K, N, R), xo_, yo_ in zip(launches, x_off, y_off):
-            m = mats[(K, N)]
-            W = m["copies"][counter[0] % len(m["copies"])]
-            counter[0] += 1
-            tf.lane_gemm_w4(W, dx[xo_:xo_ + R * K].view(R, K), y=dy[yo_:yo_ + R * N].view(R, N), ws=m["ws"])
+        c = counter[0]
+        counter[0] += 1
+        for copies, xv, yv, ws in plan:
+            tf.lane_gemm_w4(copies[c % len(copies)], xv, y=yv, ws=ws)
         hy.copy_(dy, non_blocking=True)
 
     for _ in range(warmup):

@@ -30,6 +30,8 @@
 // own activations; the rows 8..15 MMA is skipped when R <= 8), and the cut of
 // the iteration space, the stage schedule, the k-group split, the fixed-order
 // k-group combine and the fixed-order split-K sums depend on (T, Kc, Pv) only.
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
@@ -561,12 +563,21 @@ __global__ void pack_scales_kernel(const uint16_t *scales, int K, int N, uint8_t
     *reinterpret_cast<uint32_t *>(dst) = lo | (hi << 16);
 }
 
+constexpr int kMaxDevices = 64;
+
 template <int G, bool HI>
 cudaError_t launch_gemm_g(const GemmArgs &a, int u_max, cudaStream_t s) {
     const size_t smem = gemm_smem_bytes(G, HI);
-    cudaError_t err = cudaFuncSetAttribute(w4_lane_gemm_kernel<G, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           int(smem));
+    // the shared-memory opt-in is a per-device property of the kernel: set it once
+    static std::atomic<bool> opted_in[kMaxDevices];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
+        err = cudaFuncSetAttribute(w4_lane_gemm_kernel<G, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (err != cudaSuccess) return err;
+        if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
+    }
     cudaLaunchConfig_t cfg = {};
     // persistent over work items: at most one CTA per SM
     const long long items = (long long)a.Pv * u_max;
@@ -665,9 +676,12 @@ cudaError_t launch_pack_w4(const uint8_t *codes, const uint16_t *scales, int K, 
 }
 
 int device_sm_count() {
+    static std::atomic<int> cached[kMaxDevices];
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices && (n = cached[dev].load(std::memory_order_relaxed)) > 0) return n;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

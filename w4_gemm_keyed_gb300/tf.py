@@ -102,12 +102,25 @@ def _check(status: int):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int converts to void* through the declared argtypes
+    return None if t is None else t.data_ptr()
+
+
+def _current_raw_stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+try:  # cheaper lookup of the current stream's handle where this build of torch has it
+    _raw = torch._C._cuda_getCurrentRawStream
+
+    def _current_raw_stream():  # noqa: F811
+        return _raw(torch.cuda.current_device())
+except AttributeError:  # pragma: no cover
+    pass
 
 
 def _stream(stream=None):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    return stream.cuda_stream if stream is not None else _current_raw_stream()
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
@@ -127,9 +140,10 @@ class W4Matrix:
 
     def __init__(self, packed: torch.Tensor, K: int, N: int, group: int, gate_up: bool = False):
         self.packed, self.K, self.N, self.group, self.gate_up = packed, K, N, group, gate_up
+        self._c = W4MatrixC(packed.data_ptr(), K, N, group)
 
     def c(self) -> W4MatrixC:
-        return W4MatrixC(self.packed.data_ptr(), self.K, self.N, self.group)
+        return self._c
 
 
 def packed_bytes(K: int, N: int, group: int) -> int:
