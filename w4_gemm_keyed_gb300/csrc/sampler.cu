@@ -395,45 +395,51 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleAr
     const double T = double(a.temperature);
     const double p = double(a.top_p);
     const int64_t pos = a.pos ? a.pos[r] : (*a.pos_base + r);
-    if (p < 1.0) {
-        __shared__ double s_Z;
-        if (tid < n_sel) ex[tid] = exp((double(srt_val[tid]) - double(srt_val[0])) / T);
-        __syncthreads();
-        if (tid == 0) {
-            double Z = 0.0;
-            for (int i = 0; i < n_sel; ++i) Z += ex[i];
-            s_Z = Z;
-        }
-        __syncthreads();
-        if (tid < n_sel) score[tid] = ex[tid] / s_Z;   // q_i, each term on its own thread
-        __syncthreads();
-        if (tid == 0) {
-            double S = 0.0;
-            int m = n_sel;
-            for (int i = 0; i < n_sel; ++i) {   // renormalised mass summed left to right
-                S += score[i];
-                if (S >= p) {
-                    m = i + 1;
-                    break;
-                }
+    // Warps 2-3 compute every candidate's Gumbel score (only the first m are
+    // used) while warps 0-1 run the top-p prefix on their own barrier.
+    __shared__ double gsc[kMaxTopK];
+    if (tid >= 64 && tid < 64 + n_sel) {
+        const int i = tid - 64;
+        gsc[i] = double(srt_val[i]) / T + gumbel(a.seed, pos, srt_id[i]);
+    }
+    if (tid < 64) {
+        if (p < 1.0) {
+            __shared__ double s_Z;
+            if (tid < n_sel) ex[tid] = exp((double(srt_val[tid]) - double(srt_val[0])) / T);
+            bar_sync_named(1, 64);
+            if (tid == 0) {
+                double Z = 0.0;
+                for (int i = 0; i < n_sel; ++i) Z += ex[i];
+                s_Z = Z;
             }
-            s_m = m;
+            bar_sync_named(1, 64);
+            if (tid < n_sel) score[tid] = ex[tid] / s_Z;   // q_i, each term on its own thread
+            bar_sync_named(1, 64);
+            if (tid == 0) {
+                double S = 0.0;
+                int m = n_sel;
+                for (int i = 0; i < n_sel; ++i) {   // renormalised mass summed left to right
+                    S += score[i];
+                    if (S >= p) {
+                        m = i + 1;
+                        break;
+                    }
+                }
+                s_m = m;
+            }
+        } else if (tid == 0) {
+            s_m = n_sel;
         }
-    } else if (tid == 0) {
-        s_m = n_sel;
     }
     __syncthreads();
     const int m = s_m;
-    // Gumbel-max over the m candidates (ties to the lower id): one score per
-    // thread, then a shuffle reduction in warp 0
-    if (tid < m) score[tid] = double(srt_val[tid]) / T + gumbel(a.seed, pos, srt_id[tid]);
-    __syncthreads();
+    // Gumbel-max over the m candidates (ties to the lower id): shuffle reduction in warp 0
     if (tid < 32) {
         double best = -1.0 / 0.0;
         int best_id = 0x7FFFFFFF;
         for (int i = tid; i < m; i += 32) {
-            if (score[i] > best || (score[i] == best && srt_id[i] < best_id)) {
-                best = score[i];
+            if (gsc[i] > best || (gsc[i] == best && srt_id[i] < best_id)) {
+                best = gsc[i];
                 best_id = srt_id[i];
             }
         }

@@ -265,6 +265,11 @@ inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, 
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
 }
 
+// Named barrier over the first n threads that use it (n a multiple of 32).
+__device__ __forceinline__ void bar_sync_named(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Record the first device-side error of a launch in the workspace status word.
 __device__ __forceinline__ void set_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
