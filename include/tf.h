@@ -2,13 +2,13 @@
  * tf.h -- C ABI of the exact speculative-decoding verify pass for GB300 (sm_103a).
  *
  * The method (TensorFold README, section on its two guarantees):
- *   1. every token is the model's own sample: the token at position p is the
- *      argmax over the top-k / top-p candidates of  logit / T + g(seed, p, token),
- *      g being Gumbel noise from a hash of the seed, the position and the token id;
- *   2. a row of a multi-row verify pass gets the same bits as a one-row step;
- * so a draft is accepted exactly when it equals the token serial decoding
- * would sample there, and drafted decoding writes the same bytes as serial
- * decoding.  Weights are 4-bit codes with one fp16 scale per group of 64
+ *   1. keyed sampling: the token chosen for position p maximises
+ *      logit / T + g(seed, p, token) over the top-k / top-p candidates, where g
+ *      is Gumbel noise derived by hashing seed, position and token id;
+ *   2. row invariance: each row of a verify pass over several drafted rows
+ *      comes out bit for bit as it would in a pass of one row;
+ * hence a draft survives only if it matches what one-row decoding samples at
+ * that position, and a drafted run emits exactly the serial run's tokens.  Weights are 4-bit codes with one fp16 scale per group of 64
  * (dense model) or 32 (MoE model) input features (README, "What each
  * checkpoint needs").
  *
@@ -129,9 +129,9 @@ TF_API tf_status tf_pack_w4_gate_up(const uint8_t *codes, const uint16_t *scales
 /* ------------------------------------------------------------------------
  * tf_lane_gemm_w4 -- the verify pass's linear layer
  * ------------------------------------------------------------------------
- * README, "Every token ..." / "A row of a multi-row verify pass gets the same
- * bits as a one-row step": all R drafted rows go through one launch that reads
- * each weight once, and row r's result is bit-identical whatever R is.
+ * README, the two guarantees (row invariance): all R drafted rows go through
+ * one launch that reads each weight once, and row r's result is bit-identical
+ * whatever R is.
  *
  *   y[r][n] = sum_g scale(n, g) * ( sum_{k in g} code(n, k) * x[r][k] )
  *
@@ -180,8 +180,8 @@ TF_API tf_status tf_lane_gemm_w4_noalloc(const tf_w4_matrix *W, const uint16_t *
 /* ------------------------------------------------------------------------
  * tf_keyed_sample -- keyed Gumbel-max sampling over top-k / top-p
  * ------------------------------------------------------------------------
- * README, "Every token is the model's own sample", and the CLI table
- * ("--temperature 0 is greedy").  Per row r, at position pos[r]:
+ * README, the two guarantees (keyed sampling), and the CLI options table
+ * (a temperature of 0 selects greedy decoding).  Per row r, at position pos[r]:
  *   T == 0: token = argmax_i logit_i (ties: lower id);
  *   T  > 0: order the V tokens by (logit desc, id asc); keep the first
  *           k' = (top_k <= 0 || top_k >= V) ? V : top_k; if top_p < 1 keep the
@@ -210,8 +210,8 @@ TF_API tf_status tf_keyed_sample(const float *logits, int32_t ldl, int32_t R, in
 /* ------------------------------------------------------------------------
  * tf_accept -- longest-prefix acceptance
  * ------------------------------------------------------------------------
- * README: "a draft is accepted exactly when it equals the token one-token-
- * at-a-time decoding would sample there".  Row i samples position pos0 + i;
+ * README, the two guarantees: a draft counts only if one-row decoding would
+ * sample that same token at its position.  Row i samples position pos0 + i;
  * draft d[i] (i < R-1) proposes position pos0 + i.
  *   a = first i with d[i] != t[i], else R-1;  commit t[0..a];  bonus = t[a].
  * drafts dev int32 [R-1] (may be NULL when R == 1); sampled dev int32 [R];
@@ -276,6 +276,30 @@ TF_API size_t tf_verify_step_workspace_bytes(const tf_model *m, int32_t R);
 TF_API tf_status tf_verify_step(const tf_model *m, int32_t R, int32_t *last_token, int64_t *pos,
                          const int32_t *drafts, const tf_sampling *p, uint64_t seed, int32_t *tokens,
                          int32_t *accepted, float *logits, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Device-side decode loop: drafts in, committed tokens out
+ * ------------------------------------------------------------------------
+ * README, the paragraph on the two guarantees (drafted and serial decoding
+ * write the same tokens): a decode loop is verify passes chained on the device
+ * (tf_verify_step advances *last_token and *pos itself).  With these two calls no pass needs the host,
+ * so a run of passes can be captured in one CUDA graph and the host
+ * synchronises only between runs.
+ *
+ * tf_gather_drafts: drafts[i] = table[*pos + i] for i < R - 1 -- the proposals
+ *   for the positions the next pass verifies (draft i proposes position
+ *   *pos + i); entries outside [0, table_len) read as token 0.  table dev int32
+ *   [table_len], pos dev int64 [1], drafts dev int32 [R - 1].  R == 1: no-op.
+ * tf_commit_tokens: after a pass that advanced *pos by a + 1 (a = *accepted),
+ *   log[p - 1] = t for each committed token t at position p, i.e.
+ *   log[*pos - a - 2 + i] = tokens[i] for i <= a; entries outside
+ *   [0, log_len) are skipped.  tokens dev int32 [R], accepted dev int32 [1],
+ *   pos dev int64 [1], log dev int32 [log_len].
+ */
+TF_API tf_status tf_gather_drafts(const int32_t *table, int64_t table_len, const int64_t *pos, int32_t R,
+                                  int32_t *drafts, void *stream);
+TF_API tf_status tf_commit_tokens(const int32_t *tokens, const int32_t *accepted, const int64_t *pos, int32_t *log,
+                                  int64_t log_len, void *stream);
 
 /* ------------------------------------------------------------------------
  * Pieces of the synthetic decoder (the steps tf_verify_step chains), public so

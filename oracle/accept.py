@@ -1,9 +1,8 @@
 """Longest-prefix acceptance of drafts (test infrastructure).
 
-TensorFold README, section on the two guarantees: a draft is accepted
-exactly when it equals the token that one-token-at-a-time decoding would
-sample at that position, so drafted decoding writes the bytes of serial
-decoding.
+TensorFold README, section on the two guarantees: a draft is kept only when
+it matches the token one-row decoding samples at its position, which is why a
+drafted run emits exactly the serial run's tokens.
 
 Indexing (the pages give none; this reading is used everywhere): a verify
 pass has R rows; row i samples position ``pos0 + i`` and yields ``t[i]``;

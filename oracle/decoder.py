@@ -16,8 +16,8 @@ only on its input token; the position enters only through the sampling key.
 ``serial_decode`` samples one token per step (the pages' ``"draft": false``
 reference).  ``drafted_decode`` verifies R rows per step and accepts the
 longest matching prefix (``accept.accept``).  The invariant the pages state
-("drafted decoding writes the same bytes as serial decoding") is checked
-by comparing ``token_sha`` of the two.
+-- a drafted run emits exactly the serial run's tokens -- is checked by
+comparing ``token_sha`` of the two.
 """
 
 from __future__ import annotations

@@ -1,7 +1,7 @@
 """Top-k routed W4 SwiGLU experts (test infrastructure).
 
 TensorFold README, "What each checkpoint needs" / source layout: the MoE
-model's fused kernels read 4-bit weights in groups of 32.  The routing and
+model is served from 4-bit weights quantised in groups of 32.  The routing and
 expert shapes are those of a 30B-A3B-class model (128 experts, top-8,
 hidden 2048, expert FFN 768); the pages name the model class, not its
 arithmetic, so these readings are used:

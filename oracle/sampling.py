@@ -1,10 +1,10 @@
 """Keyed Gumbel-max sampling over the top-k / top-p candidates (test infrastructure).
 
-Source: TensorFold README, section on the two guarantees ("Every token is
-the model's own sample"): the token at position p is the argmax, over the
-top-k/top-p candidates, of ``logit / T + g(seed, p, token)`` with ``g``
-Gumbel noise from a hash of the seed, the position and the token id; a
-temperature of 0 is greedy decoding (CLI table, ``--temperature 0``).
+Source: TensorFold README, section on the two guarantees (keyed sampling):
+position p gets the top-k/top-p candidate that maximises
+``logit / T + g(seed, p, token)``, where ``g`` is Gumbel noise computed from a
+hash of seed, position and token id; the CLI options table makes temperature 0
+plain greedy decoding.
 
 Readings fixed here where the pages are silent:
 

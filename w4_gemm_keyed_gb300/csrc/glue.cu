@@ -164,7 +164,45 @@ __global__ void rmsnorm_bf16_kernel(const float *x, int H, float eps, uint16_t *
     }
 }
 
+// Device-side decode loop helpers: the next verify pass's drafts come from a
+// table of proposals indexed by position, and each pass's committed tokens are
+// written into a log indexed by position, so consecutive passes chain on the
+// device (and can be captured in one CUDA graph).
+__global__ void gather_drafts_kernel(const int32_t *table, long long table_len, const int64_t *pos, int n,
+                                     int32_t *drafts) {
+    grid_dependency_wait();     // *pos comes from the preceding pass
+    grid_launch_dependents();
+    const int i = threadIdx.x;
+    if (i < n) {
+        const long long q = *pos + i;   // draft i proposes position *pos + i
+        drafts[i] = (q >= 0 && q < table_len) ? table[q] : 0;
+    }
+}
+
+__global__ void commit_tokens_kernel(const int32_t *tokens, const int32_t *accepted, const int64_t *pos,
+                                     int32_t *log, long long log_len) {
+    grid_dependency_wait();     // tokens, accepted and the advanced *pos come from the pass
+    grid_launch_dependents();
+    const int a = *accepted;
+    const long long first = *pos - (a + 1);   // position of t[0]; *pos was advanced by a + 1
+    const int i = threadIdx.x;
+    if (i <= a) {
+        const long long q = first - 1 + i;  // position 1 is the first generated token
+        if (q >= 0 && q < log_len) log[q] = tokens[i];
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_drafts(const int32_t *table, long long table_len, const int64_t *pos, int n,
+                                 int32_t *drafts, cudaStream_t s) {
+    return launch_pdl(gather_drafts_kernel, dim3(1), dim3(32), 0, s, table, table_len, pos, n, drafts);
+}
+
+cudaError_t launch_commit_tokens(const int32_t *tokens, const int32_t *accepted, const int64_t *pos, int32_t *log,
+                                 long long log_len, cudaStream_t s) {
+    return launch_pdl(commit_tokens_kernel, dim3(1), dim3(32), 0, s, tokens, accepted, pos, log, log_len);
+}
 
 cudaError_t launch_route_list(const float *router, int R, int E, int top_k, int32_t *ids, float *w,
                               int32_t *expert_ids, int32_t *n_problems, int32_t *slot_of, int *err, cudaStream_t s) {

@@ -15,6 +15,12 @@ constexpr int kMaxRows = 16;
 // slot_of[r][j] = index u of ids[r][j].  One CTA, R <= kMaxRows.
 cudaError_t launch_route_list(const float *router, int R, int E, int top_k, int32_t *ids, float *w,
                               int32_t *expert_ids, int32_t *n_problems, int32_t *slot_of, int *err, cudaStream_t s);
+// drafts[i] = table[*pos + i] (0 outside the table), i < n.
+cudaError_t launch_gather_drafts(const int32_t *table, long long table_len, const int64_t *pos, int n,
+                                 int32_t *drafts, cudaStream_t s);
+// After a verify pass that advanced *pos by a + 1: log[*pos - (a + 1) - 1 + i] = tokens[i], i <= a.
+cudaError_t launch_commit_tokens(const int32_t *tokens, const int32_t *accepted, const int64_t *pos, int32_t *log,
+                                 long long log_len, cudaStream_t s);
 // out[r][n] = sum_j w[r][j] * Y[slot_of[r][j]][r][n], j ascending (fp32 FMA chain).
 cudaError_t launch_combine(const float *Y, const int32_t *slot_of, const float *w, int R, int H, int top_k,
                            float *out, cudaStream_t s);

@@ -1,10 +1,10 @@
 // Keyed Gumbel-max sampling over top-k / top-p candidates, and acceptance.
 //
-// TensorFold README, "Every token is the model's own sample": the token at
-// position p is the argmax over the top-k/top-p candidates of
-// logit/T + g(seed, p, token), g Gumbel noise from a hash of (seed, p, token);
-// "--temperature 0" is greedy.  Acceptance: a draft is accepted exactly when it
-// equals the token serial decoding samples there.
+// TensorFold README, section on the two guarantees (keyed sampling): position
+// p gets the top-k/top-p candidate maximising logit/T + g(seed, p, token), g
+// Gumbel noise computed from a hash of (seed, p, token); the CLI options table
+// makes temperature 0 greedy.  Acceptance keeps a draft only while it matches
+// what one-row decoding samples at its position.
 //
 // Two launches per call.  Candidates are ordered by the composite key
 // (logit desc, id asc), unique per token.

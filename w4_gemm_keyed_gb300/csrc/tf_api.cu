@@ -459,6 +459,25 @@ tf_status tf_accept(const int32_t *drafts, const int32_t *sampled, int32_t R, in
     return ok();
 }
 
+tf_status tf_gather_drafts(const int32_t *table, int64_t table_len, const int64_t *pos, int32_t R, int32_t *drafts,
+                           void *stream) {
+    if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
+    if (R == 1) return ok();  // a one-row pass has no drafts
+    if (!table || table_len < 0 || !pos || !drafts) return fail(TF_ERR_INVALID_ARG, "null pointer or negative length");
+    cudaError_t e = launch_gather_drafts(table, table_len, pos, R - 1, drafts, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_gather_drafts");
+    return ok();
+}
+
+tf_status tf_commit_tokens(const int32_t *tokens, const int32_t *accepted, const int64_t *pos, int32_t *log,
+                           int64_t log_len, void *stream) {
+    if (!tokens || !accepted || !pos || !log || log_len < 0)
+        return fail(TF_ERR_INVALID_ARG, "null pointer or negative length");
+    cudaError_t e = launch_commit_tokens(tokens, accepted, pos, log, log_len, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_commit_tokens");
+    return ok();
+}
+
 size_t tf_moe_workspace_bytes(const tf_moe_layer *L, int32_t R) {
     if (!L || R < 1 || R > TF_MAX_ROWS || L->n_experts < 1 || L->top_k < 1 || L->hidden <= 0 || L->ffn <= 0)
         return 0;

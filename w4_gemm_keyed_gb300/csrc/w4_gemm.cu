@@ -1,8 +1,8 @@
 // W4 lane GEMM for the speculative-decoding verify pass (sm_103a).
 //
-// TensorFold README, "A row of a multi-row verify pass gets the same bits as a
-// one-row step": up to 16 drafted rows share one launch that streams every
-// 4-bit weight once, and row r's bits never depend on how many rows there are.
+// TensorFold README, section on the two guarantees (row invariance): up to 16
+// drafted rows share one launch that streams every 4-bit weight once, and row
+// r's bits never depend on how many rows there are.
 //
 // At most one CTA per SM, 17 warps, persistent over work items (problem,
 // range of the tile x k-slice iteration space):
