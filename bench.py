@@ -378,7 +378,51 @@ def extra_decoder(tf, torch, steps=10):
         ms = a.elapsed_time(b) / steps
         out[f"R{R}"] = {"verify_steps_per_s": 1e3 / ms, "ms_per_step": ms,
                         "gbs": step_bytes / (ms * 1e-3) / 1e9}
+    out["decode"] = decode_loop(tf, torch, dec, V)
     return out
+
+
+def decode_loop(tf, torch, dec, V, n_tokens=64, R=8, p_match=0.75, seeds=(1234, 1235, 1236, 1237, 1238)):
+    """Synthetic decoder, decode loop on the device (CUDA-graph replays of 8 passes):
+    64 tokens serially (R = 1) and with R = 8 drafts that copy the serial token
+    with probability 0.75, T = 0.7 / top-k 20 / top-p 0.95, per seed; tokens/s,
+    mean tokens committed per drafted pass, and whether the token_sha agree."""
+    from w4_gemm_keyed_gb300 import decode, inputs
+    T, k, p, prompt = 0.7, 20, 0.95, 11
+    ser_s = dr_s = 0.0
+    committed = passes_needed = 0
+    same = True
+    for seed in seeds:
+        loop1 = decode.GraphLoop(dec, n_tokens + 2 * R, 1, T, k, p, seed, prompt_token=prompt)
+        loop1.run(prompt)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        serial, _ = loop1.run(prompt)
+        b.record()
+        torch.cuda.synchronize()
+        ser_s += a.elapsed_time(b) / 1e3 * n_tokens / (n_tokens + 2 * R)
+        rng = inputs.rng_for(701, seed)
+        truth = np.zeros(n_tokens + 12 * R, dtype=np.int64)
+        truth[1:1 + len(serial)] = serial[: len(truth) - 1]
+        table = torch.from_numpy(inputs.noisy_drafts(rng, truth, p_match, V)).cuda()
+        loop8 = decode.GraphLoop(dec, n_tokens, R, T, k, p, seed, table, prompt_token=prompt)
+        loop8.run(prompt)
+        a.record()
+        drafted, _ = loop8.run(prompt)
+        b.record()
+        torch.cuda.synchronize()
+        dr_s += a.elapsed_time(b) / 1e3
+        same &= decode.token_sha(drafted) == decode.token_sha(serial[:n_tokens])
+        host_table = table.cpu().numpy()
+        _, lens = decode.drafted_decode(dec, prompt, n_tokens, R, T, k, p, seed,
+                                        lambda pos0, m: host_table[pos0: pos0 + m])
+        committed += sum(x + 1 for x in lens)
+        passes_needed += len(lens)
+    n = len(seeds)
+    return {"tokens": n_tokens, "seeds": n, "serial_tokens_per_s": n * n_tokens / ser_s,
+            "drafted_tokens_per_s": n * n_tokens / dr_s, "drafted_R": R,
+            "mean_tokens_per_pass": committed / passes_needed, "token_sha_equal": bool(same),
+            "note": "graph replays of 8 passes; a run ends at the first replay that reaches the token count"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle

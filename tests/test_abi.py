@@ -84,6 +84,11 @@ def test_host_validation_rejects_bad_arguments(lib):
         tf.TF_ERR_INVALID_ARG
     assert lib.tf_accept(None, 256, 2, 256, 256, None) == tf.TF_ERR_INVALID_ARG
     assert lib.tf_accept(None, 256, 0, 256, 256, None) == tf.TF_ERR_INVALID_ARG
+    assert lib.tf_gather_drafts(None, 0, None, 0, None, None) == tf.TF_ERR_INVALID_ARG      # R = 0
+    assert lib.tf_gather_drafts(None, 0, None, 1, None, None) == tf.TF_OK                   # R = 1: no drafts
+    assert lib.tf_gather_drafts(None, 8, 256, 4, 256, None) == tf.TF_ERR_INVALID_ARG        # null table
+    assert lib.tf_commit_tokens(256, 256, None, 256, 8, None) == tf.TF_ERR_INVALID_ARG      # null pos
+    assert lib.tf_commit_tokens(256, 256, 256, 256, -1, None) == tf.TF_ERR_INVALID_ARG      # negative length
     L = tf.MoeLayerC(256, 256, 2048, 768, 128, 9, 32)   # top_k > 8
     assert lib.tf_moe_w4(ctypes.byref(L), 256, 256, 1, 256, 256, 1 << 30, None) == tf.TF_ERR_UNSUPPORTED
     assert lib.tf_last_error() != b""

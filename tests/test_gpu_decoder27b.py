@@ -11,6 +11,7 @@ the device status must stay clean.
 
 import numpy as np
 import pytest
+import torch
 
 from w4_gemm_keyed_gb300 import inputs
 
@@ -50,4 +51,18 @@ def test_drafted_equals_serial(tf, decoder27b, seed):
         lambda pos0, m: inputs.noisy_drafts(rng, future[pos0 - 1: pos0 - 1 + m], 0.75, V))
     assert decode.token_sha(drafted) == decode.token_sha(serial)
     assert len(lens) < n  # the drafts were used
+    assert tf.workspace_status(dec.ws) == tf.TF_DEV_OK
+
+
+def test_graph_drafted_equals_serial(tf, decoder27b):
+    from w4_gemm_keyed_gb300 import decode
+    model, dec = decoder27b
+    T, k, p, n, R, prompt, seed = 0.7, 20, 0.95, 64, 8, 11, 1234
+    serial = decode.serial_decode(dec, prompt, n + 2 * R, T, k, p, seed)
+    rng = inputs.rng_for(602, seed)
+    truth = np.zeros(n + 12 * R, dtype=np.int64)
+    truth[1:1 + len(serial)] = serial[: len(truth) - 1]
+    table = torch.from_numpy(inputs.noisy_drafts(rng, truth, 0.75, V)).cuda()
+    graph, passes = decode.graph_decode(dec, prompt, n, R, T, k, p, seed, draft_table=table, passes_per_graph=8)
+    assert decode.token_sha(graph) == decode.token_sha(serial[:n])
     assert tf.workspace_status(dec.ws) == tf.TF_DEV_OK

@@ -105,3 +105,57 @@ def drafted_decode(dec: Decoder, prompt_token: int, n_tokens: int, R: int, tempe
         lens.append(a)
         pos0 += a + 1
     return out[:n_tokens], lens
+
+
+class GraphLoop:
+    """Decoding with every verify pass chained on the device.
+
+    Each pass takes its drafts from ``draft_table`` (device int32, index =
+    position; unused when R = 1), runs ``tf_verify_step`` and writes its
+    committed tokens into a device log; ``passes_per_graph`` passes are
+    captured once as a CUDA graph (sampling settings and seed included) and
+    replayed, and the host only checks the position between replays.
+    """
+
+    def __init__(self, dec: Decoder, n_tokens: int, R: int, temperature, top_k, top_p, seed,
+                 draft_table: torch.Tensor = None, passes_per_graph: int = 8, prompt_token: int = 0):
+        if R > 1 and draft_table is None:
+            raise ValueError("a drafted run needs a draft table")
+        self.dec, self.n_tokens, self.R, self.passes_per_graph = dec, n_tokens, R, passes_per_graph
+        device = dec.last.device
+        self.log = torch.zeros(n_tokens + (passes_per_graph + 1) * R, dtype=torch.int32, device=device)
+        self.table = draft_table if draft_table is not None else torch.zeros(1, dtype=torch.int32, device=device)
+
+        def one_pass():
+            if R > 1:
+                tf.gather_drafts(self.table, dec.pos, R, dec.drafts)
+            dec.model.verify_step(R, dec.last, dec.pos, dec.drafts, temperature, top_k, top_p, seed, dec.tokens,
+                                  dec.accepted, dec.ws)
+            tf.commit_tokens(dec.tokens, dec.accepted, dec.pos, self.log)
+
+        dec.reset(prompt_token, 1)
+        one_pass()                      # first-call set-up happens outside the capture
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            for _ in range(passes_per_graph):
+                one_pass()
+
+    def run(self, prompt_token: int):
+        """Returns (tokens, passes run); passes run counts whole replays."""
+        self.dec.reset(prompt_token, 1)
+        passes = 0
+        while True:
+            self.graph.replay()
+            passes += self.passes_per_graph
+            if int(self.dec.pos.item()) - 1 >= self.n_tokens:
+                break
+        return self.log[: self.n_tokens].tolist(), passes
+
+
+def graph_decode(dec: Decoder, prompt_token: int, n_tokens: int, R: int, temperature, top_k, top_p, seed,
+                 draft_table: torch.Tensor = None, passes_per_graph: int = 8):
+    """One run of a freshly captured ``GraphLoop``: (tokens, passes run)."""
+    loop = GraphLoop(dec, n_tokens, R, temperature, top_k, top_p, seed, draft_table, passes_per_graph,
+                     prompt_token)
+    return loop.run(prompt_token)

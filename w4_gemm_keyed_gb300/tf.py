@@ -67,6 +67,8 @@ SIGNATURES = [
     ("tf_keyed_sample_workspace_bytes", SZ, [I32, I32]),
     ("tf_keyed_sample", ctypes.c_int, [P, I32, I32, I32, ctypes.POINTER(SamplingC), ctypes.c_uint64, P, P, P, SZ, P]),
     ("tf_accept", ctypes.c_int, [P, P, I32, P, P, P]),
+    ("tf_gather_drafts", ctypes.c_int, [P, ctypes.c_int64, P, I32, P, P]),
+    ("tf_commit_tokens", ctypes.c_int, [P, P, P, P, ctypes.c_int64, P]),
     ("tf_moe_workspace_bytes", SZ, [ctypes.POINTER(MoeLayerC), I32]),
     ("tf_moe_w4", ctypes.c_int, [ctypes.POINTER(MoeLayerC), P, P, I32, P, P, SZ, P]),
     ("tf_verify_step_workspace_bytes", SZ, [ctypes.POINTER(ModelC), I32]),
@@ -235,6 +237,19 @@ def accept(drafts: torch.Tensor, sampled: torch.Tensor, accepted: torch.Tensor =
     _check(lib.tf_accept(_ptr(drafts) if R > 1 else None, _ptr(sampled), R, _ptr(accepted), _ptr(bonus),
                          _stream(stream)))
     return accepted, bonus
+
+
+def gather_drafts(table: torch.Tensor, pos: torch.Tensor, R: int, drafts: torch.Tensor, stream=None):
+    """drafts[i] = table[pos + i] for i < R - 1 (device int32 table, device int64 pos)."""
+    _check(load().tf_gather_drafts(_ptr(table), table.numel(), _ptr(pos), R, _ptr(drafts), _stream(stream)))
+    return drafts
+
+
+def commit_tokens(tokens: torch.Tensor, accepted: torch.Tensor, pos: torch.Tensor, log: torch.Tensor, stream=None):
+    """Write a finished pass's committed tokens into the device log (index = position - 1)."""
+    _check(load().tf_commit_tokens(_ptr(tokens), _ptr(accepted), _ptr(pos), _ptr(log), log.numel(),
+                                   _stream(stream)))
+    return log
 
 
 def rmsnorm_bf16(x: torch.Tensor, eps: float, out: torch.Tensor = None, stream=None) -> torch.Tensor:
