@@ -40,7 +40,6 @@ tf_status cuda_fail(cudaError_t e, const char *what) {
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-constexpr int kGroupedPv = 8;   // ranges per MoE expert problem (fixed: bits must not depend on R)
 
 // Ranges of a dense launch.  When an even share of m whole tiles per CTA
 // (m = 1..4) nearly fills the SMs, no tile is split (no split-K fixup);
@@ -55,9 +54,12 @@ int dense_pv(int T, int Kc) {
     return int(tot < sms ? tot : sms);
 }
 
+// Ranges of a grouped (MoE) launch: one whole tile each, so no expert tile is
+// split and no split-K fixup runs; the persistent CTAs spread the
+// experts x tiles items.  Depends on the shape only, never on R.
 int grouped_pv(int T, int Kc) {
-    const long long tot = (long long)T * Kc;
-    return int(tot < kGroupedPv ? tot : kGroupedPv);
+    (void)Kc;
+    return T;
 }
 
 tf_status check_matrix(const tf_w4_matrix *W, const char *name) {
