@@ -74,16 +74,12 @@ __global__ void route_list_kernel(const float *router, int R, int E, int top_k, 
             // renormalised weights over the kept experts: fp64, summed in rank order
             double ej = 0.0;
             if (lane < top_k) ej = exp(double(z[s_ids[r][lane]]) - double(z[s_ids[r][0]]));
-            double e_all[kMaxRouteK];
-#pragma unroll
-            for (int j = 0; j < kMaxRouteK; ++j) e_all[j] = __shfl_sync(0xFFFFFFFFu, ej, j);
-            if (lane == 0) {
-                double tot = 0.0;
-                for (int j = 0; j < top_k; ++j) tot += e_all[j];
-                for (int j = 0; j < top_k; ++j) {
-                    ids[r * kMaxRouteK + j] = s_ids[r][j];
-                    w[r * kMaxRouteK + j] = float(e_all[j] / tot);
-                }
+            // every lane forms the same left-to-right sum; lane j divides its own term
+            double tot = 0.0;
+            for (int j = 0; j < top_k; ++j) tot += __shfl_sync(0xFFFFFFFFu, ej, j);
+            if (lane < top_k) {
+                ids[r * kMaxRouteK + lane] = s_ids[r][lane];
+                w[r * kMaxRouteK + lane] = float(ej / tot);
             }
         }
         __syncwarp();
