@@ -312,15 +312,21 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleAr
         return;
     }
     const int k = min(a.k_eff, n_total);
+    // Every chunk but the last kept exactly k_eff candidates (it had 4096 >= k_eff
+    // valid logits), so candidate i of the row sits in chunk i / k_eff, slot
+    // i % k_eff; the float quotient is exact here ((i + 0.5) / k_eff never lies
+    // within 1/128 of an integer), and the loads carry no data-dependent branch.
+    const int ke = a.k_eff;
+    const float inv_ke = 1.0f / float(ke);
     uint64_t ck[kE2];
     uint64_t tmax = 0ull;
 #pragma unroll
     for (int e = 0; e < kE2; ++e) {
-        const int p = e * kSampleThreads + tid;
-        const int c = p / kMaxTopK, s = p % kMaxTopK;
+        const int i = e * kSampleThreads + tid;
         ck[e] = 0ull;
-        if (c < nc && s < s_ccnt[c]) {
-            const long long q = (long long)(r * nc + c) * kMaxTopK + s;
+        if (i < n_total) {
+            const int c = int((float(i) + 0.5f) * inv_ke);
+            const long long q = (long long)(r * nc + c) * kMaxTopK + (i - c * ke);
             ck[e] = composite(order_key(a.cand_val[q]), a.cand_id[q]);
         }
         tmax = ck[e] > tmax ? ck[e] : tmax;
