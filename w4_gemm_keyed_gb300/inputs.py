@@ -32,6 +32,7 @@ __all__ = [
     "bf16_bits_from_f32",
     "bf16_normal",
     "w4_weights",
+    "mlx_affine_weights",
     "uniform_codes_packed",
     "fp16_scales",
     "logits_normal",
@@ -91,6 +92,25 @@ def w4_weights(rng: np.random.Generator, K: int, N: int, group: int):
     codes = uniform_codes_packed(rng, N, K)
     scales = fp16_scales(rng, N, K // group)
     return codes, scales
+
+
+def mlx_affine_weights(rng: np.random.Generator, K: int, N: int, group: int):
+    """(codes uint32 [N][K/8], scales bf16 bits [N][K/group], biases bf16 bits [N][K/group]).
+
+    MLX-style affine 4-bit layout: unsigned codes uniform in [0, 15], packed 8
+    per word (element i in bits 4i..4i+3); scales |N(0, 0.02)| + 1e-3 and
+    biases -scale * U(6, 9) (a group's minimum sits about 7.5 steps below its
+    mean), both rounded to bf16.
+    """
+    if K % group or K % 8:
+        raise ValueError("K must be a multiple of the group size and of 8")
+    q = rng.integers(0, 16, size=(N, K), dtype=np.uint32)
+    words = np.zeros((N, K // 8), dtype=np.uint32)
+    for i in range(8):
+        words |= q[:, i::8] << np.uint32(4 * i)
+    s = (np.abs(rng.standard_normal((N, K // group), dtype=np.float32)) * np.float32(0.02) + np.float32(1e-3))
+    b = -s * rng.uniform(6.0, 9.0, size=s.shape).astype(np.float32)
+    return words, bf16_bits_from_f32(s), bf16_bits_from_f32(b)
 
 
 def logits_normal(rng: np.random.Generator, R: int, V: int, std: float = 3.0) -> np.ndarray:
