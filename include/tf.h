@@ -102,10 +102,29 @@ typedef struct tf_w4_matrix {
     int32_t K;            /* input features, a positive multiple of 64 */
     int32_t N;            /* output features, >= 1 */
     int32_t group;        /* 32 or 64 */
+    int32_t affine;       /* 0: symmetric (tf_pack_w4); 1: MLX-style affine (tf_pack_w4_affine) */
 } tf_w4_matrix;
 
 /* Bytes of the packed layout, or 0 if (K, N, group) is unsupported. */
 TF_API size_t tf_w4_packed_bytes(int32_t K, int32_t N, int32_t group);
+
+/* MLX-style affine 4-bit weights (the format of MLX 4-bit checkpoints, which the
+ * README says the engine serves; its layout follows MLX's public quantisation):
+ *   codes  uint32 [N][K/8]  word j of row n holds q(n, 8j + i) in bits 4i..4i+3,
+ *                           q an unsigned integer in [0, 15];
+ *   scales uint16 [N][K/G]  bf16 scale of group g = k / G of row n;
+ *   biases uint16 [N][K/G]  bf16 bias of that group;
+ *   w[n][k] = scale(n, k / G) * q(n, k) + bias(n, k / G).
+ * tf_pack_w4_affine produces the packed layout of a matrix with affine = 1
+ * (size tf_w4_affine_packed_bytes); tf_lane_gemm_w4 and tf_lane_gemm_w4_noalloc
+ * accept it: each group's partial sum_k q x is scaled, and the bias is added
+ * times the group's activation sum sum_k x (fp32, formed by the tensor core),
+ * bits of row r still independent of R.  The MoE and decoder entry points take
+ * symmetric matrices only.  Group 32 with R > 8 runs a 3-stage pipeline. */
+TF_API size_t tf_w4_affine_packed_bytes(int32_t K, int32_t N, int32_t group);
+TF_API tf_status tf_pack_w4_affine(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
+                                   int32_t K, int32_t N, int32_t group, void *packed, size_t packed_bytes,
+                                   void *stream);
 
 /*
  * Repack canonical codes + scales (dev) into the kernel layout `packed` (dev,

@@ -69,6 +69,7 @@ tf_status check_matrix(const tf_w4_matrix *W, const char *name) {
     if (W->group != 32 && W->group != 64) return fail(TF_ERR_UNSUPPORTED, "%s: group %d not in {32, 64}", name, W->group);
     if (W->K <= 0 || W->K % kKChunk) return fail(TF_ERR_UNSUPPORTED, "%s: K=%d is not a positive multiple of 64", name, W->K);
     if (W->N <= 0) return fail(TF_ERR_INVALID_ARG, "%s: N=%d must be >= 1", name, W->N);
+    if (W->affine != 0 && W->affine != 1) return fail(TF_ERR_INVALID_ARG, "%s: affine must be 0 or 1", name);
     if ((long long)((W->N + kTileN - 1) / kTileN) * (W->K / kKChunk) > 0x7FFFFFFFLL)
         return fail(TF_ERR_UNSUPPORTED, "%s: K x N too large for the split-K index space", name);
     return TF_OK;
@@ -108,6 +109,7 @@ GemmArgs dense_args(const tf_w4_matrix &W, int R, void *y, int ldy, int mode) {
     a.K = W.K;
     a.N = W.N;
     a.G = W.group;
+    a.affine = W.affine;
     a.T = (W.N + kTileN - 1) / kTileN;
     a.Kc = W.K / kKChunk;
     a.Pv = dense_pv(a.T, a.Kc);
@@ -220,12 +222,15 @@ tf_status check_model(const tf_model *m) {
         tf_status st = check_matrix(&m->gate_up[b], "gate_up");
         if (st) return st;
         if ((st = check_matrix(&m->down[b], "down"))) return st;
+        if (m->gate_up[b].affine || m->down[b].affine)
+            return fail(TF_ERR_UNSUPPORTED, "block %d: the decoder takes symmetric matrices", b);
         if (m->gate_up[b].K != m->hidden || m->gate_up[b].N != 2 * m->ffn || m->down[b].K != m->ffn ||
             m->down[b].N != m->hidden || m->gate_up[b].group != m->group || m->down[b].group != m->group)
             return fail(TF_ERR_INVALID_ARG, "block %d: matrix shapes do not match the model", b);
     }
     tf_status st = check_matrix(&m->lm_head, "lm_head");
     if (st) return st;
+    if (m->lm_head.affine) return fail(TF_ERR_UNSUPPORTED, "lm_head: the decoder takes symmetric matrices");
     if (m->lm_head.K != m->hidden || m->lm_head.N != m->vocab)
         return fail(TF_ERR_INVALID_ARG, "lm_head shape does not match the model");
     if (m->hidden % kKChunk || m->ffn % kKChunk) return fail(TF_ERR_UNSUPPORTED, "hidden, ffn must be multiples of 64");
@@ -292,6 +297,19 @@ tf_status tf_workspace_status(void *ws, void *stream, int32_t *code) {
 }
 
 size_t tf_w4_packed_bytes(int32_t K, int32_t N, int32_t group) { return packed_bytes(K, N, group); }
+
+size_t tf_w4_affine_packed_bytes(int32_t K, int32_t N, int32_t group) { return packed_bytes(K, N, group, true); }
+
+tf_status tf_pack_w4_affine(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases, int32_t K, int32_t N,
+                            int32_t group, void *packed, size_t bytes, void *stream) {
+    if (!codes || !scales || !biases || !packed) return fail(TF_ERR_INVALID_ARG, "null pointer");
+    if (!packed_shape_ok(K, N, group)) return fail(TF_ERR_UNSUPPORTED, "unsupported shape K=%d N=%d group=%d", K, N, group);
+    if (!aligned(packed, 256)) return fail(TF_ERR_INVALID_ARG, "packed buffer not 256-B aligned");
+    if (bytes < packed_bytes(K, N, group, true)) return fail(TF_ERR_INVALID_ARG, "packed buffer too small");
+    cudaError_t e = launch_pack_w4_affine(codes, scales, biases, K, N, group, packed, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_pack_w4_affine");
+    return ok();
+}
 
 static tf_status pack_common(const uint8_t *codes, const uint16_t *scales, int32_t K, int32_t N, int32_t group,
                              void *packed, size_t bytes, void *stream, bool inter) {

@@ -44,7 +44,8 @@ namespace tfk {
 namespace {
 
 constexpr uint32_t kBf16One2 = 0x3F803F80u;     // (1.0, 1.0)
-constexpr uint32_t kBf16Neg136x2 = 0xC308C308u; // (-136, -136)
+constexpr uint32_t kBf16Neg136x2 = 0xC308C308u; // (-136, -136): symmetric codes c = u - 8
+constexpr uint32_t kBf16Neg128x2 = 0xC300C300u; // (-128, -128): affine codes q = u
 constexpr uint32_t kNibMask = 0x000F000Fu;
 constexpr uint32_t kBf16Magic = 0x43004300u;    // (128, 128): OR-ing u in gives 128 + u
 
@@ -89,20 +90,32 @@ struct Split {
     }
 };
 
+// bf16 pair -> two floats (low half, high half).
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
 // One 64-wide k slice of one 32-row feature block for this warp.  HI: the
 // launch has more than 8 rows (a second n8 MMA per sub-tile); rows 0..7 run the
-// identical instruction sequence in both instantiations.
-template <int G, bool HI>
+// identical instruction sequence in both instantiations.  AFF: MLX-style affine
+// weights (unsigned codes, bf16 scale and bias per group): the group's partial
+// sum_k q x is scaled and the bias is added times the group's activation sum,
+// which one extra MMA per k step with an all-ones A operand delivers in the
+// accumulator layout.
+template <int G, bool HI, bool AFF>
 __device__ __forceinline__ void consume_slice(const uint8_t *blk, uint32_t xslice, int lane, int gq,
                                               const uint32_t (&xoff)[4], float (&acc)[2][2][4]) {
     constexpr int NG = kKChunk / G;
     constexpr int KS = G / 16;
+    constexpr uint32_t kOffset = AFF ? kBf16Neg128x2 : kBf16Neg136x2;
+    constexpr int kGroupBytes = AFF ? 128 : 64;
     const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + lane * 16);
     const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 512 + lane * 16);
 #pragma unroll
     for (int grp = 0; grp < NG; ++grp) {
-        const uint2 sv = *reinterpret_cast<const uint2 *>(blk + 1024 + grp * 64 + gq * 8);
+        const uint2 sv = *reinterpret_cast<const uint2 *>(blk + 1024 + grp * kGroupBytes + gq * 8);
         float part[2][2][4];
+        float xs[2][4];   // AFF: group activation sums (element c: verify row 2q + (c & 1))
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
             const int j = grp * KS + kk;
@@ -112,14 +125,24 @@ __device__ __forceinline__ void consume_slice(const uint8_t *blk, uint32_t xslic
                 ldsm_x4(xa, b0, b1, b2, b3);
             else
                 ldsm_x2(xa, b0, b1);
+            if (AFF) {
+                const uint32_t ones[4] = {kBf16One2, kBf16One2, kBf16One2, kBf16One2};
+                if (kk == 0) {
+                    mma_bf16_16816_zero(xs[0], ones, b0, b1);
+                    if (HI) mma_bf16_16816_zero(xs[1], ones, b2, b3);
+                } else {
+                    mma_bf16_16816(xs[0], ones, b0, b1);
+                    if (HI) mma_bf16_16816(xs[1], ones, b2, b3);
+                }
+            }
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
                 const uint32_t w = word_of(mt ? q1 : q0, j);
                 uint32_t af[4];
-                af[0] = fma_bf16x2(lop3_and_or(w, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
-                af[1] = fma_bf16x2(lop3_and_or(w >> 4, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
-                af[2] = fma_bf16x2(lop3_and_or(w >> 8, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
-                af[3] = fma_bf16x2(lop3_and_or(w >> 12, kNibMask, kBf16Magic), kBf16One2, kBf16Neg136x2);
+                af[0] = fma_bf16x2(lop3_and_or(w, kNibMask, kBf16Magic), kBf16One2, kOffset);
+                af[1] = fma_bf16x2(lop3_and_or(w >> 4, kNibMask, kBf16Magic), kBf16One2, kOffset);
+                af[2] = fma_bf16x2(lop3_and_or(w >> 8, kNibMask, kBf16Magic), kBf16One2, kOffset);
+                af[3] = fma_bf16x2(lop3_and_or(w >> 12, kNibMask, kBf16Magic), kBf16One2, kOffset);
                 if (kk == 0) {
                     mma_bf16_16816_zero(part[mt][0], af, b0, b1);
                     if (HI) mma_bf16_16816_zero(part[mt][1], af, b2, b3);
@@ -129,16 +152,29 @@ __device__ __forceinline__ void consume_slice(const uint8_t *blk, uint32_t xslic
                 }
             }
         }
+        uint2 bv = make_uint2(0, 0);
+        if (AFF) bv = *reinterpret_cast<const uint2 *>(blk + 1024 + grp * kGroupBytes + 64 + gq * 8);
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
-            const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(mt ? &sv.y : &sv.x));
             // sc.x: row mt*16 + g, sc.y: row mt*16 + g + 8
+            const float2 sc = AFF ? bf16x2_to_float2(mt ? sv.y : sv.x)
+                                  : __half22float2(*reinterpret_cast<const __half2 *>(mt ? &sv.y : &sv.x));
 #pragma unroll
             for (int n = 0; n < (HI ? 2 : 1); ++n) {
                 acc[mt][n][0] = fmaf(sc.x, part[mt][n][0], acc[mt][n][0]);
                 acc[mt][n][1] = fmaf(sc.x, part[mt][n][1], acc[mt][n][1]);
                 acc[mt][n][2] = fmaf(sc.y, part[mt][n][2], acc[mt][n][2]);
                 acc[mt][n][3] = fmaf(sc.y, part[mt][n][3], acc[mt][n][3]);
+            }
+            if (AFF) {
+                const float2 bi = bf16x2_to_float2(mt ? bv.y : bv.x);
+#pragma unroll
+                for (int n = 0; n < (HI ? 2 : 1); ++n) {
+                    acc[mt][n][0] = fmaf(bi.x, xs[n][0], acc[mt][n][0]);
+                    acc[mt][n][1] = fmaf(bi.x, xs[n][1], acc[mt][n][1]);
+                    acc[mt][n][2] = fmaf(bi.y, xs[n][2], acc[mt][n][2]);
+                    acc[mt][n][3] = fmaf(bi.y, xs[n][3], acc[mt][n][3]);
+                }
             }
         }
     }
@@ -195,12 +231,12 @@ __device__ __forceinline__ void store_block(const GemmArgs &a, void *yb, int t, 
     }
 }
 
-template <int G, bool HI>
+template <int G, bool HI, bool AFF>
 __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_constant__ GemmArgs a) {
-    constexpr int BB = block_bytes(G);
-    constexpr int CB = chunk_bytes(G);
+    constexpr int BB = block_bytes(G, AFF);
+    constexpr int CB = chunk_bytes(G, AFF);
     constexpr int STW = kStageIters * CB;
-    constexpr int NS = kStages;
+    constexpr int NS = num_stages(G, HI, AFF);
     constexpr int XSL = x_slice_bytes(HI);
     constexpr int XST = x_stage_bytes(HI);
     constexpr int NQ = lane_vals(HI) / 4;   // float4 per lane in the combine and the fixup
@@ -350,11 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 if (!HI && n_here == kStageIters) {
 #pragma unroll
                     for (int p = 0; p < kStageIters; p += kKGroups)
-                        consume_slice<G, HI>(stage_w + (p0 + p) * CB, stage_x + (p0 + p) * XSL, lane, gq,
+                        consume_slice<G, HI, AFF>(stage_w + (p0 + p) * CB, stage_x + (p0 + p) * XSL, lane, gq,
                                              xoff, acc);
                 } else {
                     for (int p = p0; p < n_here; p += kKGroups)
-                        consume_slice<G, HI>(stage_w + p * CB, stage_x + p * XSL, lane, gq, xoff, acc);
+                        consume_slice<G, HI, AFF>(stage_w + p * CB, stage_x + p * XSL, lane, gq, xoff, acc);
                 }
             }
             __syncwarp();
@@ -565,16 +601,97 @@ __global__ void pack_scales_kernel(const uint16_t *scales, int K, int N, uint8_t
 
 constexpr int kMaxDevices = 64;
 
-template <int G, bool HI>
+// Affine (MLX-style) packing: same chunk geometry; codes are taken as they are
+// (unsigned, no offset), and each group carries bf16 scales then bf16 biases.
+template <int G>
+__global__ void pack_codes_affine_kernel(const uint32_t *codes, int K, int N, uint8_t *out, long long n_entries,
+                                         int Kc) {
+    constexpr int BB = block_bytes(G, true);
+    constexpr int CB = chunk_bytes(G, true);
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n_entries) return;
+    const int lane = int(idx % 32);
+    long long r = idx / 32;
+    const int mt = int(r % 2);
+    r /= 2;
+    const int fw = int(r % kFeatWarps);
+    r /= kFeatWarps;
+    const int kc = int(r % Kc);
+    const long long t = r / Kc;
+    const int gq = lane >> 2, tq = lane & 3;
+    uint32_t words[4];
+    for (int j = 0; j < 4; ++j) {
+        uint32_t w = 0;
+        for (int i = 0; i < 4; ++i)
+            for (int h = 0; h < 2; ++h) {
+                const long long f = t * kTileN + fw * kBlockRows + mt * 16 + gq + ((i & 1) ? 8 : 0);
+                const int k = kc * kKChunk + j * 16 + 2 * tq + h + ((i & 2) ? 8 : 0);
+                uint32_t q = 0;  // rows past N: zero codes (and zero scale and bias)
+                if (f < N) q = (codes[f * (K / 8) + k / 8] >> (4 * (k % 8))) & 0xFu;
+                w |= q << (4 * i + 16 * h);
+            }
+        words[j] = w;
+    }
+    uint8_t *dst = out + (t * Kc + kc) * (long long)CB + fw * BB + mt * 512 + lane * 16;
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+}
+
+template <int G>
+__global__ void pack_scales_affine_kernel(const uint16_t *scales, const uint16_t *biases, int K, int N, uint8_t *out,
+                                          long long n_entries, int Kc) {
+    constexpr int BB = block_bytes(G, true);
+    constexpr int CB = chunk_bytes(G, true);
+    constexpr int NG = kKChunk / G;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n_entries) return;
+    const int mt = int(idx % 2);
+    long long r = idx / 2;
+    const int g = int(r % 8);
+    r /= 8;
+    const int grp = int(r % NG);
+    r /= NG;
+    const int fw = int(r % kFeatWarps);
+    r /= kFeatWarps;
+    const int kc = int(r % Kc);
+    const long long t = r / Kc;
+    const long long f_lo = t * kTileN + fw * kBlockRows + mt * 16 + g;
+    const long long f_hi = f_lo + 8;
+    const int gi = kc * NG + grp;
+    const int ngroups = K / G;
+    const uint32_t s_lo = f_lo < N ? scales[f_lo * ngroups + gi] : 0u;
+    const uint32_t s_hi = f_hi < N ? scales[f_hi * ngroups + gi] : 0u;
+    const uint32_t b_lo = f_lo < N ? biases[f_lo * ngroups + gi] : 0u;
+    const uint32_t b_hi = f_hi < N ? biases[f_hi * ngroups + gi] : 0u;
+    uint8_t *dst = out + (t * Kc + kc) * (long long)CB + fw * BB + 1024 + grp * 128 + g * 8 + mt * 4;
+    *reinterpret_cast<uint32_t *>(dst) = s_lo | (s_hi << 16);
+    *reinterpret_cast<uint32_t *>(dst + 64) = b_lo | (b_hi << 16);
+}
+
+template <int G>
+cudaError_t launch_pack_affine_g(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases, int K, int N,
+                                 void *packed, cudaStream_t s) {
+    const int T = (N + kTileN - 1) / kTileN;
+    const int Kc = K / kKChunk;
+    const long long n_codes = (long long)T * Kc * kFeatWarps * 2 * 32;
+    const long long n_scales = (long long)T * Kc * kFeatWarps * (kKChunk / G) * 8 * 2;
+    const int th = 256;
+    pack_codes_affine_kernel<G><<<unsigned((n_codes + th - 1) / th), th, 0, s>>>(codes, K, N, (uint8_t *)packed,
+                                                                               n_codes, Kc);
+    pack_scales_affine_kernel<G><<<unsigned((n_scales + th - 1) / th), th, 0, s>>>(scales, biases, K, N,
+                                                                                 (uint8_t *)packed, n_scales, Kc);
+    return cudaGetLastError();
+}
+
+template <int G, bool HI, bool AFF>
 cudaError_t launch_gemm_g(const GemmArgs &a, int u_max, cudaStream_t s) {
-    const size_t smem = gemm_smem_bytes(G, HI);
+    const size_t smem = gemm_smem_bytes(G, HI, AFF);
     // the shared-memory opt-in is a per-device property of the kernel: set it once
     static std::atomic<bool> opted_in[kMaxDevices];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
-        err = cudaFuncSetAttribute(w4_lane_gemm_kernel<G, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        err = cudaFuncSetAttribute(w4_lane_gemm_kernel<G, HI, AFF>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (err != cudaSuccess) return err;
         if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
     }
@@ -592,7 +709,7 @@ cudaError_t launch_gemm_g(const GemmArgs &a, int u_max, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, w4_lane_gemm_kernel<G, HI>, a);
+    return cudaLaunchKernelEx(&cfg, w4_lane_gemm_kernel<G, HI, AFF>, a);
 }
 
 template <int G>
@@ -665,8 +782,19 @@ bool gemm_encode_x(GemmArgs &a, const uint16_t *x, int ldx, long long x_stride, 
 }
 
 cudaError_t launch_w4_gemm(const GemmArgs &a, int u_max, cudaStream_t s) {
-    if (a.R > 8) return a.G == 64 ? launch_gemm_g<64, true>(a, u_max, s) : launch_gemm_g<32, true>(a, u_max, s);
-    return a.G == 64 ? launch_gemm_g<64, false>(a, u_max, s) : launch_gemm_g<32, false>(a, u_max, s);
+    const bool hi = a.R > 8;
+    if (a.affine) {
+        if (hi) return a.G == 64 ? launch_gemm_g<64, true, true>(a, u_max, s) : launch_gemm_g<32, true, true>(a, u_max, s);
+        return a.G == 64 ? launch_gemm_g<64, false, true>(a, u_max, s) : launch_gemm_g<32, false, true>(a, u_max, s);
+    }
+    if (hi) return a.G == 64 ? launch_gemm_g<64, true, false>(a, u_max, s) : launch_gemm_g<32, true, false>(a, u_max, s);
+    return a.G == 64 ? launch_gemm_g<64, false, false>(a, u_max, s) : launch_gemm_g<32, false, false>(a, u_max, s);
+}
+
+cudaError_t launch_pack_w4_affine(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases, int K, int N,
+                                  int G, void *packed, cudaStream_t s) {
+    return G == 64 ? launch_pack_affine_g<64>(codes, scales, biases, K, N, packed, s)
+                   : launch_pack_affine_g<32>(codes, scales, biases, K, N, packed, s);
 }
 
 cudaError_t launch_pack_w4(const uint8_t *codes, const uint16_t *scales, int K, int N, int G, void *packed,

@@ -42,15 +42,23 @@ constexpr int kLaneAccHi = 16;             // fp32 accumulators per lane: 2 sub-
 // rows 8..15 (accumulator half n = 1) only when the launch has them
 __host__ __device__ constexpr int lane_vals(bool hi) { return hi ? kLaneAccHi : kLaneAccHi / 2; }
 
-__host__ __device__ constexpr int block_bytes(int G) { return 1024 + 64 * (kKChunk / G); }
-__host__ __device__ constexpr int chunk_bytes(int G) { return kFeatWarps * block_bytes(G); }
+// Affine (MLX-style) blocks also carry one bf16 bias per row and group after the
+// bf16 scales: [grp][scales 64 B][biases 64 B].
+__host__ __device__ constexpr int block_bytes(int G, bool aff = false) {
+    return 1024 + (aff ? 128 : 64) * (kKChunk / G);
+}
+__host__ __device__ constexpr int chunk_bytes(int G, bool aff = false) { return kFeatWarps * block_bytes(G, aff); }
 // One partial tile of the split-K fixup: 4 feature warps x 32 lanes x 16 floats.
 constexpr size_t kSlotBytes = size_t(kFeatWarps) * 32 * kLaneAccHi * 4;
 
-inline size_t gemm_smem_bytes(int G, bool hi) {
+// Pipeline depth: 4 stages, 3 where four would not fit (affine, G = 32, R > 8).
+__host__ __device__ constexpr int num_stages(int G, bool hi, bool aff) { return (aff && G == 32 && hi) ? 3 : kStages; }
+
+inline size_t gemm_smem_bytes(int G, bool hi, bool aff = false) {
+    const int ns = num_stages(G, hi, aff);
     return 1024                                                         // alignment slack
-           + size_t(kStages) * x_stage_bytes(hi)                        // activation slices (1024-B aligned)
-           + size_t(kStages) * kStageIters * chunk_bytes(G)            // weight stages
+           + size_t(ns) * x_stage_bytes(hi)                             // activation slices (1024-B aligned)
+           + size_t(ns) * kStageIters * chunk_bytes(G, aff)            // weight stages
            + 2 * size_t(kFeatWarps) * 32 * lane_vals(hi) * 4            // k-group combine buffers
            + 256;                                                       // barriers
 }
@@ -58,10 +66,10 @@ inline size_t gemm_smem_bytes(int G, bool hi) {
 inline bool packed_shape_ok(int K, int N, int G) {
     return K > 0 && N > 0 && (G == 32 || G == 64) && K % kKChunk == 0;
 }
-inline size_t packed_bytes(int K, int N, int G) {
+inline size_t packed_bytes(int K, int N, int G, bool aff = false) {
     if (!packed_shape_ok(K, N, G)) return 0;
     size_t T = (size_t(N) + kTileN - 1) / kTileN;
-    return T * size_t(K / kKChunk) * size_t(chunk_bytes(G));
+    return T * size_t(K / kKChunk) * size_t(chunk_bytes(G, aff));
 }
 
 // ---- launch description ------------------------------------------------------
@@ -90,6 +98,7 @@ struct GemmArgs {
     int mode;                  // EpilogueMode
     int F;                     // kSwiGluBf16: width of h (N = 2F)
     int R, K, N, G;
+    int affine;                // packed weights are MLX-style affine (codes + bf16 scale and bias)
     int T, Kc, Pv;
     unsigned *counters;        // [U_max][T][kFeatWarps], zero between launches
     float4 *partials;          // [U_max][Pv][2][kFeatWarps][32][4]
@@ -113,6 +122,10 @@ cudaError_t launch_w4_gemm(const GemmArgs &a, int u_max, cudaStream_t s);
 // interleave_gate_up: rows [0, N/2) are gate rows, [N/2, N) up rows; they are
 // packed so that each 32-row feature block holds 16 gate rows (sub-tile 0) and
 // the 16 matching up rows (sub-tile 1), the layout kSwiGluBf16 expects.
+// MLX-style affine weights: codes uint32 [N][K/8] (element i of a word in bits
+// 4i..4i+3, unsigned), scales and biases bf16 [N][K/G].
+cudaError_t launch_pack_w4_affine(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases, int K, int N,
+                                  int G, void *packed, cudaStream_t s);
 cudaError_t launch_pack_w4(const uint8_t *codes, const uint16_t *scales, int K, int N, int G, void *packed,
                            bool interleave_gate_up, cudaStream_t s);
 int device_sm_count();

@@ -33,7 +33,7 @@ class TFError(RuntimeError):
 
 
 class W4MatrixC(ctypes.Structure):
-    _fields_ = [("packed", P), ("K", I32), ("N", I32), ("group", I32)]
+    _fields_ = [("packed", P), ("K", I32), ("N", I32), ("group", I32), ("affine", I32)]
 
 
 class SamplingC(ctypes.Structure):
@@ -60,6 +60,8 @@ SIGNATURES = [
     ("tf_workspace_status", ctypes.c_int, [P, P, ctypes.POINTER(I32)]),
     ("tf_w4_packed_bytes", SZ, [I32, I32, I32]),
     ("tf_pack_w4", ctypes.c_int, [P, P, I32, I32, I32, P, SZ, P]),
+    ("tf_w4_affine_packed_bytes", SZ, [I32, I32, I32]),
+    ("tf_pack_w4_affine", ctypes.c_int, [P, P, P, I32, I32, I32, P, SZ, P]),
     ("tf_pack_w4_gate_up", ctypes.c_int, [P, P, I32, I32, I32, P, SZ, P]),
     ("tf_lane_gemm_workspace_bytes", SZ, [I32, I32, I32]),
     ("tf_lane_gemm_w4", ctypes.c_int, [ctypes.POINTER(W4MatrixC), P, I32, I32, P, I32, P, SZ, P]),
@@ -140,9 +142,10 @@ def workspace_status(ws: torch.Tensor, stream=None) -> int:
 class W4Matrix:
     """A packed W4 matrix living on the device."""
 
-    def __init__(self, packed: torch.Tensor, K: int, N: int, group: int, gate_up: bool = False):
-        self.packed, self.K, self.N, self.group, self.gate_up = packed, K, N, group, gate_up
-        self._c = W4MatrixC(packed.data_ptr(), K, N, group)
+    def __init__(self, packed: torch.Tensor, K: int, N: int, group: int, gate_up: bool = False,
+                 affine: bool = False):
+        self.packed, self.K, self.N, self.group, self.gate_up, self.affine = packed, K, N, group, gate_up, affine
+        self._c = W4MatrixC(packed.data_ptr(), K, N, group, int(affine))
 
     def c(self) -> W4MatrixC:
         return self._c
@@ -170,6 +173,24 @@ def pack_w4(codes: torch.Tensor, scales: torch.Tensor, group: int, gate_up: bool
     else:
         _check(lib.tf_pack_w4(_ptr(codes), _ptr(scales), K, N, group, _ptr(out), nbytes, _stream(stream)))
     return W4Matrix(out, K, N, group, gate_up)
+
+
+def pack_w4_affine(codes: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, group: int,
+                   out: torch.Tensor = None, stream=None) -> W4Matrix:
+    """MLX-style affine weights on the device: codes uint32 (or int32 bits) [N][K/8],
+    scales and biases bf16 (or int16 bits) [N][K/group]."""
+    lib = load()
+    N, K8 = codes.shape
+    K = 8 * K8
+    nbytes = int(lib.tf_w4_affine_packed_bytes(K, N, group))
+    if nbytes == 0:
+        raise TFError(TF_ERR_UNSUPPORTED, f"unsupported shape K={K} N={N} group={group}")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=codes.device)
+    codes, scales, biases = codes.contiguous(), scales.contiguous(), biases.contiguous()
+    _check(lib.tf_pack_w4_affine(_ptr(codes), _ptr(scales), _ptr(biases), K, N, group, _ptr(out), nbytes,
+                                 _stream(stream)))
+    return W4Matrix(out, K, N, group, affine=True)
 
 
 # ---------------------------------------------------------------- linear
