@@ -301,6 +301,47 @@ def extra_lmhead(tf, torch, steps=30):
     return out
 
 
+def extra_affine(tf, torch, steps=30):
+    """MLX-style affine W4 (bf16 scale and bias per group) on the 5120 -> 17408
+    projection, G = 64, R = 1 / 8 / 16: GB/s over codes + scales + biases, weights
+    rotating over copies larger than L2, CUDA-graph replay of one rotation."""
+    K, N, G = 5120, 17408, GROUP
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(9)
+    nbytes = K * N // 2 + 4 * N * (K // G)
+    n_copies = max(3, -(-3 * L2_BYTES // nbytes))
+    copies = []
+    for _ in range(n_copies):
+        codes = torch.randint(-2**31, 2**31 - 1, (N, K // 8), dtype=torch.int32, device="cuda", generator=gen)
+        sc = (torch.rand((N, K // G), device="cuda", generator=gen) * 0.02 + 1e-3).bfloat16()
+        bi = (-sc.float() * 7.5).bfloat16()
+        copies.append(tf.pack_w4_affine(codes, sc.view(torch.int16), bi.view(torch.int16), G))
+    x = (torch.randn((16, K), device="cuda", generator=gen)).bfloat16().view(torch.int16)
+    y = torch.empty((16, N), device="cuda")
+    ws = tf.workspace(tf.lane_gemm_workspace_bytes(K, N, G))
+    out = {"bytes_per_launch": nbytes}
+    for R in (1, 8, 16):
+        xv, yv = x[:R], y[:R]
+        for c in copies:
+            tf.lane_gemm_w4(c, xv, y=yv, ws=ws)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for c in copies:
+                tf.lane_gemm_w4(c, xv, y=yv, ws=ws)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (steps * n_copies)
+        out[f"R{R}"] = {"us_per_launch": us, "gbs": nbytes / us / 1e3}
+    return out
+
+
 def extra_moe(tf, torch, steps=30):
     from w4_gemm_keyed_gb300 import inputs
     E, H, F, G, k = 128, 2048, 768, 32, 8
@@ -537,7 +578,7 @@ def main():
     ap.add_argument("--impl", default="tf", choices=["tf", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the LM-head / MoE / decoder side measurements")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--only", choices=["lmhead", "dense", "moe", "decoder"],
+    ap.add_argument("--only", choices=["lmhead", "dense", "moe", "decoder", "affine"],
                     help="run one workload briefly and print its timings (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -556,7 +597,7 @@ def main():
             secs, steps, lps = time_dense(tf, torch, mats, args.steps, args.warmup)
             out = {"dense_gbs": STEP_BYTES * steps / secs / 1e9}
         else:
-            fn = {"lmhead": extra_lmhead, "moe": extra_moe, "decoder": extra_decoder}[args.only]
+            fn = {"lmhead": extra_lmhead, "moe": extra_moe, "decoder": extra_decoder, "affine": extra_affine}[args.only]
             out = fn(tf, torch, steps=args.steps)
         print(json.dumps({"only": args.only, "result": out}))
         return 0
@@ -603,7 +644,8 @@ def main():
 
     extra = {}
     if rank == 0 and not args.no_extra:
-        for name, fn in (("lmhead_sampler", extra_lmhead), ("moe30b", extra_moe), ("decoder", extra_decoder)):
+        for name, fn in (("lmhead_sampler", extra_lmhead), ("moe30b", extra_moe), ("decoder", extra_decoder),
+                         ("affine_5120x17408", extra_affine)):
             try:
                 extra[name] = fn(tf, torch)
             except Exception as exc:  # a side measurement must not hide the headline line
