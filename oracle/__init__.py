@@ -8,7 +8,8 @@ verify pass computes, written from the TensorFold pages:
 * ``sampling`` -- keyed Gumbel-max sampling over top-k / top-p candidates;
 * ``accept``   -- longest-prefix acceptance of drafts;
 * ``moe``      -- top-8 routed W4 SwiGLU experts;
-* ``decoder``  -- the attention-free synthetic decoder, serial and drafted.
+* ``decoder``  -- the attention-free synthetic decoder, serial and drafted;
+* ``attention`` -- causal grouped-head attention of verify rows over a KV cache.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline /
 reference legs of ``bench.py`` may import it.  It shares no code with the
@@ -21,4 +22,4 @@ unpinned"); the pins live in ``tests/test_oracle_*.py``.
 
 from .linear import w4_linear, half_to_f64, bf16_to_f64, unpack_codes, num_threads  # noqa: F401
 from .numerics import bf16_round, bf16_bits_of  # noqa: F401
-from . import sampling, accept, moe, decoder, affine  # noqa: F401
+from . import sampling, accept, moe, decoder, affine, attention  # noqa: F401

@@ -138,6 +138,16 @@ def noisy_drafts(rng: np.random.Generator, true_tokens, p_match: float, V: int) 
     return np.where(keep, t, rand).astype(np.int32)
 
 
+def attention_inputs(rng: np.random.Generator, R: int, n_kv: int, group: int, L: int, head_dim: int = 128,
+                     q_std: float = 1.0):
+    """bf16 bits of verify-row queries [R][n_kv*group][head_dim] and a KV cache
+    prefix k, v [n_kv][L][head_dim], all normal (keys and values N(0, 1))."""
+    q = bf16_normal(rng, (R, n_kv * group, head_dim), q_std)
+    k = bf16_normal(rng, (n_kv, L, head_dim))
+    v = bf16_normal(rng, (n_kv, L, head_dim))
+    return q, k, v
+
+
 def router_logits(rng: np.random.Generator, R: int, n_experts: int) -> np.ndarray:
     return rng.standard_normal((R, n_experts), dtype=np.float32)
 
