@@ -69,6 +69,7 @@ typedef enum tf_status {
 #define TF_DEV_TIMEOUT 1          /* an mbarrier wait exceeded its iteration limit */
 #define TF_DEV_NONFINITE_LOGIT 2  /* a logit was NaN or +-inf (its row's token is -1) */
 #define TF_DEV_BAD_TOKEN 3        /* a token id outside [0, vocab) reached the embedding */
+#define TF_DEV_BAD_POSITION 4     /* a KV-cache call saw *pos < 0 or *pos + R > max_len (nothing written) */
 
 /* Thread-local description of the last host-side error ("" when none). */
 TF_API const char *tf_last_error(void);
@@ -319,6 +320,59 @@ TF_API tf_status tf_gather_drafts(const int32_t *table, int64_t table_len, const
                                   int32_t *drafts, void *stream);
 TF_API tf_status tf_commit_tokens(const int32_t *tokens, const int32_t *accepted, const int64_t *pos, int32_t *log,
                                   int64_t log_len, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Attention of the verify rows over a KV cache.
+ *
+ * The README's note on drafting says that drafted and serial decoding from the
+ * same cache agree, and the 0.3.4.1 release note ("TensorFold: the contract is
+ * what it does not change", section "The regression it published against
+ * itself") keeps cached bits independent of where a conversation resumed.  The
+ * pages do not spell out the attention; these calls compute causal scaled
+ * dot-product attention with grouped key/value heads (head dimension 128,
+ * query head h reads KV head h / group), and make each row's bits depend only
+ * on its own query, its own position p and cache entries 0..p:
+ *   s_t = q . k_t / sqrt(128),  out = sum_{t <= p} exp(s_t - max s) v_t / sum exp(s_t - max s).
+ * Keys are processed on a fixed grid of absolute positions (partitions of 256,
+ * steps of 64), never relative to the launch, so a verify pass of R rows gives
+ * every row the bits of a one-row pass at that position.  Rolling back
+ * rejected rows needs no call: the next pass starts at the advanced *pos and
+ * rewrites those entries before any row can read them.
+ * ------------------------------------------------------------------------
+ * tf_kv_cache: k and v are dev bf16 arrays [n_kv][max_len][128]; the element
+ *   (head j, position t, dimension d) is stored at
+ *     (j * max_len + t) * 128 + 8 * ((d / 8) XOR (t % 8)) + d % 8
+ *   (the 16-byte chunks of each entry permuted by its position, so that one
+ *   contiguous copy of 64 entries reads without shared-memory bank conflicts).
+ *   Only tf_kv_append writes entries.  Caller-owned, 16-B aligned; n_kv in
+ *   1..128; max_len a positive multiple of 256.  Entries at positions past
+ *   *pos + R - 1 are never read; entries a call reads must be finite.
+ * tf_kv_append: writes k_new[r] and v_new[r] (dev bf16 [R][ld], KV head j at
+ *   columns j*128 .. j*128+127; ld a multiple of 8, rows 16-B aligned) as the
+ *   entries at position *pos + r, r < R, R in 1..max_len (a whole prompt may be
+ *   appended in one call).  pos: dev int64 [1], read on the device.  A bad
+ *   position records TF_DEV_BAD_POSITION in ws (>= 256 B) and writes nothing.
+ * tf_attention_verify: out[r][h*128 + d] (dev fp32 [R][ldo], ldo >= n_kv*group*128)
+ *   for rows r < R (R in 1..16) at positions *pos + r, over the entries
+ *   already appended (append the pass's own rows first).  q: dev bf16 [R][ldq],
+ *   query head h at columns h*128 (ldq a multiple of 8, 16-B aligned).  group
+ *   in {1, 2, 4, 8}.  ws: tf_attention_workspace_bytes(c, group, R) bytes of
+ *   scratch for per-partition partial results.  A bad position records
+ *   TF_DEV_BAD_POSITION and leaves out unwritten.
+ */
+typedef struct tf_kv_cache {
+    uint16_t *k;
+    uint16_t *v;
+    int32_t n_kv;
+    int32_t max_len;
+} tf_kv_cache;
+
+TF_API tf_status tf_kv_append(const tf_kv_cache *c, const uint16_t *k_new, const uint16_t *v_new, int32_t ld,
+                              int32_t R, const int64_t *pos, void *ws, size_t ws_bytes, void *stream);
+TF_API size_t tf_attention_workspace_bytes(const tf_kv_cache *c, int32_t group, int32_t R);
+TF_API tf_status tf_attention_verify(const tf_kv_cache *c, int32_t group, const uint16_t *q, int32_t ldq,
+                                     int32_t R, const int64_t *pos, float *out, int32_t ldo, void *ws,
+                                     size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
  * Pieces of the synthetic decoder (the steps tf_verify_step chains), public so

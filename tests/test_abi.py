@@ -94,6 +94,37 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.tf_last_error() != b""
 
 
+def test_kv_cache_validation_rejects_bad_arguments(lib):
+    from w4_gemm_keyed_gb300 import tf
+    big = 1 << 30
+    C = tf.KVCacheC(256, 512, 8, 4096)
+    assert lib.tf_attention_workspace_bytes(ctypes.byref(C), 8, 16) == \
+        256 + 16 * 16 * 64 * 128 * 4 + 16 * 16 * 64 * 2 * 4
+    assert lib.tf_attention_workspace_bytes(ctypes.byref(C), 3, 16) == 0
+    assert lib.tf_attention_workspace_bytes(ctypes.byref(C), 8, 17) == 0
+    ok_args = (256, 1024, 1, 256, 256, 1024, 256, big, None)     # q, ldq, R, pos, out, ldo, ws, ws_bytes, stream
+    for bad, code in [(tf.KVCacheC(None, 512, 8, 4096), tf.TF_ERR_INVALID_ARG),     # null k
+                      (tf.KVCacheC(258, 512, 8, 4096), tf.TF_ERR_INVALID_ARG),      # misaligned k
+                      (tf.KVCacheC(256, 512, 0, 4096), tf.TF_ERR_UNSUPPORTED),      # n_kv = 0
+                      (tf.KVCacheC(256, 512, 8, 1000), tf.TF_ERR_UNSUPPORTED)]:     # max_len % 256
+        assert lib.tf_attention_verify(ctypes.byref(bad), 1, *ok_args) == code
+        assert lib.tf_kv_append(ctypes.byref(bad), 256, 256, 1024, 1, 256, 256, 256, None) == code
+    assert lib.tf_attention_verify(ctypes.byref(C), 3, *ok_args) == tf.TF_ERR_UNSUPPORTED          # group 3
+    assert lib.tf_attention_verify(ctypes.byref(C), 8, 256, 1024, 17, 256, 256, 8192, 256, big, None) == \
+        tf.TF_ERR_INVALID_ARG                                                                       # R = 17
+    assert lib.tf_attention_verify(ctypes.byref(C), 8, 256, 1000, 1, 256, 256, 8192, 256, big, None) == \
+        tf.TF_ERR_INVALID_ARG                                                                       # ldq < n_q*128
+    assert lib.tf_attention_verify(ctypes.byref(C), 1, 264, 1024, 1, 256, 256, 1024, 256, big, None) == \
+        tf.TF_ERR_INVALID_ARG                                                                       # q not 16-B aligned
+    assert lib.tf_attention_verify(ctypes.byref(C), 1, 256, 1024, 1, None, 256, 1024, 256, big, None) == \
+        tf.TF_ERR_INVALID_ARG                                                                       # null pos
+    assert lib.tf_attention_verify(ctypes.byref(C), 1, 256, 1024, 1, 256, 256, 1024, 256, 100, None) == \
+        tf.TF_ERR_WORKSPACE                                                                         # ws too small
+    assert lib.tf_kv_append(ctypes.byref(C), 256, 256, 1000, 1, 256, 256, 256, None) == tf.TF_ERR_INVALID_ARG
+    assert lib.tf_kv_append(ctypes.byref(C), 256, 256, 1024, 4097, 256, 256, 256, None) == tf.TF_ERR_INVALID_ARG
+    assert lib.tf_kv_append(ctypes.byref(C), 256, 256, 1024, 1, 256, 256, 128, None) == tf.TF_ERR_WORKSPACE
+
+
 def _start(p, q, rem):
     return p * q + min(p, rem)
 

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libtf.so")
-SOURCES = ["w4_gemm.cu", "sampler.cu", "glue.cu", "tf_api.cu"]
+SOURCES = ["w4_gemm.cu", "sampler.cu", "glue.cu", "attention.cu", "tf_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

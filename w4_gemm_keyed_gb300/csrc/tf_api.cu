@@ -1,6 +1,7 @@
 // extern "C" entry points of libtf: argument validation, workspace layout and
 // launch sequencing.  Every step of the verify pass runs in this library's own
-// kernels (w4_gemm.cu, sampler.cu, glue.cu); nothing here computes on the host.
+// kernels (w4_gemm.cu, sampler.cu, glue.cu, attention.cu); nothing here computes
+// on the host.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -8,6 +9,7 @@
 #include <string>
 
 #include "../../include/tf.h"
+#include "attention.cuh"
 #include "glue.cuh"
 #include "sampler.cuh"
 #include "w4_gemm.cuh"
@@ -486,6 +488,76 @@ tf_status tf_gather_drafts(const int32_t *table, int64_t table_len, const int64_
     if (!table || table_len < 0 || !pos || !drafts) return fail(TF_ERR_INVALID_ARG, "null pointer or negative length");
     cudaError_t e = launch_gather_drafts(table, table_len, pos, R - 1, drafts, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tf_gather_drafts");
+    return ok();
+}
+
+namespace {
+
+tf_status check_cache(const tf_kv_cache *c) {
+    if (!c) return fail(TF_ERR_INVALID_ARG, "null KV cache");
+    if (!c->k || !c->v) return fail(TF_ERR_INVALID_ARG, "KV cache: null k or v");
+    if (!aligned(c->k, 16) || !aligned(c->v, 16)) return fail(TF_ERR_INVALID_ARG, "KV cache: k, v not 16-B aligned");
+    if (c->n_kv < 1 || c->n_kv > 128) return fail(TF_ERR_UNSUPPORTED, "KV cache: n_kv=%d outside [1, 128]", c->n_kv);
+    if (c->max_len <= 0 || c->max_len % kKvPart)
+        return fail(TF_ERR_UNSUPPORTED, "KV cache: max_len=%d is not a positive multiple of %d", c->max_len, kKvPart);
+    return TF_OK;
+}
+
+}  // namespace
+
+tf_status tf_kv_append(const tf_kv_cache *c, const uint16_t *k_new, const uint16_t *v_new, int32_t ld, int32_t R,
+                       const int64_t *pos, void *ws, size_t ws_bytes, void *stream) {
+    tf_status st = check_cache(c);
+    if (st != TF_OK) return st;
+    if (R < 1 || R > c->max_len) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, max_len=%d]", R, c->max_len);
+    if (!k_new || !v_new || !pos) return fail(TF_ERR_INVALID_ARG, "null k_new, v_new or pos");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return fail(TF_ERR_INVALID_ARG, "k_new, v_new not 16-B aligned");
+    if (ld < c->n_kv * kHeadDim || ld % 8)
+        return fail(TF_ERR_INVALID_ARG, "ld=%d must be a multiple of 8 and >= n_kv * 128", ld);
+    if ((st = check_ws(ws, ws_bytes, 256)) != TF_OK) return st;
+    cudaError_t e = launch_kv_append(k_new, v_new, ld, R, pos, c->k, c->v, c->n_kv, c->max_len,
+                                     static_cast<int *>(ws), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_kv_append");
+    return ok();
+}
+
+size_t tf_attention_workspace_bytes(const tf_kv_cache *c, int32_t group, int32_t R) {
+    if (!c || c->n_kv < 1 || c->max_len <= 0 || c->max_len % kKvPart || R < 1 || R > TF_MAX_ROWS) return 0;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return 0;
+    return 256 + attn_opart_bytes(c->n_kv, group, c->max_len, R) + attn_ml_bytes(c->n_kv, group, c->max_len, R);
+}
+
+tf_status tf_attention_verify(const tf_kv_cache *c, int32_t group, const uint16_t *q, int32_t ldq, int32_t R,
+                              const int64_t *pos, float *out, int32_t ldo, void *ws, size_t ws_bytes, void *stream) {
+    tf_status st = check_cache(c);
+    if (st != TF_OK) return st;
+    if (group != 1 && group != 2 && group != 4 && group != 8)
+        return fail(TF_ERR_UNSUPPORTED, "group=%d not in {1, 2, 4, 8}", group);
+    if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
+    if (!q || !pos || !out) return fail(TF_ERR_INVALID_ARG, "null q, pos or out");
+    const int n_q = c->n_kv * group;
+    if (!aligned(q, 16) || ldq < n_q * kHeadDim || ldq % 8)
+        return fail(TF_ERR_INVALID_ARG, "q must be 16-B aligned with ldq a multiple of 8 and >= %d", n_q * kHeadDim);
+    if (!aligned(out, 4) || ldo < n_q * kHeadDim)
+        return fail(TF_ERR_INVALID_ARG, "out must be 4-B aligned with ldo >= %d", n_q * kHeadDim);
+    if ((st = check_ws(ws, ws_bytes, tf_attention_workspace_bytes(c, group, R))) != TF_OK) return st;
+    AttnArgs a{};
+    a.k = c->k;
+    a.v = c->v;
+    a.q = q;
+    a.ldq = ldq;
+    a.R = R;
+    a.group = group;
+    a.n_kv = c->n_kv;
+    a.max_len = c->max_len;
+    a.pos = pos;
+    a.err = static_cast<int *>(ws);
+    a.opart = reinterpret_cast<float *>(static_cast<char *>(ws) + 256);
+    a.ml = reinterpret_cast<float *>(static_cast<char *>(ws) + 256 + attn_opart_bytes(c->n_kv, group, c->max_len, R));
+    a.out = out;
+    a.ldo = ldo;
+    cudaError_t e = launch_attention(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_attention_verify");
     return ok();
 }
 

@@ -17,7 +17,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtf.so")
 
 TF_OK, TF_ERR_INVALID_ARG, TF_ERR_UNSUPPORTED, TF_ERR_CUDA, TF_ERR_TIMEOUT, TF_ERR_WORKSPACE = range(6)
-TF_DEV_OK, TF_DEV_TIMEOUT, TF_DEV_NONFINITE_LOGIT, TF_DEV_BAD_TOKEN = range(4)
+TF_DEV_OK, TF_DEV_TIMEOUT, TF_DEV_NONFINITE_LOGIT, TF_DEV_BAD_TOKEN, TF_DEV_BAD_POSITION = range(5)
+HEAD_DIM = 128
 MAX_ROWS = 16
 MAX_TOP_K = 64
 
@@ -43,6 +44,10 @@ class SamplingC(ctypes.Structure):
 class MoeLayerC(ctypes.Structure):
     _fields_ = [("gate_up", P), ("down", P), ("hidden", I32), ("ffn", I32), ("n_experts", I32),
                 ("top_k", I32), ("group", I32)]
+
+
+class KVCacheC(ctypes.Structure):
+    _fields_ = [("k", P), ("v", P), ("n_kv", I32), ("max_len", I32)]
 
 
 class ModelC(ctypes.Structure):
@@ -71,6 +76,9 @@ SIGNATURES = [
     ("tf_accept", ctypes.c_int, [P, P, I32, P, P, P]),
     ("tf_gather_drafts", ctypes.c_int, [P, ctypes.c_int64, P, I32, P, P]),
     ("tf_commit_tokens", ctypes.c_int, [P, P, P, P, ctypes.c_int64, P]),
+    ("tf_kv_append", ctypes.c_int, [ctypes.POINTER(KVCacheC), P, P, I32, I32, P, P, SZ, P]),
+    ("tf_attention_workspace_bytes", SZ, [ctypes.POINTER(KVCacheC), I32, I32]),
+    ("tf_attention_verify", ctypes.c_int, [ctypes.POINTER(KVCacheC), I32, P, I32, I32, P, P, I32, P, SZ, P]),
     ("tf_moe_workspace_bytes", SZ, [ctypes.POINTER(MoeLayerC), I32]),
     ("tf_moe_w4", ctypes.c_int, [ctypes.POINTER(MoeLayerC), P, P, I32, P, P, SZ, P]),
     ("tf_verify_step_workspace_bytes", SZ, [ctypes.POINTER(ModelC), I32]),
@@ -271,6 +279,44 @@ def commit_tokens(tokens: torch.Tensor, accepted: torch.Tensor, pos: torch.Tenso
     _check(load().tf_commit_tokens(_ptr(tokens), _ptr(accepted), _ptr(pos), _ptr(log), log.numel(),
                                    _stream(stream)))
     return log
+
+
+# ---------------------------------------------------------------- KV cache attention
+class KVCache:
+    """A KV cache on the device: k, v bf16 bits (int16) [n_kv][max_len][128] in the
+    library's position-swizzled layout (tf.h), zero-filled at creation."""
+
+    def __init__(self, n_kv: int, max_len: int, device="cuda"):
+        self.k = torch.zeros((n_kv, max_len, HEAD_DIM), dtype=torch.int16, device=device)
+        self.v = torch.zeros((n_kv, max_len, HEAD_DIM), dtype=torch.int16, device=device)
+        self.n_kv, self.max_len = n_kv, max_len
+        self._c = KVCacheC(self.k.data_ptr(), self.v.data_ptr(), n_kv, max_len)
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, pos: torch.Tensor, ws: torch.Tensor = None,
+               stream=None):
+        """Entries at positions pos .. pos + R - 1 from k_new, v_new bf16 [R][n_kv*128]."""
+        if ws is None:
+            ws = workspace(256, device=k_new.device)
+        R = k_new.shape[0]
+        _check(load().tf_kv_append(ctypes.byref(self._c), _ptr(k_new), _ptr(v_new), k_new.stride(0), R, _ptr(pos),
+                                   _ptr(ws), ws.numel(), _stream(stream)))
+        return ws
+
+    def workspace_bytes(self, group: int, R: int) -> int:
+        return int(load().tf_attention_workspace_bytes(ctypes.byref(self._c), group, R))
+
+    def attention(self, q: torch.Tensor, group: int, pos: torch.Tensor, out: torch.Tensor = None,
+                  ws: torch.Tensor = None, stream=None) -> torch.Tensor:
+        """fp32 [R][n_q*128]: rows at positions pos + r attending over entries 0..pos + r."""
+        R = q.shape[0]
+        n_q = self.n_kv * group
+        if out is None:
+            out = torch.empty((R, n_q * HEAD_DIM), dtype=torch.float32, device=q.device)
+        if ws is None:
+            ws = workspace(self.workspace_bytes(group, R), device=q.device)
+        _check(load().tf_attention_verify(ctypes.byref(self._c), group, _ptr(q), q.stride(0), R, _ptr(pos), _ptr(out),
+                                          out.stride(0), _ptr(ws), ws.numel(), _stream(stream)))
+        return out
 
 
 def rmsnorm_bf16(x: torch.Tensor, eps: float, out: torch.Tensor = None, stream=None) -> torch.Tensor:
