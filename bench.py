@@ -342,6 +342,59 @@ def extra_affine(tf, torch, steps=30):
     return out
 
 
+def attention_bytes(ctx, R, n_kv=8, group=8):
+    """Algorithmic bytes of one verify attention call over ctx cached positions:
+    K and V entries 0..ctx-1 (bf16), the bf16 queries and the fp32 outputs."""
+    n_q = n_kv * group
+    return ctx * n_kv * 128 * 2 * 2 + R * n_q * 128 * 2 + R * n_q * 128 * 4
+
+
+def extra_attention(tf, torch, steps=30, ctxs=(8192, 32768), rows=(1, 8, 16)):
+    """Verify attention over a KV cache (8 KV heads, group 8, head dim 128) at
+    8192 and 32768 cached positions, R = 1 / 8 / 16: partial + combine kernels,
+    caches rotating over copies larger than L2, CUDA-graph replay."""
+    n_kv, group = 8, 8
+    out = {}
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(11)
+    for ctx in ctxs:
+        cache_bytes = ctx * n_kv * 128 * 2 * 2
+        n_copies = max(3, -(-3 * L2_BYTES // cache_bytes))
+        caches = []
+        for _ in range(n_copies):
+            c = tf.KVCache(n_kv, ctx)
+            c.k.copy_((torch.randn(c.k.shape, device="cuda", generator=gen)).bfloat16().view(torch.int16))
+            c.v.copy_((torch.randn(c.v.shape, device="cuda", generator=gen)).bfloat16().view(torch.int16))
+            caches.append(c)
+        q = torch.randn((16, n_kv * group * 128), device="cuda", generator=gen).bfloat16().view(torch.int16)
+        y = torch.empty((16, n_kv * group * 128), device="cuda")
+        ws = tf.workspace(caches[0].workspace_bytes(group, 16))
+        for R in rows:
+            pos = torch.tensor([ctx - R], dtype=torch.int64, device="cuda")
+            for c in caches:
+                c.attention(q[:R], group, pos, out=y[:R], ws=ws)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for c in caches:
+                    c.attention(q[:R], group, pos, out=y[:R], ws=ws)
+            g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(steps):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / (steps * n_copies)
+            nbytes = attention_bytes(ctx, R, n_kv, group)
+            out[f"ctx{ctx}_R{R}"] = {"us_per_call": us, "gbs": nbytes / us / 1e3, "bytes_per_call": nbytes}
+        assert tf.workspace_status(ws) == tf.TF_DEV_OK
+        del caches
+        torch.cuda.empty_cache()
+    return out
+
+
 def extra_moe(tf, torch, steps=30):
     from w4_gemm_keyed_gb300 import inputs
     E, H, F, G, k = 128, 2048, 768, 32, 8
@@ -578,8 +631,10 @@ def main():
     ap.add_argument("--impl", default="tf", choices=["tf", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the LM-head / MoE / decoder side measurements")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--only", choices=["lmhead", "dense", "moe", "decoder", "affine"],
+    ap.add_argument("--only", choices=["lmhead", "dense", "moe", "decoder", "affine", "attention"],
                     help="run one workload briefly and print its timings (for profiler captures)")
+    ap.add_argument("--ctx", type=int, nargs="*", help="with --only attention: cached positions to time")
+    ap.add_argument("--rows", type=int, nargs="*", help="with --only attention: verify rows R to time")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -597,8 +652,14 @@ def main():
             secs, steps, lps = time_dense(tf, torch, mats, args.steps, args.warmup)
             out = {"dense_gbs": STEP_BYTES * steps / secs / 1e9}
         else:
-            fn = {"lmhead": extra_lmhead, "moe": extra_moe, "decoder": extra_decoder, "affine": extra_affine}[args.only]
-            out = fn(tf, torch, steps=args.steps)
+            fn = {"lmhead": extra_lmhead, "moe": extra_moe, "decoder": extra_decoder, "affine": extra_affine,
+                  "attention": extra_attention}[args.only]
+            kw = {}
+            if args.only == "attention" and args.ctx:
+                kw["ctxs"] = tuple(args.ctx)
+            if args.only == "attention" and args.rows:
+                kw["rows"] = tuple(args.rows)
+            out = fn(tf, torch, steps=args.steps, **kw)
         print(json.dumps({"only": args.only, "result": out}))
         return 0
     if world > 1:
@@ -645,7 +706,7 @@ def main():
     extra = {}
     if rank == 0 and not args.no_extra:
         for name, fn in (("lmhead_sampler", extra_lmhead), ("moe30b", extra_moe), ("decoder", extra_decoder),
-                         ("affine_5120x17408", extra_affine)):
+                         ("affine_5120x17408", extra_affine), ("attention_kv", extra_attention)):
             try:
                 extra[name] = fn(tf, torch)
             except Exception as exc:  # a side measurement must not hide the headline line

@@ -23,6 +23,7 @@
 
 #include "attention.cuh"
 #include "tf_ptx.cuh"
+#include "w4_gemm.cuh"
 
 namespace tfk {
 
@@ -48,31 +49,37 @@ __device__ __forceinline__ bool bad_position(long long pos0, int R, int max_len)
     return pos0 < 0 || pos0 + R > max_len;
 }
 
-// One CTA per (partition c, KV head j); warp w takes 16 query vectors
-// (query vector v = row * group + head-in-group).  Thread 0 also streams the
-// partition's K and V into a two-stage ring with bulk copies: it refills a
-// stage once every warp has released it.
+// Persistent CTAs over items (KV head j, partition c), j-major; each CTA takes
+// a contiguous run of items.  Warp w takes 16 query vectors (query vector
+// v = row * group + head-in-group).  Thread 0 also streams the items' 64-key
+// steps of K and V through a ring of kKvStages stages with bulk copies,
+// running ahead across item boundaries; it refills a stage once every warp
+// has released it.  Each item's state starts afresh, so its partial result is
+// the same whichever CTA computes it.
 __global__ void __launch_bounds__(32 * kAttnMaxGroup, 1) attn_partial_kernel(AttnArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     grid_dependency_wait();     // the cache entries and queries come from the preceding grids
     grid_launch_dependents();
     const long long pos0 = *a.pos;
     if (bad_position(pos0, a.R, a.max_len)) {
-        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) set_error(a.err, kDevBadPosition);
+        if (blockIdx.x == 0 && threadIdx.x == 0) set_error(a.err, kDevBadPosition);
         return;
     }
-    const int c = blockIdx.x, j = blockIdx.y;
     const long long p_max = pos0 + a.R - 1;
-    const long long t_begin = (long long)c * kKvPart;
-    if (t_begin > p_max) return;
-    const int n_sub = int(min((long long)(kKvPart / kKvSub), (p_max - t_begin) / kKvSub + 1));
+    const int n_parts = int(p_max / kKvPart) + 1;
+    const int n_items = n_parts * a.n_kv;
+    const int P = int(gridDim.x);
+    const int q_it = n_items / P, rem = n_items % P;
+    const int it_begin = int(blockIdx.x) * q_it + min(int(blockIdx.x), rem);
+    const int it_end = it_begin + q_it + (int(blockIdx.x) < rem ? 1 : 0);
+    if (it_begin >= it_end) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_cw = int(blockDim.x >> 5);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kKvStages * kStageBytes);
     uint64_t *empty = full + kKvStages;
 
     // V rows past the copied prefix of a step must hold finite values (their
-    // weight is 0, and 0 * finite = 0): zero both V halves once.
+    // weight is 0, and 0 * finite = 0): zero the V halves once.
     for (int i = threadIdx.x; i < kKvStages * kSubBytes / 16; i += blockDim.x) {
         const int st = i / (kSubBytes / 16), o = i % (kSubBytes / 16);
         reinterpret_cast<uint4 *>(smem + st * kStageBytes + kSubBytes)[o] = make_uint4(0u, 0u, 0u, 0u);
@@ -87,21 +94,29 @@ __global__ void __launch_bounds__(32 * kAttnMaxGroup, 1) attn_partial_kernel(Att
     fence_proxy_async_smem();   // the zero fill precedes the bulk copies into the same bytes
     __syncthreads();
 
-    const size_t head_off = ((size_t)j * a.max_len + (size_t)t_begin) * kHeadDim;
+    // steps of partition c: 64-key steps up to the last position any row needs
+    auto steps_of = [&](int c) { return int(min((long long)(kKvPart / kKvSub), (p_max - (long long)c * kKvPart) / kKvSub + 1)); };
+
+    // producer cursor (thread 0 only): next item / step to copy, steps issued
+    int p_it = it_begin, p_sub = 0, n_issued = 0;
     const uint64_t pol = l2_policy_evict_first();
-    // step i -> stage i % 2: the valid prefix (keys <= p_max) of 64 K rows and 64 V rows
-    auto issue = [&](int i) {
-        const int st = i % kKvStages;
-        const long long t0 = t_begin + (long long)i * kKvSub;
+    auto issue_next = [&]() {
+        const int j = p_it / n_parts, c = p_it % n_parts;
+        const int st = n_issued % kKvStages;
+        const long long t0 = (long long)c * kKvPart + (long long)p_sub * kKvSub;
         const uint32_t bytes = uint32_t(min((long long)kKvSub, p_max - t0 + 1)) * kRowBytes;
+        const size_t off = ((size_t)j * a.max_len + (size_t)t0) * kHeadDim;
         mbar_arrive_expect_tx(&full[st], 2 * bytes);
-        bulk_g2s_hint(smem + st * kStageBytes, a.k + head_off + (size_t)i * kKvSub * kHeadDim, bytes, &full[st],
-                      pol);
-        bulk_g2s_hint(smem + st * kStageBytes + kSubBytes, a.v + head_off + (size_t)i * kKvSub * kHeadDim, bytes,
-                      &full[st], pol);
+        bulk_g2s_hint(smem + st * kStageBytes, a.k + off, bytes, &full[st], pol);
+        bulk_g2s_hint(smem + st * kStageBytes + kSubBytes, a.v + off, bytes, &full[st], pol);
+        ++n_issued;
+        if (++p_sub == steps_of(c)) {
+            p_sub = 0;
+            ++p_it;
+        }
     };
     if (threadIdx.x == 0)
-        for (int i = 0; i < min(kKvStages, n_sub); ++i) issue(i);
+        for (int i = 0; i < kKvStages && p_it < it_end; ++i) issue_next();
 
     // ------------------------------------------------------------------ consumers
     const int gq = lane >> 2, tq = lane & 3;
@@ -109,178 +124,212 @@ __global__ void __launch_bounds__(32 * kAttnMaxGroup, 1) attn_partial_kernel(Att
     const int v0 = 16 * warp + gq, v1 = v0 + 8;
     const bool ok0 = v0 < nqv, ok1 = v1 < nqv;
     const int r0 = v0 / g, r1 = v1 / g;
-    const int h0 = j * g + v0 % g, h1 = j * g + v1 % g;
     // positions of the slot's two rows (-1: the slot holds no row)
     const long long p0 = ok0 ? pos0 + r0 : -1, p1 = ok1 ? pos0 + r1 : -1;
-
-    uint32_t qa[8][4];
-    {
-        const uint32_t *q0 = ok0 ? reinterpret_cast<const uint32_t *>(a.q + (size_t)r0 * a.ldq + h0 * kHeadDim)
-                                 : nullptr;
-        const uint32_t *q1 = ok1 ? reinterpret_cast<const uint32_t *>(a.q + (size_t)r1 * a.ldq + h1 * kHeadDim)
-                                 : nullptr;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            qa[ks][0] = ok0 ? q0[8 * ks + tq] : 0u;
-            qa[ks][1] = ok1 ? q1[8 * ks + tq] : 0u;
-            qa[ks][2] = ok0 ? q0[8 * ks + 4 + tq] : 0u;
-            qa[ks][3] = ok1 ? q1[8 * ks + 4 + tq] : 0u;
-        }
-    }
-
-    float o[16][4];
-#pragma unroll
-    for (int dn = 0; dn < 16; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     const uint32_t sbase = smem_u32(smem);
     const int sw = lane & 7;    // key & 7 of the rows this lane addresses (steps start at multiples of 8)
 
-    for (int i = 0; i < n_sub; ++i) {
-        const int st = i % kKvStages;
-        if (!mbar_wait(&full[st], (i / kKvStages) & 1)) {
-            set_error(a.err, kDevTimeout);
-            return;
+    uint32_t qa[8][4];
+    int q_head = -1;            // KV head whose queries qa holds
+    int s = 0;                  // steps consumed
+    for (int it = it_begin; it < it_end; ++it) {
+        const int j = it / n_parts, c = it % n_parts;
+        const int h0 = j * g + v0 % g, h1 = j * g + v1 % g;
+        if (j != q_head) {
+            q_head = j;
+            const uint32_t *q0 = ok0 ? reinterpret_cast<const uint32_t *>(a.q + (size_t)r0 * a.ldq + h0 * kHeadDim)
+                                     : nullptr;
+            const uint32_t *q1 = ok1 ? reinterpret_cast<const uint32_t *>(a.q + (size_t)r1 * a.ldq + h1 * kHeadDim)
+                                     : nullptr;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                qa[ks][0] = ok0 ? q0[8 * ks + tq] : 0u;
+                qa[ks][1] = ok1 ? q1[8 * ks + tq] : 0u;
+                qa[ks][2] = ok0 ? q0[8 * ks + 4 + tq] : 0u;
+                qa[ks][3] = ok1 ? q1[8 * ks + 4 + tq] : 0u;
+            }
         }
-        const uint32_t kaddr = sbase + st * kStageBytes, vaddr = kaddr + kSubBytes;
-        const long long t0 = t_begin + (long long)i * kKvSub;
-        const int lim0 = int(max(-1LL, min((long long)kKvSub, p0 - t0)));
-        const int lim1 = int(max(-1LL, min((long long)kKvSub, p1 - t0)));
+        const long long t_begin = (long long)c * kKvPart;
+        const int n_sub = steps_of(c);
 
-        // scores S[query][key] = q . k over 64 keys (8 n-tiles), fp32
-        float sc[8][4];
+        float o[16][4];
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-            const uint32_t row = kaddr + (nt * 8 + sw) * kRowBytes;
-#pragma unroll
-            for (int kp = 0; kp < 4; ++kp) {
-                const int chunk = 4 * kp + (lane >> 3);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(row + ((chunk ^ sw) << 4), b0, b1, b2, b3);
-                mma_bf16_16816(sc[nt], qa[2 * kp], b0, b1);
-                mma_bf16_16816(sc[nt], qa[2 * kp + 1], b2, b3);
-            }
-        }
-        // causal mask, then the step's row max (exact, any order)
-        float mt0 = -INFINITY, mt1 = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            const int kk = nt * 8 + 2 * tq;
-            sc[nt][0] = kk <= lim0 ? sc[nt][0] : -INFINITY;
-            sc[nt][1] = kk + 1 <= lim0 ? sc[nt][1] : -INFINITY;
-            sc[nt][2] = kk <= lim1 ? sc[nt][2] : -INFINITY;
-            sc[nt][3] = kk + 1 <= lim1 ? sc[nt][3] : -INFINITY;
-            mt0 = fmaxf(mt0, fmaxf(sc[nt][0], sc[nt][1]));
-            mt1 = fmaxf(mt1, fmaxf(sc[nt][2], sc[nt][3]));
-        }
-        mt0 = fmaxf(mt0, __shfl_xor_sync(0xFFFFFFFFu, mt0, 1));
-        mt0 = fmaxf(mt0, __shfl_xor_sync(0xFFFFFFFFu, mt0, 2));
-        mt1 = fmaxf(mt1, __shfl_xor_sync(0xFFFFFFFFu, mt1, 1));
-        mt1 = fmaxf(mt1, __shfl_xor_sync(0xFFFFFFFFu, mt1, 2));
-        const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);
-        // rescale of the running state: exactly 1 when the max did not move
-        const float al0 = mn0 == m0 ? 1.f : exp2f(__fmul_rn(__fsub_rn(m0, mn0), kScoreLog2));
-        const float al1 = mn1 == m1 ? 1.f : exp2f(__fmul_rn(__fsub_rn(m1, mn1), kScoreLog2));
-        m0 = mn0;
-        m1 = mn1;
-        const float mc0 = mn0 == -INFINITY ? 0.f : __fmul_rn(mn0, kScoreLog2);
-        const float mc1 = mn1 == -INFINITY ? 0.f : __fmul_rn(mn1, kScoreLog2);
-        float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            sc[nt][0] = exp2f(fmaf(sc[nt][0], kScoreLog2, -mc0));
-            sc[nt][1] = exp2f(fmaf(sc[nt][1], kScoreLog2, -mc0));
-            sc[nt][2] = exp2f(fmaf(sc[nt][2], kScoreLog2, -mc1));
-            sc[nt][3] = exp2f(fmaf(sc[nt][3], kScoreLog2, -mc1));
-            sum0 += sc[nt][0];
-            sum0 += sc[nt][1];
-            sum1 += sc[nt][2];
-            sum1 += sc[nt][3];
-        }
-        l0 = fmaf(l0, al0, sum0);
-        l1 = fmaf(l1, al1, sum1);
-#pragma unroll
-        for (int dn = 0; dn < 16; ++dn) {
-            o[dn][0] *= al0;
-            o[dn][1] *= al0;
-            o[dn][2] *= al1;
-            o[dn][3] *= al1;
-        }
-        // o += P.V, 16 keys per k step; P as bf16 hi + lo
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            uint32_t ah[4], alo[4];
-            split_bf16x2(sc[2 * kk][0], sc[2 * kk][1], ah[0], alo[0]);
-            split_bf16x2(sc[2 * kk][2], sc[2 * kk][3], ah[1], alo[1]);
-            split_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ah[2], alo[2]);
-            split_bf16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ah[3], alo[3]);
-            const int mi = lane >> 3;
-            const uint32_t row = vaddr + (16 * kk + ((mi & 1) << 3) + sw) * kRowBytes;
-#pragma unroll
-            for (int dp = 0; dp < 8; ++dp) {
-                const int chunk = 2 * dp + (mi >> 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(row + ((chunk ^ sw) << 4), b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * dp], ah, b0, b1);
-                mma_bf16_16816(o[2 * dp], alo, b0, b1);
-                mma_bf16_16816(o[2 * dp + 1], ah, b2, b3);
-                mma_bf16_16816(o[2 * dp + 1], alo, b2, b3);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-        if (threadIdx.x == 0 && i + kKvStages < n_sub) {
-            // every issued step is consumed by every warp before it exits, so no
-            // copy is left in flight; a refill that cannot start makes the
-            // warps' next full-barrier waits run out instead
-            if (mbar_wait(&empty[st], (i / kKvStages) & 1))
-                issue(i + kKvStages);
-            else
+        for (int dn = 0; dn < 16; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+        for (int i = 0; i < n_sub; ++i, ++s) {
+            const int st = s % kKvStages;
+            if (!mbar_wait(&full[st], (s / kKvStages) & 1)) {
                 set_error(a.err, kDevTimeout);
-        }
-    }
+                return;
+            }
+            const uint32_t kaddr = sbase + st * kStageBytes, vaddr = kaddr + kSubBytes;
+            const long long t0 = t_begin + (long long)i * kKvSub;
+            const int lim0 = int(max(-1LL, min((long long)kKvSub, p0 - t0)));
+            const int lim1 = int(max(-1LL, min((long long)kKvSub, p1 - t0)));
 
-    // weight sums over the quad (same order on all four lanes)
-    l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
-    l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
-    l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
-    l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
-    if (ok0 && t_begin <= p0) {
-        const size_t b = ((size_t)c * a.R + r0) * n_q + h0;
-        float *op = a.opart + b * kHeadDim + 2 * tq;
+            // scores S[query][key] = q . k over 64 keys (8 n-tiles), fp32
+            float sc[8][4];
 #pragma unroll
-        for (int dn = 0; dn < 16; ++dn) *reinterpret_cast<float2 *>(op + 8 * dn) = make_float2(o[dn][0], o[dn][1]);
-        if (tq == 0) *reinterpret_cast<float2 *>(a.ml + 2 * b) = make_float2(m0, l0);
-    }
-    if (ok1 && t_begin <= p1) {
-        const size_t b = ((size_t)c * a.R + r1) * n_q + h1;
-        float *op = a.opart + b * kHeadDim + 2 * tq;
+            for (int nt = 0; nt < 8; ++nt) {
+                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                const uint32_t row = kaddr + (nt * 8 + sw) * kRowBytes;
 #pragma unroll
-        for (int dn = 0; dn < 16; ++dn) *reinterpret_cast<float2 *>(op + 8 * dn) = make_float2(o[dn][2], o[dn][3]);
-        if (tq == 0) *reinterpret_cast<float2 *>(a.ml + 2 * b) = make_float2(m1, l1);
+                for (int kp = 0; kp < 4; ++kp) {
+                    const int chunk = 4 * kp + (lane >> 3);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(row + ((chunk ^ sw) << 4), b0, b1, b2, b3);
+                    mma_bf16_16816(sc[nt], qa[2 * kp], b0, b1);
+                    mma_bf16_16816(sc[nt], qa[2 * kp + 1], b2, b3);
+                }
+            }
+            // causal mask, then the step's row max (exact, any order)
+            float mt0 = -INFINITY, mt1 = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const int kk = nt * 8 + 2 * tq;
+                sc[nt][0] = kk <= lim0 ? sc[nt][0] : -INFINITY;
+                sc[nt][1] = kk + 1 <= lim0 ? sc[nt][1] : -INFINITY;
+                sc[nt][2] = kk <= lim1 ? sc[nt][2] : -INFINITY;
+                sc[nt][3] = kk + 1 <= lim1 ? sc[nt][3] : -INFINITY;
+                mt0 = fmaxf(mt0, fmaxf(sc[nt][0], sc[nt][1]));
+                mt1 = fmaxf(mt1, fmaxf(sc[nt][2], sc[nt][3]));
+            }
+            mt0 = fmaxf(mt0, __shfl_xor_sync(0xFFFFFFFFu, mt0, 1));
+            mt0 = fmaxf(mt0, __shfl_xor_sync(0xFFFFFFFFu, mt0, 2));
+            mt1 = fmaxf(mt1, __shfl_xor_sync(0xFFFFFFFFu, mt1, 1));
+            mt1 = fmaxf(mt1, __shfl_xor_sync(0xFFFFFFFFu, mt1, 2));
+            const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);
+            // rescale of the running state: exactly 1 when the max did not move
+            const float al0 = mn0 == m0 ? 1.f : exp2f(__fmul_rn(__fsub_rn(m0, mn0), kScoreLog2));
+            const float al1 = mn1 == m1 ? 1.f : exp2f(__fmul_rn(__fsub_rn(m1, mn1), kScoreLog2));
+            m0 = mn0;
+            m1 = mn1;
+            const float mc0 = mn0 == -INFINITY ? 0.f : __fmul_rn(mn0, kScoreLog2);
+            const float mc1 = mn1 == -INFINITY ? 0.f : __fmul_rn(mn1, kScoreLog2);
+            float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                sc[nt][0] = exp2f(fmaf(sc[nt][0], kScoreLog2, -mc0));
+                sc[nt][1] = exp2f(fmaf(sc[nt][1], kScoreLog2, -mc0));
+                sc[nt][2] = exp2f(fmaf(sc[nt][2], kScoreLog2, -mc1));
+                sc[nt][3] = exp2f(fmaf(sc[nt][3], kScoreLog2, -mc1));
+                sum0 += sc[nt][0];
+                sum0 += sc[nt][1];
+                sum1 += sc[nt][2];
+                sum1 += sc[nt][3];
+            }
+            l0 = fmaf(l0, al0, sum0);
+            l1 = fmaf(l1, al1, sum1);
+#pragma unroll
+            for (int dn = 0; dn < 16; ++dn) {
+                o[dn][0] *= al0;
+                o[dn][1] *= al0;
+                o[dn][2] *= al1;
+                o[dn][3] *= al1;
+            }
+            // o += P.V, 16 keys per k step; P as bf16 hi + lo
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                uint32_t ah[4], alo[4];
+                split_bf16x2(sc[2 * kk][0], sc[2 * kk][1], ah[0], alo[0]);
+                split_bf16x2(sc[2 * kk][2], sc[2 * kk][3], ah[1], alo[1]);
+                split_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ah[2], alo[2]);
+                split_bf16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ah[3], alo[3]);
+                const int mi = lane >> 3;
+                const uint32_t row = vaddr + (16 * kk + ((mi & 1) << 3) + sw) * kRowBytes;
+#pragma unroll
+                for (int dp = 0; dp < 8; ++dp) {
+                    const int chunk = 2 * dp + (mi >> 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_trans(row + ((chunk ^ sw) << 4), b0, b1, b2, b3);
+                    mma_bf16_16816(o[2 * dp], ah, b0, b1);
+                    mma_bf16_16816(o[2 * dp], alo, b0, b1);
+                    mma_bf16_16816(o[2 * dp + 1], ah, b2, b3);
+                    mma_bf16_16816(o[2 * dp + 1], alo, b2, b3);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+            if (threadIdx.x == 0 && p_it < it_end) {
+                // every issued step is consumed by every warp before it exits, so no
+                // copy is left in flight; a refill that cannot start makes the
+                // warps' next full-barrier waits run out instead
+                if (mbar_wait(&empty[st], (s / kKvStages) & 1))
+                    issue_next();
+                else
+                    set_error(a.err, kDevTimeout);
+            }
+        }
+
+        // weight sums over the quad (same order on all four lanes)
+        l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
+        l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
+        l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
+        l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
+        if (ok0 && t_begin <= p0) {
+            const size_t b = ((size_t)c * a.R + r0) * n_q + h0;
+            float *op = a.opart + b * kHeadDim + 2 * tq;
+#pragma unroll
+            for (int dn = 0; dn < 16; ++dn) *reinterpret_cast<float2 *>(op + 8 * dn) = make_float2(o[dn][0], o[dn][1]);
+            if (tq == 0) *reinterpret_cast<float2 *>(a.ml + 2 * b) = make_float2(m0, l0);
+        }
+        if (ok1 && t_begin <= p1) {
+            const size_t b = ((size_t)c * a.R + r1) * n_q + h1;
+            float *op = a.opart + b * kHeadDim + 2 * tq;
+#pragma unroll
+            for (int dn = 0; dn < 16; ++dn) *reinterpret_cast<float2 *>(op + 8 * dn) = make_float2(o[dn][2], o[dn][3]);
+            if (tq == 0) *reinterpret_cast<float2 *>(a.ml + 2 * b) = make_float2(m1, l1);
+        }
     }
 }
 
-// One CTA of 128 threads (one per output dimension) per (query head, row):
-// partitions 0..p/256 weighted against their common max, ascending.
+// One CTA of 128 threads per (query head, row): partitions 0..p/256 weighted
+// against their common max and summed in ascending order.  The weights of up to
+// 128 partitions at a time are formed in parallel (thread k: partition base + k)
+// and every thread runs the same ascending fmaf chains over them.
 __global__ void attn_combine_kernel(AttnArgs a) {
+    __shared__ float s_w[kHeadDim], s_l[kHeadDim], s_max[kHeadDim / 32];
     grid_dependency_wait();     // partials come from the preceding grid
     grid_launch_dependents();
     const long long pos0 = *a.pos;
     if (bad_position(pos0, a.R, a.max_len)) return;
     const int h = blockIdx.x, r = blockIdx.y, d = threadIdx.x;
     const int n_q = a.n_kv * a.group;
-    const int last = int((pos0 + r) / kKvPart);
+    const int n_c = int((pos0 + r) / kKvPart) + 1;
     const size_t stride = (size_t)a.R * n_q, base = (size_t)r * n_q + h;
     float M = -INFINITY;
-    for (int c = 0; c <= last; ++c) M = fmaxf(M, a.ml[2 * (c * stride + base)]);
+    for (int c = d; c < n_c; c += kHeadDim) M = fmaxf(M, a.ml[2 * (c * stride + base)]);
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    if ((d & 31) == 0) s_max[d >> 5] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
     float L = 0.f, O = 0.f;
-    for (int c = 0; c <= last; ++c) {
-        const size_t b = c * stride + base;
-        const float2 mlc = *reinterpret_cast<const float2 *>(a.ml + 2 * b);
-        const float w = exp2f(__fmul_rn(__fsub_rn(mlc.x, M), kScoreLog2));
-        L = fmaf(mlc.y, w, L);
-        O = fmaf(a.opart[b * kHeadDim + d], w, O);
+    for (int c0 = 0; c0 < n_c; c0 += kHeadDim) {
+        const int n = min(kHeadDim, n_c - c0);
+        __syncthreads();        // the previous chunk's weights are no longer read
+        if (d < n) {
+            const float2 mlc = *reinterpret_cast<const float2 *>(a.ml + 2 * ((c0 + d) * stride + base));
+            s_w[d] = exp2f(__fmul_rn(__fsub_rn(mlc.x, M), kScoreLog2));
+            s_l[d] = mlc.y;
+        }
+        __syncthreads();
+        const float *op = a.opart + (c0 * stride + base) * kHeadDim + d;
+        int k = 0;
+        for (; k + 8 <= n; k += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = op[(size_t)(k + u) * stride * kHeadDim];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                L = fmaf(s_l[k + u], s_w[k + u], L);
+                O = fmaf(v[u], s_w[k + u], O);
+            }
+        }
+        for (; k < n; ++k) {
+            L = fmaf(s_l[k], s_w[k], L);
+            O = fmaf(op[(size_t)k * stride * kHeadDim], s_w[k], O);
+        }
     }
     a.out[(size_t)r * a.ldo + h * kHeadDim + d] = __fdiv_rn(O, L);
 }
@@ -339,7 +388,10 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s) {
         if (dev >= 0 && dev < kMaxDevices) opted_in[dev] = true;
     }
     const int n_cw = (a.R * a.group + 15) / 16;
-    e = launch_pdl(attn_partial_kernel, dim3(a.max_len / kKvPart, a.n_kv), dim3(32 * n_cw), kAttnSmem, s, a);
+    const long long items_max = (long long)(a.max_len / kKvPart) * a.n_kv;
+    const long long per_sm = n_cw <= kAttnMaxGroup / 2 ? 2 : 1;   // CTAs resident per SM (shared memory, registers)
+    const int grid = int(min(items_max, per_sm * device_sm_count()));
+    e = launch_pdl(attn_partial_kernel, dim3(grid), dim3(32 * n_cw), kAttnSmem, s, a);
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_combine_kernel, dim3(a.n_kv * a.group, a.R), dim3(kHeadDim), 0, s, a);
 }
