@@ -10,8 +10,8 @@
 //     each partition into 4 steps of 64 keys; a row folds the steps of a
 //     partition in ascending order with an online softmax (running max m,
 //     weight sum l, unnormalised output o, all fp32);
-//   * the partitions 0..p/256 of a row are combined in ascending order
-//     against their common max;
+//   * the partitions 0..p/256 of a row are combined against their common
+//     max in an order fixed by p (four contiguous groups, each ascending);
 //   * steps past a row's position are exact no-ops for that row (scale 1,
 //     weights 0), so rows of one launch may run more steps than they need;
 //   * scores and P.V run on mma.sync with the queries as MMA rows; MMA rows
@@ -32,7 +32,7 @@ namespace {
 constexpr int kRowBytes = kHeadDim * 2;                 // 256 B per key
 constexpr int kSubBytes = kKvSub * kRowBytes;           // 16 KB of K (or V) per step
 constexpr int kStageBytes = 2 * kSubBytes;              // K then V
-constexpr size_t kAttnSmem = size_t(kKvStages) * kStageBytes + 2 * kKvStages * sizeof(uint64_t);
+constexpr size_t attn_smem(int ns) { return size_t(ns) * kStageBytes + 2 * ns * sizeof(uint64_t); }
 constexpr float kScoreLog2 = 0.12751743074439720f;      // log2(e) / sqrt(128)
 
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 b) { return *reinterpret_cast<uint32_t *>(&b); }
@@ -52,10 +52,11 @@ __device__ __forceinline__ bool bad_position(long long pos0, int R, int max_len)
 // Persistent CTAs over items (KV head j, partition c), j-major; each CTA takes
 // a contiguous run of items.  Warp w takes 16 query vectors (query vector
 // v = row * group + head-in-group).  Thread 0 also streams the items' 64-key
-// steps of K and V through a ring of kKvStages stages with bulk copies,
-// running ahead across item boundaries; it refills a stage once every warp
-// has released it.  Each item's state starts afresh, so its partial result is
-// the same whichever CTA computes it.
+// steps of K and V through a ring of NS stages with bulk copies (NS = 2 where
+// three CTAs share an SM, else 3), running ahead across item boundaries; it
+// refills a stage once every warp has released it.  Each item's state starts
+// afresh, so its partial result is the same whichever CTA computes it.
+template <int NS>
 __global__ void __launch_bounds__(32 * kAttnMaxGroup, 1) attn_partial_kernel(AttnArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     grid_dependency_wait();     // the cache entries and queries come from the preceding grids
@@ -75,17 +76,17 @@ __global__ void __launch_bounds__(32 * kAttnMaxGroup, 1) attn_partial_kernel(Att
     if (it_begin >= it_end) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_cw = int(blockDim.x >> 5);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kKvStages * kStageBytes);
-    uint64_t *empty = full + kKvStages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * kStageBytes);
+    uint64_t *empty = full + NS;
 
     // V rows past the copied prefix of a step must hold finite values (their
     // weight is 0, and 0 * finite = 0): zero the V halves once.
-    for (int i = threadIdx.x; i < kKvStages * kSubBytes / 16; i += blockDim.x) {
+    for (int i = threadIdx.x; i < NS * kSubBytes / 16; i += blockDim.x) {
         const int st = i / (kSubBytes / 16), o = i % (kSubBytes / 16);
         reinterpret_cast<uint4 *>(smem + st * kStageBytes + kSubBytes)[o] = make_uint4(0u, 0u, 0u, 0u);
     }
     if (threadIdx.x == 0) {
-        for (int st = 0; st < kKvStages; ++st) {
+        for (int st = 0; st < NS; ++st) {
             mbar_init(&full[st], 1);
             mbar_init(&empty[st], n_cw);
         }
@@ -102,7 +103,7 @@ __global__ void __launch_bounds__(32 * kAttnMaxGroup, 1) attn_partial_kernel(Att
     const uint64_t pol = l2_policy_evict_first();
     auto issue_next = [&]() {
         const int j = p_it / n_parts, c = p_it % n_parts;
-        const int st = n_issued % kKvStages;
+        const int st = n_issued % NS;
         const long long t0 = (long long)c * kKvPart + (long long)p_sub * kKvSub;
         const uint32_t bytes = uint32_t(min((long long)kKvSub, p_max - t0 + 1)) * kRowBytes;
         const size_t off = ((size_t)j * a.max_len + (size_t)t0) * kHeadDim;
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(32 * kAttnMaxGroup, 1) attn_partial_kernel(Att
         }
     };
     if (threadIdx.x == 0)
-        for (int i = 0; i < kKvStages && p_it < it_end; ++i) issue_next();
+        for (int i = 0; i < NS && p_it < it_end; ++i) issue_next();
 
     // ------------------------------------------------------------------ consumers
     const int gq = lane >> 2, tq = lane & 3;
@@ -158,8 +159,8 @@ __global__ void __launch_bounds__(32 * kAttnMaxGroup, 1) attn_partial_kernel(Att
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
         for (int i = 0; i < n_sub; ++i, ++s) {
-            const int st = s % kKvStages;
-            if (!mbar_wait(&full[st], (s / kKvStages) & 1)) {
+            const int st = s % NS;
+            if (!mbar_wait(&full[st], (s / NS) & 1)) {
                 set_error(a.err, kDevTimeout);
                 return;
             }
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(32 * kAttnMaxGroup, 1) attn_partial_kernel(Att
                 // every issued step is consumed by every warp before it exits, so no
                 // copy is left in flight; a refill that cannot start makes the
                 // warps' next full-barrier waits run out instead
-                if (mbar_wait(&empty[st], (s / kKvStages) & 1))
+                if (mbar_wait(&empty[st], (s / NS) & 1))
                     issue_next();
                 else
                     set_error(a.err, kDevTimeout);
@@ -284,54 +285,75 @@ __global__ void __launch_bounds__(32 * kAttnMaxGroup, 1) attn_partial_kernel(Att
     }
 }
 
-// One CTA of 128 threads per (query head, row): partitions 0..p/256 weighted
-// against their common max and summed in ascending order.  The weights of up to
-// 128 partitions at a time are formed in parallel (thread k: partition base + k)
-// and every thread runs the same ascending fmaf chains over them.
-__global__ void attn_combine_kernel(AttnArgs a) {
-    __shared__ float s_w[kHeadDim], s_l[kHeadDim], s_max[kHeadDim / 32];
+// One CTA per (query head, row): the row's partitions 0..n_c-1 (n_c = p/256 + 1)
+// weighted against their common max.  Four groups of 128 threads (one per
+// output dimension) each sum a contiguous quarter of every chunk of up to 512
+// partitions in ascending order; the group sums are then added in group
+// order.  The grouping is a function of n_c alone, i.e. of the row's position.
+constexpr int kCombThreads = 512;
+constexpr int kCombGroups = kCombThreads / kHeadDim;
+constexpr int kCombUnroll = 16;
+
+__global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a) {
+    __shared__ float s_w[kCombThreads], s_l[kCombThreads], s_red[kCombThreads / 32];
+    __shared__ float s_o[kCombGroups][kHeadDim], s_lg[kCombGroups];
     grid_dependency_wait();     // partials come from the preceding grid
     grid_launch_dependents();
     const long long pos0 = *a.pos;
     if (bad_position(pos0, a.R, a.max_len)) return;
-    const int h = blockIdx.x, r = blockIdx.y, d = threadIdx.x;
+    const int h = blockIdx.x, r = blockIdx.y, tid = threadIdx.x, d = tid % kHeadDim, grp = tid / kHeadDim;
     const int n_q = a.n_kv * a.group;
     const int n_c = int((pos0 + r) / kKvPart) + 1;
     const size_t stride = (size_t)a.R * n_q, base = (size_t)r * n_q + h;
     float M = -INFINITY;
-    for (int c = d; c < n_c; c += kHeadDim) M = fmaxf(M, a.ml[2 * (c * stride + base)]);
+    for (int c = tid; c < n_c; c += kCombThreads) M = fmaxf(M, a.ml[2 * (c * stride + base)]);
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-    if ((d & 31) == 0) s_max[d >> 5] = M;
+    if ((tid & 31) == 0) s_red[tid >> 5] = M;
     __syncthreads();
-    M = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
+    M = s_red[0];
+    for (int w = 1; w < kCombThreads / 32; ++w) M = fmaxf(M, s_red[w]);
     float L = 0.f, O = 0.f;
-    for (int c0 = 0; c0 < n_c; c0 += kHeadDim) {
-        const int n = min(kHeadDim, n_c - c0);
+    for (int c0 = 0; c0 < n_c; c0 += kCombThreads) {
+        const int n = min(kCombThreads, n_c - c0);
         __syncthreads();        // the previous chunk's weights are no longer read
-        if (d < n) {
-            const float2 mlc = *reinterpret_cast<const float2 *>(a.ml + 2 * ((c0 + d) * stride + base));
-            s_w[d] = exp2f(__fmul_rn(__fsub_rn(mlc.x, M), kScoreLog2));
-            s_l[d] = mlc.y;
+        if (tid < n) {
+            const float2 mlc = *reinterpret_cast<const float2 *>(a.ml + 2 * ((c0 + tid) * stride + base));
+            s_w[tid] = exp2f(__fmul_rn(__fsub_rn(mlc.x, M), kScoreLog2));
+            s_l[tid] = mlc.y;
         }
         __syncthreads();
-        const float *op = a.opart + (c0 * stride + base) * kHeadDim + d;
-        int k = 0;
-        for (; k + 8 <= n; k += 8) {
-            float v[8];
+        const int qn = n / kCombGroups, rn = n % kCombGroups;
+        const int k0 = grp * qn + min(grp, rn), k1 = k0 + qn + (grp < rn ? 1 : 0);
+        const size_t step = stride * kHeadDim;
+        const float *op = a.opart + ((c0 + k0) * stride + base) * kHeadDim + d;
+        int k = k0;
+        for (; k + kCombUnroll <= k1; k += kCombUnroll, op += kCombUnroll * step) {
+            float v[kCombUnroll];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = op[(size_t)(k + u) * stride * kHeadDim];
+            for (int u = 0; u < kCombUnroll; ++u) v[u] = op[u * step];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < kCombUnroll; ++u) {
                 L = fmaf(s_l[k + u], s_w[k + u], L);
                 O = fmaf(v[u], s_w[k + u], O);
             }
         }
-        for (; k < n; ++k) {
+        for (; k < k1; ++k, op += step) {
             L = fmaf(s_l[k], s_w[k], L);
-            O = fmaf(op[(size_t)k * stride * kHeadDim], s_w[k], O);
+            O = fmaf(*op, s_w[k], O);
         }
     }
-    a.out[(size_t)r * a.ldo + h * kHeadDim + d] = __fdiv_rn(O, L);
+    s_o[grp][d] = O;
+    if (d == 0) s_lg[grp] = L;
+    __syncthreads();
+    if (grp == 0) {
+        float Ot = s_o[0][d], Lt = s_lg[0];
+#pragma unroll
+        for (int g2 = 1; g2 < kCombGroups; ++g2) {
+            Ot += s_o[g2][d];
+            Lt += s_lg[g2];
+        }
+        a.out[(size_t)r * a.ldo + h * kHeadDim + d] = __fdiv_rn(Ot, Lt);
+    }
 }
 
 // 8 (row, KV head) items per CTA, one warp each: 16 lanes copy the K row and
@@ -383,17 +405,25 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices || !opted_in[dev]) {
-        e = cudaFuncSetAttribute(attn_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kAttnSmem));
+        e = cudaFuncSetAttribute(attn_partial_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(attn_smem(2)));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_partial_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     int(attn_smem(3)));
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDevices) opted_in[dev] = true;
     }
+    // CTAs resident per SM: three with a 2-stage ring (64 KB) for up to two warps,
+    // else two (3-stage ring, 96 KB) up to four warps, else one (registers)
     const int n_cw = (a.R * a.group + 15) / 16;
+    const int per_sm = n_cw <= 2 ? 3 : (n_cw <= kAttnMaxGroup / 2 ? 2 : 1);
     const long long items_max = (long long)(a.max_len / kKvPart) * a.n_kv;
-    const long long per_sm = n_cw <= kAttnMaxGroup / 2 ? 2 : 1;   // CTAs resident per SM (shared memory, registers)
-    const int grid = int(min(items_max, per_sm * device_sm_count()));
-    e = launch_pdl(attn_partial_kernel, dim3(grid), dim3(32 * n_cw), kAttnSmem, s, a);
+    const int grid = int(min(items_max, (long long)per_sm * device_sm_count()));
+    if (n_cw <= 2)
+        e = launch_pdl(attn_partial_kernel<2>, dim3(grid), dim3(32 * n_cw), attn_smem(2), s, a);
+    else
+        e = launch_pdl(attn_partial_kernel<3>, dim3(grid), dim3(32 * n_cw), attn_smem(3), s, a);
     if (e != cudaSuccess) return e;
-    return launch_pdl(attn_combine_kernel, dim3(a.n_kv * a.group, a.R), dim3(kHeadDim), 0, s, a);
+    return launch_pdl(attn_combine_kernel, dim3(a.n_kv * a.group, a.R), dim3(kCombThreads), 0, s, a);
 }
 
 }  // namespace tfk

@@ -9,7 +9,6 @@ namespace tfk {
 constexpr int kHeadDim = 128;
 constexpr int kKvPart = 256;     // keys per partition: a fixed grid of absolute positions
 constexpr int kKvSub = 64;       // keys per pipeline stage
-constexpr int kKvStages = 3;
 constexpr int kAttnMaxGroup = 8;
 constexpr int kDevTimeout = 1;        // device status: a bounded wait ran out
 constexpr int kDevBadPosition = 4;    // device status: *pos < 0 or *pos + R > max_len
