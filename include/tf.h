@@ -395,6 +395,33 @@ TF_API size_t tf_decoder_block_workspace_bytes(const tf_model *m);
 TF_API tf_status tf_decoder_block(const tf_model *m, int32_t block, float *x, int32_t R, uint16_t *n_out,
                                   uint16_t *h_out, void *ws, size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Self-check and generic workspace query.
+ * ------------------------------------------------------------------------
+ * tf_selfcheck_row_invariance: the row-invariance guarantee (README, the two
+ *   guarantees: each row of a verify pass comes out as it would alone), checked
+ *   on the caller's matrix and rows.  Runs tf_lane_gemm_w4 on x[0..R-1] for every
+ *   R in 1..16 and compares every row's output bytes with the one-row launch of
+ *   that row.  x: dev bf16 [16][ldx]; scratch: dev, 256-B aligned, at least
+ *   tf_selfcheck_scratch_bytes(W->N) bytes; ws: as for tf_lane_gemm_w4.
+ *   Synchronises `stream`.  *result (host) = 0 when every row matched, else
+ *   R * 256 + row of the first mismatch (smallest R, then smallest row).
+ * tf_workspace_size: the workspace bytes of one operation by code, for callers
+ *   that size buffers generically: TF_OP_LANE_GEMM dims {K, N, group},
+ *   TF_OP_KEYED_SAMPLE dims {R, V}, TF_OP_ATTENTION dims {n_kv, max_len, group, R}.
+ *   0 for an unknown code, a wrong dims count or unsupported dims.  The MoE layer
+ *   and the decoder step take their descriptors: tf_moe_workspace_bytes,
+ *   tf_verify_step_workspace_bytes.
+ */
+#define TF_OP_LANE_GEMM 1
+#define TF_OP_KEYED_SAMPLE 2
+#define TF_OP_ATTENTION 3
+TF_API size_t tf_selfcheck_scratch_bytes(int32_t N);
+TF_API tf_status tf_selfcheck_row_invariance(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, void *scratch,
+                                             size_t scratch_bytes, void *ws, size_t ws_bytes, void *stream,
+                                             int32_t *result);
+TF_API size_t tf_workspace_size(int32_t op, const int64_t *dims, int32_t n_dims);
+
 /* Number of SMs the split-K decomposition is sized for on the current device. */
 TF_API int32_t tf_device_sm_count(void);
 

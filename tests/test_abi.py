@@ -125,6 +125,30 @@ def test_kv_cache_validation_rejects_bad_arguments(lib):
     assert lib.tf_kv_append(ctypes.byref(C), 256, 256, 1024, 1, 256, 256, 128, None) == tf.TF_ERR_WORKSPACE
 
 
+def test_generic_workspace_size_and_selfcheck_validation(lib):
+    from w4_gemm_keyed_gb300 import tf
+    assert tf.workspace_size(tf.TF_OP_LANE_GEMM, [5120, 17408, 64]) == tf.lane_gemm_workspace_bytes(5120, 17408, 64)
+    assert tf.workspace_size(tf.TF_OP_KEYED_SAMPLE, [16, 151936]) == \
+        int(lib.tf_keyed_sample_workspace_bytes(16, 151936))
+    C = tf.KVCacheC(256, 512, 8, 4096)
+    assert tf.workspace_size(tf.TF_OP_ATTENTION, [8, 4096, 8, 16]) == \
+        lib.tf_attention_workspace_bytes(ctypes.byref(C), 8, 16)
+    assert tf.workspace_size(99, [1, 2, 3]) == 0
+    assert tf.workspace_size(tf.TF_OP_LANE_GEMM, [5120, 17408]) == 0
+    assert tf.workspace_size(tf.TF_OP_LANE_GEMM, [5120, -1, 64]) == 0
+    assert lib.tf_selfcheck_scratch_bytes(1000) == 256 + 2 * 16 * 1024 * 4
+    assert lib.tf_selfcheck_scratch_bytes(0) == 0
+    W = tf.W4MatrixC(256, 256, 64, 64, 0)
+    res = tf.I32(7)
+    assert lib.tf_selfcheck_row_invariance(ctypes.byref(W), 256, 256, 256, 1 << 30, 256, 1 << 30, None, None) == \
+        tf.TF_ERR_INVALID_ARG                                                  # null result
+    assert lib.tf_selfcheck_row_invariance(ctypes.byref(W), 256, 256, 256, 100, 256, 1 << 30, None,
+                                           ctypes.byref(res)) == tf.TF_ERR_INVALID_ARG   # scratch too small
+    assert lib.tf_selfcheck_row_invariance(ctypes.byref(W), 256, 256, 264, 1 << 30, 256, 1 << 30, None,
+                                           ctypes.byref(res)) == tf.TF_ERR_INVALID_ARG   # scratch misaligned
+    assert res.value == 7
+
+
 def _start(p, q, rem):
     return p * q + min(p, rem)
 

@@ -121,3 +121,14 @@ def test_whole_tile_ranges_match_oracle_and_are_row_invariant(tf, m):
     assert_close_rows(y16[:3], oracle.w4_linear(codes, scales, x[:3], G))
     y1 = run(tf, W, x[:1])
     assert np.array_equal(y1.view(np.uint32), y16[:1].view(np.uint32))
+
+
+def test_selfcheck_row_invariance_entry_point(tf):
+    """The library's own row-invariance self-check passes on the 5120 -> 17408
+    projection (group 64) and on a ragged 777-feature matrix (group 32)."""
+    for K, N, G in ((5120, 17408, 64), (2048, 777, 32)):
+        rng = inputs.rng_for(77, K, N)
+        codes, scales = inputs.w4_weights(rng, K, N, G)
+        W = pack(tf, codes, scales, G)
+        x = dev_bits16(inputs.bf16_normal(rng, (16, K)))
+        assert tf.selfcheck_row_invariance(W, x) == 0

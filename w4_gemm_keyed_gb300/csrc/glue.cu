@@ -188,7 +188,26 @@ __global__ void commit_tokens_kernel(const int32_t *tokens, const int32_t *accep
     }
 }
 
+// *first = min(*first, code_base + r) for every row r whose bytes differ
+// between a and b (grid-stride over R x N).
+__global__ void rows_differ_kernel(const float *a, const float *b, int R, int N, int ld, int code_base, int *first) {
+    grid_dependency_wait();     // both outputs come from preceding grids
+    grid_launch_dependents();
+    const long long total = (long long)R * N;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int r = int(i / N), n = int(i % N);
+        if (__float_as_uint(a[(long long)r * ld + n]) != __float_as_uint(b[(long long)r * ld + n]))
+            atomicMin(first, code_base + r);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_rows_differ(const float *a, const float *b, int R, int N, int ld, int code_base, int *first,
+                               cudaStream_t s) {
+    return launch_pdl(rows_differ_kernel, dim3(256), dim3(256), 0, s, a, b, R, N, ld, code_base, first);
+}
 
 cudaError_t launch_gather_drafts(const int32_t *table, long long table_len, const int64_t *pos, int n,
                                  int32_t *drafts, cudaStream_t s) {

@@ -25,6 +25,10 @@ cudaError_t launch_commit_tokens(const int32_t *tokens, const int32_t *accepted,
 cudaError_t launch_combine(const float *Y, const int32_t *slot_of, const float *w, int R, int H, int top_k,
                            float *out, cudaStream_t s);
 
+// *first = min(*first, code_base + r) over rows r < R whose N fp32 values differ in any bit.
+cudaError_t launch_rows_differ(const float *a, const float *b, int R, int N, int ld, int code_base, int *first,
+                               cudaStream_t s);
+
 // x[r][:] = emb[token_r][:] (bf16 -> fp32); token_0 = *last_token, token_r = drafts[r-1].
 cudaError_t launch_embed(const uint16_t *emb, int V, int H, const int32_t *last_token, const int32_t *drafts,
                          int R, float *x, int *err, cudaStream_t s);

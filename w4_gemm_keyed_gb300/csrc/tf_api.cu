@@ -361,6 +361,70 @@ tf_status tf_lane_gemm_w4(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx,
     return ok();
 }
 
+// ---- tf_selfcheck_row_invariance / tf_workspace_size ----
+namespace {
+size_t selfcheck_ld(int N) { return (size_t(N) + 63) / 64 * 64; }
+}  // namespace
+
+size_t tf_selfcheck_scratch_bytes(int32_t N) {
+    if (N <= 0) return 0;
+    return 256 + 2 * size_t(TF_MAX_ROWS) * selfcheck_ld(N) * sizeof(float);
+}
+
+tf_status tf_selfcheck_row_invariance(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, void *scratch,
+                                      size_t scratch_bytes, void *ws, size_t ws_bytes, void *stream,
+                                      int32_t *result) {
+    if (!result) return fail(TF_ERR_INVALID_ARG, "null result");
+    tf_status st = check_matrix(W, "W");
+    if (st) return st;
+    if (!scratch || !aligned(scratch, 256) || scratch_bytes < tf_selfcheck_scratch_bytes(W->N))
+        return fail(TF_ERR_INVALID_ARG, "scratch must be 256-B aligned and >= %zu bytes",
+                    tf_selfcheck_scratch_bytes(W->N));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int ld = int(selfcheck_ld(W->N));
+    int *flag = static_cast<int *>(scratch);
+    float *single = reinterpret_cast<float *>(static_cast<char *>(scratch) + 256);
+    float *multi = single + size_t(TF_MAX_ROWS) * ld;
+    constexpr int kNone = 0x7F7F7F7F;
+    cudaError_t e = cudaMemsetAsync(flag, 0x7F, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "tf_selfcheck_row_invariance");
+    for (int r = 0; r < TF_MAX_ROWS; ++r)
+        if ((st = tf_lane_gemm_w4(W, x + size_t(r) * ldx, ldx, 1, single + size_t(r) * ld, ld, ws, ws_bytes, stream)))
+            return st;
+    for (int R = 1; R <= TF_MAX_ROWS; ++R) {
+        if ((st = tf_lane_gemm_w4(W, x, ldx, R, multi, ld, ws, ws_bytes, stream))) return st;
+        if ((e = launch_rows_differ(multi, single, R, W->N, ld, R * 256, flag, s)) != cudaSuccess)
+            return cuda_fail(e, "tf_selfcheck_row_invariance");
+    }
+    int v = 0;
+    if ((e = cudaMemcpyAsync(&v, flag, sizeof v, cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(s)) != cudaSuccess)
+        return cuda_fail(e, "tf_selfcheck_row_invariance");
+    *result = v == kNone ? 0 : v;
+    return ok();
+}
+
+size_t tf_workspace_size(int32_t op, const int64_t *dims, int32_t n_dims) {
+    if (!dims) return 0;
+    for (int i = 0; i < n_dims; ++i)
+        if (dims[i] <= 0 || dims[i] > 0x7FFFFFFF) return 0;
+    switch (op) {
+    case TF_OP_LANE_GEMM:
+        return n_dims == 3 ? tf_lane_gemm_workspace_bytes(int32_t(dims[0]), int32_t(dims[1]), int32_t(dims[2])) : 0;
+    case TF_OP_KEYED_SAMPLE:
+        return n_dims == 2 ? tf_keyed_sample_workspace_bytes(int32_t(dims[0]), int32_t(dims[1])) : 0;
+    case TF_OP_ATTENTION: {
+        if (n_dims != 4) return 0;
+        tf_kv_cache c{};
+        c.n_kv = int32_t(dims[0]);
+        c.max_len = int32_t(dims[1]);
+        return tf_attention_workspace_bytes(&c, int32_t(dims[2]), int32_t(dims[3]));
+    }
+    default:
+        return 0;
+    }
+}
+
 // ---- tf_lane_gemm_w4_noalloc: the lane GEMM on library-owned scratch ----
 // The split-K status word, counters and partial tiles live in one fixed array
 // of this module instead of a caller workspace.  Each device has its own copy

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libtf.so")
 TF_OK, TF_ERR_INVALID_ARG, TF_ERR_UNSUPPORTED, TF_ERR_CUDA, TF_ERR_TIMEOUT, TF_ERR_WORKSPACE = range(6)
 TF_DEV_OK, TF_DEV_TIMEOUT, TF_DEV_NONFINITE_LOGIT, TF_DEV_BAD_TOKEN, TF_DEV_BAD_POSITION = range(5)
 HEAD_DIM = 128
+TF_OP_LANE_GEMM, TF_OP_KEYED_SAMPLE, TF_OP_ATTENTION = 1, 2, 3
 MAX_ROWS = 16
 MAX_TOP_K = 64
 
@@ -79,6 +80,10 @@ SIGNATURES = [
     ("tf_kv_append", ctypes.c_int, [ctypes.POINTER(KVCacheC), P, P, I32, I32, P, P, SZ, P]),
     ("tf_attention_workspace_bytes", SZ, [ctypes.POINTER(KVCacheC), I32, I32]),
     ("tf_attention_verify", ctypes.c_int, [ctypes.POINTER(KVCacheC), I32, P, I32, I32, P, P, I32, P, SZ, P]),
+    ("tf_selfcheck_scratch_bytes", SZ, [I32]),
+    ("tf_selfcheck_row_invariance", ctypes.c_int, [ctypes.POINTER(W4MatrixC), P, I32, P, SZ, P, SZ, P,
+                                                   ctypes.POINTER(I32)]),
+    ("tf_workspace_size", SZ, [I32, ctypes.POINTER(ctypes.c_int64), I32]),
     ("tf_moe_workspace_bytes", SZ, [ctypes.POINTER(MoeLayerC), I32]),
     ("tf_moe_w4", ctypes.c_int, [ctypes.POINTER(MoeLayerC), P, P, I32, P, P, SZ, P]),
     ("tf_verify_step_workspace_bytes", SZ, [ctypes.POINTER(ModelC), I32]),
@@ -279,6 +284,23 @@ def commit_tokens(tokens: torch.Tensor, accepted: torch.Tensor, pos: torch.Tenso
     _check(load().tf_commit_tokens(_ptr(tokens), _ptr(accepted), _ptr(pos), _ptr(log), log.numel(),
                                    _stream(stream)))
     return log
+
+
+def selfcheck_row_invariance(W: W4Matrix, x: torch.Tensor, stream=None) -> int:
+    """0 if every row of every R in 1..16 matches its one-row launch bit for bit,
+    else R * 256 + row of the first mismatch.  x: bf16 [16][K] on the device."""
+    lib = load()
+    scratch = workspace(int(lib.tf_selfcheck_scratch_bytes(W.N)), device=x.device)
+    ws = workspace(lane_gemm_workspace_bytes(W.K, W.N, W.group), device=x.device)
+    res = I32(-1)
+    _check(lib.tf_selfcheck_row_invariance(ctypes.byref(W.c()), _ptr(x), x.stride(0), _ptr(scratch), scratch.numel(),
+                                           _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(res)))
+    return int(res.value)
+
+
+def workspace_size(op: int, dims) -> int:
+    arr = (ctypes.c_int64 * len(dims))(*[int(d) for d in dims])
+    return int(load().tf_workspace_size(op, arr, len(dims)))
 
 
 # ---------------------------------------------------------------- KV cache attention
