@@ -212,8 +212,12 @@ def time_dense_e2e(tf, torch, mats, steps, warmup):
     """Same step through the C ABI with host buffers.  Every step copies all of
     its inputs host->device in one pinned copy, runs the ten launches on slices
     of the device buffers (leading dimensions through the ABI) and reads all
-    outputs back device->host in one copy."""
-    stream = torch.cuda.current_stream()
+    outputs back device->host in one copy.  Two buffer sets alternate: the
+    host->device copy of step i + 1 and the device->host copy of step i - 1 run
+    on their own streams while step i computes (events order each buffer's
+    reuse); the timed region ends when the last step's outputs are on the host."""
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
     launches = dense_launches()
     x_off, y_off, xo, yo = [], [], 0, 0
     for K, N, R in launches:
@@ -224,32 +228,56 @@ def time_dense_e2e(tf, torch, mats, steps, warmup):
     hx = torch.empty(xo, dtype=torch.int16).pin_memory()
     for (K, N, R), o in zip(launches, x_off):
         hx[o:o + R * K] = torch.from_numpy(mats[(K, N)]["x_host"][:R].reshape(-1).view(np.int16))
-    hy = torch.empty(yo, dtype=torch.float32).pin_memory()
-    dx = torch.empty(xo, dtype=torch.int16, device="cuda")
-    dy = torch.empty(yo, dtype=torch.float32, device="cuda")
+    hy = [torch.empty(yo, dtype=torch.float32).pin_memory() for _ in range(2)]
+    dx = [torch.empty(xo, dtype=torch.int16, device="cuda") for _ in range(2)]
+    dy = [torch.empty(yo, dtype=torch.float32, device="cuda") for _ in range(2)]
     h2d, d2h = xo * 2, yo * 4
-    # per launch: the weight copies it rotates over and its slices of the device buffers
-    plan = [(mats[(K, N)]["copies"], dx[xo_:xo_ + R * K].view(R, K), dy[yo_:yo_ + R * N].view(R, N), mats[(K, N)]["ws"])
-            for (K, N, R), xo_, yo_ in zip(launches, x_off, y_off)]
+    # per buffer set and launch: the weight copies it rotates over and its slices of the device buffers
+    plans = [[(mats[(K, N)]["copies"], dx[b][xo_:xo_ + R * K].view(R, K), dy[b][yo_:yo_ + R * N].view(R, N),
+               mats[(K, N)]["ws"]) for (K, N, R), xo_, yo_ in zip(launches, x_off, y_off)] for b in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of the set are on the device
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # outputs of the set are computed
+    ev_back = [torch.cuda.Event() for _ in range(2)]    # outputs of the set are on the host
     counter = [0]
 
     def step():
-        dx.copy_(hx, non_blocking=True)
-        c = counter[0]
+        i = counter[0]
         counter[0] += 1
-        for copies, xv, yv, ws in plan:
-            tf.lane_gemm_w4(copies[c % len(copies)], xv, y=yv, ws=ws)
-        hy.copy_(dy, non_blocking=True)
+        b = i % 2
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(ev_out[b])                # step i - 2 has finished reading dx[b]
+            dx[b].copy_(hx, non_blocking=True)
+            ev_in[b].record(up)
+        comp.wait_event(ev_in[b])
+        if i >= 2:
+            comp.wait_event(ev_back[b])                 # step i - 2's outputs have left dy[b]
+        for copies, xv, yv, ws in plans[b]:
+            tf.lane_gemm_w4(copies[i % len(copies)], xv, y=yv, ws=ws)
+        ev_out[b].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_out[b])
+            hy[b].copy_(dy[b], non_blocking=True)
+            ev_back[b].record(down)
+
+    def drain():
+        for b in range(2):
+            if counter[0] > b:
+                comp.wait_event(ev_back[(counter[0] - 1 - b) % 2])
 
     for _ in range(warmup):
         step()
+    drain()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
+    t0.record(comp)
+    up.wait_event(t0)
+    down.wait_event(t0)
     for _ in range(steps):
         step()
-    t1.record(stream)
+    drain()
+    t1.record(comp)
     torch.cuda.synchronize()
     return t0.elapsed_time(t1) / 1e3, h2d, d2h
 
