@@ -681,6 +681,7 @@ tf_status tf_moe_w4(const tf_moe_layer *L, const uint16_t *x, const float *route
     g2.w_stride = (long long)packed_bytes(L->ffn, L->hidden, L->group);
     g2.expert_ids = expert_ids;
     g2.n_problems = nprob;
+    g2.list_ready = 1;   // routed by the grid before gate/up, which has passed its own wait
     g2.y_stride = (long long)R * L->hidden;
     e = bind_and_launch(g2, h, L->ffn, (long long)R * L->ffn, m.u_max, ws, s, &why);
     if (e == cudaSuccess) e = launch_combine(Y, slot_of, w, R, L->hidden, L->top_k, out, s);

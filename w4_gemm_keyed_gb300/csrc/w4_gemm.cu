@@ -251,9 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     Sync *sy = reinterpret_cast<Sync *>(red + 2 * kFeatWarps * 32 * 4 * NQ);
 
     // Work items are (problem u, range vp) pairs, u-major; CTA b takes items
-    // b, b + gridDim.x, ...  Grouped launches take their problem list from the
-    // preceding grid.
-    if (a.n_problems || a.expert_ids) grid_dependency_wait();
+    // b, b + gridDim.x, ...  A grouped launch whose problem list comes from the
+    // preceding grid waits for it here; one whose list was complete before the
+    // preceding grid started (list_ready) reads it at once and, like a dense
+    // launch, streams its first weight stages while that grid finishes.
+    if ((a.n_problems || a.expert_ids) && !a.list_ready) grid_dependency_wait();
     const int nprob = a.n_problems ? *a.n_problems : 1;
     const int n_items = nprob * a.Pv;
     if (int(blockIdx.x) >= n_items) return;

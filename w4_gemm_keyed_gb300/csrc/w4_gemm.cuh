@@ -91,6 +91,7 @@ struct GemmArgs {
     long long w_stride;        // bytes between experts
     const int *expert_ids;     // dev [U_max] or nullptr (expert = u)
     const int *n_problems;     // dev count or nullptr (1)
+    int list_ready;            // expert_ids / n_problems were written before the preceding grid started
     int x_per_problem;         // activations differ per problem (use coordinate u)
     void *y;                   // fp32, or bf16 for kSwiGluBf16
     long long y_stride;        // elements between problems
