@@ -166,6 +166,21 @@ TF_API size_t tf_lane_gemm_workspace_bytes(int32_t K, int32_t N, int32_t group);
 TF_API tf_status tf_lane_gemm_w4(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R,
                           float *y, int32_t ldy, void *ws, size_t ws_bytes, void *stream);
 
+/*
+ * tf_lane_gemm_w4_accumulate: y[r][n] += (the tf_lane_gemm_w4 result), one
+ * fp32 add per element in the epilogue -- the residual update of a layer whose
+ * output joins the residual stream.  Arguments, layouts and row invariance as
+ * tf_lane_gemm_w4.
+ * tf_cast_bf16: y[r][n] = bf16(x[r][n]), rounded to nearest, ties to even, for
+ * r < R (1..65535) and n < N; x dev fp32 [R][ldx], y dev bf16 [R][ldy]
+ * (ldx, ldy >= N).  The bf16 operand of the next layer (queries, keys and
+ * values for the KV cache, the attention output for its projection).
+ */
+TF_API tf_status tf_lane_gemm_w4_accumulate(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R,
+                                            float *y, int32_t ldy, void *ws, size_t ws_bytes, void *stream);
+TF_API tf_status tf_cast_bf16(const float *x, int32_t R, int32_t N, int32_t ldx, uint16_t *y, int32_t ldy,
+                              void *stream);
+
 /* ------------------------------------------------------------------------
  * tf_lane_gemm_w4_noalloc -- tf_lane_gemm_w4 without a caller workspace
  * ------------------------------------------------------------------------

@@ -39,3 +39,22 @@ def assert_close_rows(gpu, ref, tol=TOL):
 
 def bits(a):
     return np.ascontiguousarray(a).view(np.uint32 if a.dtype.itemsize == 4 else np.uint16)
+
+
+HEAD_DIM = 128
+
+
+def kv_rows(kv):
+    """[n_kv][L][128] -> the [L][n_kv*128] rows tf_kv_append takes."""
+    n_kv, L, _ = kv.shape
+    return np.ascontiguousarray(kv.transpose(1, 0, 2).reshape(L, n_kv * HEAD_DIM))
+
+
+def kv_unswizzle(phys):
+    """A KV cache array in the library's layout [n_kv][max_len][128] -> plain
+    [n_kv][max_len][128], by the storage rule stated in include/tf.h."""
+    n_kv, L, _ = phys.shape
+    t = np.arange(L)[:, None]
+    d = np.arange(HEAD_DIM)[None, :]
+    src = 8 * ((d // 8) ^ (t % 8)) + d % 8
+    return np.take_along_axis(phys, np.broadcast_to(src, (n_kv, L, HEAD_DIM)), axis=2)

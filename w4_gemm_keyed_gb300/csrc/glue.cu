@@ -188,6 +188,13 @@ __global__ void commit_tokens_kernel(const int32_t *tokens, const int32_t *accep
     }
 }
 
+__global__ void cast_bf16_kernel(const float *x, int N, int ldx, uint16_t *y, int ldy) {
+    grid_dependency_wait();     // x comes from the preceding grid
+    grid_launch_dependents();
+    const int r = blockIdx.y, n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n < N) y[(long long)r * ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(x[(long long)r * ldx + n]));
+}
+
 // *first = min(*first, code_base + r) for every row r whose bytes differ
 // between a and b (grid-stride over R x N).
 __global__ void rows_differ_kernel(const float *a, const float *b, int R, int N, int ld, int code_base, int *first) {
@@ -203,6 +210,10 @@ __global__ void rows_differ_kernel(const float *a, const float *b, int R, int N,
 }
 
 }  // namespace
+
+cudaError_t launch_cast_bf16(const float *x, int R, int N, int ldx, uint16_t *y, int ldy, cudaStream_t s) {
+    return launch_pdl(cast_bf16_kernel, dim3((N + 255) / 256, R), dim3(256), 0, s, x, N, ldx, y, ldy);
+}
 
 cudaError_t launch_rows_differ(const float *a, const float *b, int R, int N, int ld, int code_base, int *first,
                                cudaStream_t s) {

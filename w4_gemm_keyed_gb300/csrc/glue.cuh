@@ -25,6 +25,8 @@ cudaError_t launch_commit_tokens(const int32_t *tokens, const int32_t *accepted,
 cudaError_t launch_combine(const float *Y, const int32_t *slot_of, const float *w, int R, int H, int top_k,
                            float *out, cudaStream_t s);
 
+// y[r][n] = bf16(x[r][n]), round to nearest even.
+cudaError_t launch_cast_bf16(const float *x, int R, int N, int ldx, uint16_t *y, int ldy, cudaStream_t s);
 // *first = min(*first, code_base + r) over rows r < R whose N fp32 values differ in any bit.
 cudaError_t launch_rows_differ(const float *a, const float *b, int R, int N, int ld, int code_base, int *first,
                                cudaStream_t s);

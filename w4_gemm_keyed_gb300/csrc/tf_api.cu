@@ -342,8 +342,33 @@ size_t tf_lane_gemm_workspace_bytes(int32_t K, int32_t N, int32_t group) {
     return dense_gemm_ws(W);
 }
 
+namespace {
+tf_status lane_gemm(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R, float *y, int32_t ldy,
+                    void *ws, size_t ws_bytes, void *stream, int mode, const char *name);
+}  // namespace
+
 tf_status tf_lane_gemm_w4(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R, float *y, int32_t ldy,
                           void *ws, size_t ws_bytes, void *stream) {
+    return lane_gemm(W, x, ldx, R, y, ldy, ws, ws_bytes, stream, kStoreF32, "tf_lane_gemm_w4");
+}
+
+tf_status tf_lane_gemm_w4_accumulate(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R, float *y,
+                                     int32_t ldy, void *ws, size_t ws_bytes, void *stream) {
+    return lane_gemm(W, x, ldx, R, y, ldy, ws, ws_bytes, stream, kAccumulateF32, "tf_lane_gemm_w4_accumulate");
+}
+
+tf_status tf_cast_bf16(const float *x, int32_t R, int32_t N, int32_t ldx, uint16_t *y, int32_t ldy, void *stream) {
+    if (!x || !y) return fail(TF_ERR_INVALID_ARG, "null x or y");
+    if (R < 1 || R > 65535 || N < 1) return fail(TF_ERR_INVALID_ARG, "R=%d (1..65535) or N=%d (>= 1) out of range", R, N);
+    if (ldx < N || ldy < N) return fail(TF_ERR_INVALID_ARG, "ldx=%d and ldy=%d must be >= N=%d", ldx, ldy, N);
+    cudaError_t e = launch_cast_bf16(x, R, N, ldx, y, ldy, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_cast_bf16");
+    return ok();
+}
+
+namespace {
+tf_status lane_gemm(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R, float *y, int32_t ldy,
+                    void *ws, size_t ws_bytes, void *stream, int mode, const char *name) {
     tf_status st = check_matrix(W, "W");
     if (st) return st;
     if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
@@ -354,12 +379,13 @@ tf_status tf_lane_gemm_w4(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx,
     if ((st = check_ws(ws, ws_bytes, dense_gemm_ws(*W)))) return st;
     if (size_t((W->N + kTileN - 1) / kTileN) * kFeatWarps > kMaxCounters)
         return fail(TF_ERR_UNSUPPORTED, "N=%d too large for the split-K counter region", W->N);
-    GemmArgs a = dense_args(*W, R, y, ldy, kStoreF32);
+    GemmArgs a = dense_args(*W, R, y, ldy, mode);
     const char *why = "";
     cudaError_t e = bind_and_launch(a, x, ldx, 0, 1, ws, static_cast<cudaStream_t>(stream), &why);
-    if (e != cudaSuccess) return fail(TF_ERR_CUDA, "tf_lane_gemm_w4: %s (%s)", cudaGetErrorString(e), why);
+    if (e != cudaSuccess) return fail(TF_ERR_CUDA, "%s: %s (%s)", name, cudaGetErrorString(e), why);
     return ok();
 }
+}  // namespace
 
 // ---- tf_selfcheck_row_invariance / tf_workspace_size ----
 namespace {

@@ -72,6 +72,8 @@ SIGNATURES = [
     ("tf_lane_gemm_workspace_bytes", SZ, [I32, I32, I32]),
     ("tf_lane_gemm_w4", ctypes.c_int, [ctypes.POINTER(W4MatrixC), P, I32, I32, P, I32, P, SZ, P]),
     ("tf_lane_gemm_w4_noalloc", ctypes.c_int, [ctypes.POINTER(W4MatrixC), P, I32, I32, P, I32, P, P]),
+    ("tf_lane_gemm_w4_accumulate", ctypes.c_int, [ctypes.POINTER(W4MatrixC), P, I32, I32, P, I32, P, SZ, P]),
+    ("tf_cast_bf16", ctypes.c_int, [P, I32, I32, I32, P, I32, P]),
     ("tf_keyed_sample_workspace_bytes", SZ, [I32, I32]),
     ("tf_keyed_sample", ctypes.c_int, [P, I32, I32, I32, ctypes.POINTER(SamplingC), ctypes.c_uint64, P, P, P, SZ, P]),
     ("tf_accept", ctypes.c_int, [P, P, I32, P, P, P]),
@@ -240,6 +242,26 @@ def lane_gemm_w4_noalloc(W: W4Matrix, x: torch.Tensor, y: torch.Tensor, status: 
 
 
 # ---------------------------------------------------------------- sampling
+def lane_gemm_w4_accumulate(W: W4Matrix, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor = None,
+                            stream=None) -> torch.Tensor:
+    """y[R][N] (fp32, in place) += W4 linear of bf16 rows x[R][K]."""
+    lib = load()
+    if ws is None:
+        ws = workspace(lane_gemm_workspace_bytes(W.K, W.N, W.group), x.device)
+    _check(lib.tf_lane_gemm_w4_accumulate(ctypes.byref(W.c()), _ptr(x), x.stride(0), x.shape[0], _ptr(y), y.stride(0),
+                                          _ptr(ws), ws.numel(), _stream(stream)))
+    return y
+
+
+def cast_bf16(x: torch.Tensor, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """bf16 bits (int16 tensor) of the fp32 rows x [R][N], nearest-even."""
+    R, N = x.shape
+    if out is None:
+        out = torch.empty((R, N), dtype=torch.int16, device=x.device)
+    _check(load().tf_cast_bf16(_ptr(x), R, N, x.stride(0), _ptr(out), out.stride(0), _stream(stream)))
+    return out
+
+
 def keyed_sample_workspace_bytes(R: int, V: int) -> int:
     return int(load().tf_keyed_sample_workspace_bytes(R, V))
 
