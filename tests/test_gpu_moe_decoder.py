@@ -133,12 +133,14 @@ def assert_rounded_close(gpu_bits, exact, rel=1e-4):
     assert not bad.any(), f"{int(bad.sum())} bf16 values off by more than rounding + {rel} * rms"
 
 
-def test_decoder_layers_teacher_forced(tf, tiny_decoder):
-    """Each layer of the GPU decoder against the oracle fed the GPU's own inputs."""
+@pytest.mark.parametrize("R", [8, 16])
+def test_decoder_layers_teacher_forced(tf, tiny_decoder, R):
+    """Each layer of the GPU decoder against the oracle fed the GPU's own inputs
+    (R = 16 takes the two-MMA path for rows 8..15)."""
     from oracle import numerics as onum
     w, model, dec = tiny_decoder
-    toks = [5, 17, 2999, 0, 42, 42, 7, 1234]
-    R, H, F, G = 8, model.hidden, model.ffn, model.group
+    toks = [5, 17, 2999, 0, 42, 42, 7, 1234, 3, 2998, 9, 64, 1, 2, 77, 512][:R]
+    H, F, G = model.hidden, model.ffn, model.group
     last = torch.tensor(toks[:1], dtype=torch.int32, device="cuda")
     drafts = torch.tensor(toks[1:], dtype=torch.int32, device="cuda")
     x = torch.empty((R, H), dtype=torch.float32, device="cuda")
@@ -165,10 +167,10 @@ def test_decoder_layers_teacher_forced(tf, tiny_decoder):
     assert_close_rows(logits, oracle.w4_linear(w["lm_codes"], w["lm_scales"], n_fin_h, G))
     # the fused verify step runs exactly this chain: identical logits
     dec.reset(toks[0], 1)
-    a, t = dec.step(8, toks[1:], 0.7, 20, 0.95, 1234)
-    assert np.array_equal(dec.logits[:8].cpu().numpy().view(np.uint32), logits.view(np.uint32))
+    a, t = dec.step(R, toks[1:], 0.7, 20, 0.95, 1234)
+    assert np.array_equal(dec.logits[:R].cpu().numpy().view(np.uint32), logits.view(np.uint32))
     # identical logits -> identical tokens (oracle sampler on the GPU's logits)
-    for i in range(8):
+    for i in range(R):
         tok, gap = osamp.sample_row(logits[i], 0.7, 20, 0.95, 1234, 1 + i)
         assert tok == t[i] or gap < 1e-9
     from oracle import accept as oacc
