@@ -13,7 +13,7 @@ the synthetic decoder's verify steps/s; plus the CPU oracle timed on a bounded
 sample (``cpu_baseline``), the end-to-end number through the C ABI with host
 buffers (``e2e``), the roofline of the dominant kernel and the SM clocks.
 
-``--impl reference`` times the CPU oracle (the reference arm of this build) on
+``--impl reference`` times the CPU oracle (the reference arm) on
 the same metric and workload.
 """
 

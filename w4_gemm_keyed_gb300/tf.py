@@ -129,7 +129,7 @@ def _current_raw_stream():
     return torch.cuda.current_stream().cuda_stream
 
 
-try:  # cheaper lookup of the current stream's handle where this build of torch has it
+try:  # cheaper lookup of the current stream's handle where this torch version has it
     _raw = torch._C._cuda_getCurrentRawStream
 
     def _current_raw_stream():  # noqa: F811
