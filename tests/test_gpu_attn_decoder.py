@@ -16,7 +16,10 @@ throughout; vocabulary 32768; KV caches of 1024 positions.
   the QKV projection (oracle W4 linear of the GPU's bf16 norm), the attention
   (oracle over the GPU's bf16 queries and cache) and the residual increment
   (oracle W4 linear of the GPU's bf16 attention output), each within
-  1e-3 * rms of the oracle row.
+  1e-3 * rms of the oracle row;
+* end to end against the oracle decoder with attention (oracle/attn_decoder.py)
+  on its tiny pinned model: first-pass logits within tolerance and equal
+  free-running tokens -- an open discrepancy, marked as an expected failure.
 """
 
 import numpy as np
@@ -144,4 +147,33 @@ def test_attention_block_matches_oracle_teacher_forced(tf, attn_model):
     ref_inc = oracle.w4_linear(attn[0]["o_codes"], attn[0]["o_scales"], a_bits, G)
     inc = x.double().cpu().numpy() - x0.double().cpu().numpy()
     assert_close_rows(inc, ref_inc)
+    assert tf.workspace_status(dec.ws_status) == tf.TF_DEV_OK
+
+
+@pytest.mark.xfail(strict=False, reason="open: first-pass logits of the tiny decoder with attention differ from "
+                   "the fp64 oracle decoder by 1.7e-2 * rms on a GB300 (each step matches the oracle on its own)")
+def test_tiny_attention_decoder_matches_oracle(tf):
+    """The pinned oracle's tiny decoder with attention (hidden 128, one KV head,
+    group 2, vocabulary 500): the first pass's logits within 1e-3 * rms of the
+    oracle's, and 24 free-running serial tokens after a 40-token prompt equal
+    the oracle's."""
+    from w4_gemm_keyed_gb300 import decode
+    from oracle import attn_decoder as oad
+    from test_oracle_attn_decoder import tiny_attn_model, T as T_TINY, K_TOP as K_TINY, P_TOP as P_TINY
+    weights, prompt = tiny_attn_model()
+    P_T = len(prompt)
+    model = decode.upload_attn_model(weights, weights["n_kv"], weights["attn_group"], 256)
+    dec = decode.AttnDecoder(model)
+    dec.prefill(prompt)
+    cache = oad.new_cache(weights, 256)
+    oad.prefill(weights, cache, prompt)
+    # first pass, teacher-forced: 4 rows at position P_T
+    rows = [prompt[-1], 11, 12, 13]
+    dec.reset(prompt[-1], P_T)
+    a, t = dec.step(4, rows[1:], T_TINY, K_TINY, P_TINY, 1234)
+    ref_logits = oad.logits_of(weights, oad.pass_rows(weights, cache, rows, P_T - 1))
+    assert_close_rows(dec.logits[:4].cpu().numpy(), ref_logits)
+    gpu = decode.attn_serial_decode(dec, prompt[-1], P_T, 24, T_TINY, K_TINY, P_TINY, 1234)
+    ref = oad.serial_decode(weights, cache, prompt[-1], P_T, 24, T_TINY, K_TINY, P_TINY, 1234)
+    assert gpu == ref
     assert tf.workspace_status(dec.ws_status) == tf.TF_DEV_OK
