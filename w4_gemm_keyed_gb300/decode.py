@@ -238,7 +238,7 @@ class AttnDecoder:
         self.accepted = torch.zeros(1, dtype=torch.int32, device=device)
         self.h_pos = torch.zeros(1 + max_rows, dtype=torch.int64).pin_memory()
         self.h_drafts = torch.zeros(max_rows, dtype=torch.int32).pin_memory()
-        self.h_out = torch.zeros(1 + max_rows, dtype=torch.int32).pin_memory()
+        self.h_result = torch.zeros(1 + max_rows, dtype=torch.int32).pin_memory()
         self._out = torch.zeros(1 + max_rows, dtype=torch.int32, device=device)
         self.pos = 1
 
@@ -303,9 +303,9 @@ class AttnDecoder:
         tf.accept(self.drafts[: max(R - 1, 1)], self.tokens[:R], accepted=self.accepted, bonus=self.last)
         self._out[0:1].copy_(self.accepted)
         self._out[1:1 + R].copy_(self.tokens[:R])
-        self.h_out[: 1 + R].copy_(self._out[: 1 + R], non_blocking=True)
+        self.h_result[: 1 + R].copy_(self._out[: 1 + R], non_blocking=True)
         torch.cuda.current_stream().synchronize()
-        out = self.h_out[: 1 + R].tolist()
+        out = self.h_result[: 1 + R].tolist()
         self.pos += out[0] + 1
         return out[0], out[1:]
 

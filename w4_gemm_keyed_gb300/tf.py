@@ -121,8 +121,14 @@ def _check(status: int):
 
 
 def _ptr(t):
-    # a plain int converts to void* through the declared argtypes
-    return None if t is None else t.data_ptr()
+    """Device address of a CUDA tensor (None passes NULL).  Every pointer the
+    library takes is a device pointer: a host tensor, pinned or not, is refused
+    here rather than handed to a kernel."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise TFError(TF_ERR_INVALID_ARG, f"expected a CUDA tensor, got one on {t.device}")
+    return t.data_ptr()
 
 
 def _current_raw_stream():
