@@ -149,6 +149,19 @@ def test_generic_workspace_size_and_selfcheck_validation(lib):
     assert res.value == 7
 
 
+def test_binding_refuses_host_tensors(lib):
+    """Every pointer the library takes is a device pointer: the binding raises
+    for a host tensor (pinned or not) before anything reaches the library."""
+    import torch
+    from w4_gemm_keyed_gb300 import tf
+    with pytest.raises(tf.TFError):
+        tf.cast_bf16(torch.zeros(2, 8))
+    with pytest.raises(tf.TFError):
+        tf.rmsnorm_bf16(torch.zeros(2, 8), 1e-6)
+    with pytest.raises(tf.TFError):
+        tf.workspace_status(torch.zeros(256, dtype=torch.uint8))
+
+
 def _start(p, q, rem):
     return p * q + min(p, rem)
 
