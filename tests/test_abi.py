@@ -123,6 +123,9 @@ def test_kv_cache_validation_rejects_bad_arguments(lib):
     assert lib.tf_kv_append(ctypes.byref(C), 256, 256, 1000, 1, 256, 256, 256, None) == tf.TF_ERR_INVALID_ARG
     assert lib.tf_kv_append(ctypes.byref(C), 256, 256, 1024, 4097, 256, 256, 256, None) == tf.TF_ERR_INVALID_ARG
     assert lib.tf_kv_append(ctypes.byref(C), 256, 256, 1024, 1, 256, 256, 128, None) == tf.TF_ERR_WORKSPACE
+    huge = tf.KVCacheC(256, 512, 128, 0x7FFFFF00)          # a launch of 2^31 x 128 / 8 CTAs is refused
+    assert lib.tf_kv_append(ctypes.byref(huge), 256, 256, 128 * 128, 0x7FFFFF00, 256, 256, 256, None) == \
+        tf.TF_ERR_UNSUPPORTED
 
 
 def test_generic_workspace_size_and_selfcheck_validation(lib):

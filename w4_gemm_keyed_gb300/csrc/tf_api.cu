@@ -600,6 +600,8 @@ tf_status tf_kv_append(const tf_kv_cache *c, const uint16_t *k_new, const uint16
     tf_status st = check_cache(c);
     if (st != TF_OK) return st;
     if (R < 1 || R > c->max_len) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, max_len=%d]", R, c->max_len);
+    if (((long long)R * c->n_kv + 7) / 8 > 0x7FFFFFFFLL)
+        return fail(TF_ERR_UNSUPPORTED, "R=%d x n_kv=%d entries exceed one launch", R, c->n_kv);
     if (!k_new || !v_new || !pos) return fail(TF_ERR_INVALID_ARG, "null k_new, v_new or pos");
     if (!aligned(k_new, 16) || !aligned(v_new, 16)) return fail(TF_ERR_INVALID_ARG, "k_new, v_new not 16-B aligned");
     if (ld < c->n_kv * kHeadDim || ld % 8)
