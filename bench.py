@@ -158,9 +158,11 @@ def dense_launches():
 
 
 def time_dense(tf, torch, mats, steps, warmup):
-    """Timed region: CUDA-graph replays of one weight-rotation cycle (n_copies steps).
+    """Timed region: exactly ``steps`` steps, as CUDA-graph replays of one
+    weight-rotation cycle (n_copies steps) followed by one graph of the first
+    ``steps % n_copies`` steps of the next cycle.
 
-    Returns (seconds, steps actually timed, launches per step)."""
+    Returns (seconds, steps timed, launches per step)."""
     n_copies = min(len(m["copies"]) for m in mats.values())
 
     def step(c):
@@ -168,25 +170,34 @@ def time_dense(tf, torch, mats, steps, warmup):
             m = mats[(K, N)]
             tf.lane_gemm_w4(m["copies"][c], m["x"][:R], y=m["y"][:R], ws=m["ws"])
 
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for c in range(n):
+                step(c)
+        return g
+
     for i in range(warmup):
         step(i % n_copies)
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for c in range(n_copies):
-            step(c)
-    g.replay()
+    full_reps, rem = divmod(steps, n_copies)
+    full = capture(n_copies)
+    tail = capture(rem) if rem else None
+    full.replay()
+    if tail is not None:
+        tail.replay()
     torch.cuda.synchronize()
-    reps = max(1, -(-steps // n_copies))
     stream = torch.cuda.current_stream()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(reps):
-        g.replay()
+    for _ in range(full_reps):
+        full.replay()
+    if tail is not None:
+        tail.replay()
     t1.record(stream)
     torch.cuda.synchronize()
-    return t0.elapsed_time(t1) / 1e3, reps * n_copies, len(dense_launches())
+    return t0.elapsed_time(t1) / 1e3, steps, len(dense_launches())
 
 
 def time_per_launch(tf, torch, mats, reps=20):
