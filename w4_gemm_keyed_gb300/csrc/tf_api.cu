@@ -281,7 +281,7 @@ const char *tf_status_string(tf_status s) {
     return "unknown status";
 }
 
-int tf_version(void) { return 100; }
+int tf_version(void) { return 200; }  // 0.2.0: KV-cache attention, affine W4, self-check, cast, accumulate
 
 int32_t tf_device_sm_count(void) { return device_sm_count(); }
 
