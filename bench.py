@@ -377,7 +377,7 @@ def extra_affine(tf, torch, steps=30):
         b.record()
         torch.cuda.synchronize()
         us = a.elapsed_time(b) * 1e3 / (steps * n_copies)
-        out[f"R{R}"] = {"us_per_launch": us, "gbs": nbytes / us / 1e3}
+        out[f"R{R}"] = {"us_per_launch": us, "gbs": nbytes / us / 1e3, "frac_of_hbm_peak": nbytes / us / 1e3 / peaks()[0]}
     return out
 
 
@@ -427,7 +427,8 @@ def extra_attention(tf, torch, steps=30, ctxs=(8192, 32768), rows=(1, 8, 16)):
             torch.cuda.synchronize()
             us = a.elapsed_time(b) * 1e3 / (steps * n_copies)
             nbytes = attention_bytes(ctx, R, n_kv, group)
-            out[f"ctx{ctx}_R{R}"] = {"us_per_call": us, "gbs": nbytes / us / 1e3, "bytes_per_call": nbytes}
+            out[f"ctx{ctx}_R{R}"] = {"us_per_call": us, "gbs": nbytes / us / 1e3, "bytes_per_call": nbytes,
+                                     "frac_of_hbm_peak": nbytes / us / 1e3 / peaks()[0]}
         assert tf.workspace_status(ws) == tf.TF_DEV_OK
         del caches
         torch.cuda.empty_cache()
