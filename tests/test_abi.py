@@ -152,6 +152,35 @@ def test_generic_workspace_size_and_selfcheck_validation(lib):
     assert res.value == 7
 
 
+def test_newer_entry_points_validate_before_launching(lib):
+    from w4_gemm_keyed_gb300 import tf
+    big = 1 << 30
+    # bf16 cast
+    assert lib.tf_cast_bf16(None, 1, 8, 8, 256, 8, None) == tf.TF_ERR_INVALID_ARG          # null x
+    assert lib.tf_cast_bf16(256, 0, 8, 8, 256, 8, None) == tf.TF_ERR_INVALID_ARG           # R = 0
+    assert lib.tf_cast_bf16(256, 65536, 8, 8, 256, 8, None) == tf.TF_ERR_INVALID_ARG       # R too large
+    assert lib.tf_cast_bf16(256, 2, 8, 4, 256, 8, None) == tf.TF_ERR_INVALID_ARG           # ldx < N
+    # accumulate GEMM: the same checks as tf_lane_gemm_w4
+    W = tf.W4MatrixC(256, 100, 64, 64, 0)                                                # K % 64 != 0
+    assert lib.tf_lane_gemm_w4_accumulate(ctypes.byref(W), 256, 128, 1, 256, 64, 256, big, None) == \
+        tf.TF_ERR_UNSUPPORTED
+    W = tf.W4MatrixC(256, 256, 64, 64, 0)
+    assert lib.tf_lane_gemm_w4_accumulate(ctypes.byref(W), 256, 256, 17, 256, 64, 256, big, None) == \
+        tf.TF_ERR_INVALID_ARG                                                           # R = 17
+    assert lib.tf_lane_gemm_w4_accumulate(ctypes.byref(W), 256, 256, 1, 256, 64, None, 0, None) == \
+        tf.TF_ERR_WORKSPACE
+    W = tf.W4MatrixC(256, 256, 64, 64, 2)                                                # affine flag not 0/1
+    assert lib.tf_lane_gemm_w4(ctypes.byref(W), 256, 256, 1, 256, 64, 256, big, None) == tf.TF_ERR_INVALID_ARG
+    # affine packing
+    assert lib.tf_pack_w4_affine(None, 256, 256, 256, 64, 64, 256, big, None) == tf.TF_ERR_INVALID_ARG
+    assert lib.tf_pack_w4_affine(256, 256, 256, 100, 64, 64, 256, big, None) == tf.TF_ERR_UNSUPPORTED
+    assert lib.tf_pack_w4_affine(256, 256, 256, 256, 64, 16, 256, big, None) == tf.TF_ERR_UNSUPPORTED
+    assert lib.tf_pack_w4_affine(256, 256, 256, 256, 64, 64, 264, big, None) == tf.TF_ERR_INVALID_ARG
+    need = lib.tf_w4_affine_packed_bytes(256, 64, 64)
+    assert need > lib.tf_w4_packed_bytes(256, 64, 64)                                   # biases take room
+    assert lib.tf_pack_w4_affine(256, 256, 256, 256, 64, 64, 256, need - 1, None) == tf.TF_ERR_INVALID_ARG
+
+
 def test_binding_refuses_host_tensors(lib):
     """Every pointer the library takes is a device pointer: the binding raises
     for a host tensor (pinned or not) before anything reaches the library."""
