@@ -158,3 +158,38 @@ def test_planted_mistakes_are_caught(monkeypatch, mutant):
         except AssertionError:
             failed += 1
     assert failed >= 1, f"no pin caught the planted mistake {mutant}"
+
+
+def test_properties_on_random_shapes():
+    """Over random small shapes: outputs are convex combinations of the visible
+    values, a key component shared by all positions cancels, verify rows equal
+    single-row calls, and entries after a row's position never matter."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    @hyp.settings(max_examples=25, deadline=None)
+    @hyp.given(R=st.integers(1, 4), n_kv=st.integers(1, 2), group=st.sampled_from([1, 2]),
+               pos0=st.integers(0, 30), seed=st.integers(0, 2**31 - 1))
+    def check(R, n_kv, group, pos0, seed):
+        rng = np.random.default_rng(seed)
+        L = pos0 + R + 3
+        q, k, v = inputs.attention_inputs(rng, R, n_kv, group, L, q_std=2.0)
+        out = attention.attention_verify(q, k, v, pos0, group)
+        kf, vf = bf16_to_f64(k), bf16_to_f64(v)
+        for r in range(R):
+            p = pos0 + r
+            for h in range(n_kv * group):
+                vis = vf[h // group, : p + 1]
+                assert np.all(out[r, h] <= vis.max(axis=0) + 1e-12)
+                assert np.all(out[r, h] >= vis.min(axis=0) - 1e-12)
+                u = rng.standard_normal(D)
+                shifted = attention.attention_row(bf16_to_f64(q[r, h]), kf[h // group] + u, vf[h // group], p)
+                assert np.allclose(shifted, out[r, h], rtol=0, atol=1e-9)
+            one = attention.attention_verify(q[r:r + 1], k, v, p, group)
+            assert np.array_equal(one[0], out[r])
+        k2, v2 = k.copy(), v.copy()
+        k2[:, pos0 + R:] = bf16(3.0)
+        v2[:, pos0 + R:] = bf16(-9.0)
+        assert np.array_equal(attention.attention_verify(q, k2, v2, pos0, group), out)
+
+    check()
