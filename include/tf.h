@@ -339,10 +339,11 @@ TF_API tf_status tf_commit_tokens(const int32_t *tokens, const int32_t *accepted
 /* ------------------------------------------------------------------------
  * Attention of the verify rows over a KV cache.
  *
- * The README's note on drafting says that drafted and serial decoding from the
- * same cache agree, and the 0.3.4.1 release note ("TensorFold: the contract is
- * what it does not change", section "The regression it published against
- * itself") keeps cached bits independent of where a conversation resumed.  The
+ * By the README's note on drafting, runs with and without drafts emit the same
+ * tokens when they start from one cache; the 0.3.4.1 release note
+ * ("TensorFold: the contract is what it does not change", section "The
+ * regression it published against itself") keeps cached bits independent of
+ * where a conversation resumed.  The
  * pages do not spell out the attention; these calls compute causal scaled
  * dot-product attention with grouped key/value heads (head dimension 128,
  * query head h reads KV head h / group), and make each row's bits depend only

@@ -1,13 +1,13 @@
 """Attention of verify rows over a KV cache (test infrastructure).
 
-The TensorFold pages speak of the KV cache only through its guarantees: the
-README's note on drafting says that drafted and serial decoding from the
-same cache always agree, and the 0.3.4.1 release note ("TensorFold: the
-contract is what it does not change", section "The regression it published
-against itself") describes prompt caches kept at points of a fixed grid so
-that cached bits do not depend on where a conversation resumed.  The pages do
-not write out the attention itself, so the oracle takes the textbook
-definition of causal scaled dot-product attention with grouped key/value
+The TensorFold pages speak of the KV cache only through its guarantees: by
+the README's note on drafting, a run with drafts and a run without them emit
+the same tokens when they start from one cache; the 0.3.4.1 release note
+("TensorFold: the contract is what it does not change", section "The
+regression it published against itself") keeps prompt caches only at points
+of a fixed grid, so that cached bits do not depend on where a conversation
+resumed.  The pages do not write out the attention itself, so the oracle
+takes the textbook definition of causal scaled dot-product attention with grouped key/value
 heads (Vaswani et al. 2017, section 3.2.1; Ainslie et al. 2023 for the
 grouping):
 

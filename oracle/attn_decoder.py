@@ -2,8 +2,9 @@
 
 The attention-free decoder of ``decoder.py`` with, before each MLP block, an
 attention sub-block over a KV cache.  The pages name the guarantee, not the
-layer: the README's note on drafting says that drafted and serial decoding
-from the same cache agree.  Each block computes, on fp64 rows x:
+layer: by the README's note on drafting, a run with drafts and a run without
+them emit the same tokens when they start from one cache.  Each block
+computes, on fp64 rows x:
 
     n   = bf16(rms_norm(x))
     qkv = n Wqkv                       (queries n_q x 128, keys n_kv x 128, values n_kv x 128)

@@ -1,9 +1,10 @@
 // Row-exact attention of verify rows over a KV cache.
 //
-// The TensorFold README promises that drafted and serial decoding from the
-// same cache agree; with attention in the pass that needs each row's result to
-// depend only on its own query, its own position p and the cache entries
-// 0..p -- never on how many rows share the launch or where the launch starts.
+// The TensorFold README's note on drafting: starting from one cache, a run
+// with drafts emits exactly the tokens of a run without them.  With attention
+// in the pass, that needs each row's result to depend only on its own query,
+// its own position p and the cache entries 0..p -- never on how many rows
+// share the launch or where the launch starts.
 // The arithmetic here is fixed by absolute positions alone:
 //
 //   * keys are cut into partitions of 256 positions (c*256 .. c*256+255) and
