@@ -258,8 +258,9 @@ TF_API tf_status tf_accept(const int32_t *drafts, const int32_t *sampled, int32_
 /* ------------------------------------------------------------------------
  * tf_moe_w4 -- top-k routed W4 SwiGLU experts (30B-A3B-class MoE layer)
  * ------------------------------------------------------------------------
- * README, "What each checkpoint needs" (MoE kernels read 4-bit weights in
- * groups of 32) and source layout (fused MoE kernels).  Per row r:
+ * README, "What each checkpoint needs" (the MoE model is served from 4-bit
+ * weights quantised in groups of 32) and source layout (fused MoE kernels).
+ * Per row r:
  *   experts ranked by (router logit desc, id asc), the first top_k kept,
  *   weights w_j = exp(z_j - z_0) / sum_{i<top_k} exp(z_i - z_0) (fp64, then fp32);
  *   for each kept expert e: h = bf16(silu(x Wg_e) * (x Wu_e)), y_e = h Wd_e;
