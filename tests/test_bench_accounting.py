@@ -50,3 +50,75 @@ def test_traffic_record_is_used_only_for_the_sources_it_was_taken_on(bench):
         assert bench.recorded_traffic() is None     # the kernel changed since the counters were taken
     # the recorded traffic is within a few per cent of the algorithmic bytes: no re-reads
     assert 1.0 <= rec["dram_bytes_per_launch"] / 47_349_760 < 1.05
+
+
+class _Counter:
+    n = 0
+
+
+class _FakeGraph:
+    def __init__(self):
+        self.calls = 0
+
+    def replay(self):
+        _Counter.n += self.calls
+
+
+class _FakeEvent:
+    def record(self, stream=None):
+        self.at = _Counter.n
+
+    def elapsed_time(self, end):
+        return float(end.at - self.at)      # "milliseconds" = launches executed in between
+
+
+class _FakeCuda:
+    capturing = None
+
+    def synchronize(self):
+        pass
+
+    def CUDAGraph(self):
+        return _FakeGraph()
+
+    def graph(self, g):
+        import contextlib
+
+        @contextlib.contextmanager
+        def cm():
+            _FakeCuda.capturing = g
+            try:
+                yield
+            finally:
+                _FakeCuda.capturing = None
+        return cm()
+
+    def current_stream(self):
+        return None
+
+    def Event(self, enable_timing=False):
+        return _FakeEvent()
+
+
+class _FakeTorch:
+    cuda = _FakeCuda()
+
+
+class _FakeTf:
+    @staticmethod
+    def lane_gemm_w4(W, x, y=None, ws=None):
+        if _FakeCuda.capturing is not None:
+            _FakeCuda.capturing.calls += 1  # recorded into the graph
+        else:
+            _Counter.n += 1
+
+
+@pytest.mark.parametrize("steps", [1, 8, 9, 10, 2000, 2007])
+def test_time_dense_times_exactly_the_requested_steps(bench, steps):
+    """The device-timed region runs exactly ``steps`` steps of the ten launches,
+    whatever the length of the weight-rotation cycle (9 copies here)."""
+    mats = {(K, N): {"copies": list(range(9)), "x": [0] * 16, "y": [0] * 16, "ws": None}
+            for K, N in {(K, N) for K, N, _ in bench.dense_launches()}}
+    secs, timed, per_step = bench.time_dense(_FakeTf, _FakeTorch, mats, steps, warmup=3)
+    assert timed == steps and per_step == 10
+    assert secs * 1e3 == steps * 10           # launches executed between the two events
