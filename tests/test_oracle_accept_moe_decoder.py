@@ -210,3 +210,150 @@ def test_planted_decoder_bonus_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(A, "accept", mutant)
     with pytest.raises(AssertionError):
         test_drafted_equals_serial_token_sha(4, 0.75)
+
+
+# ------------------------------------------------------------------ compositions in closed form
+# Hand-sized weights whose results follow from the definitions alone: SwiGLU
+# (Shazeer 2020, "GLU Variants Improve Transformer": silu of the gate
+# projection times the up projection), RMSNorm with gain 1 and eps 1e-6, the
+# residual add, and the rank-order combine of the renormalised top-k router
+# weights.  The expected numbers below were worked out once from those
+# definitions (bf16 values are exact binary fractions).
+_BF16_ONE = 0x3F80
+_FP16_ONE, _FP16_HALF, _FP16_QUARTER = 0x3C00, 0x3800, 0x3400
+
+
+def _pack_rows(codes_i8):
+    """Canonical packed codes of a small int matrix (low nibble = even k)."""
+    c = np.asarray(codes_i8, dtype=np.int16) & 0xF
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+def _mat(N, K, G, entries, scale_bits):
+    """codes [N][K] zero except entries {(n, k): code}; every group scale = scale_bits[n]."""
+    c = np.zeros((N, K), dtype=np.int8)
+    for (n, k), v in entries.items():
+        c[n, k] = v
+    s = np.zeros((N, K // G), dtype=np.uint16)
+    for n, b in enumerate(scale_bits):
+        s[n, :] = b
+    return _pack_rows(c), s
+
+
+def _expert(H, F, G, gate, up, down, down_scales):
+    gc, gs = _mat(F, H, G, gate, [_FP16_ONE] * F)
+    uc, us = _mat(F, H, G, up, [_FP16_ONE] * F)
+    dc, ds = _mat(H, F, G, down, down_scales)
+    return dict(gate_codes=gc, gate_scales=gs, up_codes=uc, up_scales=us, down_codes=dc, down_scales=ds)
+
+
+def _stack(experts):
+    return {k: np.stack([e[k] for e in experts]) for k in experts[0]}
+
+
+def _one_hot_row(H):
+    x = np.zeros((1, H), dtype=np.uint16)
+    x[0, 0] = _BF16_ONE
+    return x
+
+
+def test_expert_swiglu_closed_form():
+    # x = e_0; gate row 0 reads 2 * x_0, up row 0 reads -3 * x_0:
+    #   h_0 = bf16(silu(2) * -3) = bf16(-5.2847824678...) = -5.28125  (silu of the GATE)
+    #   (silu of the up projection instead would give bf16(silu(-3) * 2) = -0.28515625)
+    # down rows: y_0 = 0.5 * 1 * h_0, y_1 = 0.25 * -2 * h_0; every other output is 0.
+    H = F = G = 32
+    e = _expert(H, F, G, {(0, 0): 2}, {(0, 0): -3}, {(0, 0): 1, (1, 0): -2},
+                [_FP16_HALF, _FP16_QUARTER] + [_FP16_ONE] * (H - 2))
+    h_bits, y = M.expert_forward(_one_hot_row(H), _stack([e]), 0, G)
+    h = oracle.bf16_to_f64(h_bits)
+    assert h[0, 0] == -5.28125 and np.all(h[0, 1:] == 0.0)
+    assert y[0, 0] == -2.640625 and y[0, 1] == 2.640625 and np.all(y[0, 2:] == 0.0)
+
+
+def test_moe_combine_rank_order_closed_form():
+    # expert 0: y_0[0] = bf16(silu(1)) = 0.73046875; expert 1: y_1[0] = 2 * bf16(silu(2)) = 3.515625.
+    # router logits (0, 1): expert 1 ranks first with weight e / (1 + e), expert 0 second with 1 / (1 + e).
+    H = F = G = 32
+    e0 = _expert(H, F, G, {(0, 0): 1}, {(0, 0): 1}, {(0, 0): 1}, [_FP16_ONE] * H)
+    e1 = _expert(H, F, G, {(0, 0): 2}, {(0, 0): 1}, {(0, 0): 2}, [_FP16_ONE] * H)
+    z = np.array([[0.0, 1.0]], dtype=np.float32)
+    out, ids, w, ysel = M.moe(_one_hot_row(H), z, _stack([e0, e1]), G, top_k=2)
+    assert ids[0].tolist() == [1, 0]
+    assert ysel[0, 0, 0] == 3.515625 and ysel[0, 1, 0] == 0.73046875
+    w_first, w_second = 0.7310585786300049, 0.2689414213699951   # e/(1+e), 1/(1+e)
+    assert w[0, 0] == pytest.approx(w_first, rel=1e-15) and w[0, 1] == pytest.approx(w_second, rel=1e-15)
+    assert out[0, 0] == pytest.approx(w_first * 3.515625 + w_second * 0.73046875, rel=1e-15)
+    assert np.all(out[0, 1:] == 0.0)
+
+
+def _block(H, F, G, gate, up, down, down_scale_bits):
+    return _expert(H, F, G, gate, up, down, [down_scale_bits] * H)
+
+
+def test_block_residual_kept_when_down_is_zero():
+    # zero down-projection codes: the block adds nothing and x comes back unchanged
+    H = F = G = 64
+    rng = inputs.rng_for(33)
+    x = rng.standard_normal((3, H))
+    blk = _block(H, F, G, {(0, 0): 3, (5, 7): -2}, {(0, 0): 1, (5, 9): 4}, {}, _FP16_ONE)
+    assert np.array_equal(D.block_forward(x, blk, G), x)
+
+
+def test_block_rmsnorm_swiglu_residual_closed_form():
+    # a constant row c = 2^-10: RMSNorm gives c / sqrt(c^2 + 1e-6) = 0.698672998985... -> bf16 0.69921875
+    # in every entry (without the norm the GEMMs would see 2^-10).  Gate row 0 reads 1 * n_0,
+    # up row 0 reads 2 * n_0 = 1.3984375; h_0 = bf16(silu(0.69921875) * 1.3984375)
+    # = bf16(0.65319377915...) = 0.65234375; down row 0 reads 0.25 * h_0 = 0.1630859375,
+    # added to the residual: x_0 = 2^-10 + 0.1630859375 = 0.1640625, every other entry stays 2^-10.
+    H = F = G = 64
+    c = 2.0 ** -10
+    assert c / math.sqrt(c * c + 1e-6) == pytest.approx(0.6986729989854964, rel=1e-15)
+    blk = _block(H, F, G, {(0, 0): 1}, {(0, 0): 2}, {(0, 0): 1}, _FP16_QUARTER)
+    x = np.full((2, H), c)
+    out = D.block_forward(x, blk, G)
+    assert np.all(out[:, 0] == 0.1640625)
+    assert np.all(out[:, 1:] == c)
+
+
+def _mutant_block(kind):
+    def block_forward(x, blk, group):
+        n = x if kind == "no_norm" else NUM.rms_norm(x, D.EPS)
+        n_bits = NUM.bf16_bits_of(NUM.bf16_round(n))
+        g = oracle.w4_linear(blk["gate_codes"], blk["gate_scales"], n_bits, group)
+        u = oracle.w4_linear(blk["up_codes"], blk["up_scales"], n_bits, group)
+        act = NUM.silu(u) * g if kind == "silu_on_up" else NUM.silu(g) * u
+        h_bits = NUM.bf16_bits_of(NUM.bf16_round(act))
+        d = oracle.w4_linear(blk["down_codes"], blk["down_scales"], h_bits, group)
+        return d if kind == "no_residual" else x + d
+    return block_forward
+
+
+@pytest.mark.parametrize("kind", ["no_norm", "silu_on_up", "no_residual"])
+def test_planted_block_mistakes_are_caught(monkeypatch, kind):
+    monkeypatch.setattr(D, "block_forward", _mutant_block(kind))
+    with pytest.raises(AssertionError):
+        test_block_residual_kept_when_down_is_zero()
+        test_block_rmsnorm_swiglu_residual_closed_form()
+
+
+def test_planted_expert_silu_on_up_is_caught(monkeypatch):
+    def expert_forward(x_bits, W, e, group):
+        g = oracle.w4_linear(W["gate_codes"][e], W["gate_scales"][e], x_bits, group)
+        u = oracle.w4_linear(W["up_codes"][e], W["up_scales"][e], x_bits, group)
+        h_bits = NUM.bf16_bits_of(NUM.bf16_round(NUM.silu(u) * g))
+        return h_bits, oracle.w4_linear(W["down_codes"][e], W["down_scales"][e], h_bits, group)
+    monkeypatch.setattr(M, "expert_forward", expert_forward)
+    with pytest.raises(AssertionError):
+        test_expert_swiglu_closed_form()
+
+
+def test_planted_combine_weights_permuted_is_caught(monkeypatch):
+    orig = M.route
+
+    def mutant(z, top_k=8):
+        ids, w = orig(z, top_k)
+        return ids, w[:, ::-1].copy()
+    monkeypatch.setattr(M, "route", mutant)
+    with pytest.raises(AssertionError):
+        test_moe_combine_rank_order_closed_form()
