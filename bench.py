@@ -201,7 +201,8 @@ def time_dense(tf, torch, mats, steps, warmup):
 
 
 def time_per_launch(tf, torch, mats, reps=20):
-    """GPU time of each (shape, R) launch, events around single launches (rotating copies)."""
+    """Latency view: GPU time of each (shape, R) launch issued alone with events
+    around it (rotating copies) -- includes launch latency and the pipeline ramp."""
     per = {}
     n_copies = min(len(m["copies"]) for m in mats.values())
     c = 0
@@ -217,6 +218,36 @@ def time_per_launch(tf, torch, mats, reps=20):
             per.setdefault((K, N, R), []).append((a, b))
     torch.cuda.synchronize()
     return {k: [a.elapsed_time(b) for a, b in v] for k, v in per.items()}
+
+
+def time_per_r_graph(tf, torch, mats, reps=20):
+    """Device rate of each (shape, R): one CUDA graph of back-to-back launches of
+    that shape and R over every weight copy (> 3x L2 in total, so each launch
+    reads HBM), replayed ``reps`` times; microseconds per launch."""
+    out = {}
+    for K, N, R in dense_launches():
+        m = mats[(K, N)]
+        xv, yv = m["x"][:R], m["y"][:R]
+
+        def cycle():
+            for W in m["copies"]:
+                tf.lane_gemm_w4(W, xv, y=yv, ws=m["ws"])
+        cycle()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cycle()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        out[(K, N, R)] = a.elapsed_time(b) * 1e3 / (reps * len(m["copies"]))
+        del g
+    return out
 
 
 def time_dense_e2e(tf, torch, mats, steps, warmup):
@@ -294,7 +325,7 @@ def time_dense_e2e(tf, torch, mats, steps, warmup):
 
 
 def extra_lmhead(tf, torch, steps=30):
-    """LM head (5120 -> 151936) + keyed sampler + acceptance at R = 1, 8, 16."""
+    """LM head (5120 -> 151936) + keyed sampler + acceptance at R = 1, 2, 4, 8, 16."""
     from w4_gemm_keyed_gb300 import inputs
     K, V = 5120, 151936
     rng = inputs.rng_for(3)
@@ -311,7 +342,7 @@ def extra_lmhead(tf, torch, steps=30):
     bonus = torch.empty(1, dtype=torch.int32, device="cuda")
     out = {}
     by = bytes_per_launch(K, V)
-    for R in (1, 8, 16):
+    for R in ROWS:
         def one():
             tf.lane_gemm_w4(W, x[:R], y=logits[:R], ws=ws_g)
             tf.keyed_sample(logits[:R], 0.6, 20, 0.95, 1234, pos[:R], tokens=toks[:R], ws=ws_s)
@@ -335,7 +366,8 @@ def extra_lmhead(tf, torch, steps=30):
         ms = a.elapsed_time(b) / steps
         gms = g0.elapsed_time(g1) / steps
         out[f"R{R}"] = {"verify_steps_per_s": 1e3 / ms, "rows_per_s": R * 1e3 / ms,
-                        "lmhead_gbs": by / (gms * 1e-3) / 1e9, "ms_per_step": ms}
+                        "lmhead_gbs": by / (gms * 1e-3) / 1e9,
+                        "lmhead_frac_of_hbm_peak": by / (gms * 1e-3) / 1e9 / peaks()[0], "ms_per_step": ms}
     del W
     return out
 
@@ -435,49 +467,63 @@ def extra_attention(tf, torch, steps=30, ctxs=(8192, 32768), rows=(1, 8, 16)):
     return out
 
 
-def extra_moe(tf, torch, steps=30):
+def extra_moe(tf, torch, steps=32, n_router=8):
+    """30B-A3B-class MoE layer at R = 1, 4, 8, 16.  L2 is defeated twice over:
+    two full copies of the 128 experts (2 x 340 MB) alternate, and every call
+    draws one of n_router seeded router-logit sets, so the touched set changes
+    from call to call.  GB/s counts the touched experts' weight bytes of each call."""
     from w4_gemm_keyed_gb300 import inputs
     E, H, F, G, k = 128, 2048, 768, 32, 8
     rng = inputs.rng_for(4, 99)
     sz_gu, sz_d = tf.packed_bytes(H, 2 * F, G), tf.packed_bytes(F, H, G)
-    gu = torch.empty(E * sz_gu, dtype=torch.uint8, device="cuda")
-    dn = torch.empty(E * sz_d, dtype=torch.uint8, device="cuda")
     gen = torch.Generator(device="cuda")
     gen.manual_seed(4)
-    for e in range(E):
-        c = torch.randint(0, 256, (2 * F, H // 2), dtype=torch.uint8, device="cuda", generator=gen)
-        s = (torch.randn((2 * F, H // G), device="cuda", generator=gen).abs() * 0.02 + 1e-3).half().view(torch.int16)
-        tf.pack_w4(c, s, G, gate_up=True, out=gu[e * sz_gu:(e + 1) * sz_gu])
-        c = torch.randint(0, 256, (H, F // 2), dtype=torch.uint8, device="cuda", generator=gen)
-        s = (torch.randn((H, F // G), device="cuda", generator=gen).abs() * 0.02 + 1e-3).half().view(torch.int16)
-        tf.pack_w4(c, s, G, out=dn[e * sz_d:(e + 1) * sz_d])
-    layer = tf.MoeLayer(gu, dn, H, F, E, k, G)
+    layers = []
+    for _ in range(2):
+        gu = torch.empty(E * sz_gu, dtype=torch.uint8, device="cuda")
+        dn = torch.empty(E * sz_d, dtype=torch.uint8, device="cuda")
+        for e in range(E):
+            c = torch.randint(0, 256, (2 * F, H // 2), dtype=torch.uint8, device="cuda", generator=gen)
+            s = (torch.randn((2 * F, H // G), device="cuda", generator=gen).abs() * 0.02 + 1e-3).half().view(torch.int16)
+            tf.pack_w4(c, s, G, gate_up=True, out=gu[e * sz_gu:(e + 1) * sz_gu])
+            c = torch.randint(0, 256, (H, F // 2), dtype=torch.uint8, device="cuda", generator=gen)
+            s = (torch.randn((H, F // G), device="cuda", generator=gen).abs() * 0.02 + 1e-3).half().view(torch.int16)
+            tf.pack_w4(c, s, G, out=dn[e * sz_d:(e + 1) * sz_d])
+        layers.append(tf.MoeLayer(gu, dn, H, F, E, k, G))
     expert_bytes = (2 * F * H // 2 + 2 * 2 * F * (H // G)) + (H * F // 2 + 2 * H * (F // G))
-    out = {}
+    out = {"expert_bytes": expert_bytes, "l2": "two expert sets alternate; router logits rotate over 8 draws"}
     for R in (1, 4, 8, 16):
         x = torch.from_numpy(inputs.bf16_normal(rng, (R, H)).view(np.int16)).cuda()
-        z = torch.from_numpy(inputs.router_logits(rng, R, E)).cuda()
-        touched = len(np.unique(np.argsort(-z.cpu().numpy(), axis=1, kind="stable")[:, :k]))
-        ws = tf.workspace(tf.moe_workspace_bytes(layer, R))
+        zs = [inputs.router_logits(rng, R, E) for _ in range(n_router)]
+        touched = [len(np.unique(np.argsort(-z, axis=1, kind="stable")[:, :k])) for z in zs]
+        zd = [torch.from_numpy(z).cuda() for z in zs]
+        ws = tf.workspace(tf.moe_workspace_bytes(layers[0], R))
         y = torch.empty((R, H), device="cuda")
-        for _ in range(3):
-            tf.moe_w4(layer, x, z, out=y, ws=ws)
+
+        def call(i):
+            tf.moe_w4(layers[i % 2], x, zd[i % n_router], out=y, ws=ws)
+        for i in range(4):
+            call(i)
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
-        for _ in range(steps):
-            tf.moe_w4(layer, x, z, out=y, ws=ws)
+        for i in range(steps):
+            call(i)
         b.record()
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / steps
-        out[f"R{R}"] = {"touched_experts": touched, "gbs": touched * expert_bytes / (ms * 1e-3) / 1e9,
-                        "ms_per_layer": ms}
+        mean_touched = sum(touched[i % n_router] for i in range(steps)) / steps
+        gbs = mean_touched * expert_bytes / (ms * 1e-3) / 1e9
+        out[f"R{R}"] = {"touched_experts_mean": mean_touched, "touched_bytes_mean": mean_touched * expert_bytes,
+                        "gbs": gbs, "frac_of_hbm_peak": gbs / peaks()[0], "us_per_layer": ms * 1e3}
+    assert tf.workspace_status(ws) == tf.TF_DEV_OK
+    del layers
     return out
 
 
 def extra_decoder(tf, torch, steps=10):
-    """Synthetic 27B-class decoder (8 blocks + LM head): verify steps/s at R = 1 and 8."""
+    """Synthetic 27B-class decoder (8 blocks + LM head): verify steps/s at R = 1, 2, 4, 8, 16."""
     from w4_gemm_keyed_gb300 import decode
     V, H, F, L, G = 151936, 5120, 17408, 8, 64
     gen = torch.Generator(device="cuda")
@@ -496,7 +542,7 @@ def extra_decoder(tf, torch, steps=10):
     dec = decode.Decoder(model)
     step_bytes = L * (bytes_per_launch(H, 2 * F) + bytes_per_launch(F, H)) + bytes_per_launch(H, V)
     out = {"weight_bytes_per_step": step_bytes}
-    for R in (1, 8, 16):
+    for R in ROWS:
         dec.reset(1, 1)
         d = torch.zeros(16, dtype=torch.int32, device="cuda")
         for _ in range(2):
@@ -510,8 +556,9 @@ def extra_decoder(tf, torch, steps=10):
         b.record()
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / steps
-        out[f"R{R}"] = {"verify_steps_per_s": 1e3 / ms, "ms_per_step": ms,
-                        "gbs": step_bytes / (ms * 1e-3) / 1e9}
+        out[f"R{R}"] = {"verify_steps_per_s": 1e3 / ms, "rows_per_s": R * 1e3 / ms, "ms_per_step": ms,
+                        "gbs": step_bytes / (ms * 1e-3) / 1e9,
+                        "frac_of_hbm_peak": step_bytes / (ms * 1e-3) / 1e9 / peaks()[0]}
     out["decode"] = decode_loop(tf, torch, dec, V)
     return out
 
@@ -734,6 +781,10 @@ def main():
         ms = sum(v) / len(v)
         per_R[f"{K}x{N}_R{R}"] = {"us": ms * 1e3, "gbs": bytes_per_launch(K, N) / (ms * 1e-3) / 1e9,
                                   "frac": bytes_per_launch(K, N) / (ms * 1e-3) / 1e9 / peak}
+    per_graph = {}
+    for (K, N, R), us in sorted(time_per_r_graph(tf, torch, mats).items()):
+        gbs = bytes_per_launch(K, N) / us / 1e3
+        per_graph[f"{K}x{N}_R{R}"] = {"us": us, "gbs": gbs, "frac": gbs / peak}
 
     # ---- end to end through the C ABI with host buffers
     e2e_steps = max(10, args.steps // 4)
@@ -769,7 +820,11 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "traffic": recorded_traffic(), "kernel": "w4_lane_gemm_kernel<64,HI>"},
+            "per_r_device": per_graph,
+            "per_r_device_note": ("each (shape, R) as a CUDA graph of back-to-back launches over weight "
+                                  "copies > 3x L2; frac of the HBM peak above"),
             "per_launch": per_R,
+            "per_launch_note": "each launch timed alone with events: includes launch latency",
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": steps * launches_per_step,
             "clocks": clk.summary(),

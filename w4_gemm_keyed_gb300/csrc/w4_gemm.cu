@@ -21,6 +21,9 @@
 //           swizzle-aware ldmatrix and issues one mma.sync per 8 rows.  Each
 //           quantisation group's partial is formed in a fresh fp32 fragment and
 //           folded in as acc = fma(scale, partial, acc).
+// The grid signals its dependents at once (programmatic dependent launch): the
+// next launch in the stream lands on every SM this one frees and requests its
+// first weight stages before it waits for this grid to finish.
 // Why mma.sync and not tcgen05: the verify pass multiplies a weight tile by at
 // most 16 rows, so the MMA's N is 16.  A tcgen05.mma (M=128, K=16) was measured
 // on this part at ~153 cycles per instruction whatever its N (16..256), i.e.
@@ -52,11 +55,6 @@ constexpr uint32_t kBf16Magic = 0x43004300u;    // (128, 128): OR-ing u in gives
 __device__ __forceinline__ uint32_t word_of(const uint4 &q, int j) {
     return j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
 }
-
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 
 struct Sync {
     uint64_t full[kStages];
@@ -274,6 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
         fence_mbar_init();
     }
     __syncthreads();
+    // The next grid in the stream may start now: its CTAs land on every SM this
+    // grid frees and stream their first weight stages while it finishes.  It
+    // reads nothing this grid writes before its own grid_dependency_wait().
+    grid_launch_dependents();
 
     if (warp == kConsumerWarps) {
         // ---------------- producer ----------------
@@ -367,7 +369,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     int st = 0;  // stage counter, identical to the producer's
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int u = item / a.Pv, vp = item - u * a.Pv;
-    const bool last_item = item + int(gridDim.x) >= n_items;
     void *yb = static_cast<char *>(a.y) + (long long)u * a.y_stride * (long long)ysz;
     const unsigned i0 = split.start(vp);
     const int n_it = int(split.start(vp + 1) - i0);
@@ -400,7 +401,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
         }
         const unsigned seg_b = gi, seg_e = gi + unsigned(seg_len);
         j += seg_len;
-        if (j == n_it && last_item && warp == 0 && lane == 0) grid_launch_dependents();  // let the next grid start
 
         // ---- segment end: combine the k-groups in a fixed order, (0 + 1) + (2 + 3);
         // the four warps of feature block fw meet at their own named barrier
@@ -423,16 +423,16 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 acc[q >> 1][q & 1][3] += o.w;
             }
         };
-        named_bar_sync(1 + fw, 32 * kKGroups);
+        bar_sync_named(1 + fw, 32 * kKGroups);
         if (kg == 1) put_rb(rb_a);
         if (kg == 3) put_rb(rb_b);
-        named_bar_sync(1 + fw, 32 * kKGroups);
+        bar_sync_named(1 + fw, 32 * kKGroups);
         if (kg == 0) add_rb(rb_a);          // 0 + 1
         if (kg == 2) {
             add_rb(rb_b);                   // 2 + 3, written back over the slot it came from
             put_rb(rb_b);
         }
-        named_bar_sync(1 + fw, 32 * kKGroups);
+        bar_sync_named(1 + fw, 32 * kKGroups);
         if (kg == 0) {
             add_rb(rb_b);                   // (0 + 1) + (2 + 3)
             const unsigned tb = unsigned(t) * Kc, te = tb + Kc;
