@@ -15,8 +15,10 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - All pointers marked "dev" are CUDA device pointers owned by the caller.
- *   The library never allocates, frees or retains device memory; it keeps no
- *   global state besides a thread-local error message.
+ *   The library never allocates, frees or retains device memory, and it keeps
+ *   no global state besides a thread-local error message, with one exception:
+ *   tf_lane_gemm_w4_noalloc works on a fixed scratch array that the library
+ *   itself holds on every device that loads it (see that entry point).
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  Every compute call only enqueues work on that stream and returns;
  *   outputs are valid once the stream has reached that point.
@@ -194,8 +196,10 @@ TF_API tf_status tf_cast_bf16(const float *x, int32_t R, int32_t N, int32_t ldx,
  * nothing: its split-K scratch is a fixed 8 MiB array inside libtf, one copy
  * per device.
  *
- * - The first call on a device (made with that device current) looks up the
- *   array's address; make that first call before any stream capture.
+ * - Every call looks up the array's address on the current device (a
+ *   cudaGetSymbolAddress, no allocation), so the address stays right after a
+ *   device reset; the first call on a device loads the array there, so make
+ *   it before any stream capture.
  * - A launch whose scratch need exceeds the array (it grows with the device's
  *   SM count: 256 B + 256 KiB + 16 KiB per SM) returns TF_ERR_UNSUPPORTED and
  *   launches nothing.
@@ -241,6 +245,22 @@ TF_API size_t tf_keyed_sample_workspace_bytes(int32_t R, int32_t V);
 TF_API tf_status tf_keyed_sample(const float *logits, int32_t ldl, int32_t R, int32_t V, const tf_sampling *p,
                           uint64_t seed, const int64_t *pos, int32_t *tokens, void *ws,
                           size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * tf_keyed_hash -- the sampler's key and Gumbel noise for given triples
+ * ------------------------------------------------------------------------
+ * README, the two guarantees (keyed sampling): g is Gumbel noise derived from
+ * a hash of the seed, the position and the token id.  For i < n:
+ *   h[i] = sm(sm(sm(seed[i]) ^ (uint64)pos[i]) ^ (uint32)token[i])
+ *   g[i] = -ln(-ln u),  u = ((h[i] >> 11) + 0.5) / 2^53 in fp64
+ * computed by the same device functions tf_keyed_sample uses, so a caller can
+ * check the sampler's noise bit for bit.  seed dev uint64 [n], pos dev int64
+ * [n], token dev int32 [n]; h_out dev uint64 [n] and g_out dev fp64 [n] (either
+ * may be NULL).  n = 0 does nothing; n < 0 or a NULL input with n > 0 is
+ * TF_ERR_INVALID_ARG.
+ */
+TF_API tf_status tf_keyed_hash(const uint64_t *seed, const int64_t *pos, const int32_t *token, int64_t n,
+                               uint64_t *h_out, double *g_out, void *stream);
 
 /* ------------------------------------------------------------------------
  * tf_accept -- longest-prefix acceptance

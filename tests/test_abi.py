@@ -229,3 +229,28 @@ def test_stream_k_cut_formulas(T, Kc, Pv):
                 which = 0 if b[p] >= tb else 1
                 assert (p, which) not in slots
                 slots.add((p, which))
+
+
+def test_keyed_hash_validates_before_launching(lib):
+    from w4_gemm_keyed_gb300 import tf
+    assert lib.tf_keyed_hash(None, None, None, 0, None, None, None) == tf.TF_OK          # nothing to do
+    assert lib.tf_keyed_hash(256, 256, 256, -1, 256, 256, None) == tf.TF_ERR_INVALID_ARG
+    assert lib.tf_keyed_hash(None, 256, 256, 4, 256, 256, None) == tf.TF_ERR_INVALID_ARG
+    assert lib.tf_keyed_hash(256, 256, None, 4, 256, 256, None) == tf.TF_ERR_INVALID_ARG
+    assert b"null" in lib.tf_last_error()
+
+
+def test_binding_checks_output_shape_and_dtype(lib):
+    import torch
+    from w4_gemm_keyed_gb300 import tf
+    W = tf.W4Matrix(torch.zeros(tf.packed_bytes(256, 128, 64), dtype=torch.uint8), 256, 128, 64)
+    x = torch.zeros((4, 256), dtype=torch.int16)
+    for y, what in ((torch.zeros((4, 128), dtype=torch.float16), "float32"),   # 16-bit output
+                    (torch.zeros((3, 128), dtype=torch.float32), "rows"),      # fewer rows than R
+                    (torch.zeros((4, 64), dtype=torch.float32), "rows"),       # fewer columns than N
+                    (torch.zeros((128, 4), dtype=torch.float32).t(), "rows")):  # non-unit inner stride
+        with pytest.raises(tf.TFError) as e:
+            tf.lane_gemm_w4_noalloc(W, x, y)
+        assert e.value.status == tf.TF_ERR_INVALID_ARG
+    with pytest.raises(tf.TFError):
+        tf.lane_gemm_w4(W, torch.zeros((4, 128), dtype=torch.int16))          # x narrower than K

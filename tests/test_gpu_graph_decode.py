@@ -53,3 +53,17 @@ def test_graph_drafted_equals_serial(tf, tiny, R, p_match):
     if p_match == 1.0:
         assert all(a == R - 1 for a in lens[:-1])
     assert tf.workspace_status(tiny.ws) == tf.TF_DEV_OK
+
+
+@pytest.mark.parametrize("R,p_match", [(1, 0.0), (8, 0.75)])
+def test_graph_decode_matches_oracle_tokens(tf, tiny, R, p_match):
+    """The graph-replayed loop (serial and drafted) against the fp64 oracle decoder
+    on the same tiny model: identical committed tokens."""
+    from oracle import decoder as odec
+    from w4_gemm_keyed_gb300 import decode
+    T, k, p, seed, n = 0.7, 20, 0.95, 1236, 24
+    ref = odec.serial_decode(tiny_weights(), 11, n + 3 * R, T, k, p, seed)
+    table = draft_table(ref, p_match, 3000, seed, n + 8 * R + 2 * R) if R > 1 else None
+    graph, _ = decode.graph_decode(tiny, 11, n, R, T, k, p, seed, draft_table=table, passes_per_graph=4)
+    assert graph == ref[:n]
+    assert tf.workspace_status(tiny.ws) == tf.TF_DEV_OK

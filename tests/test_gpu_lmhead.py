@@ -55,7 +55,7 @@ def test_rows_are_invariant_to_R(tf, lmhead):
 
 @pytest.mark.parametrize("T,k,p", SETTINGS)
 @pytest.mark.parametrize("R", [1, 2, 4, 8, 16])
-def test_sample_and_accept_match_oracle(tf, lmhead, R, T, k, p):
+def test_sample_and_accept_match_oracle(tf, lmhead, near_tie, R, T, k, p):
     codes, scales, x, W, _ = lmhead
     rng = inputs.rng_for(301, R, int(T * 10), k)
     logits = tf.lane_gemm_w4(W, dev_bits16(x[:R]))
@@ -67,7 +67,7 @@ def test_sample_and_accept_match_oracle(tf, lmhead, R, T, k, p):
     for r in range(R):
         if tokens[r] != ref[r]:
             assert gaps[r] < 1e-9, f"row {r}: gpu {tokens[r]} oracle {ref[r]} gap {gaps[r]}"
-            print(f"near-tie row {r}: gap {gaps[r]:.3e}")
+            near_tie(f"LM head R={R} T={T} k={k} p={p} row {r}", gaps[r])
     if R > 1:
         drafts = inputs.noisy_drafts(rng, ref[:R - 1], 0.6, V)
         acc, bonus = tf.accept(torch.from_numpy(drafts).cuda(), torch.from_numpy(tokens.astype(np.int32)).cuda())

@@ -60,12 +60,23 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t z) {
     return z ^ (z >> 31);
 }
 
-__device__ __forceinline__ double gumbel(uint64_t seed, int64_t pos, int32_t token) {
+// Key of (seed, position, token id): sm(sm(sm(seed) ^ pos) ^ token), the
+// position as a 64-bit two's-complement word, the token id zero-extended.
+__device__ __forceinline__ uint64_t key_hash(uint64_t seed, int64_t pos, int32_t token) {
     uint64_t h = splitmix64(seed);
     h = splitmix64(h ^ static_cast<uint64_t>(pos));
-    h = splitmix64(h ^ static_cast<uint64_t>(static_cast<uint32_t>(token)));
+    return splitmix64(h ^ static_cast<uint64_t>(static_cast<uint32_t>(token)));
+}
+
+// Gumbel noise of a key: u = ((h >> 11) + 0.5) / 2^53 in fp64 (the top value
+// rounds to u = 1 and gives +inf), g = -ln(-ln u).
+__device__ __forceinline__ double gumbel_of_hash(uint64_t h) {
     const double u = (__ull2double_rn(h >> 11) + 0.5) * (1.0 / 9007199254740992.0);
     return -log(-log(u));
+}
+
+__device__ __forceinline__ double gumbel(uint64_t seed, int64_t pos, int32_t token) {
+    return gumbel_of_hash(key_hash(seed, pos, token));
 }
 
 struct Sel {
@@ -521,5 +532,26 @@ cudaError_t launch_accept(const int32_t *drafts, const int32_t *sampled, int R, 
 }
 
 int sample_max_vocab() { return kMaxChunks * kSampleChunk; }
+
+namespace {
+// The sampler's own key and Gumbel functions, evaluated for a list of
+// (seed, position, token) triples.
+__global__ void keyed_hash_kernel(const uint64_t *seed, const int64_t *pos, const int32_t *token, long long n,
+                                  uint64_t *h_out, double *g_out) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const uint64_t h = key_hash(seed[i], pos[i], token[i]);
+        if (h_out) h_out[i] = h;
+        if (g_out) g_out[i] = gumbel_of_hash(h);
+    }
+}
+}  // namespace
+
+cudaError_t launch_keyed_hash(const uint64_t *seed, const int64_t *pos, const int32_t *token, long long n,
+                              uint64_t *h_out, double *g_out, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const long long blocks = (n + 255) / 256;
+    keyed_hash_kernel<<<unsigned(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(seed, pos, token, n, h_out, g_out);
+    return cudaGetLastError();
+}
 
 }  // namespace tfk

@@ -40,4 +40,9 @@ int sample_max_vocab();
 cudaError_t launch_accept(const int32_t *drafts, const int32_t *sampled, int R, int32_t *accepted,
                           int32_t *bonus, int64_t *pos, cudaStream_t s);
 
+// Key and Gumbel noise of n (seed, position, token) triples, by the functions
+// the sampler uses (h_out or g_out may be null).
+cudaError_t launch_keyed_hash(const uint64_t *seed, const int64_t *pos, const int32_t *token, long long n,
+                              uint64_t *h_out, double *g_out, cudaStream_t s);
+
 }  // namespace tfk

@@ -5,7 +5,6 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
-#include <mutex>
 #include <string>
 
 #include "../../include/tf.h"
@@ -453,33 +452,20 @@ size_t tf_workspace_size(int32_t op, const int64_t *dims, int32_t n_dims) {
 
 // ---- tf_lane_gemm_w4_noalloc: the lane GEMM on library-owned scratch ----
 // The split-K status word, counters and partial tiles live in one fixed array
-// of this module instead of a caller workspace.  Each device has its own copy
-// of the array; its address is looked up once per device (with that device
-// current) and then reused.  All calls on a device share the copy.
+// of this module instead of a caller workspace.  Each device that loads the
+// library has its own copy; its device address is looked up on every call
+// (with the caller's device current), so a context rebuilt after a device
+// reset is never handed a stale address.  All calls on a device share the copy.
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
-constexpr int kNoAllocMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kNoAllocMaxDevices];
-
 tf_status noalloc_scratch(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "tf_lane_gemm_w4_noalloc: cudaGetDevice");
-    if (dev < 0 || dev >= kNoAllocMaxDevices)
-        return fail(TF_ERR_UNSUPPORTED, "tf_lane_gemm_w4_noalloc: device %d (at most %d devices)", dev,
-                    kNoAllocMaxDevices);
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "tf_lane_gemm_w4_noalloc: cudaGetSymbolAddress");
-        if (!p || !aligned(p, 256)) return fail(TF_ERR_CUDA, "tf_lane_gemm_w4_noalloc: scratch address unusable");
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "tf_lane_gemm_w4_noalloc: cudaGetSymbolAddress");
+    if (!p || !aligned(p, 256)) return fail(TF_ERR_CUDA, "tf_lane_gemm_w4_noalloc: scratch address unusable");
+    *out = p;
     return TF_OK;
 }
 }  // namespace
@@ -558,6 +544,16 @@ tf_status tf_keyed_sample(const float *logits, int32_t ldl, int32_t R, int32_t V
     }
     cudaError_t e = launch_keyed_sample(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tf_keyed_sample");
+    return ok();
+}
+
+tf_status tf_keyed_hash(const uint64_t *seed, const int64_t *pos, const int32_t *token, int64_t n, uint64_t *h_out,
+                        double *g_out, void *stream) {
+    if (n < 0) return fail(TF_ERR_INVALID_ARG, "n=%lld must be >= 0", (long long)n);
+    if (n == 0) return ok();
+    if (!seed || !pos || !token) return fail(TF_ERR_INVALID_ARG, "null seed, pos or token");
+    cudaError_t e = launch_keyed_hash(seed, pos, token, (long long)n, h_out, g_out, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_keyed_hash");
     return ok();
 }
 

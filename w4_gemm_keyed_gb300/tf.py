@@ -76,6 +76,7 @@ SIGNATURES = [
     ("tf_cast_bf16", ctypes.c_int, [P, I32, I32, I32, P, I32, P]),
     ("tf_keyed_sample_workspace_bytes", SZ, [I32, I32]),
     ("tf_keyed_sample", ctypes.c_int, [P, I32, I32, I32, ctypes.POINTER(SamplingC), ctypes.c_uint64, P, P, P, SZ, P]),
+    ("tf_keyed_hash", ctypes.c_int, [P, P, P, ctypes.c_int64, P, P, P]),
     ("tf_accept", ctypes.c_int, [P, P, I32, P, P, P]),
     ("tf_gather_drafts", ctypes.c_int, [P, ctypes.c_int64, P, I32, P, P]),
     ("tf_commit_tokens", ctypes.c_int, [P, P, P, P, ctypes.c_int64, P]),
@@ -219,13 +220,33 @@ def lane_gemm_workspace_bytes(K: int, N: int, group: int) -> int:
     return int(load().tf_lane_gemm_workspace_bytes(K, N, group))
 
 
+def _check_rows_in(x: torch.Tensor, K: int):
+    """x: CUDA bf16 (or int16 bits) [R][>= K] with unit inner stride."""
+    if x.dim() != 2 or x.dtype not in (torch.bfloat16, torch.int16):
+        raise TFError(TF_ERR_INVALID_ARG, f"x must be a 2-D bf16 / int16 tensor, got {tuple(x.shape)} {x.dtype}")
+    if x.stride(1) != 1 or x.shape[1] < K:
+        raise TFError(TF_ERR_INVALID_ARG, f"x must have unit inner stride and >= {K} columns")
+
+
+def _check_rows_out(y: torch.Tensor, R: int, N: int, device, dtype=torch.float32):
+    """y: CUDA tensor of `dtype` [>= R][>= N] with unit inner stride on x's device."""
+    if y.dim() != 2 or y.dtype != dtype:
+        raise TFError(TF_ERR_INVALID_ARG, f"y must be a 2-D {dtype} tensor, got {tuple(y.shape)} {y.dtype}")
+    if not y.is_cuda or y.device != device:
+        raise TFError(TF_ERR_INVALID_ARG, f"y must be on {device}, got {y.device}")
+    if y.shape[0] < R or y.shape[1] < N or y.stride(1) != 1:
+        raise TFError(TF_ERR_INVALID_ARG, f"y must hold >= {R} rows of >= {N} columns with unit inner stride")
+
+
 def lane_gemm_w4(W: W4Matrix, x: torch.Tensor, y: torch.Tensor = None, ws: torch.Tensor = None,
                  stream=None) -> torch.Tensor:
     """y[R][N] fp32 = W4 linear of bf16 rows x[R][K] (x may be bf16 or int16 bits)."""
     lib = load()
+    _check_rows_in(x, W.K)
     R = x.shape[0]
     if y is None:
         y = torch.empty((R, W.N), dtype=torch.float32, device=x.device)
+    _check_rows_out(y, R, W.N, x.device)
     if ws is None:
         ws = workspace(lane_gemm_workspace_bytes(W.K, W.N, W.group), x.device)
     wc = W.c()
@@ -240,7 +261,11 @@ def lane_gemm_w4_noalloc(W: W4Matrix, x: torch.Tensor, y: torch.Tensor, status: 
     memory, so the output y[R][N] fp32 must be given.  status: optional device int32
     (zeroed by the caller) that receives a device-side error code."""
     lib = load()
+    _check_rows_in(x, W.K)
     R = x.shape[0]
+    _check_rows_out(y, R, W.N, x.device)
+    if status is not None and (status.dtype != torch.int32 or status.device != x.device or status.numel() < 1):
+        raise TFError(TF_ERR_INVALID_ARG, "status must be a CUDA int32 tensor on x's device")
     wc = W.c()
     _check(lib.tf_lane_gemm_w4_noalloc(ctypes.byref(wc), _ptr(x), x.stride(0), R, _ptr(y), y.stride(0),
                                        _ptr(status), _stream(stream)))
@@ -285,6 +310,21 @@ def keyed_sample(logits: torch.Tensor, temperature: float, top_k: int, top_p: fl
     _check(lib.tf_keyed_sample(_ptr(logits), logits.stride(0), R, V, ctypes.byref(sp), ctypes.c_uint64(seed & (2**64 - 1)),
                                _ptr(pos), _ptr(tokens), _ptr(ws), ws.numel(), _stream(stream)))
     return tokens
+
+
+def keyed_hash(seed: torch.Tensor, pos: torch.Tensor, token: torch.Tensor, stream=None):
+    """(h uint64 bits as int64, g fp64) of the sampler's key and Gumbel noise for
+    device triples seed (int64 holding uint64 bits), pos int64, token int32."""
+    n = seed.numel()
+    if pos.numel() != n or token.numel() != n:
+        raise TFError(TF_ERR_INVALID_ARG, "seed, pos and token must have the same length")
+    for t, dt in ((seed, torch.int64), (pos, torch.int64), (token, torch.int32)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise TFError(TF_ERR_INVALID_ARG, f"expected a contiguous {dt} tensor, got {t.dtype}")
+    h = torch.empty(n, dtype=torch.int64, device=seed.device)
+    g = torch.empty(n, dtype=torch.float64, device=seed.device)
+    _check(load().tf_keyed_hash(_ptr(seed), _ptr(pos), _ptr(token), n, _ptr(h), _ptr(g), _stream(stream)))
+    return h, g
 
 
 def accept(drafts: torch.Tensor, sampled: torch.Tensor, accepted: torch.Tensor = None,
