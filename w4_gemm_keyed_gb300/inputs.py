@@ -113,6 +113,27 @@ def mlx_affine_weights(rng: np.random.Generator, K: int, N: int, group: int):
     return words, bf16_bits_from_f32(s), bf16_bits_from_f32(b)
 
 
+def nvfp4_weights(rng: np.random.Generator, K: int, N: int, min_scale_exp: int = 8):
+    """(codes uint8 [N][K/2], block-scale bytes uint8 [N][K/16], global scale).
+
+    Two 4-bit E2M1 codes per byte, each of the 16 patterns equally likely
+    (element 2j in the low nibble); one positive E4M3 scale byte per 16
+    elements with its exponent field uniform in [min_scale_exp, 15] and its
+    mantissa uniform in [0, 7], the one NaN pattern (0x7F) redrawn as 0x7E;
+    global scale 2^-15.  With the default exponents the block scales span
+    [2, 448] and the weights about 2^-15 .. 2^-3.5, the spread of a
+    checkpoint quantised from N(0, 0.02)-sized weights.
+    """
+    if K % 16:
+        raise ValueError("K must be a multiple of 16")
+    codes = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    e = rng.integers(min_scale_exp, 16, size=(N, K // 16), dtype=np.uint8)
+    m = rng.integers(0, 8, size=(N, K // 16), dtype=np.uint8)
+    scales = (e << np.uint8(3)) | m
+    scales[scales == 0x7F] = 0x7E
+    return codes, scales, 2.0 ** -15
+
+
 def logits_normal(rng: np.random.Generator, R: int, V: int, std: float = 3.0) -> np.ndarray:
     """float32 logits N(0, std^2) of shape [R][V]."""
     return (rng.standard_normal((R, V), dtype=np.float32) * np.float32(std)).astype(np.float32)
