@@ -413,6 +413,44 @@ def extra_affine(tf, torch, steps=30):
     return out
 
 
+def extra_nvfp4(tf, torch, steps=30):
+    """NVFP4 weights (E2M1 codes, E4M3 scale per 16 features, fp32 tensor scale)
+    on the 5120 -> 17408 projection, R = 1 / 8 / 16: GB/s over codes + scale
+    bytes, weights rotating over copies larger than L2, CUDA-graph replay."""
+    from w4_gemm_keyed_gb300 import inputs
+    K, N = 5120, 17408
+    nbytes = K * N // 2 + K * N // 16
+    n_copies = max(3, -(-3 * L2_BYTES // nbytes))
+    rng = inputs.rng_for(10)
+    codes, scales, gs = inputs.nvfp4_weights(rng, K, N)
+    dc, ds = torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda()
+    copies = [tf.pack_nvfp4(dc, ds, gs) for _ in range(n_copies)]
+    x = torch.from_numpy(inputs.bf16_normal(rng, (16, K)).view(np.int16)).cuda()
+    y = torch.empty((16, N), device="cuda")
+    ws = tf.workspace(int(tf.load().tf_lane_gemm_nvfp4_workspace_bytes(K, N)))
+    out = {"bytes_per_launch": nbytes}
+    for R in (1, 8, 16):
+        xv, yv = x[:R], y[:R]
+        for c in copies:
+            tf.lane_gemm_nvfp4(c, xv, y=yv, ws=ws)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for c in copies:
+                tf.lane_gemm_nvfp4(c, xv, y=yv, ws=ws)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (steps * n_copies)
+        out[f"R{R}"] = {"us_per_launch": us, "gbs": nbytes / us / 1e3, "frac_of_hbm_peak": nbytes / us / 1e3 / peaks()[0]}
+    return out
+
+
 def attention_bytes(ctx, R, n_kv=8, group=8):
     """Algorithmic bytes of one verify attention call over ctx cached positions:
     K and V entries 0..ctx-1 (bf16), the bf16 queries and the fp32 outputs."""
@@ -718,7 +756,7 @@ def main():
     ap.add_argument("--impl", default="tf", choices=["tf", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the LM-head / MoE / decoder side measurements")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--only", choices=["lmhead", "dense", "moe", "decoder", "affine", "attention"],
+    ap.add_argument("--only", choices=["lmhead", "dense", "moe", "decoder", "affine", "attention", "nvfp4"],
                     help="run one workload briefly and print its timings (for profiler captures)")
     ap.add_argument("--ctx", type=int, nargs="*", help="with --only attention: cached positions to time")
     ap.add_argument("--rows", type=int, nargs="*", help="with --only attention: verify rows R to time")
@@ -740,7 +778,7 @@ def main():
             out = {"dense_gbs": STEP_BYTES * steps / secs / 1e9}
         else:
             fn = {"lmhead": extra_lmhead, "moe": extra_moe, "decoder": extra_decoder, "affine": extra_affine,
-                  "attention": extra_attention}[args.only]
+                  "attention": extra_attention, "nvfp4": extra_nvfp4}[args.only]
             kw = {}
             if args.only == "attention" and args.ctx:
                 kw["ctxs"] = tuple(args.ctx)
@@ -797,7 +835,8 @@ def main():
     extra = {}
     if rank == 0 and not args.no_extra:
         for name, fn in (("lmhead_sampler", extra_lmhead), ("moe30b", extra_moe), ("decoder", extra_decoder),
-                         ("affine_5120x17408", extra_affine), ("attention_kv", extra_attention)):
+                         ("affine_5120x17408", extra_affine), ("nvfp4_5120x17408", extra_nvfp4),
+                         ("attention_kv", extra_attention)):
             try:
                 extra[name] = fn(tf, torch)
             except Exception as exc:  # a side measurement must not hide the headline line

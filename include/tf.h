@@ -123,11 +123,50 @@ TF_API size_t tf_w4_packed_bytes(int32_t K, int32_t N, int32_t group);
  * accept it: each group's partial sum_k q x is scaled, and the bias is added
  * times the group's activation sum sum_k x (fp32, formed by the tensor core),
  * bits of row r still independent of R.  The MoE and decoder entry points take
- * symmetric matrices only.  Group 32 with R > 8 runs a 3-stage pipeline. */
+ * symmetric matrices only. */
 TF_API size_t tf_w4_affine_packed_bytes(int32_t K, int32_t N, int32_t group);
 TF_API tf_status tf_pack_w4_affine(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
                                    int32_t K, int32_t N, int32_t group, void *packed, size_t packed_bytes,
                                    void *stream);
+
+/* ------------------------------------------------------------------------
+ * NVFP4 weights and their lane GEMM
+ * ------------------------------------------------------------------------
+ * Context Studios, "TensorFold: The engine that makes local LLMs 2-3x faster":
+ * the engine reads NVFP4 checkpoints on Blackwell.  The pages do not give the
+ * format; this follows NVIDIA's public description of NVFP4:
+ *   codes  uint8 [N][K/2]   4-bit E2M1 codes (bit 3 sign, bits 2..1 exponent
+ *                           with bias 1, bit 0 mantissa; values 0, 0.5, 1,
+ *                           1.5, 2, 3, 4, 6 and negatives), element 2j in the
+ *                           low nibble of byte j;
+ *   scales uint8 [N][K/16]  E4M3 bit pattern of the scale of the 16 features
+ *                           16b .. 16b + 15 of row n (NaN pattern 0x7F/0xFF
+ *                           not allowed);
+ *   global_scale            fp32, one per tensor;
+ *   w[n][k] = e2m1(n, k) * e4m3(n, k / 16) * global_scale.
+ * tf_pack_nvfp4 repacks (codes, scales) into `packed` (dev, 256-B aligned,
+ * tf_nvfp4_packed_bytes(K, N) bytes; K a positive multiple of 64, N >= 1).
+ * tf_lane_gemm_nvfp4 computes y[r][n] = sum_k w[n][k] x[r][k] with the same
+ * argument conventions, workspace rules and row invariance as
+ * tf_lane_gemm_w4.  Arithmetic: each weight times its block scale is formed
+ * exactly in fp16, the activations are taken to fp16 (exact for bf16 values
+ * with |x| <= 65504; larger values overflow to inf, values below 2^-14 round
+ * to fp16 subnormals), products accumulate in fp32 in a fixed k order, and
+ * the output is multiplied by global_scale once.
+ */
+typedef struct tf_nvfp4_matrix {
+    const void *packed;   /* dev, tf_nvfp4_packed_bytes(K, N) bytes, 256-B aligned */
+    int32_t K;            /* input features, a positive multiple of 64 */
+    int32_t N;            /* output features, >= 1 */
+    float global_scale;   /* the tensor's fp32 scale, finite */
+} tf_nvfp4_matrix;
+
+TF_API size_t tf_nvfp4_packed_bytes(int32_t K, int32_t N);
+TF_API tf_status tf_pack_nvfp4(const uint8_t *codes, const uint8_t *scales, int32_t K, int32_t N, void *packed,
+                               size_t packed_bytes, void *stream);
+TF_API size_t tf_lane_gemm_nvfp4_workspace_bytes(int32_t K, int32_t N);
+TF_API tf_status tf_lane_gemm_nvfp4(const tf_nvfp4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R, float *y,
+                                    int32_t ldy, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Repack canonical codes + scales (dev) into the kernel layout `packed` (dev,

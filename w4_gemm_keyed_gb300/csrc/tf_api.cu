@@ -110,7 +110,8 @@ GemmArgs dense_args(const tf_w4_matrix &W, int R, void *y, int ldy, int mode) {
     a.K = W.K;
     a.N = W.N;
     a.G = W.group;
-    a.affine = W.affine;
+    a.fmt = W.affine ? kFmtAffine : kFmtSym;
+    a.gscale = 1.0f;
     a.T = (W.N + kTileN - 1) / kTileN;
     a.Kc = W.K / kKChunk;
     a.Pv = dense_pv(a.T, a.Kc);
@@ -280,7 +281,7 @@ const char *tf_status_string(tf_status s) {
     return "unknown status";
 }
 
-int tf_version(void) { return 200; }  // 0.2.0: KV-cache attention, affine W4, self-check, cast, accumulate
+int tf_version(void) { return 300; }  // 0.3.0: NVFP4 lane GEMM, device key hash
 
 int32_t tf_device_sm_count(void) { return device_sm_count(); }
 
@@ -333,6 +334,52 @@ tf_status tf_pack_w4_gate_up(const uint8_t *codes, const uint16_t *scales, int32
                              void *packed, size_t packed_bytes_, void *stream) {
     if (ffn <= 0) return fail(TF_ERR_INVALID_ARG, "ffn must be >= 1");
     return pack_common(codes, scales, K, 2 * ffn, group, packed, packed_bytes_, stream, true);
+}
+
+size_t tf_nvfp4_packed_bytes(int32_t K, int32_t N) { return packed_bytes(K, N, 16, kFmtNvfp4); }
+
+tf_status tf_pack_nvfp4(const uint8_t *codes, const uint8_t *scales, int32_t K, int32_t N, void *packed, size_t bytes,
+                        void *stream) {
+    if (!codes || !scales || !packed) return fail(TF_ERR_INVALID_ARG, "null pointer");
+    if (tf_nvfp4_packed_bytes(K, N) == 0) return fail(TF_ERR_UNSUPPORTED, "unsupported shape K=%d N=%d", K, N);
+    if (!aligned(packed, 256)) return fail(TF_ERR_INVALID_ARG, "packed buffer not 256-B aligned");
+    if (bytes < tf_nvfp4_packed_bytes(K, N)) return fail(TF_ERR_INVALID_ARG, "packed buffer too small");
+    cudaError_t e = launch_pack_nvfp4(codes, scales, K, N, packed, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tf_pack_nvfp4");
+    return ok();
+}
+
+size_t tf_lane_gemm_nvfp4_workspace_bytes(int32_t K, int32_t N) {
+    if (tf_nvfp4_packed_bytes(K, N) == 0) return 0;
+    const int T = (N + kTileN - 1) / kTileN;
+    return gemm_workspace_bytes(K, N, 16, 1, dense_pv(T, K / kKChunk));
+}
+
+tf_status tf_lane_gemm_nvfp4(const tf_nvfp4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R, float *y,
+                             int32_t ldy, void *ws, size_t ws_bytes, void *stream) {
+    if (!W || !W->packed) return fail(TF_ERR_INVALID_ARG, "W: null matrix or packed pointer");
+    if (!aligned(W->packed, 256)) return fail(TF_ERR_INVALID_ARG, "W: packed pointer not 256-B aligned");
+    if (tf_nvfp4_packed_bytes(W->K, W->N) == 0)
+        return fail(TF_ERR_UNSUPPORTED, "W: K=%d must be a positive multiple of 64 and N=%d >= 1", W->K, W->N);
+    if (!std::isfinite(W->global_scale)) return fail(TF_ERR_INVALID_ARG, "W: global_scale must be finite");
+    if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
+    if (!x || !aligned(x, 16)) return fail(TF_ERR_INVALID_ARG, "x must be non-null and 16-B aligned");
+    if (ldx < W->K || ldx % 8) return fail(TF_ERR_INVALID_ARG, "ldx=%d must be >= K and a multiple of 8", ldx);
+    if (!y || !aligned(y, 4)) return fail(TF_ERR_INVALID_ARG, "y must be non-null and 4-B aligned");
+    if (ldy < W->N) return fail(TF_ERR_INVALID_ARG, "ldy=%d must be >= N", ldy);
+    tf_status st = check_ws(ws, ws_bytes, tf_lane_gemm_nvfp4_workspace_bytes(W->K, W->N));
+    if (st) return st;
+    if (size_t((W->N + kTileN - 1) / kTileN) * kFeatWarps > kMaxCounters)
+        return fail(TF_ERR_UNSUPPORTED, "N=%d too large for the split-K counter region", W->N);
+    tf_w4_matrix M{W->packed, W->K, W->N, 64, 0};
+    GemmArgs a = dense_args(M, R, y, ldy, kStoreF32);
+    a.G = 16;
+    a.fmt = kFmtNvfp4;
+    a.gscale = W->global_scale;
+    const char *why = "";
+    cudaError_t e = bind_and_launch(a, x, ldx, 0, 1, ws, static_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess) return fail(TF_ERR_CUDA, "tf_lane_gemm_nvfp4: %s (%s)", cudaGetErrorString(e), why);
+    return ok();
 }
 
 size_t tf_lane_gemm_workspace_bytes(int32_t K, int32_t N, int32_t group) {

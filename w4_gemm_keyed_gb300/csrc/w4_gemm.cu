@@ -178,7 +178,85 @@ __device__ __forceinline__ void consume_slice(const uint8_t *blk, uint32_t xslic
     }
 }
 
+// NVFP4 helpers.  e2m1x2 / e4m3x2: the low nibble (byte) goes to the low
+// fp16 half, the high one to the high half.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&a)[4]) {
+    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\tmov.b32 {t0, t1, t2, t3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, t0;\n\tcvt.rn.f16x2.e2m1x2 %1, t1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, t2;\n\tcvt.rn.f16x2.e2m1x2 %3, t3;\n\t}"
+        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+        : "r"(w));
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t s16) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(s16));
+    return d;
+}
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// bf16 pair -> fp16 pair (exact within the fp16 range; larger values overflow to inf)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t b) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(__uint_as_float(b & 0xFFFF0000u)), "f"(__uint_as_float(b << 16)));
+    return d;
+}
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One 64-wide k slice of NVFP4 weights for this warp's 32-row feature block.
+// Each 16-wide k step is one scale block: the E2M1 codes become exact fp16
+// values and are multiplied by their rows' E4M3 block scales (the product has
+// at most 6 significant bits and stays a normal fp16: exact), so the MMA adds
+// sum_k w x straight into the fp32 accumulator; the tensor scale is applied
+// once at the store.  Activations are taken to fp16 (exact within its range).
+// Rows 0..7 run the identical instruction sequence whatever R is.
+template <bool HI>
+__device__ __forceinline__ void consume_slice_nvfp4(const uint8_t *blk, uint32_t xslice, int lane, int gq,
+                                                    const uint32_t (&xoff)[4], float (&acc)[2][2][4]) {
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + lane * 16);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 512 + lane * 16);
+    const uint4 sc = *reinterpret_cast<const uint4 *>(blk + 1024 + gq * 16);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t xa = xslice + xoff[j];
+        uint32_t b0, b1, b2 = 0, b3 = 0;
+        if (HI)
+            ldsm_x4(xa, b0, b1, b2, b3);
+        else
+            ldsm_x2(xa, b0, b1);
+        b0 = bf16x2_to_f16x2(b0);
+        b1 = bf16x2_to_f16x2(b1);
+        if (HI) {
+            b2 = bf16x2_to_f16x2(b2);
+            b3 = bf16x2_to_f16x2(b3);
+        }
+        const uint32_t sw = word_of(sc, j);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            const uint32_t s2 = e4m3x2_to_f16x2(mt ? (sw >> 16) : (sw & 0xFFFFu));   // (s[row g], s[row g+8])
+            const uint32_t sg = __byte_perm(s2, 0, 0x1010), sg8 = __byte_perm(s2, 0, 0x3232);
+            uint32_t af[4];
+            e2m1x8_to_f16x2(word_of(mt ? q1 : q0, j), af);
+            af[0] = mul_f16x2(af[0], sg);
+            af[1] = mul_f16x2(af[1], sg8);
+            af[2] = mul_f16x2(af[2], sg);
+            af[3] = mul_f16x2(af[3], sg8);
+            mma_f16_16816(acc[mt][0], af, b0, b1);
+            if (HI) mma_f16_16816(acc[mt][1], af, b2, b3);
+        }
+    }
+}
+
 __device__ __forceinline__ void put(const GemmArgs &a, void *yb, int r, int f, float v) {
+    if (a.fmt == kFmtNvfp4) v *= a.gscale;   // the NVFP4 tensor scale, once per output
     float *y = static_cast<float *>(yb) + (long long)r * a.ldy + f;
     if (a.mode == kAccumulateF32)
         *y = *y + v;
@@ -229,12 +307,13 @@ __device__ __forceinline__ void store_block(const GemmArgs &a, void *yb, int t, 
     }
 }
 
-template <int G, bool HI, bool AFF>
+template <int G, bool HI, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_constant__ GemmArgs a) {
-    constexpr int BB = block_bytes(G, AFF);
-    constexpr int CB = chunk_bytes(G, AFF);
+    constexpr bool AFF = FMT == kFmtAffine;
+    constexpr int BB = block_bytes(G, FMT);
+    constexpr int CB = chunk_bytes(G, FMT);
     constexpr int STW = kStageIters * CB;
-    constexpr int NS = num_stages(G, HI, AFF);
+    constexpr int NS = num_stages(G, HI, FMT);
     constexpr int XSL = x_slice_bytes(HI);
     constexpr int XST = x_stage_bytes(HI);
     constexpr int NQ = lane_vals(HI) / 4;   // float4 per lane in the combine and the fixup
@@ -388,12 +467,21 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                 const int p0 = (kg - (j + sj)) & (kKGroups - 1);
                 if (!HI && n_here == kStageIters) {
 #pragma unroll
-                    for (int p = 0; p < kStageIters; p += kKGroups)
-                        consume_slice<G, HI, AFF>(stage_w + (p0 + p) * CB, stage_x + (p0 + p) * XSL, lane, gq,
-                                             xoff, acc);
+                    for (int p = 0; p < kStageIters; p += kKGroups) {
+                        if constexpr (FMT == kFmtNvfp4)
+                            consume_slice_nvfp4<HI>(stage_w + (p0 + p) * CB, stage_x + (p0 + p) * XSL, lane, gq, xoff,
+                                                    acc);
+                        else
+                            consume_slice<G, HI, AFF>(stage_w + (p0 + p) * CB, stage_x + (p0 + p) * XSL, lane, gq,
+                                                      xoff, acc);
+                    }
                 } else {
-                    for (int p = p0; p < n_here; p += kKGroups)
-                        consume_slice<G, HI, AFF>(stage_w + p * CB, stage_x + p * XSL, lane, gq, xoff, acc);
+                    for (int p = p0; p < n_here; p += kKGroups) {
+                        if constexpr (FMT == kFmtNvfp4)
+                            consume_slice_nvfp4<HI>(stage_w + p * CB, stage_x + p * XSL, lane, gq, xoff, acc);
+                        else
+                            consume_slice<G, HI, AFF>(stage_w + p * CB, stage_x + p * XSL, lane, gq, xoff, acc);
+                    }
                 }
             }
             __syncwarp();
@@ -684,16 +772,80 @@ cudaError_t launch_pack_affine_g(const uint32_t *codes, const uint16_t *scales, 
     return cudaGetLastError();
 }
 
-template <int G, bool HI, bool AFF>
+// NVFP4 packing: same chunk geometry.  Byte i of word j of a lane's 16-byte
+// entry is its A register i for k step j: the canonical byte of row (g or
+// g + 8) holding elements k, k + 1 (k = 16 j + 2 q (+ 8)), low nibble first --
+// exactly the canonical storage byte.  Rows past N get code 0 and scale 0.
+__global__ void pack_codes_nvfp4_kernel(const uint8_t *codes, int K, int N, uint8_t *out, long long n_entries,
+                                        int Kc) {
+    constexpr int BB = block_bytes(16, kFmtNvfp4);
+    constexpr int CB = chunk_bytes(16, kFmtNvfp4);
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n_entries) return;
+    const int lane = int(idx % 32);
+    long long r = idx / 32;
+    const int mt = int(r % 2);
+    r /= 2;
+    const int fw = int(r % kFeatWarps);
+    r /= kFeatWarps;
+    const int kc = int(r % Kc);
+    const long long t = r / Kc;
+    const int gq = lane >> 2, tq = lane & 3;
+    uint32_t words[4];
+    for (int j = 0; j < 4; ++j) {
+        uint32_t w = 0;
+        for (int i = 0; i < 4; ++i) {
+            const long long f = t * kTileN + fw * kBlockRows + mt * 16 + gq + ((i & 1) ? 8 : 0);
+            const int k = kc * kKChunk + j * 16 + 2 * tq + ((i & 2) ? 8 : 0);
+            const uint32_t byte = f < N ? codes[f * (K / 2) + k / 2] : 0u;
+            w |= byte << (8 * i);
+        }
+        words[j] = w;
+    }
+    uint8_t *dst = out + (t * Kc + kc) * (long long)CB + fw * BB + mt * 512 + lane * 16;
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+}
+
+// Scale entry of (tile t, slice kc, feature block fw, lane group g): 16 bytes
+// [j 0..3][mt 0..1] (s[row g][4 kc + j], s[row g + 8][4 kc + j]).
+__global__ void pack_scales_nvfp4_kernel(const uint8_t *scales, int K, int N, uint8_t *out, long long n_entries,
+                                         int Kc) {
+    constexpr int BB = block_bytes(16, kFmtNvfp4);
+    constexpr int CB = chunk_bytes(16, kFmtNvfp4);
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n_entries) return;
+    const int g = int(idx % 8);
+    long long r = idx / 8;
+    const int fw = int(r % kFeatWarps);
+    r /= kFeatWarps;
+    const int kc = int(r % Kc);
+    const long long t = r / Kc;
+    const int nb = K / 16;
+    uint32_t words[4];
+    for (int j = 0; j < 4; ++j) {
+        uint32_t w = 0;
+        for (int mt = 0; mt < 2; ++mt)
+            for (int h = 0; h < 2; ++h) {
+                const long long f = t * kTileN + fw * kBlockRows + mt * 16 + g + (h ? 8 : 0);
+                const uint32_t b = f < N ? scales[f * nb + kc * 4 + j] : 0u;
+                w |= b << (8 * (mt * 2 + h));
+            }
+        words[j] = w;
+    }
+    uint8_t *dst = out + (t * Kc + kc) * (long long)CB + fw * BB + 1024 + g * 16;
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+}
+
+template <int G, bool HI, int FMT>
 cudaError_t launch_gemm_g(const GemmArgs &a, int u_max, cudaStream_t s) {
-    const size_t smem = gemm_smem_bytes(G, HI, AFF);
+    const size_t smem = gemm_smem_bytes(G, HI, FMT);
     // the shared-memory opt-in is a per-device property of the kernel: set it once
     static std::atomic<bool> opted_in[kMaxDevices];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
-        err = cudaFuncSetAttribute(w4_lane_gemm_kernel<G, HI, AFF>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        err = cudaFuncSetAttribute(w4_lane_gemm_kernel<G, HI, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (err != cudaSuccess) return err;
         if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
     }
@@ -711,7 +863,7 @@ cudaError_t launch_gemm_g(const GemmArgs &a, int u_max, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, w4_lane_gemm_kernel<G, HI, AFF>, a);
+    return cudaLaunchKernelEx(&cfg, w4_lane_gemm_kernel<G, HI, FMT>, a);
 }
 
 template <int G>
@@ -785,12 +937,16 @@ bool gemm_encode_x(GemmArgs &a, const uint16_t *x, int ldx, long long x_stride, 
 
 cudaError_t launch_w4_gemm(const GemmArgs &a, int u_max, cudaStream_t s) {
     const bool hi = a.R > 8;
-    if (a.affine) {
-        if (hi) return a.G == 64 ? launch_gemm_g<64, true, true>(a, u_max, s) : launch_gemm_g<32, true, true>(a, u_max, s);
-        return a.G == 64 ? launch_gemm_g<64, false, true>(a, u_max, s) : launch_gemm_g<32, false, true>(a, u_max, s);
+    if (a.fmt == kFmtNvfp4) return hi ? launch_gemm_g<16, true, kFmtNvfp4>(a, u_max, s)
+                                      : launch_gemm_g<16, false, kFmtNvfp4>(a, u_max, s);
+    if (a.fmt == kFmtAffine) {
+        if (hi) return a.G == 64 ? launch_gemm_g<64, true, kFmtAffine>(a, u_max, s)
+                                 : launch_gemm_g<32, true, kFmtAffine>(a, u_max, s);
+        return a.G == 64 ? launch_gemm_g<64, false, kFmtAffine>(a, u_max, s)
+                         : launch_gemm_g<32, false, kFmtAffine>(a, u_max, s);
     }
-    if (hi) return a.G == 64 ? launch_gemm_g<64, true, false>(a, u_max, s) : launch_gemm_g<32, true, false>(a, u_max, s);
-    return a.G == 64 ? launch_gemm_g<64, false, false>(a, u_max, s) : launch_gemm_g<32, false, false>(a, u_max, s);
+    if (hi) return a.G == 64 ? launch_gemm_g<64, true, kFmtSym>(a, u_max, s) : launch_gemm_g<32, true, kFmtSym>(a, u_max, s);
+    return a.G == 64 ? launch_gemm_g<64, false, kFmtSym>(a, u_max, s) : launch_gemm_g<32, false, kFmtSym>(a, u_max, s);
 }
 
 cudaError_t launch_pack_w4_affine(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases, int K, int N,
@@ -803,6 +959,20 @@ cudaError_t launch_pack_w4(const uint8_t *codes, const uint16_t *scales, int K, 
                            bool interleave_gate_up, cudaStream_t s) {
     return G == 64 ? launch_pack_g<64>(codes, scales, K, N, packed, interleave_gate_up, s)
                    : launch_pack_g<32>(codes, scales, K, N, packed, interleave_gate_up, s);
+}
+
+cudaError_t launch_pack_nvfp4(const uint8_t *codes, const uint8_t *scales, int K, int N, void *packed,
+                              cudaStream_t s) {
+    const int T = (N + kTileN - 1) / kTileN;
+    const int Kc = K / kKChunk;
+    const long long n_codes = (long long)T * Kc * kFeatWarps * 2 * 32;
+    const long long n_scales = (long long)T * Kc * kFeatWarps * 8;
+    const int th = 256;
+    pack_codes_nvfp4_kernel<<<unsigned((n_codes + th - 1) / th), th, 0, s>>>(codes, K, N, (uint8_t *)packed, n_codes,
+                                                                           Kc);
+    pack_scales_nvfp4_kernel<<<unsigned((n_scales + th - 1) / th), th, 0, s>>>(scales, K, N, (uint8_t *)packed,
+                                                                             n_scales, Kc);
+    return cudaGetLastError();
 }
 
 int device_sm_count() {

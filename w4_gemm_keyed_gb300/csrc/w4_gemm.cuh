@@ -42,24 +42,32 @@ constexpr int kLaneAccHi = 16;             // fp32 accumulators per lane: 2 sub-
 // rows 8..15 (accumulator half n = 1) only when the launch has them
 __host__ __device__ constexpr int lane_vals(bool hi) { return hi ? kLaneAccHi : kLaneAccHi / 2; }
 
+// Weight formats of a packed matrix.
+enum WeightFormat : int {
+    kFmtSym = 0,     // symmetric int4 codes, one fp16 scale per (row, group of G)
+    kFmtAffine = 1,  // MLX-style affine: unsigned codes, bf16 scale and bias per (row, group of G)
+    kFmtNvfp4 = 2,   // NVFP4: E2M1 codes, one E4M3 scale per (row, 16 features), fp32 tensor scale
+};
 // Affine (MLX-style) blocks also carry one bf16 bias per row and group after the
-// bf16 scales: [grp][scales 64 B][biases 64 B].
-__host__ __device__ constexpr int block_bytes(int G, bool aff = false) {
-    return 1024 + (aff ? 128 : 64) * (kKChunk / G);
+// bf16 scales: [grp][scales 64 B][biases 64 B].  NVFP4 blocks carry the E4M3
+// scale bytes of the block's four 16-wide k steps: [g 0..7][j 0..3][mt 0..1]
+// (s[row g], s[row g+8]), 128 B.
+__host__ __device__ constexpr int block_bytes(int G, int fmt = kFmtSym) {
+    return fmt == kFmtNvfp4 ? 1024 + 128 : 1024 + (fmt == kFmtAffine ? 128 : 64) * (kKChunk / G);
 }
-__host__ __device__ constexpr int chunk_bytes(int G, bool aff = false) { return kFeatWarps * block_bytes(G, aff); }
+__host__ __device__ constexpr int chunk_bytes(int G, int fmt = kFmtSym) { return kFeatWarps * block_bytes(G, fmt); }
 // One partial tile of the split-K fixup: 4 feature warps x 32 lanes x 16 floats.
 constexpr size_t kSlotBytes = size_t(kFeatWarps) * 32 * kLaneAccHi * 4;
 
 // Pipeline depth: three stages of ~35 KB (measured faster than four, and than
 // smaller copies in more stages).
-__host__ __device__ constexpr int num_stages(int, bool, bool) { return kStages; }
+__host__ __device__ constexpr int num_stages(int, bool, int) { return kStages; }
 
-inline size_t gemm_smem_bytes(int G, bool hi, bool aff = false) {
-    const int ns = num_stages(G, hi, aff);
+inline size_t gemm_smem_bytes(int G, bool hi, int fmt = kFmtSym) {
+    const int ns = num_stages(G, hi, fmt);
     return 1024                                                         // alignment slack
            + size_t(ns) * x_stage_bytes(hi)                             // activation slices (1024-B aligned)
-           + size_t(ns) * kStageIters * chunk_bytes(G, aff)            // weight stages
+           + size_t(ns) * kStageIters * chunk_bytes(G, fmt)            // weight stages
            + 2 * size_t(kFeatWarps) * 32 * lane_vals(hi) * 4            // k-group combine buffers
            + 256;                                                       // barriers
 }
@@ -67,10 +75,10 @@ inline size_t gemm_smem_bytes(int G, bool hi, bool aff = false) {
 inline bool packed_shape_ok(int K, int N, int G) {
     return K > 0 && N > 0 && (G == 32 || G == 64) && K % kKChunk == 0;
 }
-inline size_t packed_bytes(int K, int N, int G, bool aff = false) {
-    if (!packed_shape_ok(K, N, G)) return 0;
+inline size_t packed_bytes(int K, int N, int G, int fmt = kFmtSym) {
+    if (fmt == kFmtNvfp4 ? !(K > 0 && N > 0 && K % kKChunk == 0) : !packed_shape_ok(K, N, G)) return 0;
     size_t T = (size_t(N) + kTileN - 1) / kTileN;
-    return T * size_t(K / kKChunk) * size_t(chunk_bytes(G, aff));
+    return T * size_t(K / kKChunk) * size_t(chunk_bytes(G, fmt));
 }
 
 // ---- launch description ------------------------------------------------------
@@ -100,7 +108,8 @@ struct GemmArgs {
     int mode;                  // EpilogueMode
     int F;                     // kSwiGluBf16: width of h (N = 2F)
     int R, K, N, G;
-    int affine;                // packed weights are MLX-style affine (codes + bf16 scale and bias)
+    int fmt;                   // WeightFormat of the packed weights
+    float gscale;              // kFmtNvfp4: tensor scale applied to every output (else 1)
     int T, Kc, Pv;
     unsigned *counters;        // [U_max][T][kFeatWarps], zero between launches
     float4 *partials;          // [U_max][Pv][2][kFeatWarps][32][4]
@@ -126,6 +135,10 @@ cudaError_t launch_w4_gemm(const GemmArgs &a, int u_max, cudaStream_t s);
 // the 16 matching up rows (sub-tile 1), the layout kSwiGluBf16 expects.
 // MLX-style affine weights: codes uint32 [N][K/8] (element i of a word in bits
 // 4i..4i+3, unsigned), scales and biases bf16 [N][K/G].
+// NVFP4 weights: codes uint8 [N][K/2] (E2M1, element 2j in the low nibble of
+// byte j), block scales uint8 [N][K/16] (E4M3 bit patterns).
+cudaError_t launch_pack_nvfp4(const uint8_t *codes, const uint8_t *scales, int K, int N, void *packed,
+                              cudaStream_t s);
 cudaError_t launch_pack_w4_affine(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases, int K, int N,
                                   int G, void *packed, cudaStream_t s);
 cudaError_t launch_pack_w4(const uint8_t *codes, const uint16_t *scales, int K, int N, int G, void *packed,

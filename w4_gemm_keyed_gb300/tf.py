@@ -38,6 +38,10 @@ class W4MatrixC(ctypes.Structure):
     _fields_ = [("packed", P), ("K", I32), ("N", I32), ("group", I32), ("affine", I32)]
 
 
+class Nvfp4MatrixC(ctypes.Structure):
+    _fields_ = [("packed", P), ("K", I32), ("N", I32), ("global_scale", ctypes.c_float)]
+
+
 class SamplingC(ctypes.Structure):
     _fields_ = [("temperature", ctypes.c_float), ("top_k", I32), ("top_p", ctypes.c_float)]
 
@@ -70,6 +74,10 @@ SIGNATURES = [
     ("tf_pack_w4_affine", ctypes.c_int, [P, P, P, I32, I32, I32, P, SZ, P]),
     ("tf_pack_w4_gate_up", ctypes.c_int, [P, P, I32, I32, I32, P, SZ, P]),
     ("tf_lane_gemm_workspace_bytes", SZ, [I32, I32, I32]),
+    ("tf_nvfp4_packed_bytes", SZ, [I32, I32]),
+    ("tf_pack_nvfp4", ctypes.c_int, [P, P, I32, I32, P, SZ, P]),
+    ("tf_lane_gemm_nvfp4_workspace_bytes", SZ, [I32, I32]),
+    ("tf_lane_gemm_nvfp4", ctypes.c_int, [ctypes.POINTER(Nvfp4MatrixC), P, I32, I32, P, I32, P, SZ, P]),
     ("tf_lane_gemm_w4", ctypes.c_int, [ctypes.POINTER(W4MatrixC), P, I32, I32, P, I32, P, SZ, P]),
     ("tf_lane_gemm_w4_noalloc", ctypes.c_int, [ctypes.POINTER(W4MatrixC), P, I32, I32, P, I32, P, P]),
     ("tf_lane_gemm_w4_accumulate", ctypes.c_int, [ctypes.POINTER(W4MatrixC), P, I32, I32, P, I32, P, SZ, P]),
@@ -269,6 +277,55 @@ def lane_gemm_w4_noalloc(W: W4Matrix, x: torch.Tensor, y: torch.Tensor, status: 
     wc = W.c()
     _check(lib.tf_lane_gemm_w4_noalloc(ctypes.byref(wc), _ptr(x), x.stride(0), R, _ptr(y), y.stride(0),
                                        _ptr(status), _stream(stream)))
+    return y
+
+
+# ---------------------------------------------------------------- NVFP4
+class Nvfp4Matrix:
+    """A packed NVFP4 matrix living on the device."""
+
+    def __init__(self, packed: torch.Tensor, K: int, N: int, global_scale: float):
+        self.packed, self.K, self.N, self.global_scale = packed, K, N, float(global_scale)
+        self._c = Nvfp4MatrixC(packed.data_ptr(), K, N, float(global_scale))
+
+    def c(self) -> Nvfp4MatrixC:
+        return self._c
+
+
+def nvfp4_packed_bytes(K: int, N: int) -> int:
+    return int(load().tf_nvfp4_packed_bytes(K, N))
+
+
+def pack_nvfp4(codes: torch.Tensor, scales: torch.Tensor, global_scale: float, out: torch.Tensor = None,
+               stream=None) -> Nvfp4Matrix:
+    """codes uint8 [N][K/2] (E2M1, low nibble first) and E4M3 scale bytes uint8 [N][K/16], on the device."""
+    N, K2 = codes.shape
+    K = 2 * K2
+    nbytes = nvfp4_packed_bytes(K, N)
+    if nbytes == 0:
+        raise TFError(TF_ERR_UNSUPPORTED, f"unsupported shape K={K} N={N}")
+    if tuple(scales.shape) != (N, K // 16) or codes.dtype != torch.uint8 or scales.dtype != torch.uint8:
+        raise TFError(TF_ERR_INVALID_ARG, "codes must be uint8 [N][K/2] and scales uint8 [N][K/16]")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=codes.device)
+    codes, scales = codes.contiguous(), scales.contiguous()
+    _check(load().tf_pack_nvfp4(_ptr(codes), _ptr(scales), K, N, _ptr(out), nbytes, _stream(stream)))
+    return Nvfp4Matrix(out, K, N, global_scale)
+
+
+def lane_gemm_nvfp4(W: Nvfp4Matrix, x: torch.Tensor, y: torch.Tensor = None, ws: torch.Tensor = None,
+                    stream=None) -> torch.Tensor:
+    """y[R][N] fp32 = NVFP4 linear of bf16 rows x[R][K] (x may be bf16 or int16 bits)."""
+    lib = load()
+    _check_rows_in(x, W.K)
+    R = x.shape[0]
+    if y is None:
+        y = torch.empty((R, W.N), dtype=torch.float32, device=x.device)
+    _check_rows_out(y, R, W.N, x.device)
+    if ws is None:
+        ws = workspace(int(lib.tf_lane_gemm_nvfp4_workspace_bytes(W.K, W.N)), x.device)
+    _check(lib.tf_lane_gemm_nvfp4(ctypes.byref(W.c()), _ptr(x), x.stride(0), R, _ptr(y), y.stride(0), _ptr(ws),
+                                  ws.numel(), _stream(stream)))
     return y
 
 
