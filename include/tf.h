@@ -55,7 +55,7 @@ extern "C" {
 #endif
 
 #define TF_MAX_ROWS 16
-#define TF_MAX_TOP_K 64
+#define TF_MAX_TOP_K 64   /* largest k' of the fast candidate path */
 
 typedef enum tf_status {
     TF_OK = 0,
@@ -270,8 +270,15 @@ TF_API tf_status tf_lane_gemm_w4_noalloc(const tf_w4_matrix *W, const uint16_t *
  *           h = sm(sm(sm(seed) ^ pos) ^ (uint32)token), sm = SplitMix64
  *           finaliser; ties: lower id.
  * logits dev fp32 [R][ldl] (ldl >= V); pos dev int64 [R]; tokens dev int32 [R].
- * Supported: 1 <= V <= 2^31-1, k' <= TF_MAX_TOP_K when T > 0 (else
- * TF_ERR_UNSUPPORTED), T >= 0 finite.  A non-finite logit sets
+ * Supported: 1 <= V <= tf's vocabulary limit (524288), any top_k, T >= 0
+ * finite.  k' <= TF_MAX_TOP_K takes the fast path (per-chunk top-k', one
+ * finaliser summing the top-p mass left to right in rank order); larger k'
+ * (top_k <= 0 included) take a general path: a radix select of the k'-th key,
+ * Z and the top-p boundary from fp64 sums taken in a fixed order that is not
+ * the rank order, so the boundary matches a left-to-right sum except where the
+ * mass reaching it lies within rounding (about 1e-12 relative) of top_p; then
+ * the Gumbel argmax over the kept candidates.  Both paths are deterministic and
+ * give each row the same token whatever R is.  A non-finite logit sets
  * TF_DEV_NONFINITE_LOGIT and that row's token to -1.
  */
 typedef struct tf_sampling {

@@ -104,6 +104,32 @@ def candidate_set(logits_row, temperature: float, top_k: int, top_p: float):
     return order  # rounding left the total just below p: keep all k'
 
 
+def topp_margin(logits_row, temperature: float, top_k: int, top_p: float) -> float:
+    """How close the top-p cut of ``candidate_set`` is to flipping: the smaller
+    of |S_m - p| and |S_(m-1) - p| for the cut m (the running sums as
+    ``candidate_set`` forms them), inf when no top-p cut applies."""
+    l32 = np.asarray(logits_row, dtype=np.float32)
+    if float(np.float32(top_p)) >= 1.0 or float(np.float32(temperature)) == 0.0:
+        return math.inf
+    V = l32.size
+    order = rank_order(l32)
+    kk = V if (top_k <= 0 or top_k >= V) else int(top_k)
+    order = order[:kk]
+    T = float(np.float32(temperature))
+    l0 = float(l32[order[0]])
+    e = [math.exp((float(l32[i]) - l0) / T) for i in order]
+    Z = 0.0
+    for v in e:
+        Z += v
+    p = float(np.float32(top_p))
+    S_prev, S = 0.0, 0.0
+    for v in e:
+        S_prev, S = S, S + v / Z
+        if S >= p:
+            return min(abs(S - p), abs(S_prev - p))
+    return abs(S - p)
+
+
 def sample_row(logits_row, temperature: float, top_k: int, top_p: float, seed: int, pos: int):
     """(token, gap): the keyed sample and the margin between the best and runner-up score.
 

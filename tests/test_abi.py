@@ -73,8 +73,8 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.tf_lane_gemm_w4(ctypes.byref(W), 256, 256, 17, 256, 64, 256, 1 << 30, None) == tf.TF_ERR_INVALID_ARG
     assert lib.tf_lane_gemm_w4(ctypes.byref(W), 258, 256, 1, 256, 64, 256, 1 << 30, None) == tf.TF_ERR_INVALID_ARG
     assert lib.tf_lane_gemm_w4(ctypes.byref(W), 256, 256, 1, 256, 64, None, 0, None) == tf.TF_ERR_WORKSPACE
-    sp = tf.SamplingC(0.7, 100, 0.9)  # k' = 100 > 64
-    st = lib.tf_keyed_sample(256, 1000, 1, 1000, ctypes.byref(sp), 1, 256, 256, 256, 1 << 30, None)
+    sp = tf.SamplingC(0.7, 0, 0.9)    # any k' is served; a vocabulary past the limit is not
+    st = lib.tf_keyed_sample(256, 600000, 1, 600000, ctypes.byref(sp), 1, 256, 256, 256, 1 << 30, None)
     assert st == tf.TF_ERR_UNSUPPORTED
     sp = tf.SamplingC(-1.0, 20, 0.9)
     assert lib.tf_keyed_sample(256, 1000, 1, 1000, ctypes.byref(sp), 1, 256, 256, 256, 1 << 30, None) == \

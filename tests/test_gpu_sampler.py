@@ -84,11 +84,54 @@ def test_nonfinite_logits_flag_the_row(tf):
     assert tf.workspace_status(ws) == tf.TF_DEV_OK
 
 
-def test_unsupported_candidate_count(tf):
-    with pytest.raises(tf.TFError) as e:
-        tf.keyed_sample(torch.zeros((1, 1000), device="cuda"), 0.7, 0, 0.9, 5,
-                        torch.zeros(1, dtype=torch.int64, device="cuda"))
-    assert e.value.status == tf.TF_ERR_UNSUPPORTED
+# ---------------------------------------------------------------- general candidate path (k' > 64)
+def check_tokens_general(gpu, logits, T, k, p, seed, pos, near_tie):
+    """Identical tokens, except where the oracle itself sits on a knife edge:
+    a top-2 score gap below 1e-9, or a top-p cut whose running sum lies within
+    1e-9 of top_p (the general path sums the mass in another fixed order)."""
+    ref, gaps = osamp.sample(logits, T, k, p, seed, pos)
+    for r in range(len(ref)):
+        if gpu[r] != ref[r]:
+            margin = osamp.topp_margin(logits[r], T, k, p)
+            assert gaps[r] < 1e-9 or margin < 1e-9, \
+                f"row {r}: gpu {gpu[r]} oracle {ref[r]} gap {gaps[r]} top-p margin {margin}"
+            near_tie(f"general V={logits.shape[1]} T={T} k={k} p={p} row {r}", min(gaps[r], margin))
+
+
+@pytest.mark.parametrize("k", [0, 65, 1000, 151936])
+@pytest.mark.parametrize("T,p", [(0.7, 0.95), (1.0, 0.8), (0.6, 1.0)])
+def test_general_candidate_path_matches_oracle(tf, near_tie, k, T, p):
+    rng = inputs.rng_for(205, k, int(T * 10), int(p * 100))
+    R, V = 4, 151936
+    logits = inputs.logits_normal(rng, R, V, std=2.0)
+    seed = int(inputs.seeds_u64(rng, 1)[0])
+    pos = inputs.positions(rng, R)
+    check_tokens_general(gpu_sample(tf, logits, T, k, p, seed, pos), logits, T, k, p, seed, pos, near_tie)
+
+
+def test_general_path_ties_and_small_vocabularies(tf, near_tie):
+    rng = inputs.rng_for(206)
+    for V in (65, 66, 1000, 4097):
+        logits = rng.integers(-3, 3, size=(3, V)).astype(np.float32)   # heavy ties at every boundary
+        pos = inputs.positions(rng, 3)
+        for T, k, p in ((0.8, 0, 0.9), (1.0, 65, 0.5), (0.5, V - 1, 1.0), (1.3, 100, 0.99)):
+            check_tokens_general(gpu_sample(tf, logits, T, k, p, 17, pos), logits, T, k, p, 17, pos, near_tie)
+
+
+def test_general_path_rows_independent_of_R_and_nan_rows(tf):
+    rng = inputs.rng_for(207)
+    V = 151936
+    logits = inputs.logits_normal(rng, 16, V, std=2.0)
+    pos = inputs.positions(rng, 16)
+    full = gpu_sample(tf, logits, 0.8, 0, 0.9, 31, pos)
+    for r in (0, 9, 15):
+        assert gpu_sample(tf, logits[r:r + 1], 0.8, 0, 0.9, 31, pos[r:r + 1])[0] == full[r]
+    logits[3, 1234] = np.nan
+    ws = tf.workspace(tf.keyed_sample_workspace_bytes(16, V))
+    t = tf.keyed_sample(torch.from_numpy(logits).cuda(), 0.8, 0, 0.9, 31, torch.from_numpy(pos).cuda(), ws=ws)
+    t = t.cpu().numpy()
+    assert t[3] == -1 and np.array_equal(np.delete(t, 3), np.delete(full, 3))
+    assert tf.workspace_status(ws) == tf.TF_DEV_NONFINITE_LOGIT
 
 
 def test_rows_independent_of_R(tf):

@@ -472,6 +472,299 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleAr
     }
 }
 
+// ---- general candidate path: T > 0 with k' > 64 candidates ----
+// Same candidate set and selection as the fast path (rank order by (logit
+// desc, id asc), the first k', then the top-p prefix, then the Gumbel argmax),
+// for any k' up to V.  Four launches, every reduction in a fixed order or on
+// integers, so a row's token depends on its own logits only:
+//   gen_prep   (chunk, row): the chunk's largest key; non-finite logits flag the row.
+//   gen_select (row, 1024 threads): the k'-th largest key by an 8-bit radix
+//              select over the row; e_i = exp((l_i - l_0) / T) in fp64 for the
+//              k' candidates and Z = sum e_i; then the top-p boundary: the
+//              largest key b with sum_{key >= b} e >= top_p * Z, found by a
+//              4-bit radix walk over per-bin fp64 masses, which stops once the
+//              boundary bin holds a single element.
+//   gen_score  (chunk, row): the best (l / T + g, id) among candidates >= b.
+//   gen_final  (row): the best over the chunks.
+// The masses are summed in a fixed order that is not the rank order, so the
+// boundary agrees with a left-to-right sum except when the mass reaching it
+// lies within rounding (~1e-12 relative) of top_p * Z.
+constexpr int kGenThreads = 512;
+
+__device__ __forceinline__ uint64_t row_composite(const float *row, int i) { return composite(order_key(row[i]), i); }
+
+__global__ void __launch_bounds__(kSampleThreads) gen_prep_kernel(const SampleArgs a) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    __shared__ unsigned long long s_max;
+    __shared__ int s_bad;
+    const int c = blockIdx.x, r = blockIdx.y;
+    const float *row = a.logits + (long long)r * a.ldl;
+    if (threadIdx.x == 0) {
+        s_max = 0ull;
+        s_bad = 0;
+    }
+    __syncthreads();
+    uint64_t m = 0ull;
+    bool bad = false;
+    for (int e = 0; e < kE1; ++e) {
+        const int i = c * kSampleChunk + e * kSampleThreads + threadIdx.x;
+        if (i < a.V) {
+            bad |= !isfinite(row[i]);
+            const uint64_t v = row_composite(row, i);
+            m = v > m ? v : m;
+        }
+    }
+    atomicMax(&s_max, (unsigned long long)m);
+    if (bad) atomicOr(&s_bad, 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        a.gen_cmax[r * a.n_chunks + c] = s_max;
+        if (s_bad) {
+            atomicOr(&a.row_bad[r], 1);
+            set_error(a.err, 2);
+        }
+    }
+}
+
+// Fixed-order block sum of one fp64 value per thread (kGenThreads threads).
+__device__ double block_sum_fixed(double v, double *sh) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    const int w = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sh[w] = v;
+    __syncthreads();
+    double t = 0.0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kGenThreads / 32; ++i) t += sh[i];
+        sh[32] = t;
+    }
+    __syncthreads();
+    return sh[32];
+}
+
+__global__ void __launch_bounds__(kGenThreads) gen_select_kernel(const SampleArgs a) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    __shared__ unsigned int hist[256];
+    __shared__ double shd[33];
+    __shared__ double bmass[16][kGenThreads / 32];
+    __shared__ unsigned int bcnt[16];
+    __shared__ unsigned long long s_u64;
+    __shared__ int s_int[2];
+    const int r = blockIdx.x, tid = threadIdx.x;
+    const float *row = a.logits + (long long)r * a.ldl;
+    const int V = a.V;
+    if (a.row_bad[r]) {
+        if (tid == 0) a.gen_thr[r] = ~0ull;   // no candidates: gen_final writes -1
+        return;
+    }
+    // l_0: the largest key of the row
+    if (tid == 0) s_u64 = 0ull;
+    __syncthreads();
+    for (int c = tid; c < a.n_chunks; c += kGenThreads) atomicMax(&s_u64, (unsigned long long)a.gen_cmax[r * a.n_chunks + c]);
+    __syncthreads();
+    const double l0 = double(key_value(uint32_t(s_u64 >> 32)));
+    const double T = double(a.temperature);
+
+    // tau: the k'-th largest composite key (8-bit radix select, most significant digit first)
+    uint64_t tau = 0ull;
+    if (a.k_eff < V) {
+        uint64_t prefix = 0ull, mask = 0ull;
+        int remaining = a.k_eff;
+        for (int shift = 56; shift >= 0; shift -= 8) {
+            for (int i = tid; i < 256; i += kGenThreads) hist[i] = 0u;
+            __syncthreads();
+            for (int i = tid; i < V; i += kGenThreads) {
+                const uint64_t cv = row_composite(row, i);
+                if ((cv & mask) == prefix) atomicAdd(&hist[(cv >> shift) & 0xFFu], 1u);
+            }
+            __syncthreads();
+            if (tid == 0) {
+                int run = 0, d = 255;
+                for (; d > 0; --d) {
+                    if (run + int(hist[d]) >= remaining) break;
+                    run += int(hist[d]);
+                }
+                s_int[0] = d;
+                s_int[1] = run;
+            }
+            __syncthreads();
+            prefix |= uint64_t(s_int[0]) << shift;
+            mask |= 0xFFull << shift;
+            remaining -= s_int[1];
+            __syncthreads();
+        }
+        tau = prefix;
+    }
+
+    // e_i of the k' candidates, and Z, each thread summing its own elements in index order
+    double part = 0.0;
+    double *e_row = a.gen_e + (long long)r * V;
+    for (int i = tid; i < V; i += kGenThreads) {
+        const uint64_t cv = row_composite(row, i);
+        const double e = cv >= tau ? exp((double(row[i]) - l0) / T) : 0.0;
+        e_row[i] = e;
+        part += e;
+    }
+    const double Z = block_sum_fixed(part, shd);
+    uint64_t beta = tau;
+    const double p = double(a.top_p);
+    if (p < 1.0) {
+        const double target = p * Z;
+        uint64_t prefix = 0ull, mask = 0ull;
+        double acc = 0.0;   // mass of the candidates above the current bin
+        bool found = false;
+        for (int shift = 60; shift >= 0 && !found; shift -= 4) {
+            double m16[16];
+            unsigned c16[16];
+#pragma unroll
+            for (int d = 0; d < 16; ++d) {
+                m16[d] = 0.0;
+                c16[d] = 0u;
+            }
+            for (int i = tid; i < V; i += kGenThreads) {
+                const uint64_t cv = row_composite(row, i);
+                if (cv >= tau && (cv & mask) == prefix) {
+                    const int d = int((cv >> shift) & 0xFu);
+                    const double e = e_row[i];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        if (q == d) {
+                            m16[q] += e;
+                            ++c16[q];
+                        }
+                }
+            }
+            if (tid < 16) bcnt[tid] = 0u;
+            __syncthreads();
+#pragma unroll
+            for (int d = 0; d < 16; ++d) {
+                double v = m16[d];
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                if ((tid & 31) == 0) bmass[d][tid >> 5] = v;
+                if (c16[d]) atomicAdd(&bcnt[d], c16[d]);
+            }
+            __syncthreads();
+            if (tid == 0) {
+                int chosen = -1;
+                for (int d = 15; d >= 0; --d) {
+                    if (bcnt[d] == 0u) continue;
+                    double bm = 0.0;
+                    for (int w = 0; w < kGenThreads / 32; ++w) bm += bmass[d][w];
+                    if (acc + bm >= target) {
+                        chosen = d;
+                        break;
+                    }
+                    acc += bm;
+                }
+                s_int[0] = chosen;
+                s_int[1] = chosen >= 0 ? int(bcnt[chosen]) : 0;
+            }
+            __syncthreads();
+            const int chosen = s_int[0];
+            if (chosen < 0) {                 // the whole mass stays below top_p * Z: keep all k'
+                found = true;
+            } else {
+                prefix |= uint64_t(chosen) << shift;
+                mask |= 0xFull << shift;
+                if (s_int[1] == 1 || shift == 0) {   // one element left in the bin: the boundary
+                    if (tid == 0) s_u64 = 0ull;
+                    __syncthreads();
+                    for (int i = tid; i < V; i += kGenThreads) {
+                        const uint64_t cv = row_composite(row, i);
+                        if (cv >= tau && (cv & mask) == prefix) atomicMax(&s_u64, (unsigned long long)cv);
+                    }
+                    __syncthreads();
+                    beta = s_u64;
+                    found = true;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    if (tid == 0) a.gen_thr[r] = beta;
+}
+
+__device__ __forceinline__ bool better(double s, int id, double bs, int bid) {
+    return s > bs || (s == bs && id < bid);
+}
+
+__global__ void __launch_bounds__(kSampleThreads) gen_score_kernel(const SampleArgs a) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    __shared__ double s_sc[kSampleThreads / 32];
+    __shared__ int s_id[kSampleThreads / 32];
+    const int c = blockIdx.x, r = blockIdx.y;
+    const float *row = a.logits + (long long)r * a.ldl;
+    const uint64_t thr = a.gen_thr[r];
+    const double T = double(a.temperature);
+    const int64_t pos = a.pos ? a.pos[r] : (*a.pos_base + r);
+    double best = -1.0 / 0.0;
+    int best_id = 0x7FFFFFFF;
+    for (int e = 0; e < kE1; ++e) {
+        const int i = c * kSampleChunk + e * kSampleThreads + threadIdx.x;
+        if (i < a.V && row_composite(row, i) >= thr) {
+            const double s = double(row[i]) / T + gumbel(a.seed, pos, i);
+            if (better(s, i, best, best_id)) {
+                best = s;
+                best_id = i;
+            }
+        }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        const double ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        const int oid = __shfl_xor_sync(0xFFFFFFFFu, best_id, o);
+        if (better(ob, oid, best, best_id)) {
+            best = ob;
+            best_id = oid;
+        }
+    }
+    if ((threadIdx.x & 31) == 0) {
+        s_sc[threadIdx.x >> 5] = best;
+        s_id[threadIdx.x >> 5] = best_id;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kSampleThreads / 32; ++w)
+            if (better(s_sc[w], s_id[w], best, best_id)) {
+                best = s_sc[w];
+                best_id = s_id[w];
+            }
+        a.gen_bscore[r * a.n_chunks + c] = best;
+        a.gen_bid[r * a.n_chunks + c] = best_id;
+    }
+}
+
+__global__ void gen_final_kernel(const SampleArgs a) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int r = blockIdx.x, lane = threadIdx.x;
+    double best = -1.0 / 0.0;
+    int best_id = 0x7FFFFFFF;
+    for (int c = lane; c < a.n_chunks; c += 32)
+        if (better(a.gen_bscore[r * a.n_chunks + c], a.gen_bid[r * a.n_chunks + c], best, best_id)) {
+            best = a.gen_bscore[r * a.n_chunks + c];
+            best_id = a.gen_bid[r * a.n_chunks + c];
+        }
+    for (int o = 16; o > 0; o >>= 1) {
+        const double ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        const int oid = __shfl_xor_sync(0xFFFFFFFFu, best_id, o);
+        if (better(ob, oid, best, best_id)) {
+            best = ob;
+            best_id = oid;
+        }
+    }
+    if (lane == 0) {
+        if (a.row_bad[r]) {
+            a.tokens[r] = -1;
+            a.row_bad[r] = 0;   // leave the workspace clean for the next call
+        } else {
+            a.tokens[r] = best_id;
+        }
+    }
+}
+
 __global__ void accept_kernel(const int32_t *drafts, const int32_t *sampled, int R, int32_t *accepted,
                               int32_t *bonus, int64_t *pos) {
     grid_dependency_wait();     // inputs come from the preceding grid
@@ -501,6 +794,12 @@ size_t sample_workspace_bytes(int R, int V) {
     b += size_t(R) * nc * sizeof(uint64_t);
     b += size_t(R) * nc * kMaxTopK * (sizeof(float) + sizeof(int32_t));
     b += size_t(R) * nc * sizeof(int32_t);
+    b = (b + 255) / 256 * 256;
+    // general path: chunk maxima, per-row boundary, e_i, chunk bests
+    b += size_t(R) * nc * sizeof(uint64_t) + size_t(R) * sizeof(uint64_t);
+    b = (b + 255) / 256 * 256;
+    b += size_t(R) * size_t(V) * sizeof(double);
+    b += size_t(R) * nc * (sizeof(double) + sizeof(int32_t));
     return (b + 255) / 256 * 256;
 }
 
@@ -516,11 +815,30 @@ void sample_bind_workspace(SampleArgs &a, void *ws_region, int R, int V) {
     a.cand_id = reinterpret_cast<int32_t *>(p);
     p += size_t(R) * nc * kMaxTopK * sizeof(int32_t);
     a.cand_cnt = reinterpret_cast<int32_t *>(p);
+    p += size_t(R) * nc * sizeof(int32_t);
+    p = static_cast<char *>(ws_region) + (size_t(p - static_cast<char *>(ws_region)) + 255) / 256 * 256;
+    a.gen_cmax = reinterpret_cast<uint64_t *>(p);
+    p += size_t(R) * nc * sizeof(uint64_t);
+    a.gen_thr = reinterpret_cast<uint64_t *>(p);
+    p += size_t(R) * sizeof(uint64_t);
+    p = static_cast<char *>(ws_region) + (size_t(p - static_cast<char *>(ws_region)) + 255) / 256 * 256;
+    a.gen_e = reinterpret_cast<double *>(p);
+    p += size_t(R) * size_t(V) * sizeof(double);
+    a.gen_bscore = reinterpret_cast<double *>(p);
+    p += size_t(R) * nc * sizeof(double);
+    a.gen_bid = reinterpret_cast<int32_t *>(p);
     a.n_chunks = int(nc);
 }
 
 cudaError_t launch_keyed_sample(const SampleArgs &a, cudaStream_t s) {
     if (a.n_chunks > kMaxChunks) return cudaErrorInvalidValue;
+    if (a.temperature > 0.0f && a.k_eff > kMaxTopK) {   // general candidate path
+        cudaError_t e = launch_pdl(gen_prep_kernel, dim3(a.n_chunks, a.R), dim3(kSampleThreads), 0, s, a);
+        if (e == cudaSuccess) e = launch_pdl(gen_select_kernel, dim3(a.R), dim3(kGenThreads), 0, s, a);
+        if (e == cudaSuccess) e = launch_pdl(gen_score_kernel, dim3(a.n_chunks, a.R), dim3(kSampleThreads), 0, s, a);
+        if (e == cudaSuccess) e = launch_pdl(gen_final_kernel, dim3(a.R), dim3(32), 0, s, a);
+        return e;
+    }
     cudaError_t e = launch_pdl(topk_partial_kernel, dim3(a.n_chunks, a.R), dim3(kSampleThreads), 0, s, a);
     if (e != cudaSuccess) return e;
     return launch_pdl(finalize_kernel, dim3(a.R), dim3(kSampleThreads), 0, s, a);

@@ -14,7 +14,7 @@ struct SampleArgs {
     const float *logits;
     int ldl;
     int R, V;
-    int k_eff;            // 1 for greedy, else k' = min(top_k or V, V) <= 64
+    int k_eff;            // 1 for greedy, else k' = min(top_k or V, V); > 64 takes the general path
     float temperature;
     float top_p;
     uint64_t seed;
@@ -27,6 +27,12 @@ struct SampleArgs {
     int32_t *cand_cnt;    // [R][n_chunks]
     uint64_t *cand_kth;   // [R][n_chunks]: (key, id) of the chunk's k-th best when it kept k_eff, else 0
     int32_t *row_bad;     // [R]
+    // general candidate path (k' > kMaxTopK)
+    uint64_t *gen_cmax;   // [R][n_chunks] largest composite key of each chunk
+    uint64_t *gen_thr;    // [R] smallest composite key kept
+    double *gen_e;        // [R][V] exp((l_i - l_0) / T) of the k' candidates, else 0
+    double *gen_bscore;   // [R][n_chunks] best score of each chunk
+    int32_t *gen_bid;     // [R][n_chunks] its token id
     int *err;
     int n_chunks;
 };

@@ -92,10 +92,8 @@ tf_status check_sampling(const tf_sampling *p, int V, int *k_eff) {
         *k_eff = 1;
         return TF_OK;
     }
-    const int kk = (p->top_k <= 0 || p->top_k >= V) ? V : p->top_k;
-    if (kk > kMaxTopK)
-        return fail(TF_ERR_UNSUPPORTED, "candidate count k'=%d exceeds %d (set top_k <= %d)", kk, kMaxTopK, kMaxTopK);
-    *k_eff = kk;
+    // k' <= kMaxTopK takes the fast candidate path, larger k' the general one
+    *k_eff = (p->top_k <= 0 || p->top_k >= V) ? V : p->top_k;
     return TF_OK;
 }
 
