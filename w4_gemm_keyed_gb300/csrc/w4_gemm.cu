@@ -25,10 +25,13 @@
 // next launch in the stream lands on every SM this one frees and requests its
 // first weight stages before it waits for this grid to finish.
 // Why mma.sync and not tcgen05: the verify pass multiplies a weight tile by at
-// most 16 rows, so the MMA's N is 16.  A tcgen05.mma (M=128, K=16) was measured
-// on this part at ~153 cycles per instruction whatever its N (16..256), i.e.
-// ~13 weights/cycle/SM at N=16 against the ~45 the HBM stream delivers; the
-// register-operand m16n8k16 path processes ~68 weights/cycle/SM.
+// most 16 rows (the MMA's N is 16), and per 256 weights a consumer warp issues
+// about 18 instructions of which the MMA is one (R <= 8) or two (R > 8); the
+// rest turn the 4-bit codes into exact bf16 operands and apply the group
+// scales, work a tcgen05 path would need as well (plus storing the converted
+// operand to shared or tensor memory).  The counters show the tensor pipe at
+// 27-39 % while instruction issue limits the stream, so a wider MMA unit would
+// not shorten the critical path.
 // Row invariance: rows are MMA columns (a column's result depends only on its
 // own activations; the rows 8..15 MMA is skipped when R <= 8), and the cut of
 // the iteration space, the stage schedule, the k-group split, the fixed-order
