@@ -325,7 +325,8 @@ def time_dense_e2e(tf, torch, mats, steps, warmup):
 
 
 def extra_lmhead(tf, torch, steps=30):
-    """LM head (5120 -> 151936) + keyed sampler + acceptance at R = 1, 2, 4, 8, 16."""
+    """LM head (5120 -> 151936) + keyed sampler + acceptance at R = 1, 2, 4, 8, 16: the fused
+    call, the unfused sequence and the GEMM alone, each timed back to back."""
     from w4_gemm_keyed_gb300 import inputs
     K, V = 5120, 151936
     rng = inputs.rng_for(3)
@@ -340,34 +341,41 @@ def extra_lmhead(tf, torch, steps=30):
     drafts = torch.zeros(15, dtype=torch.int32, device="cuda")
     acc = torch.empty(1, dtype=torch.int32, device="cuda")
     bonus = torch.empty(1, dtype=torch.int32, device="cuda")
-    out = {}
+    ws_f = tf.workspace(tf.lmhead_sample_workspace_bytes(W, 16))
+    out = {"step": "tf_lmhead_sample (LM head with candidate epilogue, finaliser with acceptance)",
+           "unfused_step": "tf_lane_gemm_w4 + tf_keyed_sample + tf_accept"}
     by = bytes_per_launch(K, V)
     for R in ROWS:
         def one():
+            tf.lmhead_sample(W, x[:R], 0.6, 20, 0.95, 1234, pos[:R], tokens=toks[:R], drafts=drafts[:max(R - 1, 1)],
+                             accepted=acc, bonus=bonus, ws=ws_f)
+
+        def one_unfused():
             tf.lane_gemm_w4(W, x[:R], y=logits[:R], ws=ws_g)
             tf.keyed_sample(logits[:R], 0.6, 20, 0.95, 1234, pos[:R], tokens=toks[:R], ws=ws_s)
             tf.accept(drafts[:max(R - 1, 1)], toks[:R], accepted=acc, bonus=bonus)
-        for _ in range(3):
-            one()
-        torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        g0 = torch.cuda.Event(enable_timing=True)
-        g1 = torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(steps):
-            one()
-        b.record()
-        g0.record()
-        for _ in range(steps):
+
+        def gemm():
             tf.lane_gemm_w4(W, x[:R], y=logits[:R], ws=ws_g)
-        g1.record()
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / steps
-        gms = g0.elapsed_time(g1) / steps
-        out[f"R{R}"] = {"verify_steps_per_s": 1e3 / ms, "rows_per_s": R * 1e3 / ms,
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(steps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / steps
+
+        ms, ums, gms = timed(one), timed(one_unfused), timed(gemm)
+        out[f"R{R}"] = {"verify_steps_per_s": 1e3 / ms, "rows_per_s": R * 1e3 / ms, "ms_per_step": ms,
+                        "unfused_ms_per_step": ums, "lmhead_gemm_ms": gms, "step_over_gemm": ms / gms,
                         "lmhead_gbs": by / (gms * 1e-3) / 1e9,
-                        "lmhead_frac_of_hbm_peak": by / (gms * 1e-3) / 1e9 / peaks()[0], "ms_per_step": ms}
+                        "lmhead_frac_of_hbm_peak": by / (gms * 1e-3) / 1e9 / peaks()[0]}
     del W
     return out
 

@@ -293,6 +293,43 @@ TF_API tf_status tf_keyed_sample(const float *logits, int32_t ldl, int32_t R, in
                           size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * tf_lmhead_sample -- LM head and keyed sampling in one call
+ * ------------------------------------------------------------------------
+ * README, the two guarantees (keyed sampling over the top-k / top-p
+ * candidates of the LM head's logits).  Per row r:
+ *   tokens[r] = tf_keyed_sample(tf_lane_gemm_w4(W, x)[r], p, seed, pos[r])
+ * with the same bits as those two calls in a row (same logits, same candidate
+ * set and order, same finaliser).  When W is symmetric int4, R <= 8 and every
+ * CTA of the GEMM can keep k' = (T == 0 ? 1 : k') candidates in the
+ * finaliser's pool (k' * grid <= 8192 with grid = the GEMM's CTA count, at
+ * most the SM count; k' <= 53 on 152 SMs), the GEMM's epilogue keeps each CTA's k' best
+ * (logit, id) per row as it stores them and the finaliser alone merges
+ * them: no logits are re-read and no vocabulary-wide pass runs.  Otherwise
+ * (R > 8, larger k', top_k <= 0, affine weights) the GEMM stores the logits
+ * and the sampler runs on them.
+ * W       symmetric or affine int4 matrix, K x N with N = the vocabulary V
+ *         (V <= 524288).
+ * x       dev bf16 [R][ldx] (ldx >= K, a multiple of 8; 16-B aligned).
+ * p, seed, pos, tokens: as tf_keyed_sample (pos dev int64 [R], may be NULL
+ *         for T == 0).
+ * logits  dev fp32 [R][ldl] (ldl >= V) or NULL: when given, also receives the
+ *         logits (bit-identical to tf_lane_gemm_w4's).
+ * drafts, accepted, bonus: when accepted (dev int32 [1]) is non-NULL, the
+ *         finaliser also runs tf_accept(drafts, tokens, R) on this call's
+ *         tokens: the last row to finish writes *accepted and, if bonus is
+ *         non-NULL, *bonus (drafts dev int32 [R-1], may be NULL for R == 1).
+ * ws      >= tf_lmhead_sample_workspace_bytes(W, R) bytes (GEMM scratch, the
+ *         sampler's, and logits scratch for the unfused path).
+ * Device errors as tf_lane_gemm_w4 and tf_keyed_sample (a non-finite logit
+ * sets TF_DEV_NONFINITE_LOGIT and that row's token to -1).
+ */
+TF_API size_t tf_lmhead_sample_workspace_bytes(const tf_w4_matrix *W, int32_t R);
+TF_API tf_status tf_lmhead_sample(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R,
+                                  const tf_sampling *p, uint64_t seed, const int64_t *pos, int32_t *tokens,
+                                  float *logits, int32_t ldl, const int32_t *drafts, int32_t *accepted,
+                                  int32_t *bonus, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * tf_keyed_hash -- the sampler's key and Gumbel noise for given triples
  * ------------------------------------------------------------------------
  * README, the two guarantees (keyed sampling): g is Gumbel noise derived from

@@ -181,6 +181,35 @@ def test_newer_entry_points_validate_before_launching(lib):
     assert lib.tf_pack_w4_affine(256, 256, 256, 256, 64, 64, 256, need - 1, None) == tf.TF_ERR_INVALID_ARG
 
 
+def test_lmhead_sample_validates_before_launching(lib):
+    from w4_gemm_keyed_gb300 import tf
+    big = 1 << 30
+    W = tf.W4MatrixC(256, 256, 1000, 64, 0)
+    sp = ctypes.byref(tf.SamplingC(0.7, 20, 0.9))
+    greedy = ctypes.byref(tf.SamplingC(0.0, 0, 1.0))
+    none3 = (None, None, None)
+
+    def call(Wc, x, ldx, R, p, pos, tokens, logits=None, ldl=0, acc=none3, ws=256, ws_bytes=big):
+        return lib.tf_lmhead_sample(ctypes.byref(Wc), x, ldx, R, p, 1, pos, tokens, logits, ldl, *acc, ws, ws_bytes,
+                                    None)
+
+    assert lib.tf_lmhead_sample_workspace_bytes(ctypes.byref(W), 0) == 0
+    assert lib.tf_lmhead_sample_workspace_bytes(ctypes.byref(W), 17) == 0
+    assert lib.tf_lmhead_sample_workspace_bytes(ctypes.byref(W), 16) > 16 * 1000 * 4
+    bad = tf.TF_ERR_INVALID_ARG
+    assert call(W, 256, 256, 0, sp, 256, 256) == bad                          # R = 0
+    assert call(W, None, 256, 1, sp, 256, 256) == bad                         # null x
+    assert call(W, 256, 200, 1, sp, 256, 256) == bad                          # ldx < K
+    assert call(W, 256, 256, 1, sp, 256, None) == bad                         # null tokens
+    assert call(W, 256, 256, 1, sp, None, 256) == bad                         # T > 0 without pos
+    assert call(W, 256, 256, 1, sp, 256, 256, logits=256, ldl=999) == bad     # ldl < N
+    assert call(W, 256, 256, 1, None, 256, 256) == bad                        # null sampling
+    assert call(W, 256, 256, 2, sp, 256, 256, acc=(None, 256, 256)) == bad    # accepting 2 rows without drafts
+    assert call(W, 256, 256, 1, greedy, None, 256, ws=None, ws_bytes=0) == tf.TF_ERR_WORKSPACE
+    Wbig = tf.W4MatrixC(256, 256, 600000, 64, 0)
+    assert call(Wbig, 256, 256, 1, sp, 256, 256) == tf.TF_ERR_UNSUPPORTED     # V above the limit
+
+
 def test_binding_refuses_host_tensors(lib):
     """Every pointer the library takes is a device pointer: the binding raises
     for a host tensor (pinned or not) before anything reaches the library."""

@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include "sampler.cuh"
+#include "tf_keys.cuh"
 #include "tf_ptx.cuh"
 
 namespace tfk {
@@ -36,19 +37,24 @@ constexpr int kE2 = 32;                             // pool entries per thread i
 constexpr int kMaxChunks = kE2 * kSampleThreads / kMaxTopK;  // 128
 constexpr int kSurvMax = 1024;                      // survivors ranked directly (else radix select)
 
-__device__ __forceinline__ uint64_t composite(uint32_t key, int32_t id) {
-    return (uint64_t(key) << 32) | uint64_t(0xFFFFFFFFu - uint32_t(id));
-}
-__device__ __forceinline__ int32_t composite_id(uint64_t c) { return int32_t(0xFFFFFFFFu - uint32_t(c)); }
-
-// Order-preserving key: larger float -> larger key; -0 and +0 share a key.
-__device__ __forceinline__ uint32_t order_key(float f) {
-    uint32_t b = __float_as_uint(f);
-    if (b == 0x80000000u) b = 0u;
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+// A lower bound on the k-th largest element held by the block, from each
+// thread's largest key (0 for a thread that holds none).  Threads below
+// n_thr hold at least one element, so warps below n_thr / 32 are full.  In
+// each full warp the c-th largest thread maximum, c = ceil(k / full warps),
+// has c elements at or above it; the smallest of these over the full warps
+// therefore has at least k elements at or above it.  0 (every element
+// survives) when no warp is full or c > 32.  Call with the whole block.
+__device__ uint64_t kth_bound(uint64_t tmax, int k, int n_thr, uint64_t *s_wb) {
+    const int n_full = min(n_thr, int(blockDim.x)) >> 5;
+    const uint64_t v = warp_sort_desc(tmax);
+    const int c = n_full > 0 ? (k + n_full - 1) / n_full : 33;
+    const uint64_t vc = __shfl_sync(0xFFFFFFFFu, v, c <= 32 ? c - 1 : 0);
+    if ((threadIdx.x & 31) == 0) s_wb[threadIdx.x >> 5] = vc;
+    __syncthreads();
+    if (c > 32) return 0ull;
+    uint64_t L = ~0ull;
+    for (int w = 0; w < n_full; ++w) L = s_wb[w] < L ? s_wb[w] : L;
+    return L;
 }
 
 // SplitMix64 output function (Steele, Lea & Flood 2014): advance by the golden
@@ -210,10 +216,9 @@ __global__ void __launch_bounds__(kSampleThreads) topk_partial_kernel(const Samp
     float *out_val = a.cand_val + (long long)slot0 * kMaxTopK;
     int32_t *out_id = a.cand_id + (long long)slot0 * kMaxTopK;
 
-    // lower bound: the k-th largest per-thread maximum (0 when fewer than k threads hold one)
-    __shared__ uint64_t s_tmax[kSampleThreads];
+    // lower bound on the chunk's k-th best from the per-thread maxima
+    __shared__ uint64_t s_wb[kSampleThreads / 32];
     __shared__ uint64_t s_surv[kSurvMax];
-    __shared__ uint64_t s_L;
     __shared__ int s_ns;
     uint64_t ck[kE1];
     uint64_t tmax = 0;
@@ -222,19 +227,8 @@ __global__ void __launch_bounds__(kSampleThreads) topk_partial_kernel(const Samp
         ck[e] = ((valid >> e) & 1u) ? composite(key[e], id[e]) : 0ull;
         tmax = ck[e] > tmax ? ck[e] : tmax;
     }
-    s_tmax[threadIdx.x] = tmax;
-    if (threadIdx.x == 0) {
-        s_L = 0ull;
-        s_ns = 0;
-    }
-    __syncthreads();
-    if (tmax != 0ull) {
-        int above = 0;
-        for (int j = 0; j < kSampleThreads; ++j) above += s_tmax[j] > tmax;
-        if (above == k - 1) s_L = tmax;
-    }
-    __syncthreads();
-    const uint64_t L = s_L;
+    if (threadIdx.x == 0) s_ns = 0;
+    const uint64_t L = kth_bound(tmax, k, n_valid, s_wb);   // its barrier also publishes s_ns = 0
 #pragma unroll
     for (int e = 0; e < kE1; ++e)
         if (ck[e] != 0ull && ck[e] >= L) {
@@ -280,53 +274,232 @@ __global__ void __launch_bounds__(kSampleThreads) topk_partial_kernel(const Samp
     if (threadIdx.x == 0) a.cand_cnt[slot0] = k;
 }
 
+// Acceptance by the last row to finish (a.accepted set): the rows' tokens are
+// published with a fence before the count, and read after it.
+__device__ void accept_by_last_row(const SampleArgs &a) {
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(a.done, 1u) == unsigned(a.R - 1);
+    }
+    __syncthreads();
+    if (!s_last || threadIdx.x >= 32) return;
+    __threadfence();
+    const int lane = threadIdx.x, R = a.R;
+    const bool mismatch = lane < R - 1 && __ldcg(&a.drafts[lane]) != __ldcg(&a.tokens[lane]);
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, mismatch);
+    const int acc = m ? __ffs(m) - 1 : R - 1;
+    if (lane == 0) {
+        const int32_t t = __ldcg(&a.tokens[acc]);
+        *a.accepted = acc;
+        if (a.bonus) *a.bonus = t;
+        if (a.acc_pos) *a.acc_pos += acc + 1;
+        *a.done = 0u;   // leave the counter zero for the next call
+    }
+}
+
+__device__ __forceinline__ bool better(double s, int id, double bs, int bid) {
+    return s > bs || (s == bs && id < bid);
+}
+
+// One row's token from a pool of candidate words (E per thread of NT, index
+// e * NT + tid, 0 = none; n_total pool entries) holding the row's k best, L, a
+// lower bound on the k-th best (0: none known), and per thread a word tmax of
+// the pool such that threads below n_thr hold distinct ones (kth_bound turns
+// them into a second bound).  The candidates at or above the larger bound are
+// ranked (radix select when too many survive), giving the k best in order;
+// then the top-p prefix in fp64 summed left to right in rank order, and the
+// Gumbel argmax over it.  Call with the whole block.
+template <int NT, int E>
+__device__ void finalize_row(const SampleArgs &a, const int r, const uint64_t (&ck)[E], uint64_t L, uint64_t tmax,
+                             int n_thr, const int k, const int n_total, const bool bad) {
+    __shared__ uint32_t hist[256];
+    __shared__ int sh[4];
+    __shared__ int s_cnt, s_m, s_ns, s_token;
+    __shared__ float sel_val[kMaxTopK], srt_val[kMaxTopK];
+    __shared__ int32_t sel_id[kMaxTopK], srt_id[kMaxTopK], pb_id[kMaxTopK];
+    __shared__ double ex[kMaxTopK], score[kMaxTopK], gsc[kMaxTopK];
+    __shared__ uint64_t s_surv[kSurvMax];
+    __shared__ uint64_t s_wb[NT / 32];
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        s_ns = 0;
+        s_cnt = 0;
+        s_token = -1;
+    }
+    __syncthreads();
+    if (!bad && n_total > 0) {   // uniform over the block
+        const uint64_t L2 = kth_bound(tmax, k, n_thr, s_wb);
+        L = L > L2 ? L : L2;
+        // candidates at or above the bound
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            if (ck[e] != 0ull && ck[e] >= L) {
+                const int q = atomicAdd(&s_ns, 1);
+                if (q < kSurvMax) s_surv[q] = ck[e];
+            }
+        __syncthreads();
+        const int ns = s_ns;
+        const double T = double(a.temperature);
+        const double p = double(a.top_p);
+        const int64_t pos = a.pos ? a.pos[r] : (*a.pos_base + r);
+        const bool ranked_direct = ns <= kSurvMax;   // uniform over the block
+        if (ranked_direct) {
+            for (int i = tid; i < ns; i += NT) {
+                const uint64_t v = s_surv[i];
+                int rank = 0;
+                for (int j = 0; j < ns; ++j) rank += s_surv[j] > v;
+                if (rank < k) {
+                    srt_val[rank] = key_value(uint32_t(v >> 32));
+                    srt_id[rank] = composite_id(v);
+                }
+            }
+            if (tid == 0) s_cnt = k;
+        } else {
+            uint32_t key[E];
+            int32_t id[E];
+            uint32_t valid = 0;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                key[e] = uint32_t(ck[e] >> 32);
+                id[e] = composite_id(ck[e]);
+                if (ck[e] != 0ull) valid |= 1u << e;
+            }
+            const uint32_t chosen = select_top<E>(key, id, valid, k, hist, sh);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                if ((chosen >> e) & 1u) {
+                    const int q = atomicAdd(&s_cnt, 1);
+                    if (q < kMaxTopK) {
+                        sel_val[q] = key_value(key[e]);
+                        sel_id[q] = id[e];
+                    }
+                }
+            }
+            __syncthreads();
+            const int n_sel = min(s_cnt, kMaxTopK);
+            if (tid < n_sel) {  // rank sort by (logit desc, id asc)
+                const uint64_t ki = composite(order_key(sel_val[tid]), sel_id[tid]);
+                int rank = 0;
+                for (int j = 0; j < n_sel; ++j) rank += composite(order_key(sel_val[j]), sel_id[j]) > ki;
+                srt_val[rank] = sel_val[tid];
+                srt_id[rank] = sel_id[tid];
+            }
+        }
+        __syncthreads();
+        const int n_sel = min(s_cnt, kMaxTopK);
+        if (a.temperature == 0.0f) {
+            if (tid == 0) s_token = srt_id[0];
+        } else {
+            // Warps 2-3 compute every candidate's Gumbel score and warp 2 the
+            // best of every prefix (ties to the lower id), while warps 0-1 run
+            // the top-p prefix; the token is then the best of the kept prefix.
+            if (tid >= 64 && tid < 128) {
+                const int i = tid - 64;
+                if (i < n_sel) gsc[i] = double(srt_val[i]) / T + gumbel(a.seed, pos, srt_id[i]);
+                bar_sync_named(2, 64);
+                if (tid < 96) {
+                    const int lane = tid - 64;
+                    const int i0 = 2 * lane, i1 = 2 * lane + 1;
+                    const double s0 = i0 < n_sel ? gsc[i0] : -1.0 / 0.0, s1 = i1 < n_sel ? gsc[i1] : -1.0 / 0.0;
+                    const int d0 = i0 < n_sel ? srt_id[i0] : 0x7FFFFFFF, d1 = i1 < n_sel ? srt_id[i1] : 0x7FFFFFFF;
+                    double bs = s0;
+                    int bd = d0;
+                    if (better(s1, d1, bs, bd)) {
+                        bs = s1;
+                        bd = d1;
+                    }
+                    // inclusive scan of the pair bests over the lanes
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const double os = __shfl_up_sync(0xFFFFFFFFu, bs, o);
+                        const int od = __shfl_up_sync(0xFFFFFFFFu, bd, o);
+                        if (lane >= o && better(os, od, bs, bd)) {
+                            bs = os;
+                            bd = od;
+                        }
+                    }
+                    double es = __shfl_up_sync(0xFFFFFFFFu, bs, 1);
+                    int ed = __shfl_up_sync(0xFFFFFFFFu, bd, 1);
+                    if (lane == 0) {
+                        es = -1.0 / 0.0;
+                        ed = 0x7FFFFFFF;
+                    }
+                    if (i0 < n_sel) pb_id[i0] = better(s0, d0, es, ed) ? d0 : ed;
+                    if (i1 < n_sel) pb_id[i1] = bd;
+                }
+            }
+            if (tid < 64) {
+                if (p < 1.0) {
+                    __shared__ double s_Z;
+                    if (tid < n_sel) ex[tid] = exp((double(srt_val[tid]) - double(srt_val[0])) / T);
+                    bar_sync_named(1, 64);
+                    if (tid == 0) {
+                        double Z = 0.0;
+                        for (int i = 0; i < n_sel; ++i) Z += ex[i];
+                        s_Z = Z;
+                    }
+                    bar_sync_named(1, 64);
+                    if (tid < n_sel) score[tid] = ex[tid] / s_Z;   // q_i, each term on its own thread
+                    bar_sync_named(1, 64);
+                    if (tid == 0) {
+                        double S = 0.0;
+                        int m = n_sel;
+                        for (int i = 0; i < n_sel; ++i) {   // renormalised mass summed left to right
+                            S += score[i];
+                            if (S >= p) {
+                                m = i + 1;
+                                break;
+                            }
+                        }
+                        s_m = m;
+                    }
+                } else if (tid == 0) {
+                    s_m = n_sel;
+                }
+            }
+            __syncthreads();
+            if (tid == 0) s_token = pb_id[s_m - 1];
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        a.tokens[r] = s_token;           // -1 for a row with a non-finite logit
+        if (bad) a.row_bad[r] = 0;       // leave the workspace clean for the next call
+    }
+    if (a.accepted) accept_by_last_row(a);
+}
+
+// Finaliser over the per-chunk candidates of topk_partial.
 __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleArgs a) {
     grid_dependency_wait();     // inputs come from the preceding grid
     grid_launch_dependents();
-    __shared__ uint32_t hist[256];
-    __shared__ int sh[4];
-    __shared__ int s_cnt, s_m;
-    __shared__ float sel_val[kMaxTopK], srt_val[kMaxTopK];
-    __shared__ int32_t sel_id[kMaxTopK], srt_id[kMaxTopK];
-    __shared__ double ex[kMaxTopK], score[kMaxTopK];
     const int r = blockIdx.x;
     const int tid = threadIdx.x;
     const int nc = a.n_chunks;
-    __shared__ int s_ccnt[kMaxChunks];
     __shared__ unsigned long long s_L;
-    __shared__ int s_total, s_ns;
-    __shared__ uint64_t s_surv[kSurvMax];
-    __shared__ uint64_t s_tmax[kSampleThreads];
+    __shared__ int s_total;
     if (tid == 0) {
         s_L = 0ull;
         s_total = 0;
-        s_ns = 0;
-        s_cnt = 0;
     }
     __syncthreads();
     // chunk counts, their total, and the bound: the largest chunk k-th best
     for (int c = tid; c < nc; c += kSampleThreads) {
-        const int cnt = a.cand_cnt[r * nc + c];
-        s_ccnt[c] = cnt;
-        atomicAdd(&s_total, cnt);
+        atomicAdd(&s_total, a.cand_cnt[r * nc + c]);
         const unsigned long long kth = a.cand_kth[r * nc + c];
         if (kth) atomicMax(&s_L, kth);
     }
     __syncthreads();
     const int n_total = s_total;
     const bool bad = a.row_bad[r] != 0;
-    if (bad || n_total == 0) {
-        if (tid == 0) {
-            a.tokens[r] = -1;
-            a.row_bad[r] = 0;  // leave the workspace clean for the next call
-        }
-        return;
-    }
     const int k = min(a.k_eff, n_total);
     // Every chunk but the last kept exactly k_eff candidates (it had 4096 >= k_eff
     // valid logits), so candidate i of the row sits in chunk i / k_eff, slot
     // i % k_eff; the float quotient is exact here ((i + 0.5) / k_eff never lies
-    // within 1/128 of an integer), and the loads carry no data-dependent branch.
+    // within 1/128 of an integer for i < 8192), and the loads carry no
+    // data-dependent branch.
     const int ke = a.k_eff;
     const float inv_ke = 1.0f / float(ke);
     uint64_t ck[kE2];
@@ -335,141 +508,67 @@ __global__ void __launch_bounds__(kSampleThreads) finalize_kernel(const SampleAr
     for (int e = 0; e < kE2; ++e) {
         const int i = e * kSampleThreads + tid;
         ck[e] = 0ull;
-        if (i < n_total) {
+        if (!bad && i < n_total) {
             const int c = int((float(i) + 0.5f) * inv_ke);
             const long long q = (long long)(r * nc + c) * kMaxTopK + (i - c * ke);
             ck[e] = composite(order_key(a.cand_val[q]), a.cand_id[q]);
         }
         tmax = ck[e] > tmax ? ck[e] : tmax;
     }
-    // a second bound, as in topk_partial: the k-th largest per-thread maximum
-    s_tmax[tid] = tmax;
-    __syncthreads();
-    if (tmax != 0ull) {
-        int above = 0;
-        for (int j = 0; j < kSampleThreads; ++j) above += s_tmax[j] > tmax;
-        if (above == k - 1) atomicMax(&s_L, (unsigned long long)tmax);
-    }
-    __syncthreads();
-    const uint64_t L = s_L;
-    // candidates at or above the bounds
+    // the second bound from the per-thread maxima of the pool
+    finalize_row<kSampleThreads, kE2>(a, r, ck, s_L, tmax, n_total, k, n_total, bad);
+}
+
+// Finaliser over the LM head epilogue's lists: n_chunks lists of exactly
+// k_eff words per row (padded with the empty word).  Every load is issued
+// before any is used: the k-th best words of the lists (their maximum bounds
+// the row's k-th best from below) and the pool, E words per thread.
+constexpr int kListThreads = 512;
+constexpr int kE3 = 16;
+__global__ void __launch_bounds__(kListThreads) finalize_lists_kernel(const SampleArgs a) {
+    grid_dependency_wait();     // inputs come from the preceding grid
+    grid_launch_dependents();
+    const int r = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int nc = a.n_chunks, ke = a.k_eff;
+    const int n_total = nc * ke;
+    __shared__ unsigned long long s_L;
+    if (tid == 0) s_L = 0ull;
+    const uint64_t kth = tid < nc ? a.cand_kth[r * nc + tid] : 0ull;
+    // each list's best word (entry 0: the lists are in descending order)
+    const long long q0 = (long long)(r * nc + (tid < nc ? tid : 0)) * kMaxTopK;
+    const float v0 = a.cand_val[q0];
+    const int32_t id0 = a.cand_id[q0];
+    const float inv_ke = 1.0f / float(ke);
+    float v[kE3];
+    int32_t id[kE3];
 #pragma unroll
-    for (int e = 0; e < kE2; ++e)
-        if (ck[e] != 0ull && ck[e] >= L) {
-            const int q = atomicAdd(&s_ns, 1);
-            if (q < kSurvMax) s_surv[q] = ck[e];
-        }
-    __syncthreads();
-    const int ns = s_ns;
-    if (ns <= kSurvMax) {
-        for (int i = tid; i < ns; i += kSampleThreads) {
-            const uint64_t v = s_surv[i];
-            int rank = 0;
-            for (int j = 0; j < ns; ++j) rank += s_surv[j] > v;
-            if (rank < k) {
-                srt_val[rank] = key_value(uint32_t(v >> 32));
-                srt_id[rank] = composite_id(v);
-            }
-        }
-        if (tid == 0) s_cnt = k;
-    } else {
-        uint32_t key[kE2];
-        int32_t id[kE2];
-        uint32_t valid = 0;
+    for (int e = 0; e < kE3; ++e) {
+        const int i = e * kListThreads + tid;
+        const int ii = i < n_total ? i : 0;
+        const int c = int((float(ii) + 0.5f) * inv_ke);
+        const long long q = (long long)(r * nc + c) * kMaxTopK + (ii - c * ke);
+        v[e] = a.cand_val[q];
+        id[e] = a.cand_id[q];
+    }
+    const bool bad = a.row_bad[r] != 0;
+    uint64_t wm = kth;
 #pragma unroll
-        for (int e = 0; e < kE2; ++e) {
-            key[e] = uint32_t(ck[e] >> 32);
-            id[e] = composite_id(ck[e]);
-            if (ck[e] != 0ull) valid |= 1u << e;
-        }
-        const uint32_t chosen = select_top<kE2>(key, id, valid, k, hist, sh);
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t x = __shfl_xor_sync(0xFFFFFFFFu, wm, o);
+        wm = x > wm ? x : wm;
+    }
+    __syncthreads();
+    if ((tid & 31) == 0 && wm) atomicMax(&s_L, (unsigned long long)wm);
+    uint64_t ck[kE3];
 #pragma unroll
-        for (int e = 0; e < kE2; ++e) {
-            if ((chosen >> e) & 1u) {
-                const int q = atomicAdd(&s_cnt, 1);
-                if (q < kMaxTopK) {
-                    sel_val[q] = key_value(key[e]);
-                    sel_id[q] = id[e];
-                }
-            }
-        }
-        __syncthreads();
-        const int n_sel = min(s_cnt, kMaxTopK);
-        if (tid < n_sel) {  // rank sort by (logit desc, id asc)
-            const uint64_t ki = composite(order_key(sel_val[tid]), sel_id[tid]);
-            int rank = 0;
-            for (int j = 0; j < n_sel; ++j) rank += composite(order_key(sel_val[j]), sel_id[j]) > ki;
-            srt_val[rank] = sel_val[tid];
-            srt_id[rank] = sel_id[tid];
-        }
-    }
+    for (int e = 0; e < kE3; ++e)
+        ck[e] = (!bad && e * kListThreads + tid < n_total) ? composite(order_key(v[e]), id[e]) : 0ull;
+    // the second bound from the lists' best words: thread c < nc holds list c's
+    const uint64_t lmax = (!bad && tid < nc) ? composite(order_key(v0), id0) : 0ull;
     __syncthreads();
-    const int n_sel = min(s_cnt, kMaxTopK);
-    if (a.temperature == 0.0f) {
-        if (tid == 0) a.tokens[r] = srt_id[0];
-        return;
-    }
-    const double T = double(a.temperature);
-    const double p = double(a.top_p);
-    const int64_t pos = a.pos ? a.pos[r] : (*a.pos_base + r);
-    // Warps 2-3 compute every candidate's Gumbel score (only the first m are
-    // used) while warps 0-1 run the top-p prefix on their own barrier.
-    __shared__ double gsc[kMaxTopK];
-    if (tid >= 64 && tid < 64 + n_sel) {
-        const int i = tid - 64;
-        gsc[i] = double(srt_val[i]) / T + gumbel(a.seed, pos, srt_id[i]);
-    }
-    if (tid < 64) {
-        if (p < 1.0) {
-            __shared__ double s_Z;
-            if (tid < n_sel) ex[tid] = exp((double(srt_val[tid]) - double(srt_val[0])) / T);
-            bar_sync_named(1, 64);
-            if (tid == 0) {
-                double Z = 0.0;
-                for (int i = 0; i < n_sel; ++i) Z += ex[i];
-                s_Z = Z;
-            }
-            bar_sync_named(1, 64);
-            if (tid < n_sel) score[tid] = ex[tid] / s_Z;   // q_i, each term on its own thread
-            bar_sync_named(1, 64);
-            if (tid == 0) {
-                double S = 0.0;
-                int m = n_sel;
-                for (int i = 0; i < n_sel; ++i) {   // renormalised mass summed left to right
-                    S += score[i];
-                    if (S >= p) {
-                        m = i + 1;
-                        break;
-                    }
-                }
-                s_m = m;
-            }
-        } else if (tid == 0) {
-            s_m = n_sel;
-        }
-    }
-    __syncthreads();
-    const int m = s_m;
-    // Gumbel-max over the m candidates (ties to the lower id): shuffle reduction in warp 0
-    if (tid < 32) {
-        double best = -1.0 / 0.0;
-        int best_id = 0x7FFFFFFF;
-        for (int i = tid; i < m; i += 32) {
-            if (gsc[i] > best || (gsc[i] == best && srt_id[i] < best_id)) {
-                best = gsc[i];
-                best_id = srt_id[i];
-            }
-        }
-        for (int o = 16; o > 0; o >>= 1) {
-            const double ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-            const int oid = __shfl_xor_sync(0xFFFFFFFFu, best_id, o);
-            if (ob > best || (ob == best && oid < best_id)) {
-                best = ob;
-                best_id = oid;
-            }
-        }
-        if (tid == 0) a.tokens[r] = best_id;
-    }
+    if (tid == 0) a.bound[r] = 0ull;   // the GEMM that shared it has finished
+    finalize_row<kListThreads, kE3>(a, r, ck, s_L, lmax, nc, ke, n_total, bad);
 }
 
 // ---- general candidate path: T > 0 with k' > 64 candidates ----
@@ -598,19 +697,19 @@ __global__ void __launch_bounds__(kGenThreads) gen_select_kernel(const SampleArg
         tau = prefix;
     }
 
-    // e_i of the k' candidates, and Z, each thread summing its own elements in index order
-    double part = 0.0;
-    double *e_row = a.gen_e + (long long)r * V;
-    for (int i = tid; i < V; i += kGenThreads) {
-        const uint64_t cv = row_composite(row, i);
-        const double e = cv >= tau ? exp((double(row[i]) - l0) / T) : 0.0;
-        e_row[i] = e;
-        part += e;
-    }
-    const double Z = block_sum_fixed(part, shd);
     uint64_t beta = tau;
     const double p = double(a.top_p);
-    if (p < 1.0) {
+    if (p < 1.0) {   // top_p >= 1 keeps all k' candidates: no masses needed
+        // e_i of the k' candidates, and Z, each thread summing its own elements in index order
+        double part = 0.0;
+        double *e_row = a.gen_e + (long long)r * V;
+        for (int i = tid; i < V; i += kGenThreads) {
+            const uint64_t cv = row_composite(row, i);
+            const double e = cv >= tau ? exp((double(row[i]) - l0) / T) : 0.0;
+            e_row[i] = e;
+            part += e;
+        }
+        const double Z = block_sum_fixed(part, shd);
         const double target = p * Z;
         uint64_t prefix = 0ull, mask = 0ull;
         double acc = 0.0;   // mass of the candidates above the current bin
@@ -684,10 +783,6 @@ __global__ void __launch_bounds__(kGenThreads) gen_select_kernel(const SampleArg
         }
     }
     if (tid == 0) a.gen_thr[r] = beta;
-}
-
-__device__ __forceinline__ bool better(double s, int id, double bs, int bid) {
-    return s > bs || (s == bs && id < bid);
 }
 
 __global__ void __launch_bounds__(kSampleThreads) gen_score_kernel(const SampleArgs a) {
@@ -785,12 +880,22 @@ __global__ void accept_kernel(const int32_t *drafts, const int32_t *sampled, int
 
 static int n_chunks_of(int V) { return (V + kSampleChunk - 1) / kSampleChunk; }
 
-// Region layout: row_bad flags first, at a fixed offset and sized for the
+// The 256-B header both layouts start with, every word left zero by the calls
+// that use it: row_bad[kMaxRows] at 0, the finished-row counter at 64, the
+// candidate epilogue's shared bounds [kMaxRows] at 128.  A workspace can
+// serve calls of either path and any R.
+static void bind_header(SampleArgs &a, char *p) {
+    a.row_bad = reinterpret_cast<int32_t *>(p);
+    a.done = reinterpret_cast<unsigned *>(p + 64);
+    a.bound = reinterpret_cast<uint64_t *>(p + 128);
+}
+
+// Region layout: the header (bind_header) at a fixed offset and sized for the
 // largest R, so a workspace reused by calls with different R never sees stale
 // flags; the candidate arrays that follow are always written before read.
 size_t sample_workspace_bytes(int R, int V) {
     const size_t nc = size_t(n_chunks_of(V));
-    size_t b = 256;  // row_bad[kMaxRows]
+    size_t b = 256;  // header (bind_header)
     b += size_t(R) * nc * sizeof(uint64_t);
     b += size_t(R) * nc * kMaxTopK * (sizeof(float) + sizeof(int32_t));
     b += size_t(R) * nc * sizeof(int32_t);
@@ -806,7 +911,7 @@ size_t sample_workspace_bytes(int R, int V) {
 void sample_bind_workspace(SampleArgs &a, void *ws_region, int R, int V) {
     const size_t nc = size_t(n_chunks_of(V));
     char *p = static_cast<char *>(ws_region);
-    a.row_bad = reinterpret_cast<int32_t *>(p);
+    bind_header(a, p);
     p += 256;
     a.cand_kth = reinterpret_cast<uint64_t *>(p);
     p += size_t(R) * nc * sizeof(uint64_t);
@@ -837,11 +942,45 @@ cudaError_t launch_keyed_sample(const SampleArgs &a, cudaStream_t s) {
         if (e == cudaSuccess) e = launch_pdl(gen_select_kernel, dim3(a.R), dim3(kGenThreads), 0, s, a);
         if (e == cudaSuccess) e = launch_pdl(gen_score_kernel, dim3(a.n_chunks, a.R), dim3(kSampleThreads), 0, s, a);
         if (e == cudaSuccess) e = launch_pdl(gen_final_kernel, dim3(a.R), dim3(32), 0, s, a);
+        if (e == cudaSuccess && a.accepted) e = launch_accept(a.drafts, a.tokens, a.R, a.accepted, a.bonus, a.acc_pos, s);
         return e;
     }
     cudaError_t e = launch_pdl(topk_partial_kernel, dim3(a.n_chunks, a.R), dim3(kSampleThreads), 0, s, a);
     if (e != cudaSuccess) return e;
-    return launch_pdl(finalize_kernel, dim3(a.R), dim3(kSampleThreads), 0, s, a);
+    return launch_pdl(finalize_kernel, dim3(a.R), dim3(kSampleThreads), 0, s, a);   // accepts too
+}
+
+// ---- candidates written by the LM head's epilogue ----
+size_t sample_candidate_bytes(int R, int nc) {
+    size_t b = 256;  // the header of sample_workspace_bytes
+    b += size_t(R) * nc * sizeof(uint64_t);
+    b += size_t(R) * nc * kMaxTopK * (sizeof(float) + sizeof(int32_t));
+    b += size_t(R) * nc * sizeof(int32_t);
+    return (b + 255) / 256 * 256;
+}
+
+void sample_bind_candidates(SampleArgs &a, void *region, int R, int nc) {
+    char *p = static_cast<char *>(region);
+    bind_header(a, p);
+    p += 256;
+    a.cand_kth = reinterpret_cast<uint64_t *>(p);
+    p += size_t(R) * nc * sizeof(uint64_t);
+    a.cand_val = reinterpret_cast<float *>(p);
+    p += size_t(R) * nc * kMaxTopK * sizeof(float);
+    a.cand_id = reinterpret_cast<int32_t *>(p);
+    p += size_t(R) * nc * kMaxTopK * sizeof(int32_t);
+    a.cand_cnt = reinterpret_cast<int32_t *>(p);
+    a.n_chunks = nc;
+}
+
+bool sample_candidates_fit(int nc, int k_eff) {
+    return nc >= 1 && nc <= kListThreads && k_eff >= 1 && k_eff <= kMaxTopK &&
+           (long long)nc * k_eff <= (long long)kE3 * kListThreads;
+}
+
+cudaError_t launch_sample_finalize(const SampleArgs &a, cudaStream_t s) {
+    if (!sample_candidates_fit(a.n_chunks, a.k_eff)) return cudaErrorInvalidValue;
+    return launch_pdl(finalize_lists_kernel, dim3(a.R), dim3(kListThreads), 0, s, a);
 }
 
 cudaError_t launch_accept(const int32_t *drafts, const int32_t *sampled, int R, int32_t *accepted, int32_t *bonus,

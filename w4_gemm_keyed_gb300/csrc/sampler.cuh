@@ -35,12 +35,30 @@ struct SampleArgs {
     int32_t *gen_bid;     // [R][n_chunks] its token id
     int *err;
     int n_chunks;
+    // acceptance (accepted non-null): a = first i < R - 1 with drafts[i] !=
+    // tokens[i], else R - 1; *accepted = a, *bonus = tokens[a] (bonus may be
+    // null), *acc_pos += a + 1 (acc_pos may be null)
+    const int32_t *drafts;
+    int32_t *accepted;
+    int32_t *bonus;
+    int64_t *acc_pos;
+    unsigned *done;       // workspace counter of finished rows, zero between calls
+    uint64_t *bound;      // [R] candidate epilogue's shared bounds: zeroed by finalize_lists
 };
 
 size_t sample_workspace_bytes(int R, int V);
 void sample_bind_workspace(SampleArgs &a, void *ws_region, int R, int V);
 cudaError_t launch_keyed_sample(const SampleArgs &a, cudaStream_t s);
 int sample_max_vocab();
+
+// Candidates from the LM head's epilogue: nc lists of k_eff (logit, id) per row
+// (every list padded to k_eff with the empty entry: value bits 0xFFFFFFFF, id
+// -1) in the cand_* arrays with chunk stride nc.  finalize alone then merges
+// them, applies top-p and draws the token.
+size_t sample_candidate_bytes(int R, int nc);
+void sample_bind_candidates(SampleArgs &a, void *region, int R, int nc);
+bool sample_candidates_fit(int nc, int k_eff);
+cudaError_t launch_sample_finalize(const SampleArgs &a, cudaStream_t s);
 // Acceptance; if last_token / pos are non-null also writes the bonus to
 // *last_token and advances *pos by a + 1 (device-side chaining of steps).
 cudaError_t launch_accept(const int32_t *drafts, const int32_t *sampled, int R, int32_t *accepted,

@@ -129,6 +129,95 @@ size_t dense_gemm_ws(const tf_w4_matrix &W) {
     return gemm_workspace_bytes(W.K, W.N, W.group, 1, dense_pv(T, W.K / kKChunk));
 }
 
+// ---- LM head + keyed sampling ----
+// Fused when the matrix is symmetric int4, R <= 8 and every CTA's k'
+// candidates fit the finaliser's pool: the GEMM's selector warps leave
+// per-CTA candidate lists, and the finaliser alone merges them.  Otherwise the GEMM writes the
+// logits and the whole sampler runs on them.  Both give the same tokens: the
+// finaliser sees the same k' best (logit, id) in the same order.
+struct LmLayout {
+    size_t gemm, sample, logits, total;
+};
+
+int lmhead_grid(const tf_w4_matrix &W) {
+    GemmArgs a = dense_args(W, 1, nullptr, W.N, kStoreF32);
+    return gemm_grid(a, 1);
+}
+
+LmLayout lm_layout(const tf_w4_matrix &W, int R) {
+    LmLayout l{};
+    size_t off = round256(dense_gemm_ws(W));
+    l.gemm = 0;
+    l.sample = off;
+    const size_t full = sample_workspace_bytes(R, W.N), cand = sample_candidate_bytes(R, lmhead_grid(W));
+    off += round256(full > cand ? full : cand);
+    l.logits = off;
+    off += round256(size_t(R) * W.N * 4);
+    l.total = off;
+    return l;
+}
+
+bool lmhead_fused(const tf_w4_matrix &W, int R, int k_eff) {
+    return !W.affine && R <= kSelMaxRows && sample_candidates_fit(lmhead_grid(W), k_eff);
+}
+
+// gemm_ws: a GEMM workspace (status word first, also the sampler's);
+// sample_ws: >= max(sample_workspace_bytes, sample_candidate_bytes) bytes;
+// logits: where to store the logits (may be null when fused; then the
+// unfused path uses scratch).  pos per row, or pos_base + r when pos is null.
+// accepted non-null: the finaliser also accepts (drafts, bonus, acc_pos as in
+// SampleArgs).
+cudaError_t run_lmhead_sample(const tf_w4_matrix &W, const uint16_t *x, int ldx, int R, const tf_sampling &p,
+                              int k_eff, uint64_t seed, const int64_t *pos, const int64_t *pos_base, int32_t *tokens,
+                              float *logits, int ldl, float *scratch, void *gemm_ws, void *sample_ws,
+                              const int32_t *drafts, int32_t *accepted, int32_t *bonus, int64_t *acc_pos,
+                              cudaStream_t s, const char **why) {
+    int *err = static_cast<int *>(gemm_ws);
+    SampleArgs sa{};
+    sa.drafts = drafts;
+    sa.accepted = accepted;
+    sa.bonus = bonus;
+    sa.acc_pos = acc_pos;
+    sa.R = R;
+    sa.V = W.N;
+    sa.k_eff = k_eff;
+    sa.temperature = p.temperature;
+    sa.top_p = p.top_p;
+    sa.seed = seed;
+    sa.pos = pos;
+    sa.pos_base = pos_base;
+    sa.tokens = tokens;
+    sa.err = err;
+    if (!sa.pos && !sa.pos_base) sa.pos = reinterpret_cast<const int64_t *>(gemm_ws);   // greedy: never read
+    if (lmhead_fused(W, R, k_eff)) {
+        GemmArgs a = dense_args(W, R, logits, logits ? ldl : W.N, kStoreF32);
+        const int nc = gemm_grid(a, 1);
+        sample_bind_candidates(sa, sample_ws, R, nc);
+        a.sel_k = k_eff;
+        a.sel_nc = nc;
+        a.sel_val = sa.cand_val;
+        a.sel_id = sa.cand_id;
+        a.sel_cnt = sa.cand_cnt;
+        a.sel_kth = sa.cand_kth;
+        a.sel_bad = sa.row_bad;
+        a.sel_bound = sa.bound;
+        gemm_bind_workspace(a, gemm_ws, 1);
+        if (!gemm_encode_x(a, x, ldx, 0, 1, why)) return cudaErrorInvalidValue;
+        cudaError_t e = launch_w4_gemm_select(a, s);
+        if (e == cudaSuccess) e = launch_sample_finalize(sa, s);
+        return e;
+    }
+    float *lg = logits ? logits : scratch;
+    const int ld = logits ? ldl : W.N;
+    GemmArgs a = dense_args(W, R, lg, ld, kStoreF32);
+    cudaError_t e = bind_and_launch(a, x, ldx, 0, 1, gemm_ws, s, why);
+    if (e != cudaSuccess) return e;
+    sa.logits = lg;
+    sa.ldl = ld;
+    sample_bind_workspace(sa, sample_ws, R, W.N);
+    return launch_keyed_sample(sa, s);
+}
+
 // ---- MoE workspace layout ----
 struct MoeLayout {
     size_t gemm, ids, w, expert_ids, nprob, slot_of, h, Y, total;
@@ -198,7 +287,10 @@ StepLayout step_layout(const tf_model &m, int R) {
     size_t off = round256(g);
     s.gemm = 0;
     s.sample = off;
-    off += round256(sample_workspace_bytes(R, m.vocab));
+    {
+        const size_t full = sample_workspace_bytes(R, m.vocab), cand = sample_candidate_bytes(R, lmhead_grid(m.lm_head));
+        off += round256(full > cand ? full : cand);
+    }
     s.x = off;
     off += round256(size_t(R) * m.hidden * 4);
     s.n = off;
@@ -592,6 +684,41 @@ tf_status tf_keyed_sample(const float *logits, int32_t ldl, int32_t R, int32_t V
     return ok();
 }
 
+size_t tf_lmhead_sample_workspace_bytes(const tf_w4_matrix *W, int32_t R) {
+    if (R < 1 || R > TF_MAX_ROWS || check_matrix(W, "W") != TF_OK) return 0;
+    return lm_layout(*W, R).total;
+}
+
+tf_status tf_lmhead_sample(const tf_w4_matrix *W, const uint16_t *x, int32_t ldx, int32_t R, const tf_sampling *p,
+                           uint64_t seed, const int64_t *pos, int32_t *tokens, float *logits, int32_t ldl,
+                           const int32_t *drafts, int32_t *accepted, int32_t *bonus, void *ws, size_t ws_bytes,
+                           void *stream) {
+    tf_status st = check_matrix(W, "W");
+    if (st) return st;
+    if (R < 1 || R > TF_MAX_ROWS) return fail(TF_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, TF_MAX_ROWS);
+    if (W->N > sample_max_vocab()) return fail(TF_ERR_UNSUPPORTED, "N=%d exceeds %d", W->N, sample_max_vocab());
+    if (!x || !aligned(x, 16)) return fail(TF_ERR_INVALID_ARG, "x must be non-null and 16-B aligned");
+    if (ldx < W->K || ldx % 8) return fail(TF_ERR_INVALID_ARG, "ldx=%d must be >= K and a multiple of 8", ldx);
+    if (!tokens) return fail(TF_ERR_INVALID_ARG, "tokens must be non-null");
+    if (logits && (!aligned(logits, 4) || ldl < W->N))
+        return fail(TF_ERR_INVALID_ARG, "logits must be 4-B aligned with ldl >= N");
+    if (accepted && R > 1 && !drafts) return fail(TF_ERR_INVALID_ARG, "drafts must be non-null when accepting R > 1 rows");
+    int k_eff = 0;
+    if ((st = check_sampling(p, W->N, &k_eff))) return st;
+    if (p->temperature > 0.f && !pos) return fail(TF_ERR_INVALID_ARG, "pos must be non-null when T > 0");
+    if (size_t((W->N + kTileN - 1) / kTileN) * kFeatWarps > kMaxCounters)
+        return fail(TF_ERR_UNSUPPORTED, "N=%d too large for the split-K counter region", W->N);
+    const LmLayout L = lm_layout(*W, R);
+    if ((st = check_ws(ws, ws_bytes, L.total))) return st;
+    char *base = static_cast<char *>(ws);
+    const char *why = "";
+    cudaError_t e = run_lmhead_sample(*W, x, ldx, R, *p, k_eff, seed, pos, nullptr, tokens, logits, ldl,
+                                      reinterpret_cast<float *>(base + L.logits), ws, base + L.sample, drafts,
+                                      accepted, bonus, nullptr, static_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess) return fail(TF_ERR_CUDA, "tf_lmhead_sample: %s (%s)", cudaGetErrorString(e), why);
+    return ok();
+}
+
 tf_status tf_keyed_hash(const uint64_t *seed, const int64_t *pos, const int32_t *token, int64_t n, uint64_t *h_out,
                         double *g_out, void *stream) {
     if (n < 0) return fail(TF_ERR_INVALID_ARG, "n=%lld must be >= 0", (long long)n);
@@ -781,34 +908,15 @@ tf_status tf_verify_step(const tf_model *m, int32_t R, int32_t *last_token, int6
     float *x = reinterpret_cast<float *>(base + L.x);
     uint16_t *n = reinterpret_cast<uint16_t *>(base + L.n);
     uint16_t *h = reinterpret_cast<uint16_t *>(base + L.h);
-    float *lg = logits ? logits : reinterpret_cast<float *>(base + L.logits);
 
     const char *why = "";
     cudaError_t e = launch_embed(m->embedding, m->vocab, m->hidden, last_token, drafts, R, x, err, s);
     for (int b = 0; b < m->n_blocks && e == cudaSuccess; ++b) e = run_block(*m, b, x, R, n, h, ws, s, &why);
     if (e == cudaSuccess) e = launch_rmsnorm_bf16(x, R, m->hidden, m->rms_eps, n, s);
-    if (e == cudaSuccess) {
-        GemmArgs g = dense_args(m->lm_head, R, lg, m->vocab, kStoreF32);
-        e = bind_and_launch(g, n, m->hidden, 0, 1, ws, s, &why);
-    }
-    if (e == cudaSuccess) {
-        SampleArgs a{};
-        a.logits = lg;
-        a.ldl = m->vocab;
-        a.R = R;
-        a.V = m->vocab;
-        a.k_eff = k_eff;
-        a.temperature = p->temperature;
-        a.top_p = p->top_p;
-        a.seed = seed;
-        a.pos = nullptr;
-        a.pos_base = pos;
-        a.tokens = tokens;
-        a.err = err;
-        sample_bind_workspace(a, base + L.sample, R, m->vocab);
-        e = launch_keyed_sample(a, s);
-    }
-    if (e == cudaSuccess) e = launch_accept(drafts, tokens, R, accepted, last_token, pos, s);
+    if (e == cudaSuccess)
+        e = run_lmhead_sample(m->lm_head, n, m->hidden, R, *p, k_eff, seed, nullptr, pos, tokens, logits, m->vocab,
+                              reinterpret_cast<float *>(base + L.logits), ws, base + L.sample, drafts, accepted,
+                              last_token, pos, s, &why);
     if (e != cudaSuccess) return fail(TF_ERR_CUDA, "tf_verify_step: %s %s", cudaGetErrorString(e), why);
     return ok();
 }

@@ -42,6 +42,7 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include "tf_keys.cuh"
 #include "tf_ptx.cuh"
 #include "w4_gemm.cuh"
 
@@ -310,8 +311,157 @@ __device__ __forceinline__ void store_block(const GemmArgs &a, void *yb, int t, 
     }
 }
 
-template <int G, bool HI, int FMT>
-__global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_constant__ GemmArgs a) {
+// Shared-memory view of the candidate epilogue (selector launches only).
+template <bool HI>
+struct SelView {
+    static constexpr int SR = x_rows(HI);
+    float *ring;          // [kSelSlots][SR][kSelStride]
+    int *f0;              // [kSelSlots]: first feature of the block, -1 = the sender's last
+    int *tail;            // tickets handed out
+    uint64_t *full;       // [kSelSlots]
+    uint64_t *empty;      // [kSelSlots]: one arrival per selector warp
+    uint64_t *lists;      // [SR][kSelList], descending, 0-padded
+    uint64_t *pend;       // [SR][32]: words above the list's k'-th best, not yet merged
+    int *npend;           // [SR]
+    __device__ SelView(uint8_t *base) {
+        ring = reinterpret_cast<float *>(base);
+        f0 = reinterpret_cast<int *>(base + sel_ring_bytes(HI));
+        tail = f0 + kSelSlots;
+        full = reinterpret_cast<uint64_t *>(base + sel_ring_bytes(HI) + 256);
+        empty = full + kSelSlots;
+        lists = empty + kSelSlots;
+        pend = lists + SR * kSelList;
+        npend = reinterpret_cast<int *>(pend + SR * 32);
+    }
+};
+
+// Merges row r's pending words into its list.
+__device__ __forceinline__ void sel_flush(uint64_t *L, uint64_t *P, int *np, int lane) {
+    const int n = *np;
+    if (n == 0) return;
+    warp_merge_rank(L, P, n);
+    if (lane == 0) *np = 0;
+    __syncwarp();
+}
+
+// A selector warp: takes the blocks the storing warps hand over, in ticket
+// order, and for each of its rows (r % kSelWarps == sw) queues the words above
+// the row's current k'-th best; a full queue is merged into the row's list
+// (each word placed by its rank in the merged order).  Once every storing
+// warp has sent its last block it merges what is queued and writes the lists.
+// The kept set of a CTA is exact (its sel_k best over the blocks it stored),
+// whatever the arrival order.  Waits poll with short sleeps (a suspended warp
+// wakes late; a polling one takes few issue slots from the consumers) and
+// give up after kWaitLimit polls.
+template <bool HI>
+__device__ void run_selector(const GemmArgs &a, SelView<HI> v, Sync *sy, int sw) {
+    constexpr int SR = SelView<HI>::SR;
+    const int lane = threadIdx.x & 31;
+    const int kk = a.sel_k;
+    for (int r = sw; r < SR; r += kSelWarps) {
+        for (int i = lane; i < kSelList; i += 32) v.lists[r * kSelList + i] = 0ull;
+        if (lane == 0) v.npend[r] = 0;
+    }
+    __syncwarp();
+    unsigned bad = 0;
+    const unsigned lt = (1u << lane) - 1u;
+    constexpr int RW = (SR + kSelWarps - 1) / kSelWarps;   // rows of this warp
+    uint64_t gb[RW];   // the shared bound of each row, as read during the previous block
+#pragma unroll
+    for (int q = 0; q < RW; ++q) gb[q] = 0ull;
+    bool timed_out = false;
+    for (int t = 0, done = 0; done < kFeatWarps && !timed_out; ++t) {
+        const int slot = t % kSelSlots;
+        const uint32_t par = uint32_t(t / kSelSlots) & 1u;
+        for (uint32_t i = 0;; ++i) {
+            if (__all_sync(0xFFFFFFFFu, mbar_test_wait(&v.full[slot], par))) break;
+            __nanosleep(128);
+            if (i >= kWaitLimit || ((i & 1023u) == 1023u && *reinterpret_cast<volatile int *>(&sy->abort))) {
+                *reinterpret_cast<volatile int *>(&sy->abort) = 1;
+                set_error(a.err, 1);
+                timed_out = true;
+                break;
+            }
+        }
+        if (timed_out) break;
+        const int f0 = v.f0[slot];
+        if (f0 < 0) {
+            ++done;
+        } else {
+            const float *src = v.ring + slot * SR * kSelStride;
+            const int fi = f0 + lane;
+            const bool fv = fi < a.N;
+            // this warp's rows: every value and every threshold first (the row's
+            // own k'-th best, or the shared bound if higher); the shared bounds
+            // for the next block are requested now and arrive meanwhile
+            float xv[RW];
+            uint64_t th[RW], gn[RW];
+#pragma unroll
+            for (int q = 0; q < RW; ++q) {
+                const int r = sw + q * kSelWarps;
+                xv[q] = r < a.R ? src[r * kSelStride + lane] : 0.f;
+                const uint64_t own = r < a.R ? v.lists[r * kSelList + kk - 1] : 0ull;
+                th[q] = own > gb[q] ? own : gb[q];
+                gn[q] = r < a.R ? __ldcg(&a.sel_bound[r]) : 0ull;
+            }
+#pragma unroll
+            for (int q = 0; q < RW; ++q) {
+                const int r = sw + q * kSelWarps;
+                if (r >= a.R) break;
+                const float x = xv[q];
+                if (__any_sync(0xFFFFFFFFu, fv && !isfinite(x))) bad |= 1u << r;
+                const uint64_t key = fv ? composite(order_key(x), fi) : 0ull;
+                uint64_t *L = v.lists + r * kSelList;
+                uint64_t *P = v.pend + r * 32;
+                bool s = key > th[q];
+                unsigned m = __ballot_sync(0xFFFFFFFFu, s);
+                if (!m) continue;
+                int np = v.npend[r];
+                if (np + __popc(m) > 32) {   // queue full: merge it, publish, then re-test against the new k'-th best
+                    sel_flush(L, P, &v.npend[r], lane);
+                    const uint64_t own = L[kk - 1];
+                    if (lane == 0 && own) atomicMax(reinterpret_cast<unsigned long long *>(&a.sel_bound[r]),
+                                                    (unsigned long long)own);
+                    np = 0;
+                    th[q] = own > th[q] ? own : th[q];
+                    s = key > th[q];
+                    m = __ballot_sync(0xFFFFFFFFu, s);
+                }
+                if (s) P[np + __popc(m & lt)] = key;
+                __syncwarp();
+                if (lane == 0) v.npend[r] = np + __popc(m);
+                __syncwarp();
+            }
+#pragma unroll
+            for (int q = 0; q < RW; ++q) gb[q] = gn[q];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&v.empty[slot]);
+    }
+    const long long c = blockIdx.x;
+    for (int r = sw; r < a.R; r += kSelWarps) {
+        uint64_t *L = v.lists + r * kSelList;
+        sel_flush(L, v.pend + r * 32, &v.npend[r], lane);
+        const long long slot = r * (long long)a.sel_nc + c;
+        for (int i = lane; i < kk; i += 32) {
+            const uint64_t w = L[i];
+            a.sel_val[slot * kSelList + i] = w ? key_value(uint32_t(w >> 32)) : __uint_as_float(0xFFFFFFFFu);
+            a.sel_id[slot * kSelList + i] = w ? composite_id(w) : -1;
+        }
+        if (lane == 0) {
+            a.sel_cnt[slot] = kk;
+            a.sel_kth[slot] = L[kk - 1];
+            if ((bad >> r) & 1u) {
+                atomicOr(&a.sel_bad[r], 1);
+                set_error(a.err, 2);
+            }
+        }
+    }
+}
+
+template <int G, bool HI, int FMT, bool SEL = false>
+__global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
+    w4_lane_gemm_kernel(const __grid_constant__ GemmArgs a) {
     constexpr bool AFF = FMT == kFmtAffine;
     constexpr int BB = block_bytes(G, FMT);
     constexpr int CB = chunk_bytes(G, FMT);
@@ -329,6 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
     uint8_t *sw = sx + NS * XST;                         // [NS][STW]
     float *red = reinterpret_cast<float *>(sw + NS * STW);   // [2][kFeatWarps][32][4 * NQ]
     Sync *sy = reinterpret_cast<Sync *>(red + 2 * kFeatWarps * 32 * 4 * NQ);
+    uint8_t *selb = reinterpret_cast<uint8_t *>(sy) + 256;   // SEL: SelView<HI> region
 
     // Work items are (problem u, range vp) pairs, u-major; CTA b takes items
     // b, b + gridDim.x, ...  A grouped launch whose problem list comes from the
@@ -351,6 +502,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
             mbar_init(&sy->empty[s], kConsumerWarps);
         }
         sy->abort = 0;
+        if constexpr (SEL) {
+            SelView<HI> v(selb);
+            for (int i = 0; i < kSelSlots; ++i) {
+                mbar_init(&v.full[i], 1);
+                mbar_init(&v.empty[i], kSelWarps);
+            }
+            *v.tail = 0;
+        }
         fence_mbar_init();
     }
     __syncthreads();
@@ -419,6 +578,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
         return;
     }
 
+    if constexpr (SEL) {
+        if (warp > kConsumerWarps) {
+            grid_dependency_wait();   // the candidate arrays may still be read by a preceding grid
+            run_selector<HI>(a, SelView<HI>(selb), sy, warp - kConsumerWarps - 1);
+            return;
+        }
+    }
+
     // ---------------- consumers ----------------
     const int kg = warp / kFeatWarps;   // k-group: slices kg, kg + 4, ... of each stage
     const int fw = warp % kFeatWarps;   // feature block
@@ -446,6 +613,37 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
         for (int n = 0; n < 2; ++n)
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[mt][n][c] = 0.f;
+
+    // SEL: a storing warp (kg == 0) hands each finished block to the selectors
+    // through the shared ring; f0 < 0 signals its last block
+    auto sel_push = [&](int f0, const float (&v)[2][2][4]) {
+        SelView<HI> sv(selb);
+        int ticket = 0;
+        if (lane == 0) ticket = atomicAdd(sv.tail, 1);
+        ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
+        const int slot = ticket % kSelSlots;
+        bool free_slot = true;
+        if (ticket >= kSelSlots)
+            free_slot = wait_bar(&sv.empty[slot], uint32_t(ticket / kSelSlots - 1) & 1u, sy, a.err);
+        if (free_slot) {
+            if (f0 >= 0) {
+                float *dst = sv.ring + slot * SelView<HI>::SR * kSelStride;
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int n = 0; n < 2; ++n) {
+                        if (n == 1 && !HI) continue;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            dst[(n * 8 + tq * 2 + (c & 1)) * kSelStride + mt * 16 + gq + (c >= 2 ? 8 : 0)] =
+                                v[mt][n][c];
+                    }
+            }
+            if (lane == 0) sv.f0[slot] = f0;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sv.full[slot]);
+    };
 
     grid_dependency_wait();  // activations, workspace and outputs come from earlier grids
     int st = 0;  // stage counter, identical to the producer's
@@ -528,7 +726,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
             add_rb(rb_b);                   // (0 + 1) + (2 + 3)
             const unsigned tb = unsigned(t) * Kc, te = tb + Kc;
             if (seg_b == tb && seg_e == te) {
-                store_block(a, yb, t, fw, gq, tq, hi, acc);
+                if (!SEL || a.y) store_block(a, yb, t, fw, gq, tq, hi, acc);
+                if constexpr (SEL) sel_push(t * kTileN + fw * kBlockRows, acc);
             } else {
                 // stream-K partial.  The last segment to finish sums every
                 // segment of this tile in ascending k order.  A warp that finds
@@ -598,7 +797,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
                         }
                     }
                     if (lane == 0) *ctr = 0u;  // leave the counter zero for the next launch
-                    store_block(a, yb, t, fw, gq, tq, hi, sum);
+                    if (!SEL || a.y) store_block(a, yb, t, fw, gq, tq, hi, sum);
+                    if constexpr (SEL) sel_push(t * kTileN + fw * kBlockRows, sum);
                 }
             }
         }
@@ -609,6 +809,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4_lane_gemm_kernel(const __grid_
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[mt][n][c] = 0.f;
     }
+    }
+    if constexpr (SEL) {
+        if (kg == 0) sel_push(-1, acc);
     }
 }
 
@@ -839,26 +1042,31 @@ __global__ void pack_scales_nvfp4_kernel(const uint8_t *scales, int K, int N, ui
     *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
 }
 
-template <int G, bool HI, int FMT>
+int grid_of(const GemmArgs &a, int u_max) {
+    // persistent over work items: at most one CTA per SM
+    const long long items = (long long)a.Pv * u_max;
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 1;
+    return int(items < sms ? items : sms);
+}
+
+template <int G, bool HI, int FMT, bool SEL = false>
 cudaError_t launch_gemm_g(const GemmArgs &a, int u_max, cudaStream_t s) {
-    const size_t smem = gemm_smem_bytes(G, HI, FMT);
+    const size_t smem = gemm_smem_bytes(G, HI, FMT, SEL);
     // the shared-memory opt-in is a per-device property of the kernel: set it once
     static std::atomic<bool> opted_in[kMaxDevices];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
-        err = cudaFuncSetAttribute(w4_lane_gemm_kernel<G, HI, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        err = cudaFuncSetAttribute(w4_lane_gemm_kernel<G, HI, FMT, SEL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   int(smem));
         if (err != cudaSuccess) return err;
         if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
-    // persistent over work items: at most one CTA per SM
-    const long long items = (long long)a.Pv * u_max;
-    int sms = device_sm_count();
-    if (sms <= 0) sms = 1;
-    cfg.gridDim = dim3(unsigned(items < sms ? items : sms));
-    cfg.blockDim = dim3(kThreads);
+    cfg.gridDim = dim3(unsigned(grid_of(a, u_max)));
+    cfg.blockDim = dim3(SEL ? kThreads + 32 * kSelWarps : kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -866,7 +1074,7 @@ cudaError_t launch_gemm_g(const GemmArgs &a, int u_max, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, w4_lane_gemm_kernel<G, HI, FMT>, a);
+    return cudaLaunchKernelEx(&cfg, w4_lane_gemm_kernel<G, HI, FMT, SEL>, a);
 }
 
 template <int G>
@@ -950,6 +1158,17 @@ cudaError_t launch_w4_gemm(const GemmArgs &a, int u_max, cudaStream_t s) {
     }
     if (hi) return a.G == 64 ? launch_gemm_g<64, true, kFmtSym>(a, u_max, s) : launch_gemm_g<32, true, kFmtSym>(a, u_max, s);
     return a.G == 64 ? launch_gemm_g<64, false, kFmtSym>(a, u_max, s) : launch_gemm_g<32, false, kFmtSym>(a, u_max, s);
+}
+
+int gemm_grid(const GemmArgs &a, int u_max) { return grid_of(a, u_max); }
+
+cudaError_t launch_w4_gemm_select(const GemmArgs &a, cudaStream_t s) {
+    if (a.fmt != kFmtSym || a.n_problems || a.expert_ids || a.mode != kStoreF32 || a.sel_k < 1 ||
+        a.sel_k > kSelList || a.sel_nc != grid_of(a, 1) || !a.sel_val || !a.sel_id || !a.sel_cnt || !a.sel_kth ||
+        !a.sel_bad || !a.sel_bound)
+        return cudaErrorInvalidValue;
+    if (a.R > kSelMaxRows) return cudaErrorInvalidValue;
+    return a.G == 64 ? launch_gemm_g<64, false, kFmtSym, true>(a, 1, s) : launch_gemm_g<32, false, kFmtSym, true>(a, 1, s);
 }
 
 cudaError_t launch_pack_w4_affine(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases, int K, int N,

@@ -63,13 +63,37 @@ constexpr size_t kSlotBytes = size_t(kFeatWarps) * 32 * kLaneAccHi * 4;
 // smaller copies in more stages).
 __host__ __device__ constexpr int num_stages(int, bool, int) { return kStages; }
 
-inline size_t gemm_smem_bytes(int G, bool hi, int fmt = kFmtSym) {
+// Candidate epilogue (LM head): kSelWarps extra warps, the selectors, keep
+// for every row the kSelList best (logit, id) words of the feature blocks its
+// CTA stores.  A storing consumer warp takes a ticket, waits for slot
+// ticket % kSelSlots of one shared ring to be free, writes its finished
+// 32-feature block there ([rows][kSelStride] fp32; the stride keeps the
+// lanes' stores on distinct banks) and signals the slot's barrier; the
+// selectors take the slots in ticket order.
+constexpr int kSelSlots = 16;
+constexpr int kSelStride = 36;
+constexpr int kSelList = 64;
+constexpr int kSelMaxRows = 8;             // launches of up to 8 rows only: at 16 rows the consumers are
+                                           // issue-bound and the selectors' scan slows them (measured)
+constexpr int kSelWarps = 3;               // selector warps; row r belongs to warp r % kSelWarps (20 warps
+                                           // in all keep 96 registers a thread; 21 cap them at 80)
+__host__ __device__ constexpr int sel_ring_bytes(bool hi) { return kSelSlots * x_rows(hi) * kSelStride * 4; }
+__host__ __device__ constexpr int sel_smem_bytes(bool hi) {
+    return sel_ring_bytes(hi) + 256                   // ring + slot headers and the ticket counter
+           + 2 * kSelSlots * 8                        // full / empty barriers
+           + x_rows(hi) * kSelList * 8                // per-row lists
+           + x_rows(hi) * 32 * 8                      // per-row pending words
+           + 64;                                      // pending counts
+}
+
+inline size_t gemm_smem_bytes(int G, bool hi, int fmt = kFmtSym, bool sel = false) {
     const int ns = num_stages(G, hi, fmt);
     return 1024                                                         // alignment slack
            + size_t(ns) * x_stage_bytes(hi)                             // activation slices (1024-B aligned)
            + size_t(ns) * kStageIters * chunk_bytes(G, fmt)            // weight stages
            + 2 * size_t(kFeatWarps) * 32 * lane_vals(hi) * 4            // k-group combine buffers
-           + 256;                                                       // barriers
+           + 256                                                        // barriers
+           + (sel ? size_t(sel_smem_bytes(hi)) : 0);
 }
 
 inline bool packed_shape_ok(int K, int N, int G) {
@@ -114,6 +138,23 @@ struct GemmArgs {
     unsigned *counters;        // [U_max][T][kFeatWarps], zero between launches
     float4 *partials;          // [U_max][Pv][2][kFeatWarps][32][4]
     int *err;
+    // candidate epilogue (launch_w4_gemm_select; dense launches only): CTA c
+    // writes, for every row r, its sel_k best (logit, id) in descending order
+    // at [r][c][0..sel_k) of sel_val / sel_id (padded with value bits
+    // 0xFFFFFFFF and id -1), sel_cnt[r][c] = sel_k and sel_kth[r][c] = its
+    // sel_k-th best word (0 if it saw fewer); rows with a non-finite logit
+    // set sel_bad[r].  y may be null (no logits stored).  CTAs share, per
+    // row, the largest k'-th best any of them has reached (sel_bound): a
+    // word at or below it cannot be among the row's k' best, so no CTA keeps
+    // it; a list may then hold fewer than sel_k words (padded).
+    int sel_k;
+    int sel_nc;                // chunk stride of the candidate arrays = the launch's grid size
+    float *sel_val;
+    int32_t *sel_id;
+    int32_t *sel_cnt;
+    uint64_t *sel_kth;
+    int32_t *sel_bad;
+    uint64_t *sel_bound;       // [R], zero before the launch: the largest k'-th best any CTA has published
 };
 
 // GEMM workspace: [0, 256) status word | [256, 256 + kCounterBytes) split-K
@@ -130,6 +171,11 @@ void gemm_bind_workspace(GemmArgs &a, void *ws, int u_max);
 // if the driver rejects the description.
 bool gemm_encode_x(GemmArgs &a, const uint16_t *x, int ldx, long long x_stride, int u_max, const char **why);
 cudaError_t launch_w4_gemm(const GemmArgs &a, int u_max, cudaStream_t s);
+// Grid size of a launch of a (one CTA per work item, at most one per SM).
+int gemm_grid(const GemmArgs &a, int u_max);
+// Dense symmetric-int4 launch with the candidate epilogue (a.sel_* set, sel_nc
+// = gemm_grid(a, 1), 1 <= sel_k <= kSelList, R <= kSelMaxRows).
+cudaError_t launch_w4_gemm_select(const GemmArgs &a, cudaStream_t s);
 // interleave_gate_up: rows [0, N/2) are gate rows, [N/2, N) up rows; they are
 // packed so that each 32-row feature block holds 16 gate rows (sub-tile 0) and
 // the 16 matching up rows (sub-tile 1), the layout kSwiGluBf16 expects.

@@ -85,6 +85,9 @@ SIGNATURES = [
     ("tf_keyed_sample_workspace_bytes", SZ, [I32, I32]),
     ("tf_keyed_sample", ctypes.c_int, [P, I32, I32, I32, ctypes.POINTER(SamplingC), ctypes.c_uint64, P, P, P, SZ, P]),
     ("tf_keyed_hash", ctypes.c_int, [P, P, P, ctypes.c_int64, P, P, P]),
+    ("tf_lmhead_sample_workspace_bytes", SZ, [ctypes.POINTER(W4MatrixC), I32]),
+    ("tf_lmhead_sample", ctypes.c_int, [ctypes.POINTER(W4MatrixC), P, I32, I32, ctypes.POINTER(SamplingC),
+                                        ctypes.c_uint64, P, P, P, I32, P, P, P, P, SZ, P]),
     ("tf_accept", ctypes.c_int, [P, P, I32, P, P, P]),
     ("tf_gather_drafts", ctypes.c_int, [P, ctypes.c_int64, P, I32, P, P]),
     ("tf_commit_tokens", ctypes.c_int, [P, P, P, P, ctypes.c_int64, P]),
@@ -366,6 +369,38 @@ def keyed_sample(logits: torch.Tensor, temperature: float, top_k: int, top_p: fl
     sp = SamplingC(temperature, top_k, top_p)
     _check(lib.tf_keyed_sample(_ptr(logits), logits.stride(0), R, V, ctypes.byref(sp), ctypes.c_uint64(seed & (2**64 - 1)),
                                _ptr(pos), _ptr(tokens), _ptr(ws), ws.numel(), _stream(stream)))
+    return tokens
+
+
+def lmhead_sample_workspace_bytes(W: W4Matrix, R: int) -> int:
+    wc = W.c()
+    return int(load().tf_lmhead_sample_workspace_bytes(ctypes.byref(wc), R))
+
+
+def lmhead_sample(W: W4Matrix, x: torch.Tensor, temperature: float, top_k: int, top_p: float, seed: int,
+                  pos: torch.Tensor = None, tokens: torch.Tensor = None, logits: torch.Tensor = None,
+                  drafts: torch.Tensor = None, accepted: torch.Tensor = None, bonus: torch.Tensor = None,
+                  ws: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """tokens[R] = keyed sample of the LM head's logits W x[R] in one call; logits
+    (fp32 [R][>= N]) are also stored when given; with `accepted` (int32 [1]) the
+    drafts are accepted against the tokens in the same call."""
+    lib = load()
+    _check_rows_in(x, W.K)
+    R = x.shape[0]
+    if tokens is None:
+        tokens = torch.empty(R, dtype=torch.int32, device=x.device)
+    if tokens.dtype != torch.int32 or tokens.numel() < R or not tokens.is_contiguous():
+        raise TFError(TF_ERR_INVALID_ARG, "tokens must be a contiguous int32 tensor of >= R entries")
+    if logits is not None:
+        _check_rows_out(logits, R, W.N, x.device)
+    if ws is None:
+        ws = workspace(lmhead_sample_workspace_bytes(W, R), x.device)
+    wc = W.c()
+    sp = SamplingC(temperature, top_k, top_p)
+    _check(lib.tf_lmhead_sample(ctypes.byref(wc), _ptr(x), x.stride(0), R, ctypes.byref(sp),
+                                ctypes.c_uint64(seed & (2**64 - 1)), _ptr(pos), _ptr(tokens), _ptr(logits),
+                                logits.stride(0) if logits is not None else 0, _ptr(drafts), _ptr(accepted),
+                                _ptr(bonus), _ptr(ws), ws.numel(), _stream(stream)))
     return tokens
 
 
