@@ -118,6 +118,25 @@ def test_general_path_ties_and_small_vocabularies(tf, near_tie):
             check_tokens_general(gpu_sample(tf, logits, T, k, p, 17, pos), logits, T, k, p, 17, pos, near_tie)
 
 
+@pytest.mark.parametrize("dist", ["narrow", "wide", "quantised"])
+@pytest.mark.parametrize("k,T,p", [(0, 0.7, 0.01), (0, 1.0, 0.999999), (3000, 0.9, 0.9), (0, 0.05, 0.5)])
+def test_general_path_logit_shapes(tf, near_tie, dist, k, T, p):
+    """Logit distributions that take the radix select and the top-p walk
+    through their gathering steps at different depths: a narrow spread (the
+    leading digits never split), a wide one, and coarse steps (long runs of
+    equal logits, broken by id)."""
+    rng = inputs.rng_for(208, ["narrow", "wide", "quantised"].index(dist), k, int(p * 1e6))
+    R, V = 3, 151936
+    if dist == "narrow":
+        logits = (1.5 + 0.01 * rng.standard_normal((R, V))).astype(np.float32)
+    elif dist == "wide":
+        logits = (10.0 * rng.standard_normal((R, V))).astype(np.float32)
+    else:
+        logits = np.round(2.0 * rng.standard_normal((R, V)) * 8.0).astype(np.float32) / 8.0
+    pos = inputs.positions(rng, R)
+    check_tokens_general(gpu_sample(tf, logits, T, k, p, 23, pos), logits, T, k, p, 23, pos, near_tie)
+
+
 def test_general_path_rows_independent_of_R_and_nan_rows(tf):
     rng = inputs.rng_for(207)
     V = 151936

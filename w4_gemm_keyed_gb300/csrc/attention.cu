@@ -400,7 +400,6 @@ cudaError_t launch_kv_append(const uint16_t *k_new, const uint16_t *v_new, int l
 }
 
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s) {
-    constexpr int kMaxDevices = 64;
     static std::atomic<bool> opted_in[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -22,6 +22,8 @@
 //      order; then the top-p prefix in fp64 left to right and the Gumbel argmax.
 // Every decision depends on the row's own logits only, so a row's token is the
 // same whatever R is.
+#include <atomic>
+
 #include <cuda_runtime.h>
 
 #include "sampler.cuh"
@@ -574,21 +576,34 @@ __global__ void __launch_bounds__(kListThreads) finalize_lists_kernel(const Samp
 // ---- general candidate path: T > 0 with k' > 64 candidates ----
 // Same candidate set and selection as the fast path (rank order by (logit
 // desc, id asc), the first k', then the top-p prefix, then the Gumbel argmax),
-// for any k' up to V.  Four launches, every reduction in a fixed order or on
-// integers, so a row's token depends on its own logits only:
+// for any k' up to V.  Every reduction runs in a fixed order or on integers,
+// so a row's token depends on its own logits only:
 //   gen_prep   (chunk, row): the chunk's largest key; non-finite logits flag the row.
-//   gen_select (row, 1024 threads): the k'-th largest key by an 8-bit radix
-//              select over the row; e_i = exp((l_i - l_0) / T) in fp64 for the
-//              k' candidates and Z = sum e_i; then the top-p boundary: the
-//              largest key b with sum_{key >= b} e >= top_p * Z, found by a
-//              4-bit radix walk over per-bin fp64 masses, which stops once the
-//              boundary bin holds a single element.
-//   gen_score  (chunk, row): the best (l / T + g, id) among candidates >= b.
-//   gen_final  (row): the best over the chunks.
+//   gen_select (row): the k'-th largest key tau by an 8-bit radix select,
+//              most significant digit first; once the digit's bin is small
+//              its keys are gathered into shared memory and the remaining
+//              digits are read there.  (tau = 0 when k' = V.)
+//   gen_exp    (sub-chunk of 1024, row; top_p < 1): e_i = exp((l_i - l_0) / T)
+//              in fp64 for the candidates (key >= tau), and the sub-chunk's
+//              sum of them in a fixed order.
+//   gen_walk   (row; top_p < 1): Z = the sub-chunk sums in order; the top-p
+//              boundary b, the largest key with sum_{key >= b} e >= top_p * Z,
+//              by a 4-bit radix walk over per-bin fp64 masses (each thread
+//              adds its own elements into private bins; the bins are then
+//              summed in a fixed order); once the boundary bin is small its
+//              (key, e) pairs are gathered in a fixed order into shared memory.
+//   gen_score  (sub-chunk, row): the best (l / T + g, id) among keys >= b.
+//   gen_final  (row): the best over the sub-chunks.
 // The masses are summed in a fixed order that is not the rank order, so the
 // boundary agrees with a left-to-right sum except when the mass reaching it
 // lies within rounding (~1e-12 relative) of top_p * Z.
 constexpr int kGenThreads = 512;
+constexpr int kGenSub = 1024;                        // sub-chunk of gen_exp / gen_score
+constexpr int kGenSubThreads = 256;
+constexpr int kGenE = kGenSub / kGenSubThreads;      // 4 elements a thread
+constexpr int kSelectCompact = 8192;                 // keys gen_select gathers (64 KB)
+constexpr int kWalkCompact = 4096;                   // (key, e) pairs gen_walk gathers (64 KB)
+constexpr size_t kWalkSmem = size_t(16) * kGenThreads * 8 + size_t(16) * kGenThreads * 4 + size_t(kWalkCompact) * 16;
 
 __device__ __forceinline__ uint64_t row_composite(const float *row, int i) { return composite(order_key(row[i]), i); }
 
@@ -626,31 +641,22 @@ __global__ void __launch_bounds__(kSampleThreads) gen_prep_kernel(const SampleAr
     }
 }
 
-// Fixed-order block sum of one fp64 value per thread (kGenThreads threads).
-__device__ double block_sum_fixed(double v, double *sh) {
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    const int w = threadIdx.x >> 5;
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) sh[w] = v;
-    __syncthreads();
-    double t = 0.0;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kGenThreads / 32; ++i) t += sh[i];
-        sh[32] = t;
-    }
-    __syncthreads();
-    return sh[32];
+// Counts key into hist[digit] with one shared atomic per distinct digit of the warp.
+__device__ __forceinline__ void hist_add(unsigned *hist, bool take, unsigned digit) {
+    const unsigned act = __ballot_sync(0xFFFFFFFFu, take);
+    if (!act) return;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, take ? digit : 0xFFFFFFFFu);
+    const int lane = threadIdx.x & 31;
+    if (take && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], unsigned(__popc(peers)));
 }
 
 __global__ void __launch_bounds__(kGenThreads) gen_select_kernel(const SampleArgs a) {
     grid_dependency_wait();
     grid_launch_dependents();
-    __shared__ unsigned int hist[256];
-    __shared__ double shd[33];
-    __shared__ double bmass[16][kGenThreads / 32];
-    __shared__ unsigned int bcnt[16];
-    __shared__ unsigned long long s_u64;
-    __shared__ int s_int[2];
+    extern __shared__ uint64_t gsel[];   // [kSelectCompact] gathered keys
+    __shared__ unsigned hist[256];
+    __shared__ int s_int[3];
+    __shared__ int s_n;
     const int r = blockIdx.x, tid = threadIdx.x;
     const float *row = a.logits + (long long)r * a.ldl;
     const int V = a.V;
@@ -658,25 +664,25 @@ __global__ void __launch_bounds__(kGenThreads) gen_select_kernel(const SampleArg
         if (tid == 0) a.gen_thr[r] = ~0ull;   // no candidates: gen_final writes -1
         return;
     }
-    // l_0: the largest key of the row
-    if (tid == 0) s_u64 = 0ull;
-    __syncthreads();
-    for (int c = tid; c < a.n_chunks; c += kGenThreads) atomicMax(&s_u64, (unsigned long long)a.gen_cmax[r * a.n_chunks + c]);
-    __syncthreads();
-    const double l0 = double(key_value(uint32_t(s_u64 >> 32)));
-    const double T = double(a.temperature);
-
-    // tau: the k'-th largest composite key (8-bit radix select, most significant digit first)
-    uint64_t tau = 0ull;
+    uint64_t tau = 0ull;   // k' = V: every key
     if (a.k_eff < V) {
         uint64_t prefix = 0ull, mask = 0ull;
-        int remaining = a.k_eff;
+        int remaining = a.k_eff, n_c = -1;   // n_c >= 0: the bin's keys sit in gsel[0, n_c)
         for (int shift = 56; shift >= 0; shift -= 8) {
             for (int i = tid; i < 256; i += kGenThreads) hist[i] = 0u;
             __syncthreads();
-            for (int i = tid; i < V; i += kGenThreads) {
-                const uint64_t cv = row_composite(row, i);
-                if ((cv & mask) == prefix) atomicAdd(&hist[(cv >> shift) & 0xFFu], 1u);
+            if (n_c < 0) {
+                for (int i0 = 0; i0 < V; i0 += kGenThreads) {   // whole warps, for the vote
+                    const int i = i0 + tid;
+                    const uint64_t cv = i < V ? row_composite(row, i) : 0ull;
+                    hist_add(hist, i < V && (cv & mask) == prefix, unsigned(cv >> shift) & 0xFFu);
+                }
+            } else {
+                for (int j0 = 0; j0 < n_c; j0 += kGenThreads) {
+                    const int j = j0 + tid;
+                    const uint64_t cv = j < n_c ? gsel[j] : 0ull;
+                    hist_add(hist, j < n_c && (cv & mask) == prefix, unsigned(cv >> shift) & 0xFFu);
+                }
             }
             __syncthreads();
             if (tid == 0) {
@@ -687,109 +693,224 @@ __global__ void __launch_bounds__(kGenThreads) gen_select_kernel(const SampleArg
                 }
                 s_int[0] = d;
                 s_int[1] = run;
+                s_int[2] = int(hist[d]);
             }
             __syncthreads();
             prefix |= uint64_t(s_int[0]) << shift;
             mask |= 0xFFull << shift;
             remaining -= s_int[1];
+            if (n_c < 0 && shift > 0 && s_int[2] <= kSelectCompact) {   // gather the bin (any order: counts only)
+                if (tid == 0) s_n = 0;
+                __syncthreads();
+                for (int i = tid; i < V; i += kGenThreads) {
+                    const uint64_t cv = row_composite(row, i);
+                    if ((cv & mask) == prefix) gsel[atomicAdd(&s_n, 1)] = cv;
+                }
+                __syncthreads();
+                n_c = s_n;
+            }
             __syncthreads();
         }
         tau = prefix;
     }
+    if (tid == 0) a.gen_thr[r] = tau;
+}
 
-    uint64_t beta = tau;
-    const double p = double(a.top_p);
-    if (p < 1.0) {   // top_p >= 1 keeps all k' candidates: no masses needed
-        // e_i of the k' candidates, and Z, each thread summing its own elements in index order
-        double part = 0.0;
-        double *e_row = a.gen_e + (long long)r * V;
-        for (int i = tid; i < V; i += kGenThreads) {
-            const uint64_t cv = row_composite(row, i);
-            const double e = cv >= tau ? exp((double(row[i]) - l0) / T) : 0.0;
-            e_row[i] = e;
-            part += e;
-        }
-        const double Z = block_sum_fixed(part, shd);
-        const double target = p * Z;
-        uint64_t prefix = 0ull, mask = 0ull;
-        double acc = 0.0;   // mass of the candidates above the current bin
-        bool found = false;
-        for (int shift = 60; shift >= 0 && !found; shift -= 4) {
-            double m16[16];
-            unsigned c16[16];
+__global__ void __launch_bounds__(kGenSubThreads) gen_exp_kernel(const SampleArgs a) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    __shared__ unsigned long long s_top;
+    __shared__ double s_w[kGenSubThreads / 32];
+    const int c = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
+    const uint64_t tau = a.gen_thr[r];
+    if (tid == 0) s_top = 0ull;
+    __syncthreads();
+    for (int k = tid; k < a.n_chunks; k += kGenSubThreads) atomicMax(&s_top, (unsigned long long)a.gen_cmax[r * a.n_chunks + k]);
+    __syncthreads();
+    if (tau == ~0ull) return;   // row with a non-finite logit
+    const float *row = a.logits + (long long)r * a.ldl;
+    const double l0 = double(key_value(uint32_t(s_top >> 32)));
+    const double T = double(a.temperature);
+    double part = 0.0;
 #pragma unroll
-            for (int d = 0; d < 16; ++d) {
-                m16[d] = 0.0;
-                c16[d] = 0u;
-            }
+    for (int e = 0; e < kGenE; ++e) {   // this thread's elements in index order
+        const int i = c * kGenSub + e * kGenSubThreads + tid;
+        if (i < a.V) {
+            const double v = row_composite(row, i) >= tau ? exp((double(row[i]) - l0) / T) : 0.0;
+            a.gen_e[(long long)r * a.V + i] = v;
+            part += v;
+        }
+    }
+    // fixed order: a butterfly within each warp, then the warps in order
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
+    if ((tid & 31) == 0) s_w[tid >> 5] = part;
+    __syncthreads();
+    if (tid == 0) {
+        double z = 0.0;
+        for (int w = 0; w < kGenSubThreads / 32; ++w) z += s_w[w];
+        a.gen_zp[r * a.n_sub + c] = z;
+    }
+}
+
+// Inclusive scan (integer) over the block of kGenThreads threads.
+__device__ __forceinline__ int block_scan_incl(int v, int *sh) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= o) v += x;
+    }
+    if (lane == 31) sh[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        int t = lane < kGenThreads / 32 ? sh[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xFFFFFFFFu, t, o);
+            if (lane >= o) t += x;
+        }
+        if (lane < kGenThreads / 32) sh[lane] = t;
+    }
+    __syncthreads();
+    const int add = w > 0 ? sh[w - 1] : 0;
+    __syncthreads();
+    return v + add;
+}
+
+__global__ void __launch_bounds__(kGenThreads) gen_walk_kernel(const SampleArgs a) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    extern __shared__ uint8_t gwalk[];
+    double *bins = reinterpret_cast<double *>(gwalk);                                  // [16][kGenThreads]
+    int *cnts = reinterpret_cast<int *>(bins + 16 * kGenThreads);                      // [16][kGenThreads]
+    uint64_t *ckey = reinterpret_cast<uint64_t *>(cnts + 16 * kGenThreads);            // [kWalkCompact]
+    double *ce = reinterpret_cast<double *>(ckey + kWalkCompact);                      // [kWalkCompact]
+    __shared__ double bm[16];
+    __shared__ int bc[16];
+    __shared__ double s_z;
+    __shared__ int s_int[2];
+    __shared__ int s_scan[32];
+    __shared__ unsigned long long s_u64;
+    const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int V = a.V;
+    const uint64_t tau = a.gen_thr[r];
+    if (tau == ~0ull) return;
+    const float *row = a.logits + (long long)r * a.ldl;
+    const double *e_row = a.gen_e + (long long)r * V;
+    if (w == 0) {   // Z: lane l sums sub-chunks l, l + 32, ... in order, then a butterfly
+        double z = 0.0;
+        for (int c = lane; c < a.n_sub; c += 32) z += a.gen_zp[r * a.n_sub + c];
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+        if (lane == 0) s_z = z;
+    }
+    __syncthreads();
+    const double target = double(a.top_p) * s_z;
+    uint64_t prefix = 0ull, mask = 0ull, beta = tau;
+    double acc = 0.0;   // mass of the candidates above the current bin
+    int n_c = -1;       // n_c >= 0: the bin's pairs sit in ckey / ce, thread t's at t, t + kGenThreads, ...
+    for (int shift = 60; shift >= 0; shift -= 4) {
+#pragma unroll
+        for (int d = 0; d < 16; ++d) {
+            bins[d * kGenThreads + tid] = 0.0;
+            cnts[d * kGenThreads + tid] = 0;
+        }
+        if (n_c < 0) {
             for (int i = tid; i < V; i += kGenThreads) {
                 const uint64_t cv = row_composite(row, i);
                 if (cv >= tau && (cv & mask) == prefix) {
                     const int d = int((cv >> shift) & 0xFu);
-                    const double e = e_row[i];
-#pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        if (q == d) {
-                            m16[q] += e;
-                            ++c16[q];
-                        }
+                    bins[d * kGenThreads + tid] += e_row[i];
+                    cnts[d * kGenThreads + tid] += 1;
                 }
             }
-            if (tid < 16) bcnt[tid] = 0u;
-            __syncthreads();
-#pragma unroll
-            for (int d = 0; d < 16; ++d) {
-                double v = m16[d];
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                if ((tid & 31) == 0) bmass[d][tid >> 5] = v;
-                if (c16[d]) atomicAdd(&bcnt[d], c16[d]);
-            }
-            __syncthreads();
-            if (tid == 0) {
-                int chosen = -1;
-                for (int d = 15; d >= 0; --d) {
-                    if (bcnt[d] == 0u) continue;
-                    double bm = 0.0;
-                    for (int w = 0; w < kGenThreads / 32; ++w) bm += bmass[d][w];
-                    if (acc + bm >= target) {
-                        chosen = d;
-                        break;
-                    }
-                    acc += bm;
-                }
-                s_int[0] = chosen;
-                s_int[1] = chosen >= 0 ? int(bcnt[chosen]) : 0;
-            }
-            __syncthreads();
-            const int chosen = s_int[0];
-            if (chosen < 0) {                 // the whole mass stays below top_p * Z: keep all k'
-                found = true;
-            } else {
-                prefix |= uint64_t(chosen) << shift;
-                mask |= 0xFull << shift;
-                if (s_int[1] == 1 || shift == 0) {   // one element left in the bin: the boundary
-                    if (tid == 0) s_u64 = 0ull;
-                    __syncthreads();
-                    for (int i = tid; i < V; i += kGenThreads) {
-                        const uint64_t cv = row_composite(row, i);
-                        if (cv >= tau && (cv & mask) == prefix) atomicMax(&s_u64, (unsigned long long)cv);
-                    }
-                    __syncthreads();
-                    beta = s_u64;
-                    found = true;
+        } else {
+            for (int j = tid; j < n_c; j += kGenThreads) {
+                const uint64_t cv = ckey[j];
+                if ((cv & mask) == prefix) {
+                    const int d = int((cv >> shift) & 0xFu);
+                    bins[d * kGenThreads + tid] += ce[j];
+                    cnts[d * kGenThreads + tid] += 1;
                 }
             }
-            __syncthreads();
         }
+        __syncthreads();
+        if (w < 16) {   // warp d: the bin's mass over the threads in a fixed order, and its count
+            double m = 0.0;
+            int n = 0;
+            for (int t = lane; t < kGenThreads; t += 32) {
+                m += bins[w * kGenThreads + t];
+                n += cnts[w * kGenThreads + t];
+            }
+            for (int o = 16; o > 0; o >>= 1) {
+                m += __shfl_xor_sync(0xFFFFFFFFu, m, o);
+                n += __shfl_xor_sync(0xFFFFFFFFu, n, o);
+            }
+            if (lane == 0) {
+                bm[w] = m;
+                bc[w] = n;
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int chosen = -1;
+            for (int d = 15; d >= 0; --d) {
+                if (bc[d] == 0) continue;
+                if (acc + bm[d] >= target) {
+                    chosen = d;
+                    break;
+                }
+                acc += bm[d];
+            }
+            s_int[0] = chosen;
+            s_int[1] = chosen >= 0 ? bc[chosen] : 0;
+        }
+        __syncthreads();
+        const int chosen = s_int[0], n_in = s_int[1];
+        if (chosen < 0) break;   // the whole mass stays below top_p * Z: keep all k' (beta = tau)
+        const int my = cnts[chosen * kGenThreads + tid];   // this thread's share of the chosen bin
+        prefix |= uint64_t(chosen) << shift;
+        mask |= 0xFull << shift;
+        if (n_in == 1 || shift == 0) {   // the bin is one key: the boundary
+            if (tid == 0) s_u64 = 0ull;
+            __syncthreads();
+            if (n_c < 0) {
+                for (int i = tid; i < V; i += kGenThreads) {
+                    const uint64_t cv = row_composite(row, i);
+                    if (cv >= tau && (cv & mask) == prefix) atomicMax(&s_u64, (unsigned long long)cv);
+                }
+            } else {
+                for (int j = tid; j < n_c; j += kGenThreads)
+                    if ((ckey[j] & mask) == prefix) atomicMax(&s_u64, (unsigned long long)ckey[j]);
+            }
+            __syncthreads();
+            beta = s_u64;
+            break;
+        }
+        if (n_c < 0 && n_in <= kWalkCompact) {
+            // gather the bin in a fixed order: thread t's elements, in index
+            // order, at t's offset (the exclusive scan of the threads' shares)
+            const int off = block_scan_incl(my, s_scan) - my;
+            int q = off;
+            for (int i = tid; i < V; i += kGenThreads) {
+                const uint64_t cv = row_composite(row, i);
+                if (cv >= tau && (cv & mask) == prefix) {
+                    ckey[q] = cv;
+                    ce[q] = e_row[i];
+                    ++q;
+                }
+            }
+            n_c = n_in;
+        }
+        __syncthreads();
     }
     if (tid == 0) a.gen_thr[r] = beta;
 }
 
-__global__ void __launch_bounds__(kSampleThreads) gen_score_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kGenSubThreads) gen_score_kernel(const SampleArgs a) {
     grid_dependency_wait();
     grid_launch_dependents();
-    __shared__ double s_sc[kSampleThreads / 32];
-    __shared__ int s_id[kSampleThreads / 32];
+    __shared__ double s_sc[kGenSubThreads / 32];
+    __shared__ int s_id[kGenSubThreads / 32];
     const int c = blockIdx.x, r = blockIdx.y;
     const float *row = a.logits + (long long)r * a.ldl;
     const uint64_t thr = a.gen_thr[r];
@@ -797,8 +918,9 @@ __global__ void __launch_bounds__(kSampleThreads) gen_score_kernel(const SampleA
     const int64_t pos = a.pos ? a.pos[r] : (*a.pos_base + r);
     double best = -1.0 / 0.0;
     int best_id = 0x7FFFFFFF;
-    for (int e = 0; e < kE1; ++e) {
-        const int i = c * kSampleChunk + e * kSampleThreads + threadIdx.x;
+#pragma unroll
+    for (int e = 0; e < kGenE; ++e) {
+        const int i = c * kGenSub + e * kGenSubThreads + threadIdx.x;
         if (i < a.V && row_composite(row, i) >= thr) {
             const double s = double(row[i]) / T + gumbel(a.seed, pos, i);
             if (better(s, i, best, best_id)) {
@@ -821,13 +943,13 @@ __global__ void __launch_bounds__(kSampleThreads) gen_score_kernel(const SampleA
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < kSampleThreads / 32; ++w)
+        for (int w = 1; w < kGenSubThreads / 32; ++w)
             if (better(s_sc[w], s_id[w], best, best_id)) {
                 best = s_sc[w];
                 best_id = s_id[w];
             }
-        a.gen_bscore[r * a.n_chunks + c] = best;
-        a.gen_bid[r * a.n_chunks + c] = best_id;
+        a.gen_bscore[r * a.n_sub + c] = best;
+        a.gen_bid[r * a.n_sub + c] = best_id;
     }
 }
 
@@ -837,10 +959,10 @@ __global__ void gen_final_kernel(const SampleArgs a) {
     const int r = blockIdx.x, lane = threadIdx.x;
     double best = -1.0 / 0.0;
     int best_id = 0x7FFFFFFF;
-    for (int c = lane; c < a.n_chunks; c += 32)
-        if (better(a.gen_bscore[r * a.n_chunks + c], a.gen_bid[r * a.n_chunks + c], best, best_id)) {
-            best = a.gen_bscore[r * a.n_chunks + c];
-            best_id = a.gen_bid[r * a.n_chunks + c];
+    for (int c = lane; c < a.n_sub; c += 32)
+        if (better(a.gen_bscore[r * a.n_sub + c], a.gen_bid[r * a.n_sub + c], best, best_id)) {
+            best = a.gen_bscore[r * a.n_sub + c];
+            best_id = a.gen_bid[r * a.n_sub + c];
         }
     for (int o = 16; o > 0; o >>= 1) {
         const double ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
@@ -900,11 +1022,12 @@ size_t sample_workspace_bytes(int R, int V) {
     b += size_t(R) * nc * kMaxTopK * (sizeof(float) + sizeof(int32_t));
     b += size_t(R) * nc * sizeof(int32_t);
     b = (b + 255) / 256 * 256;
-    // general path: chunk maxima, per-row boundary, e_i, chunk bests
+    // general path: chunk maxima, per-row boundary, e_i, sub-chunk sums and bests
+    const size_t ns = size_t((V + kGenSub - 1) / kGenSub);
     b += size_t(R) * nc * sizeof(uint64_t) + size_t(R) * sizeof(uint64_t);
     b = (b + 255) / 256 * 256;
     b += size_t(R) * size_t(V) * sizeof(double);
-    b += size_t(R) * nc * (sizeof(double) + sizeof(int32_t));
+    b += size_t(R) * ns * (2 * sizeof(double) + sizeof(int32_t));
     return (b + 255) / 256 * 256;
 }
 
@@ -929,18 +1052,43 @@ void sample_bind_workspace(SampleArgs &a, void *ws_region, int R, int V) {
     p = static_cast<char *>(ws_region) + (size_t(p - static_cast<char *>(ws_region)) + 255) / 256 * 256;
     a.gen_e = reinterpret_cast<double *>(p);
     p += size_t(R) * size_t(V) * sizeof(double);
+    const size_t ns = size_t((V + kGenSub - 1) / kGenSub);
+    a.gen_zp = reinterpret_cast<double *>(p);
+    p += size_t(R) * ns * sizeof(double);
     a.gen_bscore = reinterpret_cast<double *>(p);
-    p += size_t(R) * nc * sizeof(double);
+    p += size_t(R) * ns * sizeof(double);
     a.gen_bid = reinterpret_cast<int32_t *>(p);
     a.n_chunks = int(nc);
+    a.n_sub = int(ns);
+}
+
+// The general path's shared-memory opt-in, once per device.
+cudaError_t gen_opt_in() {
+    static std::atomic<bool> done[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(gen_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kSelectCompact * sizeof(uint64_t)));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gen_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kWalkSmem));
+    if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev].store(true, std::memory_order_release);
+    return e;
 }
 
 cudaError_t launch_keyed_sample(const SampleArgs &a, cudaStream_t s) {
     if (a.n_chunks > kMaxChunks) return cudaErrorInvalidValue;
     if (a.temperature > 0.0f && a.k_eff > kMaxTopK) {   // general candidate path
-        cudaError_t e = launch_pdl(gen_prep_kernel, dim3(a.n_chunks, a.R), dim3(kSampleThreads), 0, s, a);
-        if (e == cudaSuccess) e = launch_pdl(gen_select_kernel, dim3(a.R), dim3(kGenThreads), 0, s, a);
-        if (e == cudaSuccess) e = launch_pdl(gen_score_kernel, dim3(a.n_chunks, a.R), dim3(kSampleThreads), 0, s, a);
+        cudaError_t e = gen_opt_in();
+        if (e == cudaSuccess) e = launch_pdl(gen_prep_kernel, dim3(a.n_chunks, a.R), dim3(kSampleThreads), 0, s, a);
+        if (e == cudaSuccess)
+            e = launch_pdl(gen_select_kernel, dim3(a.R), dim3(kGenThreads), kSelectCompact * sizeof(uint64_t), s, a);
+        if (a.top_p < 1.0f) {
+            if (e == cudaSuccess) e = launch_pdl(gen_exp_kernel, dim3(a.n_sub, a.R), dim3(kGenSubThreads), 0, s, a);
+            if (e == cudaSuccess) e = launch_pdl(gen_walk_kernel, dim3(a.R), dim3(kGenThreads), kWalkSmem, s, a);
+        }
+        if (e == cudaSuccess) e = launch_pdl(gen_score_kernel, dim3(a.n_sub, a.R), dim3(kGenSubThreads), 0, s, a);
         if (e == cudaSuccess) e = launch_pdl(gen_final_kernel, dim3(a.R), dim3(32), 0, s, a);
         if (e == cudaSuccess && a.accepted) e = launch_accept(a.drafts, a.tokens, a.R, a.accepted, a.bonus, a.acc_pos, s);
         return e;

@@ -31,8 +31,10 @@ struct SampleArgs {
     uint64_t *gen_cmax;   // [R][n_chunks] largest composite key of each chunk
     uint64_t *gen_thr;    // [R] smallest composite key kept
     double *gen_e;        // [R][V] exp((l_i - l_0) / T) of the k' candidates, else 0
-    double *gen_bscore;   // [R][n_chunks] best score of each chunk
-    int32_t *gen_bid;     // [R][n_chunks] its token id
+    double *gen_zp;       // [R][n_sub] sum of gen_e over each 1024-entry sub-chunk
+    double *gen_bscore;   // [R][n_sub] best score of each sub-chunk
+    int32_t *gen_bid;     // [R][n_sub] its token id
+    int n_sub;            // 1024-entry sub-chunks of the vocabulary
     int *err;
     int n_chunks;
     // acceptance (accepted non-null): a = first i < R - 1 with drafts[i] !=

@@ -5,6 +5,10 @@
 
 namespace tfk {
 
+// Device ordinals whose per-device launch state (shared-memory opt-ins, SM
+// counts) the library caches.
+constexpr int kMaxDevices = 64;
+
 // A bounded mbarrier wait gives up after this many try_wait polls (each poll
 // may itself suspend for a short hardware-defined time), so a broken pipeline
 // reports TF_DEV_TIMEOUT instead of hanging the GPU.

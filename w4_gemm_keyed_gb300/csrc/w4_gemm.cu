@@ -895,8 +895,6 @@ __global__ void pack_scales_kernel(const uint16_t *scales, int K, int N, uint8_t
     *reinterpret_cast<uint32_t *>(dst) = lo | (hi << 16);
 }
 
-constexpr int kMaxDevices = 64;
-
 // Affine (MLX-style) packing: same chunk geometry; codes are taken as they are
 // (unsigned, no offset), and each group carries bf16 scales then bf16 biases.
 template <int G>
