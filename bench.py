@@ -380,6 +380,41 @@ def extra_lmhead(tf, torch, steps=30):
     return out
 
 
+def extra_sampler(tf, torch, steps=20):
+    """tf_keyed_sample alone on V = 151936 fp32 logits (N(0, 2)), R = 1 and 16:
+    greedy, the fast candidate path (top-k 20, top-p 0.95) and the general one
+    (top-k <= 0 with top-p 0.95 and 1.0); CUDA-graph replays of 10 calls."""
+    from w4_gemm_keyed_gb300 import inputs
+    V = 151936
+    out = {}
+    rng = inputs.rng_for(12)
+    for R in (1, 16):
+        lg = torch.from_numpy(inputs.logits_normal(rng, R, V, std=2.0)).cuda()
+        pos = torch.arange(R, dtype=torch.int64, device="cuda")
+        toks = torch.empty(R, dtype=torch.int32, device="cuda")
+        ws = tf.workspace(tf.keyed_sample_workspace_bytes(R, V))
+        for name, (T, k, p) in {"greedy": (0.0, 0, 1.0), "k20_p0.95": (0.6, 20, 0.95),
+                                "k0_p0.95": (0.7, 0, 0.95), "k0_p1": (0.7, 0, 1.0)}.items():
+            def call():
+                tf.keyed_sample(lg, T, k, p, 1234, pos, tokens=toks, ws=ws)
+            call()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(10):
+                    call()
+            g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(steps):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            out[f"R{R}_{name}_us"] = a.elapsed_time(b) * 1e3 / (10 * steps)
+    return out
+
+
 def extra_affine(tf, torch, steps=30):
     """MLX-style affine W4 (bf16 scale and bias per group) on the 5120 -> 17408
     projection, G = 64, R = 1 / 8 / 16: GB/s over codes + scales + biases, weights
@@ -764,7 +799,7 @@ def main():
     ap.add_argument("--impl", default="tf", choices=["tf", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the LM-head / MoE / decoder side measurements")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--only", choices=["lmhead", "dense", "moe", "decoder", "affine", "attention", "nvfp4"],
+    ap.add_argument("--only", choices=["lmhead", "dense", "moe", "decoder", "affine", "attention", "nvfp4", "sampler"],
                     help="run one workload briefly and print its timings (for profiler captures)")
     ap.add_argument("--ctx", type=int, nargs="*", help="with --only attention: cached positions to time")
     ap.add_argument("--rows", type=int, nargs="*", help="with --only attention: verify rows R to time")
@@ -786,7 +821,7 @@ def main():
             out = {"dense_gbs": STEP_BYTES * steps / secs / 1e9}
         else:
             fn = {"lmhead": extra_lmhead, "moe": extra_moe, "decoder": extra_decoder, "affine": extra_affine,
-                  "attention": extra_attention, "nvfp4": extra_nvfp4}[args.only]
+                  "attention": extra_attention, "nvfp4": extra_nvfp4, "sampler": extra_sampler}[args.only]
             kw = {}
             if args.only == "attention" and args.ctx:
                 kw["ctxs"] = tuple(args.ctx)
@@ -844,7 +879,7 @@ def main():
     if rank == 0 and not args.no_extra:
         for name, fn in (("lmhead_sampler", extra_lmhead), ("moe30b", extra_moe), ("decoder", extra_decoder),
                          ("affine_5120x17408", extra_affine), ("nvfp4_5120x17408", extra_nvfp4),
-                         ("attention_kv", extra_attention)):
+                         ("attention_kv", extra_attention), ("sampler_151936", extra_sampler)):
             try:
                 extra[name] = fn(tf, torch)
             except Exception as exc:  # a side measurement must not hide the headline line
