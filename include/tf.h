@@ -274,10 +274,12 @@ TF_API tf_status tf_lane_gemm_w4_noalloc(const tf_w4_matrix *W, const uint16_t *
  * finite.  k' <= TF_MAX_TOP_K takes the fast path (per-chunk top-k', one
  * finaliser summing the top-p mass left to right in rank order); larger k'
  * (top_k <= 0 included) take a general path: a radix select of the k'-th key,
- * Z and the top-p boundary from fp64 sums taken in a fixed order that is not
- * the rank order, so the boundary matches a left-to-right sum except where the
- * mass reaching it lies within rounding (about 1e-12 relative) of top_p; then
- * the Gumbel argmax over the kept candidates.  Both paths are deterministic and
+ * the fp64 weights exp((l_i - l_0)/T) kept as exact 53-bit fixed-point masses
+ * (floor(2^53 w)), Z and the top-p boundary from exact integer sums of them,
+ * so the boundary matches the left-to-right fp64 sum except where the mass
+ * reaching it lies within about V * 2^-53 (relative to Z) of top_p; then the
+ * Gumbel argmax over the kept candidates (fp64 for every score that an fp32
+ * estimate with a stated error bound cannot rule out).  Both paths are deterministic and
  * give each row the same token whatever R is.  A non-finite logit sets
  * TF_DEV_NONFINITE_LOGIT and that row's token to -1.
  */

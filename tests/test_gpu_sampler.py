@@ -137,6 +137,21 @@ def test_general_path_logit_shapes(tf, near_tie, dist, k, T, p):
     check_tokens_general(gpu_sample(tf, logits, T, k, p, 23, pos), logits, T, k, p, 23, pos, near_tie)
 
 
+@pytest.mark.parametrize("T", [1.0, 0.05, 30.0])
+def test_general_path_noise_decides(tf, near_tie, T):
+    """Equal logits over the whole vocabulary (top-k <= 0, top-p 1): the token
+    is the argmax of the Gumbel noise alone, which the general path first
+    estimates in fp32 with an error bound and then settles in fp64; 16 rows
+    x 4 seeds against the oracle."""
+    R, V = 16, 151936
+    rng = inputs.rng_for(209, int(T * 100))
+    logits = np.full((R, V), 0.25, dtype=np.float32)
+    for seed in inputs.seeds_u64(rng, 4):
+        pos = inputs.positions(rng, R)
+        check_tokens_general(gpu_sample(tf, logits, T, 0, 1.0, int(seed), pos), logits, T, 0, 1.0, int(seed), pos,
+                             near_tie)
+
+
 def test_general_path_rows_independent_of_R_and_nan_rows(tf):
     rng = inputs.rng_for(207)
     V = 151936

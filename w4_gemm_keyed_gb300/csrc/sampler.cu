@@ -584,28 +584,185 @@ __global__ void __launch_bounds__(kListThreads) finalize_lists_kernel(const Samp
 //              its keys are gathered into shared memory and the remaining
 //              digits are read there.  (tau = 0 when k' = V.)
 //   gen_exp    (sub-chunk of 1024, row; top_p < 1): e_i = exp((l_i - l_0) / T)
-//              in fp64 for the candidates (key >= tau), and the sub-chunk's
-//              sum of them in a fixed order.
-//   gen_walk   (row; top_p < 1): Z = the sub-chunk sums in order; the top-p
-//              boundary b, the largest key with sum_{key >= b} e >= top_p * Z,
-//              by a 4-bit radix walk over per-bin fp64 masses (each thread
-//              adds its own elements into private bins; the bins are then
-//              summed in a fixed order); once the boundary bin is small its
-//              (key, e) pairs are gathered in a fixed order into shared memory.
-//   gen_score  (sub-chunk, row): the best (l / T + g, id) among keys >= b.
+//              in fp64 for the candidates (key >= tau), kept as the 53-bit
+//              fixed-point mass q_i = floor(2^53 e_i) (e_i <= 1), and the
+//              sub-chunk's sum of them.
+//   gen_walk   (sub-chunk, row; top_p < 1; passes 1..7, then gen_walk_final):
+//              the top-p boundary b, the largest key with sum_{key >= b} q >=
+//              top_p * Z (Z = sum q), by an 8-bit radix walk, most significant
+//              digit first.  Pass k adds the masses, counts and largest keys of
+//              the digit at bit 56 - 8k of the keys inside the bins chosen so
+//              far into global bins (integer atomics: exact in any order);
+//              every CTA of pass k + 1 reads them and takes the same decision
+//              (a scan over the bins from the top), so the walk needs no grid
+//              barrier.  gen_exp is pass 0.  It stops at a bin of one key.
+//   gen_score  (sub-chunk, row): the best (l / T + g, id) among keys >= b; an
+//              fp32 estimate of every score with a bound on its error leaves
+//              fp64 only to the scores that can still be the best.
 //   gen_final  (row): the best over the sub-chunks.
-// The masses are summed in a fixed order that is not the rank order, so the
-// boundary agrees with a left-to-right sum except when the mass reaching it
-// lies within rounding (~1e-12 relative) of top_p * Z.
+// The masses are exact sums of weights truncated to multiples of 2^-53, so
+// the boundary agrees with the left-to-right fp64 sum of the definition
+// except when the mass reaching it lies within about V * 2^-53 (~2e-11 for
+// V = 151936) of top_p * Z, relative to Z >= 1.
 constexpr int kGenThreads = 512;
 constexpr int kGenSub = 1024;                        // sub-chunk of gen_exp / gen_score
 constexpr int kGenSubThreads = 256;
 constexpr int kGenE = kGenSub / kGenSubThreads;      // 4 elements a thread
 constexpr int kSelectCompact = 8192;                 // keys gen_select gathers (64 KB)
-constexpr int kWalkCompact = 4096;                   // (key, e) pairs gen_walk gathers (64 KB)
-constexpr size_t kWalkSmem = size_t(16) * kGenThreads * 8 + size_t(16) * kGenThreads * 4 + size_t(kWalkCompact) * 16;
+constexpr int kWalkPasses = 8;                       // 8-bit digits of the 64-bit keys
 
 __device__ __forceinline__ uint64_t row_composite(const float *row, int i) { return composite(order_key(row[i]), i); }
+
+// 128-bit unsigned sums of the 53-bit fixed-point masses (at most 2^19
+// entries of at most 2^53 each).
+struct U128 {
+    unsigned long long lo, hi;
+};
+__device__ __forceinline__ U128 add128(U128 a, U128 b) {
+    U128 r;
+    r.lo = a.lo + b.lo;
+    r.hi = a.hi + b.hi + (r.lo < a.lo ? 1ull : 0ull);
+    return r;
+}
+__device__ __forceinline__ U128 warp_sum128(U128 v) {
+    for (int o = 16; o > 0; o >>= 1) {
+        U128 x;
+        x.lo = __shfl_xor_sync(0xFFFFFFFFu, v.lo, o);
+        x.hi = __shfl_xor_sync(0xFFFFFFFFu, v.hi, o);
+        v = add128(v, x);
+    }
+    return v;
+}
+__device__ __forceinline__ double to_double(U128 a) { return double(a.hi) * 18446744073709551616.0 + double(a.lo); }
+
+// Walk bins of one pass and row: 256 digits of (mass as 128 bits, count,
+// largest key).  Buffer (pass % 3) is written by pass `pass`, read by pass
+// + 1 and cleared by pass - 1 (gen_prep clears buffer 0).
+struct WalkBin {
+    unsigned long long lo, hi, maxkey;
+    unsigned cnt, pad;
+};
+__device__ __forceinline__ WalkBin *walk_bins(const SampleArgs &a, int pass, int r) {
+    return reinterpret_cast<WalkBin *>(a.gen_walk) + ((long long)(pass % 3) * a.R + r) * 256;
+}
+
+// The row's walk state after a decision: prefix / mask of the digits chosen,
+// the mass of the candidates above the current bin, the target top_p * Z,
+// and once done the boundary.
+struct WalkState {
+    unsigned long long prefix, mask, acc_lo, acc_hi, beta;
+    double target;
+    int done, pad;
+};
+
+// Clears this CTA's share of the buffer of `pass` for row r (blocks of the
+// grid's x dimension split the 256 bins).
+__device__ __forceinline__ void walk_clear(const SampleArgs &a, int pass, int r) {
+    WalkBin *b = walk_bins(a, pass, r);
+    for (int d = blockIdx.x * blockDim.x + threadIdx.x; d < 256; d += gridDim.x * blockDim.x) b[d] = WalkBin{0, 0, 0, 0, 0};
+}
+
+// Adds this CTA's keys (candidate, inside prefix / mask) to the bins of the
+// digit at `shift`: shared-memory bins first, then one global update per
+// bin that was hit.
+__device__ void walk_histogram(const SampleArgs &a, int pass, int r, int shift, uint64_t prefix, uint64_t mask,
+                               const uint64_t (&key)[kGenE], const uint64_t (&q)[kGenE], bool (&in)[kGenE]) {
+    __shared__ unsigned long long s_m[256], s_k[256];
+    __shared__ unsigned s_c[256];
+    for (int d = threadIdx.x; d < 256; d += blockDim.x) {
+        s_m[d] = 0ull;
+        s_k[d] = 0ull;
+        s_c[d] = 0u;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < kGenE; ++e)
+        if (in[e] && (key[e] & mask) == prefix) {
+            const int d = int((key[e] >> shift) & 0xFFu);
+            atomicAdd(&s_m[d], (unsigned long long)q[e]);   // < 1024 * 2^53 per CTA
+            atomicAdd(&s_c[d], 1u);
+            atomicMax(&s_k[d], (unsigned long long)key[e]);
+        }
+    __syncthreads();
+    WalkBin *b = walk_bins(a, pass, r);
+    for (int d = threadIdx.x; d < 256; d += blockDim.x) {
+        if (!s_c[d]) continue;
+        const unsigned long long old = atomicAdd(&b[d].lo, s_m[d]);
+        if (old + s_m[d] < old) atomicAdd(&b[d].hi, 1ull);   // the carries add up to the same in any order
+        atomicAdd(&b[d].cnt, s_c[d]);
+        atomicMax(&b[d].maxkey, s_k[d]);
+    }
+}
+
+// The decision on the bins of the digit at `shift` (buffer of `pass`): the
+// highest non-empty digit whose mass, added to the mass above it, reaches the
+// target.  256 threads, one digit each; the same result in every CTA.
+__device__ void walk_decide(const SampleArgs &a, int pass, int r, int shift, WalkState &st, uint64_t tau) {
+    __shared__ unsigned long long s_lo[8], s_hi[8];
+    __shared__ int s_pick;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int d = 255 - t;   // thread t: digit 255 - t, so the scan runs from the top
+    const WalkBin bn = walk_bins(a, pass, r)[d];
+    // inclusive scan of the masses from digit 255 down to d
+    U128 v{bn.lo, bn.hi};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        U128 x;
+        x.lo = __shfl_up_sync(0xFFFFFFFFu, v.lo, o);
+        x.hi = __shfl_up_sync(0xFFFFFFFFu, v.hi, o);
+        if (lane >= o) v = add128(v, x);
+    }
+    if (lane == 31) {
+        s_lo[w] = v.lo;
+        s_hi[w] = v.hi;
+    }
+    if (t == 0) s_pick = 256;
+    __syncthreads();
+    for (int k = 0; k < w; ++k) v = add128(v, U128{s_lo[k], s_hi[k]});
+    const U128 reach = add128(U128{st.acc_lo, st.acc_hi}, v);
+    if (bn.cnt && to_double(reach) >= st.target) atomicMin(&s_pick, t);   // the first from the top
+    __syncthreads();
+    const int pick = s_pick;
+    if (pick == 256) {   // the whole mass stays below top_p * Z: keep all k'
+        st.done = 1;
+        st.beta = tau;
+    } else {
+        __shared__ WalkBin s_bin;
+        __shared__ U128 s_acc;
+        if (t == pick) {
+            s_bin = bn;
+            // the mass above the chosen digit: reach minus its own
+            U128 above = reach;
+            above.hi -= bn.hi + (above.lo < bn.lo ? 1ull : 0ull);
+            above.lo -= bn.lo;
+            s_acc = above;
+        }
+        __syncthreads();
+        st.prefix |= uint64_t(255 - pick) << shift;
+        st.mask |= 0xFFull << shift;
+        st.acc_lo = s_acc.lo;
+        st.acc_hi = s_acc.hi;
+        if (s_bin.cnt == 1u || shift == 0) {
+            st.done = 1;
+            st.beta = s_bin.maxkey;
+        }
+    }
+    __syncthreads();
+}
+
+// Loads this CTA's keys and masses (the candidates of sub-chunk c of row r).
+__device__ __forceinline__ void walk_load(const SampleArgs &a, int r, int c, uint64_t tau, uint64_t (&key)[kGenE],
+                                          uint64_t (&q)[kGenE], bool (&in)[kGenE]) {
+    const float *row = a.logits + (long long)r * a.ldl;
+#pragma unroll
+    for (int e = 0; e < kGenE; ++e) {
+        const int i = c * kGenSub + e * kGenSubThreads + threadIdx.x;
+        in[e] = i < a.V;
+        key[e] = in[e] ? row_composite(row, i) : 0ull;
+        q[e] = in[e] ? a.gen_q[(long long)r * a.V + i] : 0ull;
+        in[e] = in[e] && key[e] >= tau;
+    }
+}
 
 __global__ void __launch_bounds__(kSampleThreads) gen_prep_kernel(const SampleArgs a) {
     grid_dependency_wait();
@@ -631,6 +788,7 @@ __global__ void __launch_bounds__(kSampleThreads) gen_prep_kernel(const SampleAr
     }
     atomicMax(&s_max, (unsigned long long)m);
     if (bad) atomicOr(&s_bad, 1);
+    if (a.top_p < 1.0f) walk_clear(a, 0, r);   // the top-p walk's first bins
     __syncthreads();
     if (threadIdx.x == 0) {
         a.gen_cmax[r * a.n_chunks + c] = s_max;
@@ -720,36 +878,49 @@ __global__ void __launch_bounds__(kGenSubThreads) gen_exp_kernel(const SampleArg
     grid_dependency_wait();
     grid_launch_dependents();
     __shared__ unsigned long long s_top;
-    __shared__ double s_w[kGenSubThreads / 32];
+    __shared__ unsigned long long s_w[kGenSubThreads / 32];
     const int c = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
     const uint64_t tau = a.gen_thr[r];
     if (tid == 0) s_top = 0ull;
     __syncthreads();
     for (int k = tid; k < a.n_chunks; k += kGenSubThreads) atomicMax(&s_top, (unsigned long long)a.gen_cmax[r * a.n_chunks + k]);
     __syncthreads();
-    if (tau == ~0ull) return;   // row with a non-finite logit
+    if (tau == ~0ull) {   // row with a non-finite logit: no walk
+        walk_clear(a, 1, r);
+        return;
+    }
     const float *row = a.logits + (long long)r * a.ldl;
     const double l0 = double(key_value(uint32_t(s_top >> 32)));
     const double T = double(a.temperature);
-    double part = 0.0;
+    unsigned long long part = 0ull;   // < 1024 * 2^53: no overflow
+    uint64_t key[kGenE], q[kGenE];
+    bool in[kGenE];
 #pragma unroll
-    for (int e = 0; e < kGenE; ++e) {   // this thread's elements in index order
+    for (int e = 0; e < kGenE; ++e) {
         const int i = c * kGenSub + e * kGenSubThreads + tid;
+        key[e] = 0ull;
+        q[e] = 0ull;
+        in[e] = false;
         if (i < a.V) {
-            const double v = row_composite(row, i) >= tau ? exp((double(row[i]) - l0) / T) : 0.0;
-            a.gen_e[(long long)r * a.V + i] = v;
-            part += v;
+            key[e] = row_composite(row, i);
+            in[e] = key[e] >= tau;
+            // e <= 1 (l_0 is the largest logit), so 2^53 e is at most 2^53
+            q[e] = in[e] ? __double2ull_rz(9007199254740992.0 * exp((double(row[i]) - l0) / T)) : 0ull;
+            a.gen_q[(long long)r * a.V + i] = q[e];
+            part += q[e];
         }
     }
-    // fixed order: a butterfly within each warp, then the warps in order
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
     if ((tid & 31) == 0) s_w[tid >> 5] = part;
     __syncthreads();
     if (tid == 0) {
-        double z = 0.0;
+        unsigned long long z = 0ull;
         for (int w = 0; w < kGenSubThreads / 32; ++w) z += s_w[w];
         a.gen_zp[r * a.n_sub + c] = z;
     }
+    // walk pass 0: the top digit of every candidate key
+    walk_clear(a, 1, r);
+    walk_histogram(a, 0, r, 56, 0ull, 0ull, key, q, in);
 }
 
 // Inclusive scan (integer) over the block of kGenThreads threads.
@@ -777,133 +948,72 @@ __device__ __forceinline__ int block_scan_incl(int v, int *sh) {
     return v + add;
 }
 
-__global__ void __launch_bounds__(kGenThreads) gen_walk_kernel(const SampleArgs a) {
+
+// Pass `pass` (1..7): decide on the previous pass's bins, then (if the walk
+// goes on) histogram the next digit.
+__global__ void __launch_bounds__(kGenSubThreads) gen_walk_kernel(const SampleArgs a, int pass) {
     grid_dependency_wait();
     grid_launch_dependents();
-    extern __shared__ uint8_t gwalk[];
-    double *bins = reinterpret_cast<double *>(gwalk);                                  // [16][kGenThreads]
-    int *cnts = reinterpret_cast<int *>(bins + 16 * kGenThreads);                      // [16][kGenThreads]
-    uint64_t *ckey = reinterpret_cast<uint64_t *>(cnts + 16 * kGenThreads);            // [kWalkCompact]
-    double *ce = reinterpret_cast<double *>(ckey + kWalkCompact);                      // [kWalkCompact]
-    __shared__ double bm[16];
-    __shared__ int bc[16];
-    __shared__ double s_z;
-    __shared__ int s_int[2];
-    __shared__ int s_scan[32];
-    __shared__ unsigned long long s_u64;
-    const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int V = a.V;
+    const int c = blockIdx.x, r = blockIdx.y;
     const uint64_t tau = a.gen_thr[r];
-    if (tau == ~0ull) return;
-    const float *row = a.logits + (long long)r * a.ldl;
-    const double *e_row = a.gen_e + (long long)r * V;
-    if (w == 0) {   // Z: lane l sums sub-chunks l, l + 32, ... in order, then a butterfly
-        double z = 0.0;
-        for (int c = lane; c < a.n_sub; c += 32) z += a.gen_zp[r * a.n_sub + c];
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
-        if (lane == 0) s_z = z;
-    }
-    __syncthreads();
-    const double target = double(a.top_p) * s_z;
-    uint64_t prefix = 0ull, mask = 0ull, beta = tau;
-    double acc = 0.0;   // mass of the candidates above the current bin
-    int n_c = -1;       // n_c >= 0: the bin's pairs sit in ckey / ce, thread t's at t, t + kGenThreads, ...
-    for (int shift = 60; shift >= 0; shift -= 4) {
-#pragma unroll
-        for (int d = 0; d < 16; ++d) {
-            bins[d * kGenThreads + tid] = 0.0;
-            cnts[d * kGenThreads + tid] = 0;
-        }
-        if (n_c < 0) {
-            for (int i = tid; i < V; i += kGenThreads) {
-                const uint64_t cv = row_composite(row, i);
-                if (cv >= tau && (cv & mask) == prefix) {
-                    const int d = int((cv >> shift) & 0xFu);
-                    bins[d * kGenThreads + tid] += e_row[i];
-                    cnts[d * kGenThreads + tid] += 1;
-                }
-            }
-        } else {
-            for (int j = tid; j < n_c; j += kGenThreads) {
-                const uint64_t cv = ckey[j];
-                if ((cv & mask) == prefix) {
-                    const int d = int((cv >> shift) & 0xFu);
-                    bins[d * kGenThreads + tid] += ce[j];
-                    cnts[d * kGenThreads + tid] += 1;
-                }
-            }
-        }
-        __syncthreads();
-        if (w < 16) {   // warp d: the bin's mass over the threads in a fixed order, and its count
-            double m = 0.0;
-            int n = 0;
-            for (int t = lane; t < kGenThreads; t += 32) {
-                m += bins[w * kGenThreads + t];
-                n += cnts[w * kGenThreads + t];
-            }
-            for (int o = 16; o > 0; o >>= 1) {
-                m += __shfl_xor_sync(0xFFFFFFFFu, m, o);
-                n += __shfl_xor_sync(0xFFFFFFFFu, n, o);
-            }
-            if (lane == 0) {
-                bm[w] = m;
-                bc[w] = n;
-            }
-        }
-        __syncthreads();
-        if (tid == 0) {
-            int chosen = -1;
-            for (int d = 15; d >= 0; --d) {
-                if (bc[d] == 0) continue;
-                if (acc + bm[d] >= target) {
-                    chosen = d;
-                    break;
-                }
-                acc += bm[d];
-            }
-            s_int[0] = chosen;
-            s_int[1] = chosen >= 0 ? bc[chosen] : 0;
-        }
-        __syncthreads();
-        const int chosen = s_int[0], n_in = s_int[1];
-        if (chosen < 0) break;   // the whole mass stays below top_p * Z: keep all k' (beta = tau)
-        const int my = cnts[chosen * kGenThreads + tid];   // this thread's share of the chosen bin
-        prefix |= uint64_t(chosen) << shift;
-        mask |= 0xFull << shift;
-        if (n_in == 1 || shift == 0) {   // the bin is one key: the boundary
-            if (tid == 0) s_u64 = 0ull;
-            __syncthreads();
-            if (n_c < 0) {
-                for (int i = tid; i < V; i += kGenThreads) {
-                    const uint64_t cv = row_composite(row, i);
-                    if (cv >= tau && (cv & mask) == prefix) atomicMax(&s_u64, (unsigned long long)cv);
-                }
-            } else {
-                for (int j = tid; j < n_c; j += kGenThreads)
-                    if ((ckey[j] & mask) == prefix) atomicMax(&s_u64, (unsigned long long)ckey[j]);
+    WalkState *gst = reinterpret_cast<WalkState *>(a.gen_state) + r;
+    WalkState st;
+    if (pass == 1) {
+        st = WalkState{0ull, 0ull, 0ull, 0ull, 0ull, 0.0, tau == ~0ull ? 1 : 0, 0};
+        if (!st.done) {   // Z = the sub-chunk sums (integers: any order gives the same)
+            __shared__ U128 s_z;
+            if (threadIdx.x < 32) {
+                U128 z{0ull, 0ull};
+                for (int k = threadIdx.x; k < a.n_sub; k += 32) z = add128(z, U128{a.gen_zp[r * a.n_sub + k], 0ull});
+                z = warp_sum128(z);
+                if (threadIdx.x == 0) s_z = z;
             }
             __syncthreads();
-            beta = s_u64;
-            break;
+            st.target = double(a.top_p) * to_double(s_z);
         }
-        if (n_c < 0 && n_in <= kWalkCompact) {
-            // gather the bin in a fixed order: thread t's elements, in index
-            // order, at t's offset (the exclusive scan of the threads' shares)
-            const int off = block_scan_incl(my, s_scan) - my;
-            int q = off;
-            for (int i = tid; i < V; i += kGenThreads) {
-                const uint64_t cv = row_composite(row, i);
-                if (cv >= tau && (cv & mask) == prefix) {
-                    ckey[q] = cv;
-                    ce[q] = e_row[i];
-                    ++q;
-                }
-            }
-            n_c = n_in;
-        }
-        __syncthreads();
+    } else {
+        st = *gst;
     }
-    if (tid == 0) a.gen_thr[r] = beta;
+    if (!st.done) walk_decide(a, pass - 1, r, 56 - 8 * (pass - 1), st, tau);
+    if (c == 0 && threadIdx.x == 0) *gst = st;
+    walk_clear(a, pass + 1, r);
+    if (st.done) return;
+    uint64_t key[kGenE], q[kGenE];
+    bool in[kGenE];
+    walk_load(a, r, c, tau, key, q, in);
+    walk_histogram(a, pass, r, 56 - 8 * pass, st.prefix, st.mask, key, q, in);
+}
+
+// The last decision (digit at bit 0): the boundary is then one key.
+__global__ void gen_walk_final_kernel(const SampleArgs a) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int r = blockIdx.x;
+    const uint64_t tau = a.gen_thr[r];
+    WalkState st = reinterpret_cast<WalkState *>(a.gen_state)[r];
+    if (!st.done) walk_decide(a, kWalkPasses - 1, r, 0, st, tau);
+    if (threadIdx.x == 0 && tau != ~0ull) a.gen_thr[r] = st.beta;
+}
+
+// fp32 estimate of the Gumbel noise of key h, g = -ln(-ln u) with
+// u = ((h >> 11) + 1/2) / 2^53.  -ln u is formed from u itself when u <= 1/2
+// and as -log1p(-(1 - u)) from the exact integer 1 - u otherwise, so every
+// step is well conditioned: -ln u comes out within a few 2^-24 relative and g
+// within 6e-6 absolute (|g| < 23; logf and log1pf are within 1 ulp).  Keys
+// with 1 - u below 2^-33 (g above ~22, and u rounding to 1 in fp64) are
+// flagged for the fp64 formula.
+__device__ __forceinline__ float gumbel_f32(uint64_t h, bool &needs_fp64) {
+    const uint64_t k = h >> 11;
+    float x;
+    if (k >= (1ull << 52)) {
+        const uint64_t m = ((1ull << 53) - 1ull) - k;   // 1 - u = (m + 1/2) / 2^53
+        needs_fp64 = m < (1ull << 20);
+        x = -log1pf(-((__ull2float_rn(m) + 0.5f) * 0x1p-53f));
+    } else {
+        needs_fp64 = false;
+        x = -logf((__ull2float_rn(k) + 0.5f) * 0x1p-53f);
+    }
+    return -logf(x);
 }
 
 __global__ void __launch_bounds__(kGenSubThreads) gen_score_kernel(const SampleArgs a) {
@@ -911,20 +1021,50 @@ __global__ void __launch_bounds__(kGenSubThreads) gen_score_kernel(const SampleA
     grid_launch_dependents();
     __shared__ double s_sc[kGenSubThreads / 32];
     __shared__ int s_id[kGenSubThreads / 32];
-    const int c = blockIdx.x, r = blockIdx.y;
+    __shared__ float s_lb[kGenSubThreads / 32];
+    const int c = blockIdx.x, r = blockIdx.y, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const float *row = a.logits + (long long)r * a.ldl;
     const uint64_t thr = a.gen_thr[r];
-    const double T = double(a.temperature);
+    const float Tf = a.temperature;
+    const double T = double(Tf);
     const int64_t pos = a.pos ? a.pos[r] : (*a.pos_base + r);
+    // fp32 scores s with an error bound: s + err bounds the exact l / T + g
+    // from above, s - err from below; only a score whose upper bound reaches
+    // the chunk's best lower bound can be the chunk's best
+    float s32[kGenE], err[kGenE];
+    uint64_t hk[kGenE];
+    bool cand[kGenE], exact[kGenE];
+    float lb = -1.0f / 0.0f;
+#pragma unroll
+    for (int e = 0; e < kGenE; ++e) {
+        const int i = c * kGenSub + e * kGenSubThreads + threadIdx.x;
+        cand[e] = i < a.V && row_composite(row, i) >= thr;
+        exact[e] = false;
+        s32[e] = -1.0f / 0.0f;
+        err[e] = 0.f;
+        hk[e] = 0ull;
+        if (cand[e]) {
+            hk[e] = key_hash(a.seed, pos, i);
+            const float lt = __fdiv_rn(row[i], Tf);
+            s32[e] = lt + gumbel_f32(hk[e], exact[e]);
+            err[e] = 3e-5f + 2.4e-7f * (fabsf(lt) + fabsf(s32[e]));
+            if (!exact[e]) lb = fmaxf(lb, s32[e] - err[e]);
+        }
+    }
+    for (int o = 16; o > 0; o >>= 1) lb = fmaxf(lb, __shfl_xor_sync(0xFFFFFFFFu, lb, o));
+    if (lane == 0) s_lb[w] = lb;
+    __syncthreads();
+    lb = s_lb[0];
+    for (int k = 1; k < kGenSubThreads / 32; ++k) lb = fmaxf(lb, s_lb[k]);
     double best = -1.0 / 0.0;
     int best_id = 0x7FFFFFFF;
 #pragma unroll
     for (int e = 0; e < kGenE; ++e) {
         const int i = c * kGenSub + e * kGenSubThreads + threadIdx.x;
-        if (i < a.V && row_composite(row, i) >= thr) {
-            const double s = double(row[i]) / T + gumbel(a.seed, pos, i);
-            if (better(s, i, best, best_id)) {
-                best = s;
+        if (cand[e] && (exact[e] || s32[e] + err[e] >= lb)) {
+            const double sc = double(row[i]) / T + gumbel_of_hash(hk[e]);
+            if (better(sc, i, best, best_id)) {
+                best = sc;
                 best_id = i;
             }
         }
@@ -937,16 +1077,16 @@ __global__ void __launch_bounds__(kGenSubThreads) gen_score_kernel(const SampleA
             best_id = oid;
         }
     }
-    if ((threadIdx.x & 31) == 0) {
-        s_sc[threadIdx.x >> 5] = best;
-        s_id[threadIdx.x >> 5] = best_id;
+    if (lane == 0) {
+        s_sc[w] = best;
+        s_id[w] = best_id;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < kGenSubThreads / 32; ++w)
-            if (better(s_sc[w], s_id[w], best, best_id)) {
-                best = s_sc[w];
-                best_id = s_id[w];
+        for (int k = 1; k < kGenSubThreads / 32; ++k)
+            if (better(s_sc[k], s_id[k], best, best_id)) {
+                best = s_sc[k];
+                best_id = s_id[k];
             }
         a.gen_bscore[r * a.n_sub + c] = best;
         a.gen_bid[r * a.n_sub + c] = best_id;
@@ -1028,6 +1168,8 @@ size_t sample_workspace_bytes(int R, int V) {
     b = (b + 255) / 256 * 256;
     b += size_t(R) * size_t(V) * sizeof(double);
     b += size_t(R) * ns * (2 * sizeof(double) + sizeof(int32_t));
+    b = (b + 255) / 256 * 256;
+    b += size_t(3) * R * 256 * sizeof(WalkBin) + size_t(R) * sizeof(WalkState);   // top-p walk
     return (b + 255) / 256 * 256;
 }
 
@@ -1050,14 +1192,19 @@ void sample_bind_workspace(SampleArgs &a, void *ws_region, int R, int V) {
     a.gen_thr = reinterpret_cast<uint64_t *>(p);
     p += size_t(R) * sizeof(uint64_t);
     p = static_cast<char *>(ws_region) + (size_t(p - static_cast<char *>(ws_region)) + 255) / 256 * 256;
-    a.gen_e = reinterpret_cast<double *>(p);
-    p += size_t(R) * size_t(V) * sizeof(double);
+    a.gen_q = reinterpret_cast<uint64_t *>(p);
+    p += size_t(R) * size_t(V) * sizeof(uint64_t);
     const size_t ns = size_t((V + kGenSub - 1) / kGenSub);
-    a.gen_zp = reinterpret_cast<double *>(p);
-    p += size_t(R) * ns * sizeof(double);
+    a.gen_zp = reinterpret_cast<uint64_t *>(p);
+    p += size_t(R) * ns * sizeof(uint64_t);
     a.gen_bscore = reinterpret_cast<double *>(p);
     p += size_t(R) * ns * sizeof(double);
     a.gen_bid = reinterpret_cast<int32_t *>(p);
+    p += size_t(R) * ns * sizeof(int32_t);
+    p = static_cast<char *>(ws_region) + (size_t(p - static_cast<char *>(ws_region)) + 255) / 256 * 256;
+    a.gen_walk = p;
+    p += size_t(3) * R * 256 * sizeof(WalkBin);
+    a.gen_state = p;
     a.n_chunks = int(nc);
     a.n_sub = int(ns);
 }
@@ -1071,8 +1218,6 @@ cudaError_t gen_opt_in() {
     if (dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
     e = cudaFuncSetAttribute(gen_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kSelectCompact * sizeof(uint64_t)));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gen_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kWalkSmem));
     if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev].store(true, std::memory_order_release);
     return e;
 }
@@ -1086,7 +1231,9 @@ cudaError_t launch_keyed_sample(const SampleArgs &a, cudaStream_t s) {
             e = launch_pdl(gen_select_kernel, dim3(a.R), dim3(kGenThreads), kSelectCompact * sizeof(uint64_t), s, a);
         if (a.top_p < 1.0f) {
             if (e == cudaSuccess) e = launch_pdl(gen_exp_kernel, dim3(a.n_sub, a.R), dim3(kGenSubThreads), 0, s, a);
-            if (e == cudaSuccess) e = launch_pdl(gen_walk_kernel, dim3(a.R), dim3(kGenThreads), kWalkSmem, s, a);
+            for (int pass = 1; pass < kWalkPasses && e == cudaSuccess; ++pass)
+                e = launch_pdl(gen_walk_kernel, dim3(a.n_sub, a.R), dim3(kGenSubThreads), 0, s, a, pass);
+            if (e == cudaSuccess) e = launch_pdl(gen_walk_final_kernel, dim3(a.R), dim3(256), 0, s, a);
         }
         if (e == cudaSuccess) e = launch_pdl(gen_score_kernel, dim3(a.n_sub, a.R), dim3(kGenSubThreads), 0, s, a);
         if (e == cudaSuccess) e = launch_pdl(gen_final_kernel, dim3(a.R), dim3(32), 0, s, a);

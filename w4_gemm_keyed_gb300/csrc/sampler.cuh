@@ -30,8 +30,10 @@ struct SampleArgs {
     // general candidate path (k' > kMaxTopK)
     uint64_t *gen_cmax;   // [R][n_chunks] largest composite key of each chunk
     uint64_t *gen_thr;    // [R] smallest composite key kept
-    double *gen_e;        // [R][V] exp((l_i - l_0) / T) of the k' candidates, else 0
-    double *gen_zp;       // [R][n_sub] sum of gen_e over each 1024-entry sub-chunk
+    uint64_t *gen_q;      // [R][V] floor(2^53 exp((l_i - l_0) / T)) of the k' candidates, else 0
+    uint64_t *gen_zp;     // [R][n_sub] sum of gen_q over each 1024-entry sub-chunk (exact)
+    void *gen_walk;       // [3][R][256] top-p walk bins
+    void *gen_state;      // [R] top-p walk state
     double *gen_bscore;   // [R][n_sub] best score of each sub-chunk
     int32_t *gen_bid;     // [R][n_sub] its token id
     int n_sub;            // 1024-entry sub-chunks of the vocabulary
