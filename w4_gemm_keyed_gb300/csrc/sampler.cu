@@ -277,8 +277,17 @@ __global__ void __launch_bounds__(kSampleThreads) topk_partial_kernel(const Samp
 }
 
 // Acceptance by the last row to finish (a.accepted set): the rows' tokens are
-// published with a fence before the count, and read after it.
-__device__ void accept_by_last_row(const SampleArgs &a) {
+// published with a fence before the count, and read after it.  One row needs
+// no count: it accepts nothing and its token is the bonus.
+__device__ void accept_by_last_row(const SampleArgs &a, int32_t token) {
+    if (a.R == 1) {   // one row: nothing to compare, it is its own bonus
+        if (threadIdx.x == 0) {
+            *a.accepted = 0;
+            if (a.bonus) *a.bonus = token;
+            if (a.acc_pos) *a.acc_pos += 1;
+        }
+        return;
+    }
     __shared__ int s_last;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -315,7 +324,8 @@ __device__ __forceinline__ bool better(double s, int id, double bs, int bid) {
 // Gumbel argmax over it.  Call with the whole block.
 template <int NT, int E>
 __device__ void finalize_row(const SampleArgs &a, const int r, const uint64_t (&ck)[E], uint64_t L, uint64_t tmax,
-                             int n_thr, const int k, const int n_total, const bool bad) {
+                             int n_thr, const int k, const int n_total, const bool bad,
+                             const uint64_t *wmax = nullptr) {
     __shared__ uint32_t hist[256];
     __shared__ int sh[4];
     __shared__ int s_cnt, s_m, s_ns, s_token;
@@ -325,15 +335,16 @@ __device__ void finalize_row(const SampleArgs &a, const int r, const uint64_t (&
     __shared__ uint64_t s_surv[kSurvMax];
     __shared__ uint64_t s_wb[NT / 32];
     const int tid = threadIdx.x;
-    if (tid == 0) {
+    if (tid == 0) {   // published by the next barrier (kth_bound's, or the one before the token)
         s_ns = 0;
         s_cnt = 0;
         s_token = -1;
     }
-    __syncthreads();
     if (!bad && n_total > 0) {   // uniform over the block
         const uint64_t L2 = kth_bound(tmax, k, n_thr, s_wb);
         L = L > L2 ? L : L2;
+        if (wmax)   // per-warp maxima of a third bound, written before the call
+            for (int w = 0; w < NT / 32; ++w) L = wmax[w] > L ? wmax[w] : L;
         // candidates at or above the bound
 #pragma unroll
         for (int e = 0; e < E; ++e)
@@ -470,7 +481,7 @@ __device__ void finalize_row(const SampleArgs &a, const int r, const uint64_t (&
         a.tokens[r] = s_token;           // -1 for a row with a non-finite logit
         if (bad) a.row_bad[r] = 0;       // leave the workspace clean for the next call
     }
-    if (a.accepted) accept_by_last_row(a);
+    if (a.accepted) accept_by_last_row(a, s_token);
 }
 
 // Finaliser over the per-chunk candidates of topk_partial.
@@ -534,8 +545,7 @@ __global__ void __launch_bounds__(kListThreads) finalize_lists_kernel(const Samp
     const int tid = threadIdx.x;
     const int nc = a.n_chunks, ke = a.k_eff;
     const int n_total = nc * ke;
-    __shared__ unsigned long long s_L;
-    if (tid == 0) s_L = 0ull;
+    __shared__ uint64_t s_wmax[kListThreads / 32];
     const uint64_t kth = tid < nc ? a.cand_kth[r * nc + tid] : 0ull;
     // each list's best word (entry 0: the lists are in descending order)
     const long long q0 = (long long)(r * nc + (tid < nc ? tid : 0)) * kMaxTopK;
@@ -560,17 +570,15 @@ __global__ void __launch_bounds__(kListThreads) finalize_lists_kernel(const Samp
         const uint64_t x = __shfl_xor_sync(0xFFFFFFFFu, wm, o);
         wm = x > wm ? x : wm;
     }
-    __syncthreads();
-    if ((tid & 31) == 0 && wm) atomicMax(&s_L, (unsigned long long)wm);
+    if ((tid & 31) == 0) s_wmax[tid >> 5] = wm;   // the largest list k-th best: a bound on the row's
     uint64_t ck[kE3];
 #pragma unroll
     for (int e = 0; e < kE3; ++e)
         ck[e] = (!bad && e * kListThreads + tid < n_total) ? composite(order_key(v[e]), id[e]) : 0ull;
     // the second bound from the lists' best words: thread c < nc holds list c's
     const uint64_t lmax = (!bad && tid < nc) ? composite(order_key(v0), id0) : 0ull;
-    __syncthreads();
     if (tid == 0) a.bound[r] = 0ull;   // the GEMM that shared it has finished
-    finalize_row<kListThreads, kE3>(a, r, ck, s_L, lmax, nc, ke, n_total, bad);
+    finalize_row<kListThreads, kE3>(a, r, ck, 0ull, lmax, nc, ke, n_total, bad, s_wmax);
 }
 
 // ---- general candidate path: T > 0 with k' > 64 candidates ----
