@@ -85,6 +85,22 @@ def test_moe30b_rows_invariant_to_R(tf, moe30b):
         assert np.array_equal(out.view(np.uint32), single[:R].view(np.uint32))
 
 
+def test_moe30b_nonfinite_router_row(tf, moe30b):
+    """A row whose router logits hold a NaN is routed nowhere (weights 0, its
+    output 0) and sets TF_DEV_NONFINITE_LOGIT; the other rows keep their bits."""
+    cfg, W, layer, x, z = moe30b
+    R = 5
+    zb = z[:R].copy()
+    zb[2, 17] = np.nan
+    ws = tf.workspace(tf.moe_workspace_bytes(layer, R))
+    out = tf.moe_w4(layer, dev_bits16(x[:R]), torch.from_numpy(zb).cuda(), ws=ws).cpu().numpy()
+    assert tf.workspace_status(ws) == tf.TF_DEV_NONFINITE_LOGIT
+    assert np.all(out[2] == 0.0)
+    clean = run_moe(tf, layer, x[:R], z[:R])
+    keep = [0, 1, 3, 4]
+    assert np.array_equal(out[keep].view(np.uint32), clean[keep].view(np.uint32))
+
+
 # ---------------------------------------------------------------- decoder
 def tiny_weights(seed=401, V=3000, H=256, F=512, n_blocks=2, G=64):
     rng = inputs.rng_for(seed)

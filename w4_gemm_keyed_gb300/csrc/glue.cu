@@ -4,74 +4,87 @@
 #include <cuda_bf16.h>
 
 #include "glue.cuh"
+#include "tf_keys.cuh"
 #include "tf_ptx.cuh"
 
 namespace tfk {
 
 namespace {
 
-__device__ __forceinline__ uint32_t order_key(float f) {
-    uint32_t b = __float_as_uint(f);
-    if (b == 0x80000000u) b = 0u;
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
 // MoE routing (TensorFold README: MoE kernels over 4-bit group-32 weights; the
 // 30B-A3B class routes each token to its top-8 of 128 experts), followed by the
-// list of touched experts, in one CTA: warp r routes row r, then warp 0 numbers
-// the touched experts in ascending id.
+// list of touched experts, in one CTA of R + 1 warps.
+//   1. Warp r routes row r: the k-th largest of the lanes' largest keys bounds
+//      the row's k-th best from below (k lanes hold a key at or above it), so
+//      only the few keys at or above it are ranked; their ranks give the
+//      row's k best in order (key = (logit desc, expert id asc)).
+//   2. Warp r forms row r's renormalised weights in fp64 (summed in rank
+//      order) while warp R numbers the touched experts in ascending id and
+//      maps every (row, rank) to its expert's slot.
 __global__ void route_list_kernel(const float *router, int R, int E, int top_k, int32_t *ids, float *w,
                                   int32_t *expert_ids, int32_t *n_problems, int32_t *slot_of, int *err) {
     grid_dependency_wait();     // inputs come from the preceding grid
     grid_launch_dependents();
     constexpr int KE = kMaxExperts / 32;   // experts per lane
+    __shared__ int s_ids[kMaxRows][kMaxRouteK];
+    __shared__ int s_bad[kMaxRows];
+    __shared__ uint64_t s_surv[kMaxRows][kMaxExperts];
     __shared__ int touched[kMaxExperts];
     __shared__ int pos[kMaxExperts];
-    __shared__ int s_ids[kMaxRows][kMaxRouteK];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int e = tid; e < kMaxExperts; e += blockDim.x) touched[e] = 0;
-    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
     if (warp < R) {
         const int r = warp;
         const float *z = router + (long long)r * E;
-        // composite key (logit desc, id asc), distinct for distinct ids; 0 = absent
-        unsigned long long key[KE];
+        uint64_t key[KE];
         bool bad = false;
+        uint64_t lmax = 0ull;
 #pragma unroll
         for (int i = 0; i < KE; ++i) {
             const int e = lane + 32 * i;
+            key[i] = 0ull;
             if (e < E) {
                 const float v = z[e];
                 bad |= !isfinite(v);
-                key[i] = ((unsigned long long)order_key(v) << 32) | (0xFFFFFFFFull - (unsigned)e);
-            } else {
-                key[i] = 0ull;
+                key[i] = composite(order_key(v), e);
+                lmax = key[i] > lmax ? key[i] : lmax;
             }
         }
-        if (__any_sync(0xFFFFFFFFu, bad)) {
+        bad = __any_sync(0xFFFFFFFFu, bad);
+        if (lane == 0) s_bad[r] = bad ? 1 : 0;
+        if (bad) {
             if (lane == 0) set_error(err, 2);
+            if (lane < top_k) s_ids[r][lane] = lane;
+        } else {
+            const uint64_t L = __shfl_sync(0xFFFFFFFFu, warp_sort_desc(lmax), top_k - 1);
+            int ns = 0;
+#pragma unroll
+            for (int i = 0; i < KE; ++i) {
+                const bool sv = key[i] != 0ull && key[i] >= L;
+                const unsigned m = __ballot_sync(0xFFFFFFFFu, sv);
+                if (sv) s_surv[r][ns + __popc(m & lt)] = key[i];
+                ns += __popc(m);
+            }
+            __syncwarp();
+            for (int j = lane; j < ns; j += 32) {
+                const uint64_t v = s_surv[r][j];
+                int rank = 0;
+                for (int t = 0; t < ns; ++t) rank += s_surv[r][t] > v;
+                if (rank < top_k) s_ids[r][rank] = composite_id(v);
+            }
+        }
+    }
+    __syncthreads();
+    if (warp < R) {
+        const int r = warp;
+        if (s_bad[r]) {
             if (lane < top_k) {
-                s_ids[r][lane] = lane;
                 ids[r * kMaxRouteK + lane] = lane;
                 w[r * kMaxRouteK + lane] = 0.f;
             }
         } else {
-            for (int j = 0; j < top_k; ++j) {
-                unsigned long long m = key[0];
-#pragma unroll
-                for (int i = 1; i < KE; ++i) m = key[i] > m ? key[i] : m;
-                for (int o = 16; o > 0; o >>= 1) {
-                    const unsigned long long v = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-                    m = v > m ? v : m;
-                }
-                const int sel = int(0xFFFFFFFFull - (m & 0xFFFFFFFFull));
-#pragma unroll
-                for (int i = 0; i < KE; ++i)
-                    if (lane + 32 * i == sel) key[i] = 0ull;   // remove the chosen expert
-                if (lane == 0) s_ids[r][j] = sel;
-            }
-            __syncwarp();
             // renormalised weights over the kept experts: fp64, summed in rank order
+            const float *z = router + (long long)r * E;
             double ej = 0.0;
             if (lane < top_k) ej = exp(double(z[s_ids[r][lane]]) - double(z[s_ids[r][0]]));
             // every lane forms the same left-to-right sum; lane j divides its own term
@@ -82,27 +95,26 @@ __global__ void route_list_kernel(const float *router, int R, int E, int top_k, 
                 w[r * kMaxRouteK + lane] = float(ej / tot);
             }
         }
+    } else if (warp == R) {
+        for (int e = lane; e < kMaxExperts; e += 32) touched[e] = 0;
         __syncwarp();
-        if (lane < top_k) touched[s_ids[r][lane]] = 1;
-    }
-    __syncthreads();
-    if (warp == 0) {
+        for (int i = lane; i < R * top_k; i += 32) touched[s_ids[i / top_k][i % top_k]] = 1;
+        __syncwarp();
         int base = 0;
         for (int c = 0; c < KE; ++c) {
             const int e = c * 32 + lane;
             const int f = e < E ? touched[e] : 0;
             const unsigned b = __ballot_sync(0xFFFFFFFFu, f);
-            const int before = __popc(b & ((1u << lane) - 1u));
-            pos[e] = base + before;
-            if (f) expert_ids[base + before] = e;
+            pos[e] = base + __popc(b & lt);
+            if (f) expert_ids[base + __popc(b & lt)] = e;
             base += __popc(b);
         }
         if (lane == 0) *n_problems = base;
-    }
-    __syncthreads();
-    for (int i = tid; i < R * top_k; i += blockDim.x) {
-        const int r = i / top_k, j = i % top_k;
-        slot_of[r * kMaxRouteK + j] = pos[s_ids[r][j]];
+        __syncwarp();
+        for (int i = lane; i < R * top_k; i += 32) {
+            const int r = i / top_k, j = i % top_k;
+            slot_of[r * kMaxRouteK + j] = pos[s_ids[r][j]];
+        }
     }
 }
 
@@ -232,8 +244,8 @@ cudaError_t launch_commit_tokens(const int32_t *tokens, const int32_t *accepted,
 
 cudaError_t launch_route_list(const float *router, int R, int E, int top_k, int32_t *ids, float *w,
                               int32_t *expert_ids, int32_t *n_problems, int32_t *slot_of, int *err, cudaStream_t s) {
-    return launch_pdl(route_list_kernel, dim3(1), dim3(32 * R), 0, s, router, R, E, top_k, ids, w, expert_ids, n_problems,
-                      slot_of, err);
+    return launch_pdl(route_list_kernel, dim3(1), dim3(32 * (R + 1)), 0, s, router, R, E, top_k, ids, w, expert_ids,
+                      n_problems, slot_of, err);
 }
 
 cudaError_t launch_combine(const float *Y, const int32_t *slot_of, const float *w, int R, int H, int top_k,
