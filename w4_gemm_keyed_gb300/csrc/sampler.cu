@@ -931,30 +931,6 @@ __global__ void __launch_bounds__(kGenSubThreads) gen_exp_kernel(const SampleArg
     walk_histogram(a, 0, r, 56, 0ull, 0ull, key, q, in);
 }
 
-// Inclusive scan (integer) over the block of kGenThreads threads.
-__device__ __forceinline__ int block_scan_incl(int v, int *sh) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(0xFFFFFFFFu, v, o);
-        if (lane >= o) v += x;
-    }
-    if (lane == 31) sh[w] = v;
-    __syncthreads();
-    if (w == 0) {
-        int t = lane < kGenThreads / 32 ? sh[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int x = __shfl_up_sync(0xFFFFFFFFu, t, o);
-            if (lane >= o) t += x;
-        }
-        if (lane < kGenThreads / 32) sh[lane] = t;
-    }
-    __syncthreads();
-    const int add = w > 0 ? sh[w - 1] : 0;
-    __syncthreads();
-    return v + add;
-}
 
 
 // Pass `pass` (1..7): decide on the previous pass's bins, then (if the walk

@@ -87,15 +87,8 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 }
 
 // Bulk (non-tensor) TMA copy global -> this CTA's shared memory, completing
-// `bytes` of transaction count on `bar`.  dst/src 16-B aligned, bytes % 16 == 0.
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
+// `bytes` of transaction count on `bar`, with an L2 cache policy.  dst/src
+// 16-B aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
                                               uint64_t policy) {
     asm volatile(
