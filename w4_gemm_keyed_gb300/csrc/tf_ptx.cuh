@@ -172,6 +172,10 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v
     return old;
 }
 
+__device__ __forceinline__ void red_add_release_gpu(unsigned *p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

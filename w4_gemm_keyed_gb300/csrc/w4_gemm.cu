@@ -729,11 +729,18 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
                 if (!SEL || a.y) store_block(a, yb, t, fw, gq, tq, hi, acc);
                 if constexpr (SEL) sel_push(t * kTileN + fw * kBlockRows, acc);
             } else {
-                // stream-K partial.  The last segment to finish sums every
-                // segment of this tile in ascending k order.  A warp that finds
-                // all other segments already published is last: it skips
-                // publishing its own and reads the others directly.  Rows 8..15
-                // (accumulator half n = 1) travel only when the launch has them.
+                // stream-K partial.  A split tile's first k-slice lies in the
+                // range p_lo, and the tile is the last segment of that range (a
+                // range holding the tile's first and last slices holds all of
+                // it), so p_lo owns the sum: every other segment publishes its
+                // partial and bumps the tile's counter without waiting, and the
+                // owner, at the end of its range, waits (bounded) until all of
+                // them are in and adds them to its own in ascending k order.  No
+                // range stalls on a round trip in its middle.  The waits rely on
+                // every range running at once: a dense launch has one range per
+                // CTA and at most one CTA per SM (grouped launches never split a
+                // tile).  Rows 8..15 (accumulator half n = 1) travel only when
+                // the launch has them.
                 constexpr int NB = HI ? 2 : 4;   // segments loaded per round
                 const int p_lo = int(split.owner(tb));
                 const int p_hi = int(split.owner(te - 1));
@@ -744,11 +751,9 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
                     return a.partials + ((((long long)u * a.Pv + p) * 2 + which) * kFeatWarps + fw) * 128 + lane * 4;
                 };
                 unsigned *ctr = a.counters + ((long long)u * a.T + t) * kFeatWarps + fw;
-                unsigned old = 0;
-                if (lane == 0) old = ld_acquire_gpu(ctr);
-                old = __shfl_sync(0xFFFFFFFFu, old, 0);
-                const bool own_in_regs = old == unsigned(nseg - 1);
-                if (!own_in_regs) {
+                if (n_items > int(gridDim.x)) {
+                    if (lane == 0) set_error(a.err, 3);   // ranges not all resident: never launched so
+                } else if (vp != p_lo) {
                     float4 *slot = slot_of(vp);
 #pragma unroll
                     for (int jq = 0; jq < NQ; ++jq) {
@@ -756,49 +761,59 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
                         __stcg(slot + q, make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
                                                      acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3]));
                     }
-                    // the warp barrier orders every lane's stores before lane 0's
-                    // release; the acquire half orders the reads below
+                    // the warp barrier orders every lane's stores before lane 0's release
                     __syncwarp();
-                    if (lane == 0) old = atom_add_acq_rel_gpu(ctr, 1u);
-                    old = __shfl_sync(0xFFFFFFFFu, old, 0);
-                }
-                if (old == unsigned(nseg - 1)) {
-                    __syncwarp();     // every lane's reads after lane 0's acquire
-                    float sum[2][2][4];
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) sum[q >> 3][(q >> 2) & 1][q & 3] = 0.f;
-                    for (int pb = p_lo; pb <= p_hi; pb += NB) {
-                        float4 v[NB][NQ];
-#pragma unroll
-                        for (int b = 0; b < NB; ++b) {
-                            const int p = pb + b;
-                            const bool mine = own_in_regs && p == vp;
-                            const float4 *src = (p <= p_hi && !mine) ? slot_of(p) : nullptr;
-#pragma unroll
-                            for (int jq = 0; jq < NQ; ++jq) {
-                                const int q = HI ? jq : 2 * jq;
-                                v[b][jq] = src ? __ldcg(src + q)
-                                               : make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
-                                                             acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3]);
-                            }
-                        }
-                        // add in ascending k order
-#pragma unroll
-                        for (int b = 0; b < NB; ++b) {
-                            if (pb + b > p_hi) break;
-#pragma unroll
-                            for (int jq = 0; jq < NQ; ++jq) {
-                                const int q = HI ? jq : 2 * jq;
-                                sum[q >> 1][q & 1][0] += v[b][jq].x;
-                                sum[q >> 1][q & 1][1] += v[b][jq].y;
-                                sum[q >> 1][q & 1][2] += v[b][jq].z;
-                                sum[q >> 1][q & 1][3] += v[b][jq].w;
+                    if (lane == 0) red_add_release_gpu(ctr, 1u);
+                } else {
+                    bool in = true;
+                    if (lane == 0) {
+                        uint32_t it = 0;
+                        while (ld_acquire_gpu(ctr) != unsigned(nseg - 1)) {
+                            if (++it == kWaitLimit) {
+                                in = false;
+                                set_error(a.err, 1);
+                                break;
                             }
                         }
                     }
-                    if (lane == 0) *ctr = 0u;  // leave the counter zero for the next launch
-                    if (!SEL || a.y) store_block(a, yb, t, fw, gq, tq, hi, sum);
-                    if constexpr (SEL) sel_push(t * kTileN + fw * kBlockRows, sum);
+                    in = __shfl_sync(0xFFFFFFFFu, in ? 1 : 0, 0) != 0;
+                    __syncwarp();     // every lane's reads after lane 0's acquire
+                    if (in) {
+                        float sum[2][2][4];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) sum[q >> 3][(q >> 2) & 1][q & 3] = 0.f;
+                        for (int pb = p_lo; pb <= p_hi; pb += NB) {
+                            float4 v[NB][NQ];
+#pragma unroll
+                            for (int b = 0; b < NB; ++b) {
+                                const int p = pb + b;
+                                const float4 *src = (p <= p_hi && p != vp) ? slot_of(p) : nullptr;
+#pragma unroll
+                                for (int jq = 0; jq < NQ; ++jq) {
+                                    const int q = HI ? jq : 2 * jq;
+                                    v[b][jq] = src ? __ldcg(src + q)
+                                                   : make_float4(acc[q >> 1][q & 1][0], acc[q >> 1][q & 1][1],
+                                                                 acc[q >> 1][q & 1][2], acc[q >> 1][q & 1][3]);
+                                }
+                            }
+                            // add in ascending k order
+#pragma unroll
+                            for (int b = 0; b < NB; ++b) {
+                                if (pb + b > p_hi) break;
+#pragma unroll
+                                for (int jq = 0; jq < NQ; ++jq) {
+                                    const int q = HI ? jq : 2 * jq;
+                                    sum[q >> 1][q & 1][0] += v[b][jq].x;
+                                    sum[q >> 1][q & 1][1] += v[b][jq].y;
+                                    sum[q >> 1][q & 1][2] += v[b][jq].z;
+                                    sum[q >> 1][q & 1][3] += v[b][jq].w;
+                                }
+                            }
+                        }
+                        if (lane == 0) *ctr = 0u;  // leave the counter zero for the next launch
+                        if (!SEL || a.y) store_block(a, yb, t, fw, gq, tq, hi, sum);
+                        if constexpr (SEL) sel_push(t * kTileN + fw * kBlockRows, sum);
+                    }
                 }
             }
         }
