@@ -522,11 +522,16 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
         // ---------------- producer ----------------
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            // Weights are read-only model data: the first NS stages are
+            // Weights are read-only model data: the first NP stages are
             // requested before waiting for the preceding grid (programmatic
-            // dependent launch), their activation slices only after it.
+            // dependent launch), their activation slices only after it.  Two,
+            // not the whole ring: the copies of CTAs that land early compete
+            // with the preceding grid's last L2 round trips (its split-K sums),
+            // and a smaller burst there shortens that grid's tail by more than
+            // it delays this one.
+            constexpr int NP = NS < kPreWaitStages ? NS : kPreWaitStages;
             int st = 0, x_issued = 0;
-            int stage_kc[NS], stage_u[NS];
+            int stage_kc[NP], stage_u[NP];
             bool ok = true;
             for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const int u = item / a.Pv, vp = item - u * a.Pv;
@@ -541,9 +546,9 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
                 for (int sj = 0; sj < seg_len; sj += kStageIters, ++st) {
                     const int n_here = min(kStageIters, seg_len - sj);
                     const int s = st % NS;
-                    if (st == NS) {
+                    if (st == NP) {
                         grid_dependency_wait();
-                        for (; x_issued < NS; ++x_issued)
+                        for (; x_issued < NP; ++x_issued)
                             tma_load_4d(sx + x_issued * XST, &a.xmap, 0, 0, stage_kc[x_issued],
                                         stage_u[x_issued], &sy->full[x_issued]);
                     }
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
                     mbar_arrive_expect_tx(&sy->full[s], uint32_t(n_here * CB + XST));
                     bulk_g2s_hint(sw + s * STW, wb + (long long)(gi + sj) * CB, uint32_t(n_here * CB), &sy->full[s],
                                   pol);
-                    if (st < NS) {
+                    if (st < NP) {
                         stage_kc[st] = kc0 + sj;
                         stage_u[st] = xu;
                     } else {
@@ -564,9 +569,9 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
                 j += seg_len;
             }
             }
-            if (x_issued < min(st, NS)) {  // short ranges: fewer than NS stages
+            if (x_issued < min(st, NP)) {  // short ranges: fewer than NP stages
                 grid_dependency_wait();
-                for (; x_issued < min(st, NS); ++x_issued)
+                for (; x_issued < min(st, NP); ++x_issued)
                     tma_load_4d(sx + x_issued * XST, &a.xmap, 0, 0, stage_kc[x_issued], stage_u[x_issued],
                                 &sy->full[x_issued]);
             }

@@ -31,6 +31,7 @@ constexpr int kConsumerWarps = kFeatWarps * kKGroups;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
 constexpr int kStageIters = 8;             // iterations per pipeline stage (one weight copy of ~35 KB)
 constexpr int kStages = 3;
+constexpr int kPreWaitStages = 2;   // weight stages requested before the grid-dependency wait
 
 // Activation slice in shared memory: [rows][64 k] bf16, 128-byte swizzled; 16
 // rows when the launch has more than 8, else 8 (rows >= R are zero-filled).
