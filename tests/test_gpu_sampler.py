@@ -58,6 +58,35 @@ def test_ties_follow_the_lower_id(tf, near_tie, T, k, p):
     check_tokens(gpu_sample(tf, logits, T, k, p, seed, pos), logits, T, k, p, seed, pos, near_tie)
 
 
+@pytest.mark.parametrize("n_top,p", [(4, 0.5), (4, 0.25), (4, 0.75), (8, 0.125), (8, 0.5 + 1e-6), (8, 0.5 - 1e-6)])
+def test_top_p_cut_on_a_mass_boundary(tf, near_tie, n_top, p):
+    """n_top equal leading logits (the rest negligible) put the cumulative mass
+    exactly on, or within 1e-6 of, p at the cut: the fp32 pass cannot decide
+    there and the fp64 sums must give the oracle's prefix."""
+    R, V = 16, 3000
+    logits = np.full((R, V), -1.0e4, dtype=np.float32)
+    rng = inputs.rng_for(205, n_top, int(p * 1e6))
+    for r in range(R):
+        ids = rng.choice(V, size=n_top, replace=False)
+        logits[r, ids] = 1.5
+    seed, pos = 77, np.arange(R, dtype=np.int64) * 3
+    for T, k in ((1.0, 20), (0.7, 64), (2.0, 0)):
+        check_tokens(gpu_sample(tf, logits, T, k, p, seed, pos), logits, T, k, p, seed, pos, near_tie)
+
+
+@pytest.mark.parametrize("T,k,p", [(1.0, 64, 1.0), (1.0, 20, 0.9), (3.0, 50, 0.95)])
+def test_large_logits_take_the_fp64_decision(tf, near_tie, T, k, p):
+    """Logits near 1e5 widen the fp32 scores' error bound to ~0.05, so several
+    candidates often survive the fp32 filter and the fp64 scores decide."""
+    rng = inputs.rng_for(206, k, int(T * 10))
+    R, V = 16, 2048
+    for _ in range(4):
+        logits = (1.0e5 + rng.normal(0.0, 0.3, size=(R, V))).astype(np.float32)
+        seed = int(inputs.seeds_u64(rng, 1)[0])
+        pos = inputs.positions(rng, R)
+        check_tokens(gpu_sample(tf, logits, T, k, p, seed, pos), logits, T, k, p, seed, pos, near_tie)
+
+
 @pytest.mark.parametrize("V", [1, 2, 5, 63, 64, 4096, 4097])
 def test_small_and_ragged_vocabularies(tf, near_tie, V):
     rng = inputs.rng_for(203, V)

@@ -83,9 +83,34 @@ __device__ __forceinline__ double gumbel_of_hash(uint64_t h) {
     return -log(-log(u));
 }
 
-__device__ __forceinline__ double gumbel(uint64_t seed, int64_t pos, int32_t token) {
-    return gumbel_of_hash(key_hash(seed, pos, token));
+// fp32 estimate of the Gumbel noise of key h, g = -ln(-ln u) with
+// u = ((h >> 11) + 1/2) / 2^53.  -ln u is formed from u itself when u <= 1/2
+// and as -log1p(-(1 - u)) from the exact integer 1 - u otherwise, so every
+// step is well conditioned: -ln u comes out within a few 2^-24 relative and g
+// within 6e-6 absolute (|g| < 23; logf and log1pf are within 1 ulp).  Keys
+// with 1 - u below 2^-33 (g above ~22, and u rounding to 1 in fp64) are
+// flagged for the fp64 formula.
+__device__ __forceinline__ float gumbel_f32(uint64_t h, bool &needs_fp64) {
+    const uint64_t k = h >> 11;
+    float x;
+    if (k >= (1ull << 52)) {
+        const uint64_t m = ((1ull << 53) - 1ull) - k;   // 1 - u = (m + 1/2) / 2^53
+        needs_fp64 = m < (1ull << 20);
+        x = -log1pf(-((__ull2float_rn(m) + 0.5f) * 0x1p-53f));
+    } else {
+        needs_fp64 = false;
+        x = -logf((__ull2float_rn(k) + 0.5f) * 0x1p-53f);
+    }
+    return -logf(x);
 }
+
+// Bound on the error of the fp32 top-p pass below: every candidate's
+// exp((l_i - l_0) / T) comes within 2^-22 relative plus 2^-23 |x| e^x <= 4.4e-8
+// absolute of the exact value (two roundings in the argument, expf within
+// 2 ulp), and the sums of at most 64 such terms within 64 * 2^-24 relative, so
+// the cumulative mass C_i / Z is within 1.5e-5 of the exact one; twice that
+// also covers the roundings of (p +- eps) * Z.
+constexpr float kTopPEps = 3e-5f;
 
 struct Sel {
     uint32_t thr;  // key of the k-th largest element
@@ -330,8 +355,11 @@ __device__ void finalize_row(const SampleArgs &a, const int r, const uint64_t (&
     __shared__ int sh[4];
     __shared__ int s_cnt, s_m, s_ns, s_token;
     __shared__ float sel_val[kMaxTopK], srt_val[kMaxTopK];
-    __shared__ int32_t sel_id[kMaxTopK], srt_id[kMaxTopK], pb_id[kMaxTopK];
-    __shared__ double ex[kMaxTopK], score[kMaxTopK], gsc[kMaxTopK];
+    __shared__ int32_t sel_id[kMaxTopK], srt_id[kMaxTopK];
+    __shared__ double ex[kMaxTopK], score[kMaxTopK], gsc[kMaxTopK], g_lo[kMaxTopK], g_hi[kMaxTopK];
+    __shared__ float e32[kMaxTopK];
+    __shared__ uint64_t g_hash[kMaxTopK];
+    __shared__ int8_t g_exact[kMaxTopK];
     __shared__ uint64_t s_surv[kSurvMax];
     __shared__ uint64_t s_wb[NT / 32];
     const int tid = threadIdx.x;
@@ -405,75 +433,129 @@ __device__ void finalize_row(const SampleArgs &a, const int r, const uint64_t (&
         if (a.temperature == 0.0f) {
             if (tid == 0) s_token = srt_id[0];
         } else {
-            // Warps 2-3 compute every candidate's Gumbel score and warp 2 the
-            // best of every prefix (ties to the lower id), while warps 0-1 run
-            // the top-p prefix; the token is then the best of the kept prefix.
+            // fp32 first, fp64 where fp32 cannot decide.  Warps 2-3 form
+            // every candidate's fp32 score l/T + g with an error bound (fp64 at
+            // once for a key whose 1 - u is below 2^-33), while warps 0-1 find
+            // the top-p prefix from fp32 masses, falling back to the fp64 sums
+            // when the cumulative mass lies within kTopPEps of p at the cut.
+            // Then warp 0 takes the kept candidates whose upper bound reaches
+            // the best lower bound; a single one is the token, several are
+            // decided by their fp64 scores (ties to the lower id).
             if (tid >= 64 && tid < 128) {
                 const int i = tid - 64;
-                if (i < n_sel) gsc[i] = double(srt_val[i]) / T + gumbel(a.seed, pos, srt_id[i]);
-                bar_sync_named(2, 64);
-                if (tid < 96) {
-                    const int lane = tid - 64;
-                    const int i0 = 2 * lane, i1 = 2 * lane + 1;
-                    const double s0 = i0 < n_sel ? gsc[i0] : -1.0 / 0.0, s1 = i1 < n_sel ? gsc[i1] : -1.0 / 0.0;
-                    const int d0 = i0 < n_sel ? srt_id[i0] : 0x7FFFFFFF, d1 = i1 < n_sel ? srt_id[i1] : 0x7FFFFFFF;
-                    double bs = s0;
-                    int bd = d0;
-                    if (better(s1, d1, bs, bd)) {
-                        bs = s1;
-                        bd = d1;
+                if (i < n_sel) {
+                    const uint64_t h = key_hash(a.seed, pos, srt_id[i]);
+                    const float lt = __fdiv_rn(srt_val[i], a.temperature);
+                    bool exact = false;
+                    const float sf = lt + gumbel_f32(h, exact);
+                    g_hash[i] = h;
+                    g_exact[i] = exact ? 1 : 0;
+                    if (exact) {
+                        gsc[i] = double(srt_val[i]) / T + gumbel_of_hash(h);
+                    } else {
+                        const double e = double(3e-5f + 2.4e-7f * (fabsf(lt) + fabsf(sf)));
+                        g_lo[i] = double(sf) - e;
+                        g_hi[i] = double(sf) + e;
                     }
-                    // inclusive scan of the pair bests over the lanes
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const double os = __shfl_up_sync(0xFFFFFFFFu, bs, o);
-                        const int od = __shfl_up_sync(0xFFFFFFFFu, bd, o);
-                        if (lane >= o && better(os, od, bs, bd)) {
-                            bs = os;
-                            bd = od;
-                        }
-                    }
-                    double es = __shfl_up_sync(0xFFFFFFFFu, bs, 1);
-                    int ed = __shfl_up_sync(0xFFFFFFFFu, bd, 1);
-                    if (lane == 0) {
-                        es = -1.0 / 0.0;
-                        ed = 0x7FFFFFFF;
-                    }
-                    if (i0 < n_sel) pb_id[i0] = better(s0, d0, es, ed) ? d0 : ed;
-                    if (i1 < n_sel) pb_id[i1] = bd;
                 }
             }
             if (tid < 64) {
                 if (p < 1.0) {
                     __shared__ double s_Z;
-                    if (tid < n_sel) ex[tid] = exp((double(srt_val[tid]) - double(srt_val[0])) / T);
+                    __shared__ int s_sure;
+                    const float pf = a.top_p;
+                    if (tid < n_sel) e32[tid] = expf(__fdiv_rn(srt_val[tid] - srt_val[0], a.temperature));
                     bar_sync_named(1, 64);
                     if (tid == 0) {
-                        double Z = 0.0;
-                        for (int i = 0; i < n_sel; ++i) Z += ex[i];
-                        s_Z = Z;
-                    }
-                    bar_sync_named(1, 64);
-                    if (tid < n_sel) score[tid] = ex[tid] / s_Z;   // q_i, each term on its own thread
-                    bar_sync_named(1, 64);
-                    if (tid == 0) {
-                        double S = 0.0;
-                        int m = n_sel;
-                        for (int i = 0; i < n_sel; ++i) {   // renormalised mass summed left to right
-                            S += score[i];
-                            if (S >= p) {
+                        float Z = 0.f;
+                        for (int i = 0; i < n_sel; ++i) Z += e32[i];
+                        float C = 0.f, Cprev = 0.f;
+                        int m = n_sel, sure = 0;
+                        for (int i = 0; i < n_sel; ++i) {   // the same left-to-right cut as the fp64 sums
+                            C += e32[i];
+                            if (C >= pf * Z) {
                                 m = i + 1;
+                                sure = C >= (pf + kTopPEps) * Z && (i == 0 || Cprev < (pf - kTopPEps) * Z);
                                 break;
                             }
+                            Cprev = C;
                         }
                         s_m = m;
+                        s_sure = sure;
+                    }
+                    bar_sync_named(1, 64);
+                    if (!s_sure) {
+                        if (tid < n_sel) ex[tid] = exp((double(srt_val[tid]) - double(srt_val[0])) / T);
+                        bar_sync_named(1, 64);
+                        if (tid == 0) {
+                            double Z = 0.0;
+                            for (int i = 0; i < n_sel; ++i) Z += ex[i];
+                            s_Z = Z;
+                        }
+                        bar_sync_named(1, 64);
+                        if (tid < n_sel) score[tid] = ex[tid] / s_Z;   // q_i, each term on its own thread
+                        bar_sync_named(1, 64);
+                        if (tid == 0) {
+                            double S = 0.0;
+                            int m = n_sel;
+                            for (int i = 0; i < n_sel; ++i) {   // renormalised mass summed left to right
+                                S += score[i];
+                                if (S >= p) {
+                                    m = i + 1;
+                                    break;
+                                }
+                            }
+                            s_m = m;
+                        }
                     }
                 } else if (tid == 0) {
                     s_m = n_sel;
                 }
             }
             __syncthreads();
-            if (tid == 0) s_token = pb_id[s_m - 1];
+            if (tid < 32) {
+                const int m = s_m;
+                double lo = -1.0 / 0.0;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int i = tid + 32 * h;
+                    if (i < m) lo = fmax(lo, g_exact[i] ? gsc[i] : g_lo[i]);
+                }
+                for (int o = 16; o > 0; o >>= 1) lo = fmax(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+                bool surv[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int i = tid + 32 * h;
+                    surv[h] = i < m && (g_exact[i] ? gsc[i] : g_hi[i]) >= lo;
+                }
+                const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, surv[0]), b1 = __ballot_sync(0xFFFFFFFFu, surv[1]);
+                if (__popc(b0) + __popc(b1) == 1) {
+                    if (tid == 0) s_token = srt_id[b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1];
+                } else {
+                    double bs = -1.0 / 0.0;
+                    int bd = 0x7FFFFFFF;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int i = tid + 32 * h;
+                        if (surv[h]) {
+                            const double sc = g_exact[i] ? gsc[i] : double(srt_val[i]) / T + gumbel_of_hash(g_hash[i]);
+                            if (better(sc, srt_id[i], bs, bd)) {
+                                bs = sc;
+                                bd = srt_id[i];
+                            }
+                        }
+                    }
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const double os = __shfl_xor_sync(0xFFFFFFFFu, bs, o);
+                        const int od = __shfl_xor_sync(0xFFFFFFFFu, bd, o);
+                        if (better(os, od, bs, bd)) {
+                            bs = os;
+                            bd = od;
+                        }
+                    }
+                    if (tid == 0) s_token = bd;
+                }
+            }
         }
     }
     __syncthreads();
@@ -977,27 +1059,6 @@ __global__ void gen_walk_final_kernel(const SampleArgs a) {
     WalkState st = reinterpret_cast<WalkState *>(a.gen_state)[r];
     if (!st.done) walk_decide(a, kWalkPasses - 1, r, 0, st, tau);
     if (threadIdx.x == 0 && tau != ~0ull) a.gen_thr[r] = st.beta;
-}
-
-// fp32 estimate of the Gumbel noise of key h, g = -ln(-ln u) with
-// u = ((h >> 11) + 1/2) / 2^53.  -ln u is formed from u itself when u <= 1/2
-// and as -log1p(-(1 - u)) from the exact integer 1 - u otherwise, so every
-// step is well conditioned: -ln u comes out within a few 2^-24 relative and g
-// within 6e-6 absolute (|g| < 23; logf and log1pf are within 1 ulp).  Keys
-// with 1 - u below 2^-33 (g above ~22, and u rounding to 1 in fp64) are
-// flagged for the fp64 formula.
-__device__ __forceinline__ float gumbel_f32(uint64_t h, bool &needs_fp64) {
-    const uint64_t k = h >> 11;
-    float x;
-    if (k >= (1ull << 52)) {
-        const uint64_t m = ((1ull << 53) - 1ull) - k;   // 1 - u = (m + 1/2) / 2^53
-        needs_fp64 = m < (1ull << 20);
-        x = -log1pf(-((__ull2float_rn(m) + 0.5f) * 0x1p-53f));
-    } else {
-        needs_fp64 = false;
-        x = -logf((__ull2float_rn(k) + 0.5f) * 0x1p-53f);
-    }
-    return -logf(x);
 }
 
 __global__ void __launch_bounds__(kGenSubThreads) gen_score_kernel(const SampleArgs a) {
