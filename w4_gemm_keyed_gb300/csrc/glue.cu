@@ -18,7 +18,7 @@ namespace {
 //      the row's k-th best from below (k lanes hold a key at or above it), so
 //      only the few keys at or above it are ranked; their ranks give the
 //      row's k best in order (key = (logit desc, expert id asc)).
-//   2. Warp r forms row r's renormalised weights in fp64 (summed in rank
+//   2. Warp r forms row r's renormalised weights in fp32 (summed in rank
 //      order) while warp R numbers the touched experts in ascending id and
 //      maps every (row, rank) to its expert's slot.
 __global__ void route_list_kernel(const float *router, int R, int E, int top_k, int32_t *ids, float *w,
@@ -83,16 +83,18 @@ __global__ void route_list_kernel(const float *router, int R, int E, int top_k, 
                 w[r * kMaxRouteK + lane] = 0.f;
             }
         } else {
-            // renormalised weights over the kept experts: fp64, summed in rank order
+            // renormalised weights over the kept experts, fp32, summed in rank
+            // order (within a few ulp of the exact softmax; the row warps of
+            // one CTA share the SM's few fp64 units, where this took ~1 us a row)
             const float *z = router + (long long)r * E;
-            double ej = 0.0;
-            if (lane < top_k) ej = exp(double(z[s_ids[r][lane]]) - double(z[s_ids[r][0]]));
+            float ej = 0.f;
+            if (lane < top_k) ej = expf(z[s_ids[r][lane]] - z[s_ids[r][0]]);
             // every lane forms the same left-to-right sum; lane j divides its own term
-            double tot = 0.0;
+            float tot = 0.f;
             for (int j = 0; j < top_k; ++j) tot += __shfl_sync(0xFFFFFFFFu, ej, j);
             if (lane < top_k) {
                 ids[r * kMaxRouteK + lane] = s_ids[r][lane];
-                w[r * kMaxRouteK + lane] = float(ej / tot);
+                w[r * kMaxRouteK + lane] = __fdiv_rn(ej, tot);
             }
         }
     } else if (warp == R) {
