@@ -311,6 +311,40 @@ __device__ __forceinline__ void store_block(const GemmArgs &a, void *yb, int t, 
     }
 }
 
+// Stores k-group q's quarter of a lane's results after the whole-tile combine:
+// v[mt][n] is element (mt, n, q) of the block, i.e. weight row mt*16 + g (+8
+// when q >= 2) of the feature block and verify row n*8 + 2tq + (q & 1).  The
+// arithmetic per output is store_block's.
+__device__ __forceinline__ void store_quarter(const GemmArgs &a, void *yb, int t, int fw, int gq, int tq, int q,
+                                              bool hi, const float (&v)[2][2]) {
+    const int r0 = tq * 2 + (q & 1);
+    if (a.mode == kSwiGluBf16) {
+        __nv_bfloat16 *h = static_cast<__nv_bfloat16 *>(yb);
+        const int j = t * (kTileN / 2) + fw * 16 + gq + (q >= 2 ? 8 : 0);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            if (n == 1 && !hi) continue;
+            const int r = n * 8 + r0;
+            if (j < a.F && r < a.R) {
+                const float g = v[0][n];
+                const float up = v[1][n];
+                h[(long long)r * a.ldy + j] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * up);
+            }
+        }
+        return;
+    }
+    const int fb = t * kTileN + fw * kBlockRows + gq + (q >= 2 ? 8 : 0);
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            if (n == 1 && !hi) continue;
+            const int f = fb + mt * 16, r = n * 8 + r0;
+            if (f < a.N && r < a.R) put(a, yb, r, f, v[mt][n]);
+        }
+    }
+}
+
 // Shared-memory view of the candidate epilogue (selector launches only).
 template <bool HI>
 struct SelView {
@@ -477,8 +511,10 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sx = smem;                                  // [NS][XST], 1024-B aligned
     uint8_t *sw = sx + NS * XST;                         // [NS][STW]
-    float *red = reinterpret_cast<float *>(sw + NS * STW);   // [2][kFeatWarps][32][4 * NQ]
-    Sync *sy = reinterpret_cast<Sync *>(red + 2 * kFeatWarps * 32 * 4 * NQ);
+    constexpr int CBF = comb_buf_floats(HI);
+    static_assert(2 * kFeatWarps * 32 * 4 * NQ <= CBF, "the split-tile combine must fit in buffer 0");
+    float *red = reinterpret_cast<float *>(sw + NS * STW);   // [2][CBF]: the k-group combine buffers
+    Sync *sy = reinterpret_cast<Sync *>(red + 2 * CBF);
     uint8_t *selb = reinterpret_cast<uint8_t *>(sy) + 256;   // SEL: SelView<HI> region
 
     // Work items are (problem u, range vp) pairs, u-major; CTA b takes items
@@ -652,6 +688,7 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
 
     grid_dependency_wait();  // activations, workspace and outputs come from earlier grids
     int st = 0;  // stage counter, identical to the producer's
+    int cpar = 0;   // combine buffer of the next whole-tile segment end (the same in every warp)
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int u = item / a.Pv, vp = item - u * a.Pv;
     void *yb = static_cast<char *>(a.y) + (long long)u * a.y_stride * (long long)ysz;
@@ -717,6 +754,85 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
                 acc[q >> 1][q & 1][3] += o.w;
             }
         };
+        const unsigned tb = unsigned(t) * Kc, te = tb + Kc;
+        if (!SEL && seg_b == tb && seg_e == te) {
+            // Whole tile: a reduce-scatter.  k-group q keeps element c = q of
+            // every accumulator; the others hand it their values through buffer
+            // cpar, and it adds the four in the order (0 + 1) + (2 + 3) and
+            // stores that quarter, so the four warps share the epilogue.  The
+            // buffers alternate: a warp writes buffer b again only after the
+            // barrier of the segment end in between, which every warp reaches
+            // after reading b.
+            constexpr int QV = lane_vals(HI) / kKGroups;
+            float *cb = red + cpar * CBF;
+#pragma unroll
+            for (int q = 0; q < kKGroups; ++q) {
+                if (q == kg) continue;
+                float *dst = cb + (((fw * kKGroups + q) * 3 + (((kg - q) & 3) - 1)) * 32 + lane) * QV;
+                if (HI)
+                    *reinterpret_cast<float4 *>(dst) = make_float4(acc[0][0][q], acc[1][0][q], acc[0][1][q], acc[1][1][q]);
+                else
+                    *reinterpret_cast<float2 *>(dst) = make_float2(acc[0][0][q], acc[1][0][q]);
+            }
+            float own[2][2];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    float o = acc[mt][n][0];
+                    if (kg == 1) o = acc[mt][n][1];
+                    if (kg == 2) o = acc[mt][n][2];
+                    if (kg == 3) o = acc[mt][n][3];
+                    own[mt][n] = o;
+                }
+            bar_sync_named(1 + fw, 32 * kKGroups);
+            // k-group w's values of this warp's quarter
+            auto fetch = [&](int w, float (&o)[2][2]) {
+                if (w == kg) {
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                        for (int n = 0; n < 2; ++n) o[mt][n] = own[mt][n];
+                    return;
+                }
+                const float *src = cb + (((fw * kKGroups + kg) * 3 + (((w - kg) & 3) - 1)) * 32 + lane) * QV;
+                if (HI) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src);
+                    o[0][0] = v.x;
+                    o[1][0] = v.y;
+                    o[0][1] = v.z;
+                    o[1][1] = v.w;
+                } else {
+                    const float2 v = *reinterpret_cast<const float2 *>(src);
+                    o[0][0] = v.x;
+                    o[1][0] = v.y;
+                    o[0][1] = o[1][1] = 0.f;
+                }
+            };
+            float sum[2][2], pa[2][2], pb[2][2];
+            fetch(0, pa);
+            fetch(1, pb);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int n = 0; n < 2; ++n) sum[mt][n] = pa[mt][n] + pb[mt][n];
+            fetch(2, pa);
+            fetch(3, pb);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int n = 0; n < 2; ++n) sum[mt][n] = sum[mt][n] + (pa[mt][n] + pb[mt][n]);
+            store_quarter(a, yb, t, fw, gq, tq, kg, hi, sum);
+            cpar ^= 1;
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[mt][n][c] = 0.f;
+            continue;
+        }
+        cpar = 1;   // the split-tile combine below uses buffer 0
         bar_sync_named(1 + fw, 32 * kKGroups);
         if (kg == 1) put_rb(rb_a);
         if (kg == 3) put_rb(rb_b);
@@ -729,7 +845,6 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
         bar_sync_named(1 + fw, 32 * kKGroups);
         if (kg == 0) {
             add_rb(rb_b);                   // (0 + 1) + (2 + 3)
-            const unsigned tb = unsigned(t) * Kc, te = tb + Kc;
             if (seg_b == tb && seg_e == te) {
                 if (!SEL || a.y) store_block(a, yb, t, fw, gq, tq, hi, acc);
                 if constexpr (SEL) sel_push(t * kTileN + fw * kBlockRows, acc);

@@ -42,6 +42,14 @@ constexpr int kLaneAccHi = 16;             // fp32 accumulators per lane: 2 sub-
 // fp32 values per lane exchanged by the k-group combine and the split-K fixup:
 // rows 8..15 (accumulator half n = 1) only when the launch has them
 __host__ __device__ constexpr int lane_vals(bool hi) { return hi ? kLaneAccHi : kLaneAccHi / 2; }
+// k-group combine of a whole tile: each k-group ends with one quarter of every
+// lane's sums (accumulator element c = its k-group) and stores it.  A lane
+// writes the three quarters it does not keep: per buffer [fw][quarter][3][32]
+// of lane_vals / 4 floats; two buffers alternate between segment ends.  The
+// split-tile combine (all sums to k-group 0) uses the start of buffer 0.
+__host__ __device__ constexpr int comb_buf_floats(bool hi) {
+    return kFeatWarps * kKGroups * (kKGroups - 1) * 32 * (lane_vals(hi) / kKGroups);
+}
 
 // Weight formats of a packed matrix.
 enum WeightFormat : int {
@@ -92,7 +100,7 @@ inline size_t gemm_smem_bytes(int G, bool hi, int fmt = kFmtSym, bool sel = fals
     return 1024                                                         // alignment slack
            + size_t(ns) * x_stage_bytes(hi)                             // activation slices (1024-B aligned)
            + size_t(ns) * kStageIters * chunk_bytes(G, fmt)            // weight stages
-           + 2 * size_t(kFeatWarps) * 32 * lane_vals(hi) * 4            // k-group combine buffers
+           + 2 * size_t(comb_buf_floats(hi)) * 4                        // k-group combine buffers
            + 256                                                        // barriers
            + (sel ? size_t(sel_smem_bytes(hi)) : 0);
 }
