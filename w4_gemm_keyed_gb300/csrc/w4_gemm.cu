@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
     uint8_t *sx = smem;                                  // [NS][XST], 1024-B aligned
     uint8_t *sw = sx + NS * XST;                         // [NS][STW]
     constexpr int CBF = comb_buf_floats(HI);
-    static_assert(2 * kFeatWarps * 32 * 4 * NQ <= CBF, "the split-tile combine must fit in buffer 0");
+    static_assert(2 * 32 * 4 * NQ <= CBF / kFeatWarps, "the split-tile combine must fit in a feature block's part");
     float *red = reinterpret_cast<float *>(sw + NS * STW);   // [2][CBF]: the k-group combine buffers
     Sync *sy = reinterpret_cast<Sync *>(red + 2 * CBF);
     uint8_t *selb = reinterpret_cast<uint8_t *>(sy) + 256;   // SEL: SelView<HI> region
@@ -643,8 +643,10 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
         for (int j = 0; j < 4; ++j) xoff[j] = uint32_t(lrow * 128 + (((2 * j + lcol) ^ (lrow & 7)) << 4));
     }
     const size_t ysz = a.mode == kSwiGluBf16 ? sizeof(__nv_bfloat16) : sizeof(float);
-    float4 *rb_a = reinterpret_cast<float4 *>(red) + (fw * 32 + lane) * NQ;
-    float4 *rb_b = rb_a + kFeatWarps * 32 * NQ;
+    // the split-tile combine of feature block fw stays inside fw's part of
+    // buffer 0, which only fw's four warps touch
+    float4 *rb_a = reinterpret_cast<float4 *>(red + fw * (CBF / kFeatWarps)) + lane * NQ;
+    float4 *rb_b = rb_a + 32 * NQ;
     bool ok = true;
 
     float acc[2][2][4];
@@ -832,7 +834,7 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
                     for (int c = 0; c < 4; ++c) acc[mt][n][c] = 0.f;
             continue;
         }
-        cpar = 1;   // the split-tile combine below uses buffer 0
+        cpar = 1;   // the split-tile combine below uses fw's part of buffer 0
         bar_sync_named(1 + fw, 32 * kKGroups);
         if (kg == 1) put_rb(rb_a);
         if (kg == 3) put_rb(rb_b);

@@ -46,7 +46,8 @@ __host__ __device__ constexpr int lane_vals(bool hi) { return hi ? kLaneAccHi : 
 // lane's sums (accumulator element c = its k-group) and stores it.  A lane
 // writes the three quarters it does not keep: per buffer [fw][quarter][3][32]
 // of lane_vals / 4 floats; two buffers alternate between segment ends.  The
-// split-tile combine (all sums to k-group 0) uses the start of buffer 0.
+// split-tile combine of feature block fw (all sums to k-group 0) uses the
+// start of fw's part of buffer 0.
 __host__ __device__ constexpr int comb_buf_floats(bool hi) {
     return kFeatWarps * kKGroups * (kKGroups - 1) * 32 * (lane_vals(hi) / kKGroups);
 }
