@@ -92,6 +92,15 @@ struct Split {
     }
 };
 
+// n / d for the per-item index arithmetic.  Below 2^21, (n + 0.5) / d lies at
+// least 0.5 / d from an integer and the fp32 reciprocal and product stay
+// within n * 2^-22 / d of it, so truncation gives the quotient exactly; larger
+// n take the integer division.
+__device__ __forceinline__ unsigned idx_div(unsigned n, unsigned d) {
+    if (n < (1u << 21)) return unsigned(__fmul_rz(float(n) + 0.5f, __frcp_rn(float(d))));
+    return n / d;
+}
+
 // bf16 pair -> two floats (low half, high half).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
     return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
@@ -259,8 +268,9 @@ __device__ __forceinline__ void consume_slice_nvfp4(const uint8_t *blk, uint32_t
     }
 }
 
+template <bool NV>
 __device__ __forceinline__ void put(const GemmArgs &a, void *yb, int r, int f, float v) {
-    if (a.fmt == kFmtNvfp4) v *= a.gscale;   // the NVFP4 tensor scale, once per output
+    if (NV) v *= a.gscale;   // the NVFP4 tensor scale, once per output
     float *y = static_cast<float *>(yb) + (long long)r * a.ldy + f;
     if (a.mode == kAccumulateF32)
         *y = *y + v;
@@ -270,6 +280,7 @@ __device__ __forceinline__ void put(const GemmArgs &a, void *yb, int r, int f, f
 
 // Stores a lane's 16 results: element (mt, n, c) is weight row mt*16 + g (+8
 // for c >= 2) of the feature block and verify row n*8 + 2q + (c & 1).
+template <bool NV>
 __device__ __forceinline__ void store_block(const GemmArgs &a, void *yb, int t, int fw, int gq, int tq, bool hi,
                                             const float (&v)[2][2][4]) {
     if (a.mode == kSwiGluBf16) {
@@ -300,12 +311,12 @@ __device__ __forceinline__ void store_block(const GemmArgs &a, void *yb, int t, 
             const int f = f0 + mt * 16 + gq;
             const int r = n * 8 + tq * 2;
             if (f < a.N) {
-                if (r < a.R) put(a, yb, r, f, v[mt][n][0]);
-                if (r + 1 < a.R) put(a, yb, r + 1, f, v[mt][n][1]);
+                if (r < a.R) put<NV>(a, yb, r, f, v[mt][n][0]);
+                if (r + 1 < a.R) put<NV>(a, yb, r + 1, f, v[mt][n][1]);
             }
             if (f + 8 < a.N) {
-                if (r < a.R) put(a, yb, r, f + 8, v[mt][n][2]);
-                if (r + 1 < a.R) put(a, yb, r + 1, f + 8, v[mt][n][3]);
+                if (r < a.R) put<NV>(a, yb, r, f + 8, v[mt][n][2]);
+                if (r + 1 < a.R) put<NV>(a, yb, r + 1, f + 8, v[mt][n][3]);
             }
         }
     }
@@ -315,6 +326,7 @@ __device__ __forceinline__ void store_block(const GemmArgs &a, void *yb, int t, 
 // v[mt][n] is element (mt, n, q) of the block, i.e. weight row mt*16 + g (+8
 // when q >= 2) of the feature block and verify row n*8 + 2tq + (q & 1).  The
 // arithmetic per output is store_block's.
+template <bool NV>
 __device__ __forceinline__ void store_quarter(const GemmArgs &a, void *yb, int t, int fw, int gq, int tq, int q,
                                               bool hi, const float (&v)[2][2]) {
     const int r0 = tq * 2 + (q & 1);
@@ -340,7 +352,7 @@ __device__ __forceinline__ void store_quarter(const GemmArgs &a, void *yb, int t
         for (int n = 0; n < 2; ++n) {
             if (n == 1 && !hi) continue;
             const int f = fb + mt * 16, r = n * 8 + r0;
-            if (f < a.N && r < a.R) put(a, yb, r, f, v[mt][n]);
+            if (f < a.N && r < a.R) put<NV>(a, yb, r, f, v[mt][n]);
         }
     }
 }
@@ -570,14 +582,14 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
             int stage_kc[NP], stage_u[NP];
             bool ok = true;
             for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const int u = item / a.Pv, vp = item - u * a.Pv;
+            const int u = int(idx_div(unsigned(item), unsigned(a.Pv))), vp = item - u * a.Pv;
             const int xu = a.x_per_problem ? u : 0;
             const uint8_t *wb = a.w + (long long)(a.expert_ids ? a.expert_ids[u] : u) * a.w_stride;
             const unsigned i0 = split.start(vp);
             const int n_it = int(split.start(vp + 1) - i0);
             for (int j = 0; j < n_it && ok;) {
                 const unsigned gi = i0 + unsigned(j);
-                const int kc0 = int(gi % Kc);
+                const int kc0 = int(gi - idx_div(gi, Kc) * Kc);
                 const int seg_len = min(n_it - j, a.Kc - kc0);
                 for (int sj = 0; sj < seg_len; sj += kStageIters, ++st) {
                     const int n_here = min(kStageIters, seg_len - sj);
@@ -692,13 +704,13 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
     int st = 0;  // stage counter, identical to the producer's
     int cpar = 0;   // combine buffer of the next whole-tile segment end (the same in every warp)
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int u = item / a.Pv, vp = item - u * a.Pv;
+    const int u = int(idx_div(unsigned(item), unsigned(a.Pv))), vp = item - u * a.Pv;
     void *yb = static_cast<char *>(a.y) + (long long)u * a.y_stride * (long long)ysz;
     const unsigned i0 = split.start(vp);
     const int n_it = int(split.start(vp + 1) - i0);
     for (int j = 0; j < n_it;) {
         const unsigned gi = i0 + unsigned(j);
-        const int t = int(gi / Kc);
+        const int t = int(idx_div(gi, Kc));
         const int kc0 = int(gi - unsigned(t) * Kc);
         const int seg_len = min(n_it - j, a.Kc - kc0);
         for (int sj = 0; sj < seg_len; sj += kStageIters, ++st) {
@@ -824,7 +836,7 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
                 for (int n = 0; n < 2; ++n) sum[mt][n] = sum[mt][n] + (pa[mt][n] + pb[mt][n]);
-            store_quarter(a, yb, t, fw, gq, tq, kg, hi, sum);
+            store_quarter<FMT == kFmtNvfp4>(a, yb, t, fw, gq, tq, kg, hi, sum);
             cpar ^= 1;
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
@@ -848,7 +860,7 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
         if (kg == 0) {
             add_rb(rb_b);                   // (0 + 1) + (2 + 3)
             if (seg_b == tb && seg_e == te) {
-                if (!SEL || a.y) store_block(a, yb, t, fw, gq, tq, hi, acc);
+                if (!SEL || a.y) store_block<FMT == kFmtNvfp4>(a, yb, t, fw, gq, tq, hi, acc);
                 if constexpr (SEL) sel_push(t * kTileN + fw * kBlockRows, acc);
             } else {
                 // stream-K partial.  A split tile's first k-slice lies in the
@@ -933,7 +945,7 @@ __global__ void __launch_bounds__(SEL ? kThreads + 32 * kSelWarps : kThreads, 1)
                             }
                         }
                         if (lane == 0) *ctr = 0u;  // leave the counter zero for the next launch
-                        if (!SEL || a.y) store_block(a, yb, t, fw, gq, tq, hi, sum);
+                        if (!SEL || a.y) store_block<FMT == kFmtNvfp4>(a, yb, t, fw, gq, tq, hi, sum);
                         if constexpr (SEL) sel_push(t * kTileN + fw * kBlockRows, sum);
                     }
                 }
