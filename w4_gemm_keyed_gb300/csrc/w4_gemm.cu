@@ -284,7 +284,9 @@ template <bool NV>
 __device__ __forceinline__ void store_block(const GemmArgs &a, void *yb, int t, int fw, int gq, int tq, bool hi,
                                             const float (&v)[2][2][4]) {
     if (a.mode == kSwiGluBf16) {
-        // sub-tile 0 holds gate rows, sub-tile 1 the matching up rows
+        // sub-tile 0 holds gate rows, sub-tile 1 the matching up rows; silu
+        // through the fast exponential and divide (relative error ~1e-6, far
+        // inside the bf16 rounding of h)
         __nv_bfloat16 *h = static_cast<__nv_bfloat16 *>(yb);
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
@@ -296,7 +298,7 @@ __device__ __forceinline__ void store_block(const GemmArgs &a, void *yb, int t, 
                 if (j < a.F && r < a.R) {
                     const float g = v[0][n][c];
                     const float up = v[1][n][c];
-                    h[(long long)r * a.ldy + j] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * up);
+                    h[(long long)r * a.ldy + j] = __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * up);
                 }
             }
         }
@@ -340,7 +342,7 @@ __device__ __forceinline__ void store_quarter(const GemmArgs &a, void *yb, int t
             if (j < a.F && r < a.R) {
                 const float g = v[0][n];
                 const float up = v[1][n];
-                h[(long long)r * a.ldy + j] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * up);
+                h[(long long)r * a.ldy + j] = __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * up);
             }
         }
         return;
