@@ -14,6 +14,15 @@ constexpr int kMaxDevices = 64;
 // reports TF_DEV_TIMEOUT instead of hanging the GPU.
 constexpr uint32_t kWaitLimit = 1u << 22;
 
+// n / d (d >= 1) for index arithmetic.  Below 2^21, (n + 0.5) / d lies at
+// least 0.5 / d from an integer and the fp32 reciprocal and product stay
+// within n * 2^-22 / d of it, so truncation gives the quotient exactly; larger
+// n take the integer division.  (tests/idx_div_check.cu checks it on the GPU.)
+__device__ __forceinline__ unsigned idx_div(unsigned n, unsigned d) {
+    if (n < (1u << 21)) return unsigned(__fmul_rz(float(n) + 0.5f, __frcp_rn(float(d))));
+    return n / d;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

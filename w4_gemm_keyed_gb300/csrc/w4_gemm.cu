@@ -92,15 +92,6 @@ struct Split {
     }
 };
 
-// n / d for the per-item index arithmetic.  Below 2^21, (n + 0.5) / d lies at
-// least 0.5 / d from an integer and the fp32 reciprocal and product stay
-// within n * 2^-22 / d of it, so truncation gives the quotient exactly; larger
-// n take the integer division.
-__device__ __forceinline__ unsigned idx_div(unsigned n, unsigned d) {
-    if (n < (1u << 21)) return unsigned(__fmul_rz(float(n) + 0.5f, __frcp_rn(float(d))));
-    return n / d;
-}
-
 // bf16 pair -> two floats (low half, high half).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
     return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
