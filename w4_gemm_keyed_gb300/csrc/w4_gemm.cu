@@ -20,7 +20,11 @@
 //           integer codes -8..7), loads the activation B fragment with a
 //           swizzle-aware ldmatrix and issues one mma.sync per 8 rows.  Each
 //           quantisation group's partial is formed in a fresh fp32 fragment and
-//           folded in as acc = fma(scale, partial, acc).
+//           folded in as acc = fma(scale, partial, acc).  At the end of a
+//           whole tile the four k-groups of a feature block trade partial sums
+//           through shared memory (one named barrier) and each adds and stores
+//           one quarter of the block; a split tile's sums go to k-group 0,
+//           which runs the split-K fixup.
 // The grid signals its dependents at once (programmatic dependent launch): the
 // next launch in the stream lands on every SM this one frees and requests its
 // first weight stages before it waits for this grid to finish.
